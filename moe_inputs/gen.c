@@ -1,0 +1,229 @@
+/*
+ * Seeded synthetic inputs for the routed-MoE layer: expert weights, router
+ * weights, router bias, activations and forced-routing traces.
+ *
+ * This file holds no arithmetic of the MoE method itself. It only draws random
+ * numbers, so both the CUDA library and the CPU oracle consume identical bytes.
+ *
+ * Generator: Philox-4x32-10, the counter-based generator of Salmon, Moraes,
+ * Dror and Shaw, "Parallel random numbers: as easy as 1, 2, 3" (SC'11),
+ * written here from its published definition. Each 64-bit "stream" names one
+ * tensor. Element i of a stream takes word i%4 of the block with counter
+ * (i/4, stream). Normals use the Box-Muller transform on pairs of words.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define PHILOX_M0 0xD2511F53u
+#define PHILOX_M1 0xCD9E8D57u
+#define PHILOX_W0 0x9E3779B9u
+#define PHILOX_W1 0xBB67AE85u
+
+static inline void philox_round(uint32_t c[4], const uint32_t k[2]) {
+    uint64_t p0 = (uint64_t)PHILOX_M0 * c[0];
+    uint64_t p1 = (uint64_t)PHILOX_M1 * c[2];
+    uint32_t hi0 = (uint32_t)(p0 >> 32), lo0 = (uint32_t)p0;
+    uint32_t hi1 = (uint32_t)(p1 >> 32), lo1 = (uint32_t)p1;
+    uint32_t n0 = hi1 ^ c[1] ^ k[0];
+    uint32_t n2 = hi0 ^ c[3] ^ k[1];
+    c[0] = n0;
+    c[1] = lo1;
+    c[2] = n2;
+    c[3] = lo0;
+}
+
+void mi_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]) {
+    uint32_t c[4] = {ctr[0], ctr[1], ctr[2], ctr[3]};
+    uint32_t k[2] = {key[0], key[1]};
+    for (int r = 0; r < 10; ++r) {
+        if (r > 0) {
+            k[0] += PHILOX_W0;
+            k[1] += PHILOX_W1;
+        }
+        philox_round(c, k);
+    }
+    memcpy(out, c, sizeof(c));
+}
+
+static inline void block_of(uint64_t seed, uint64_t stream, uint64_t q, uint32_t out[4]) {
+    uint32_t ctr[4] = {(uint32_t)q, (uint32_t)(q >> 32), (uint32_t)stream, (uint32_t)(stream >> 32)};
+    uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+    mi_philox4x32_10(ctr, key, out);
+}
+
+/* (0,1): the word plus one half, scaled by 2^-32 */
+static inline double unit_open(uint32_t r) { return ((double)r + 0.5) * (1.0 / 4294967296.0); }
+
+/* four standard normals from one Philox block (two Box-Muller pairs) */
+static inline void normals4(uint64_t seed, uint64_t stream, uint64_t q, double z[4]) {
+    uint32_t r[4];
+    block_of(seed, stream, q, r);
+    const double two_pi = 6.283185307179586476925286766559;
+    for (int h = 0; h < 2; ++h) {
+        double u1 = unit_open(r[2 * h]), u2 = unit_open(r[2 * h + 1]);
+        double rad = sqrt(-2.0 * log(u1));
+        z[2 * h] = rad * cos(two_pi * u2);
+        z[2 * h + 1] = rad * sin(two_pi * u2);
+    }
+}
+
+/* fp32 -> bf16 bits, round to nearest even; NaN maps to a quiet NaN */
+static inline uint16_t f32_to_bf16_rne(float f) {
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    if ((u & 0x7f800000u) == 0x7f800000u && (u & 0x007fffffu)) return 0x7fc0;
+    u += 0x7fffu + ((u >> 16) & 1u);
+    return (uint16_t)(u >> 16);
+}
+
+uint16_t mi_f32_to_bf16(float f) { return f32_to_bf16_rne(f); }
+
+/* Elements [first, first+n) of stream `stream`, each N(0, stddev) rounded to
+ * fp32 and then to bf16 (RNE). */
+void mi_normal_bf16(uint64_t seed, uint64_t stream, uint64_t first, uint64_t n, double stddev, uint16_t* out) {
+    if (n == 0) return;
+    uint64_t q0 = first / 4, q1 = (first + n + 3) / 4;
+#pragma omp parallel for schedule(static)
+    for (int64_t q = (int64_t)q0; q < (int64_t)q1; ++q) {
+        double z[4];
+        normals4(seed, stream, (uint64_t)q, z);
+        for (int w = 0; w < 4; ++w) {
+            uint64_t i = (uint64_t)q * 4 + w;
+            if (i < first || i >= first + n) continue;
+            out[i - first] = f32_to_bf16_rne((float)(z[w] * stddev));
+        }
+    }
+}
+
+void mi_normal_f32(uint64_t seed, uint64_t stream, uint64_t first, uint64_t n, double stddev, float* out) {
+    if (n == 0) return;
+    uint64_t q0 = first / 4, q1 = (first + n + 3) / 4;
+#pragma omp parallel for schedule(static)
+    for (int64_t q = (int64_t)q0; q < (int64_t)q1; ++q) {
+        double z[4];
+        normals4(seed, stream, (uint64_t)q, z);
+        for (int w = 0; w < 4; ++w) {
+            uint64_t i = (uint64_t)q * 4 + w;
+            if (i < first || i >= first + n) continue;
+            out[i - first] = (float)(z[w] * stddev);
+        }
+    }
+}
+
+void mi_uniform_u32(uint64_t seed, uint64_t stream, uint64_t first, uint64_t n, uint32_t* out) {
+    for (uint64_t i = first; i < first + n; ++i) {
+        uint32_t r[4];
+        block_of(seed, stream, i / 4, r);
+        out[i - first] = r[i % 4];
+    }
+}
+
+/* A sequential source of uniform words on one stream. */
+typedef struct {
+    uint64_t seed, stream, next;
+    uint32_t buf[4];
+} word_src;
+
+static uint32_t next_word(word_src* s) {
+    uint64_t i = s->next++;
+    if (i % 4 == 0) block_of(s->seed, s->stream, i / 4, s->buf);
+    return s->buf[i % 4];
+}
+
+/* integer in [0, n) from one word (multiply-shift) */
+static inline uint32_t bounded(uint32_t w, uint32_t n) { return (uint32_t)(((uint64_t)w * n) >> 32); }
+
+/* Zipf(s) probabilities over ranks 1..E, p_r = r^-s / sum_j j^-s. */
+static void zipf_probs(int E, double s, double* p) {
+    double tot = 0.0;
+    for (int r = 1; r <= E; ++r) tot += pow((double)r, -s);
+    for (int r = 1; r <= E; ++r) p[r - 1] = pow((double)r, -s) / tot;
+}
+
+/*
+ * Router bias that gives routing a Zipf(s) preference over experts.
+ * A seeded Fisher-Yates shuffle pi maps rank r (0-based) to an expert;
+ * bias[pi[r]] = (float) ln p_{r+1}. perm_out[r] = pi[r].
+ */
+void mi_zipf_bias(uint64_t seed, uint64_t stream, int E, double s, int32_t* perm_out, float* bias_out) {
+    word_src src = {seed, stream, 0, {0, 0, 0, 0}};
+    for (int r = 0; r < E; ++r) perm_out[r] = r;
+    for (int i = E - 1; i > 0; --i) {
+        uint32_t j = bounded(next_word(&src), (uint32_t)(i + 1));
+        int32_t t = perm_out[i];
+        perm_out[i] = perm_out[j];
+        perm_out[j] = t;
+    }
+    double* p = (double*)malloc(sizeof(double) * (size_t)E);
+    zipf_probs(E, s, p);
+    for (int r = 0; r < E; ++r) bias_out[perm_out[r]] = (float)log(p[r]);
+    free(p);
+}
+
+/* draw a rank from Zipf(s) by inverse CDF on a (0,1) uniform */
+static int zipf_draw(const double* cdf, int E, word_src* src) {
+    double u = unit_open(next_word(src));
+    int lo = 0, hi = E - 1;
+    while (lo < hi) {
+        int mid = (lo + hi) / 2;
+        if (cdf[mid] >= u) hi = mid; else lo = mid + 1;
+    }
+    return lo;
+}
+
+/*
+ * Forced-routing trace with temporal reuse, one persistent stream per batch
+ * position b. sets[((step*L + l)*B + b)*k + j] is the j-th pick.
+ * Step 0: k Zipf draws (expert = perm[l*E + rank]) without duplicates.
+ * Step s>0, each pick j: with probability p_reuse choose uniformly among the
+ * experts that position b used at step s-1 in layer l and that are not yet
+ * picked (if none are left, fall through); otherwise draw Zipf, rejecting
+ * duplicates. perm holds one rank->expert table per layer.
+ * Returns 0, or -1 when k > E.
+ */
+int mi_trace_reuse(uint64_t seed, uint64_t stream, int L, int steps, int B, int E, int k, double s,
+                   double p_reuse, const int32_t* perm, int32_t* sets) {
+    if (k > E || k <= 0) return -1;
+    double* p = (double*)malloc(sizeof(double) * (size_t)E);
+    double* cdf = (double*)malloc(sizeof(double) * (size_t)E);
+    zipf_probs(E, s, p);
+    double acc = 0.0;
+    for (int r = 0; r < E; ++r) { acc += p[r]; cdf[r] = acc; }
+    cdf[E - 1] = 1.0;
+    word_src src = {seed, stream, 0, {0, 0, 0, 0}};
+    const uint32_t reuse_thresh = (uint32_t)(p_reuse * 4294967296.0 > 4294967295.0 ? 4294967295.0 : p_reuse * 4294967296.0);
+    int32_t cand[1024];
+    for (int st = 0; st < steps; ++st)
+        for (int l = 0; l < L; ++l)
+            for (int b = 0; b < B; ++b) {
+                int32_t* cur = sets + (((size_t)st * L + l) * B + b) * k;
+                const int32_t* prev = st > 0 ? sets + (((size_t)(st - 1) * L + l) * B + b) * k : NULL;
+                for (int j = 0; j < k; ++j) {
+                    int chosen = -1;
+                    if (prev) {
+                        uint32_t w = next_word(&src);
+                        if (w < reuse_thresh) {
+                            int nc = 0;
+                            for (int q = 0; q < k; ++q) {
+                                int dup = 0;
+                                for (int jj = 0; jj < j; ++jj) dup |= (cur[jj] == prev[q]);
+                                if (!dup) cand[nc++] = prev[q];
+                            }
+                            if (nc > 0) chosen = cand[bounded(next_word(&src), (uint32_t)nc)];
+                        }
+                    }
+                    while (chosen < 0) {
+                        int e = perm[(size_t)l * E + zipf_draw(cdf, E, &src)];
+                        int dup = 0;
+                        for (int jj = 0; jj < j; ++jj) dup |= (cur[jj] == e);
+                        if (!dup) chosen = e;
+                    }
+                    cur[j] = chosen;
+                }
+            }
+    free(p);
+    free(cdf);
+    return 0;
+}

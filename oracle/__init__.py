@@ -1,0 +1,219 @@
+"""CPU oracle for the routed-MoE layer with a shared LRU cache of (layer, expert) entries.
+
+TEST INFRASTRUCTURE ONLY: imported by tests/, by ``__graft_entry__.smoke()`` and by the
+CPU-baseline leg of ``bench.py``; never by the library.  Thin ctypes wrapper over
+oracle.cpp (plain C++, double accumulation), which shares no code with the CUDA path.
+See oracle.cpp for the definitions, the page sections they follow and the readings taken
+where the pages are silent.  Every function here is pinned by tests/test_oracle_*.py.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.cpp")
+_SO = os.path.join(_HERE, "liboracle.so")
+
+EV_HIT, EV_FILL, EV_PREFETCH_FILL, EV_PREFETCH_HIT = 0, 1, 2, 3
+ACCESS_ROUTED, ACCESS_PREFETCH = 0, 1
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.cpp (g++ -O2, OpenMP, no FP contraction, no fast-math)."""
+    if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(_SRC):
+        tmp = _SO + f".tmp{os.getpid()}"
+        subprocess.check_call(["g++", "-O2", "-std=c++17", "-fopenmp", "-ffp-contract=off", "-fno-fast-math",
+                               "-shared", "-fPIC", _SRC, "-o", tmp])
+        os.replace(tmp, _SO)
+    return _SO
+
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        build()
+        L = ctypes.CDLL(_SO)
+        i32, dbl, vp = ctypes.c_int, ctypes.c_double, ctypes.c_void_p
+        L.orc_num_threads.restype = i32
+        L.orc_router_logits.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp]
+        L.orc_topk.argtypes = [vp, i32, i32, i32, vp, vp]
+        L.orc_forced_gates.argtypes = [vp, vp, i32, i32, i32, vp, vp]
+        L.orc_forced_gates.restype = i32
+        L.orc_near_ties.argtypes = [vp, i32, i32, i32, dbl, vp]
+        L.orc_near_ties.restype = i32
+        L.orc_permute.argtypes = [vp, i32, i32, i32, vp, vp]
+        L.orc_permute.restype = i32
+        L.orc_expert_ffn.argtypes = [vp, i32, i32, vp, vp]
+        L.orc_moe_layer.argtypes = [vp, i32, i32, vp, vp, i32, i32, vp, vp, vp]
+        L.orc_moe_dense.argtypes = [vp, i32, i32, i32, vp, vp, i32, i32, vp, vp, vp]
+        L.orc_layer_accesses.argtypes = [vp, i32, i32, i32, vp]
+        L.orc_layer_accesses.restype = i32
+        L.orc_lru_run.argtypes = [i32, i32, vp, vp, vp, vp, vp, vp, vp]
+        L.orc_lru_run.restype = i32
+        _lib = L
+    return _lib
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def _p(a) -> int:
+    return a.ctypes.data if a is not None else 0
+
+
+def num_threads() -> int:
+    return int(lib().orc_num_threads())
+
+
+def router_logits(x_bf16: np.ndarray, Wr: np.ndarray, b: np.ndarray, want_double: bool = True):
+    """Router logits (T, E): fp32 in the fixed order, and the same sum in double."""
+    x = _c(x_bf16, np.uint16)
+    T, H = x.shape
+    Wr = _c(Wr, np.float32)
+    E = Wr.shape[0]
+    if H % 256:
+        raise ValueError("hidden size must be a multiple of 256")
+    z32 = np.empty((T, E), dtype=np.float32)
+    z64 = np.empty((T, E), dtype=np.float64) if want_double else None
+    lib().orc_router_logits(_p(x), _p(Wr), _p(_c(b, np.float32)), T, H, E, _p(z32), _p(z64))
+    return z32, z64
+
+
+def topk(z32: np.ndarray, k: int):
+    z = _c(z32, np.float32)
+    T, E = z.shape
+    idx = np.empty((T, k), dtype=np.int32)
+    w = np.empty((T, k), dtype=np.float64)
+    lib().orc_topk(_p(z), T, E, k, _p(idx), _p(w))
+    return idx, w
+
+
+def forced_gates(z32: np.ndarray, sets: np.ndarray):
+    z = _c(z32, np.float32)
+    s = _c(sets, np.int32)
+    T, E = z.shape
+    k = s.shape[1]
+    idx = np.empty((T, k), dtype=np.int32)
+    w = np.empty((T, k), dtype=np.float64)
+    if lib().orc_forced_gates(_p(z), _p(s), T, E, k, _p(idx), _p(w)) != 0:
+        raise ValueError("forced sets must hold k distinct experts in [0, E)")
+    return idx, w
+
+
+def near_ties(z64: np.ndarray, k: int, eps: float = 1e-5) -> np.ndarray:
+    z = _c(z64, np.float64)
+    T, E = z.shape
+    flag = np.empty(T, dtype=np.int32)
+    lib().orc_near_ties(_p(z), T, E, k, eps, _p(flag))
+    return flag.astype(bool)
+
+
+def permute(idx: np.ndarray, E: int):
+    i = _c(idx, np.int32)
+    T, k = i.shape
+    offsets = np.empty(E + 1, dtype=np.int32)
+    perm = np.empty(T * k, dtype=np.int32)
+    if lib().orc_permute(_p(i), T, k, E, _p(offsets), _p(perm)) != 0:
+        raise ValueError("expert index out of range")
+    return offsets, perm
+
+
+def expert_ffn(entry: np.ndarray, H: int, I: int, x_row: np.ndarray) -> np.ndarray:
+    e = _c(entry, np.uint16)
+    x = _c(x_row, np.uint16)
+    y = np.empty(H, dtype=np.float64)
+    lib().orc_expert_ffn(_p(e), H, I, _p(x), _p(y))
+    return y
+
+
+def _entry_table(entries):
+    arrs = [_c(e, np.uint16) for e in entries]
+    table = (ctypes.c_void_p * len(arrs))(*[a.ctypes.data for a in arrs])
+    return table, arrs
+
+
+def moe_layer(entries, H: int, I: int, x_bf16, resid, idx, w) -> np.ndarray:
+    """Sparse routed layer. entries: per-expert bf16 entries of this layer (sequence or dict-like
+    indexable by expert id)."""
+    x = _c(x_bf16, np.uint16)
+    T = x.shape[0]
+    idx = _c(idx, np.int32)
+    k = idx.shape[1]
+    E = int(idx.max()) + 1 if not hasattr(entries, "__len__") else len(entries)
+    table, keep = _entry_table([entries[e] for e in range(E)])
+    out = np.empty((T, H), dtype=np.float64)
+    lib().orc_moe_layer(ctypes.addressof(table), H, I, _p(x), _p(_c(resid, np.float32)), T, k, _p(idx),
+                        _p(_c(w, np.float64)), _p(out))
+    del keep
+    return out
+
+
+def moe_layer_rows(entry_of, H: int, I: int, x_bf16, resid, idx, w) -> np.ndarray:
+    """Sparse routed layer where entry_of(e) returns expert e's entry (only routed experts are fetched)."""
+    x = _c(x_bf16, np.uint16)
+    T = x.shape[0]
+    idx = _c(idx, np.int32)
+    k = idx.shape[1]
+    used = sorted(set(int(e) for e in idx.ravel()))
+    E = max(used) + 1
+    cache = {e: _c(entry_of(e), np.uint16) for e in used}
+    dummy = np.zeros(1, dtype=np.uint16)
+    table = (ctypes.c_void_p * E)(*[(cache[e].ctypes.data if e in cache else dummy.ctypes.data) for e in range(E)])
+    out = np.empty((T, H), dtype=np.float64)
+    lib().orc_moe_layer(ctypes.addressof(table), H, I, _p(x), _p(_c(resid, np.float32)), T, k, _p(idx),
+                        _p(_c(w, np.float64)), _p(out))
+    del cache
+    return out
+
+
+def moe_dense(entries, H: int, I: int, x_bf16, resid, idx, w) -> np.ndarray:
+    x = _c(x_bf16, np.uint16)
+    T = x.shape[0]
+    idx = _c(idx, np.int32)
+    k = idx.shape[1]
+    E = len(entries)
+    table, keep = _entry_table(list(entries))
+    out = np.empty((T, H), dtype=np.float64)
+    lib().orc_moe_dense(ctypes.addressof(table), H, I, E, _p(x), _p(_c(resid, np.float32)), T, k, _p(idx),
+                        _p(_c(w, np.float64)), _p(out))
+    del keep
+    return out
+
+
+def layer_accesses(idx: np.ndarray, E: int) -> np.ndarray:
+    i = _c(idx, np.int32)
+    T, k = i.shape
+    out = np.empty(E, dtype=np.int32)
+    n = lib().orc_layer_accesses(_p(i), T, k, E, _p(out))
+    return out[:n].copy()
+
+
+def lru_run(capacity: int, layers, experts, kinds=None) -> np.ndarray:
+    """Run the LRU over an access sequence. Returns events as an int32 array (n, 6):
+    (kind, layer, expert, slot, evicted_layer, evicted_expert)."""
+    l = _c(layers, np.int32)
+    e = _c(experts, np.int32)
+    n = len(l)
+    kd = _c(np.zeros(n) if kinds is None else kinds, np.int32)
+    k_out = np.empty(n, np.int32)
+    s_out = np.empty(n, np.int32)
+    vl = np.empty(n, np.int32)
+    ve = np.empty(n, np.int32)
+    if lib().orc_lru_run(capacity, n, _p(l), _p(e), _p(kd), _p(k_out), _p(s_out), _p(vl), _p(ve)) != 0:
+        raise ValueError("capacity must be >= 1")
+    return np.stack([k_out, l, e, s_out, vl, ve], axis=1)
+
+
+def route(x_bf16, Wr, b, k):
+    """Router + top-k + gates for one layer: (idx, w, z32, z64)."""
+    z32, z64 = router_logits(x_bf16, Wr, b)
+    idx, w = topk(z32, k)
+    return idx, w, z32, z64

@@ -1,0 +1,54 @@
+"""The seeded input generator: deterministic, chunk-independent, and drawing what it claims."""
+import numpy as np
+
+import moe_inputs as mi
+
+
+def test_deterministic_and_chunk_independent():
+    a = mi.normal_bf16(0, mi.stream_id(mi.KIND_EXPERT, 2, 3), 1001, 0.02)
+    b = mi.normal_bf16(0, mi.stream_id(mi.KIND_EXPERT, 2, 3), 1001, 0.02)
+    assert np.array_equal(a, b)
+    part = mi.normal_bf16(0, mi.stream_id(mi.KIND_EXPERT, 2, 3), 500, 0.02, first=333)
+    assert np.array_equal(part, a[333:833])
+    c = mi.normal_bf16(0, mi.stream_id(mi.KIND_EXPERT, 2, 4), 1001, 0.02)
+    assert not np.array_equal(a, c)
+
+
+def test_normal_moments():
+    z = mi.bf16_bits_to_f32(mi.normal_bf16(7, 11, 2_000_000, 0.02)).astype(np.float64)
+    assert abs(z.mean()) < 1e-4 and abs(z.std() - 0.02) < 1e-4
+    f = mi.normal_f32(7, 12, 2_000_000, 1.0).astype(np.float64)
+    assert abs(f.mean()) < 5e-3 and abs(f.std() - 1.0) < 5e-3
+    assert abs(np.mean(f ** 4) - 3.0) < 0.05  # Gaussian kurtosis
+
+
+def test_bf16_rounding_is_nearest_even():
+    assert mi.f32_to_bf16_bits(1.0) == 0x3F80
+    # 1 + 2^-8 lies halfway between bf16 neighbours 1.0 and 1 + 2^-7: ties go to even
+    assert mi.f32_to_bf16_bits(1.0 + 2 ** -8) == 0x3F80
+    assert mi.f32_to_bf16_bits(1.0 + 3 * 2 ** -8) == 0x3F82
+    assert mi.f32_to_bf16_bits(-2.0) == 0xC000
+
+
+def test_zipf_bias_is_log_probabilities():
+    b, perm = mi.router_bias(0, 5, 256, 1.1)
+    assert sorted(perm.tolist()) == list(range(256))
+    assert abs(np.exp(b.astype(np.float64)).sum() - 1.0) < 1e-5
+    r = np.arange(1, 257)
+    p = r ** -1.1 / np.sum(r ** -1.1)
+    assert np.allclose(b[perm], np.log(p).astype(np.float32))
+
+
+def test_reuse_trace_properties():
+    L, steps, B, E, k = 2, 200, 4, 64, 6
+    perms = np.stack([mi.router_bias(0, l, E, 1.1)[1] for l in range(L)])
+    tr = mi.trace_reuse(0, L, steps, B, E, k, 1.1, 0.7, perms)
+    assert tr.shape == (steps, L, B, k)
+    assert tr.min() >= 0 and tr.max() < E
+    for s in range(steps):
+        for l in range(L):
+            for b in range(B):
+                assert len(set(tr[s, l, b])) == k
+    reuse = np.mean([len(set(tr[s, l, b]) & set(tr[s - 1, l, b])) / k
+                     for s in range(1, steps) for l in range(L) for b in range(B)])
+    assert reuse > 0.7  # at least the forced 70% plus chance repeats of Zipf draws
