@@ -1,0 +1,417 @@
+#!/usr/bin/env python
+"""Benchmark: routed-MoE decode layer served from the VRAM LRU expert cache on one B300.
+
+Workload (the decode-layer shape): hidden 4096, expert SwiGLU intermediate 1536, 256 routed
+experts (36 MiB bf16 each, 9.66 GB pool in pinned host memory), top-6, router bias from
+Zipf(1.1), LRU cache of 64 entries, fresh N(0,1) activations every step. One benchmark step
+= one decode step at batch 1, one at batch 4 and one at batch 16 (21 tokens): router GEMV,
+top-k, host LRU, fills of missing experts over PCIe, permutation, gate/up and down GEMVs
+through the slot table, combine.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl b300|reference]
+
+Prints one JSON line (rank 0). `value` is device-timed tok/s with inputs resident in HBM;
+`e2e` repeats the measurement through the same C-ABI calls with inputs in pinned host memory
+and the host<->device copies inside the timed region. `roofline` is the gate/up GEMV (the
+dominant kernel) against the measured HBM copy bandwidth. `--impl reference` times the CPU
+oracle on the same workload (bounded per step). Multi-GPU runs are independent replicas.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer decode tok/s (batch 1/4/16, 256 experts top-6, 64-entry LRU cache)"
+UNIT = "tok/s"
+BATCHES = (1, 4, 16)  # replaced by --batches
+FALLBACK_HBM_GBS = 6400.0
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "gemv_gateup_decode.md")
+GEMV_SOURCE = os.path.join(ROOT, "moe_expert_layer_10_b300", "csrc", "gemv.cu")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=64)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["b300", "reference"], default="b300")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batches", default="1,4,16", help="decode batch sizes of one step (profiling cases)")
+    ap.add_argument("--capacity", type=int, default=0, help="override the cache capacity (profiling cases)")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------- helpers
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def traffic_from_profile():
+    """dram bytes per launch of the gate/up GEMV from the committed ncu summary, or None if
+    the summary is missing or was taken on a different kernel source."""
+    if not os.path.exists(PROFILE_SUMMARY):
+        return None
+    text = open(PROFILE_SUMMARY).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    h = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+    if not m or not h:
+        return None
+    cur = hashlib.sha256(open(GEMV_SOURCE, "rb").read()).hexdigest()
+    return float(m.group(1)) if h.group(1) == cur else None
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- workload
+def workload():
+    import moe_inputs as mi
+    return mi.WORKLOADS["decode"]
+
+
+def step_inputs(W, step: int):
+    """Activations of one benchmark step: one batch per size (bf16 bits)."""
+    import moe_inputs as mi
+    return {B: mi.activations(W.seed, 1_000_000 + 1000 * B + step, B, W.H) for B in BATCHES}
+
+
+def cpu_oracle_step(W, Wr, b, xs, entries):
+    """The oracle on one benchmark step: route and layer for each batch size."""
+    import oracle
+    for B in BATCHES:
+        x = xs[B]
+        import moe_inputs as mi
+        resid = mi.bf16_bits_to_f32(x)
+        idx, w, _, _ = oracle.route(x, Wr, b, W.k)
+        oracle.moe_layer_rows(entries, W.H, W.I, x, resid, idx, w)
+
+
+def make_entries(W):
+    import moe_inputs as mi
+    cache = {}
+
+    def get(e):
+        if e not in cache:
+            cache[e] = mi.expert_entry(W.seed, 0, e, W.H, W.I)
+        return cache[e]
+    return get
+
+
+def cpu_baseline(W, Wr, b, target_s: float = 15.0):
+    """Time the oracle as it stands on a bounded sample: whole benchmark steps until about
+    target_s seconds of CPU work (the expert entries are regenerated outside the timing)."""
+    import oracle
+    entries = make_entries(W)
+    xs0 = step_inputs(W, 0)
+    cpu_oracle_step(W, Wr, b, xs0, entries)  # warm: builds the oracle, fetches hot entries
+    steps, t_tot = 0, 0.0
+    while t_tot < target_s and steps < 64:
+        xs = step_inputs(W, steps + 1)
+        # fetch this step's entries untimed
+        import numpy as np
+        for B in BATCHES:
+            idx, _, _, _ = oracle.route(xs[B], Wr, b, W.k)
+            for e in np.unique(idx):
+                entries(int(e))
+        t0 = time.perf_counter()
+        cpu_oracle_step(W, Wr, b, xs, entries)
+        t_tot += time.perf_counter() - t0
+        steps += 1
+    tokens = steps * sum(BATCHES)
+    return {"value": tokens / t_tot, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{steps} whole benchmark steps ({tokens} tokens: batches {list(BATCHES)}), "
+                      f"{t_tot:.1f} s of oracle time"}
+
+
+# ----------------------------------------------------------------------------- b300 arm
+def run_b300(args, rank, world, local):
+    import numpy as np
+    import torch
+
+    import moe_expert_layer_10_b300 as moe
+    import moe_inputs as mi
+
+    torch.cuda.set_device(local)
+    W = workload()
+    stream = torch.cuda.Stream()
+    C = args.capacity or W.C
+    cache = moe.MoeCache(moe.LayerShape(1, W.E, W.H, W.I, W.k, C, max(BATCHES)), flags=moe.MOE_PROFILE,
+                         stream_compute=stream)
+    for e in range(W.E):
+        mi.fill_entry_at(cache.host_entry(0, e), W.seed, 0, e, W.H, W.I)
+    Wr_h = mi.router_weights(W.seed, 0, W.E, W.H)
+    b_h, _ = mi.router_bias(W.seed, 0, W.E, W.zipf_s)
+    Wr = torch.from_numpy(Wr_h).cuda()
+    bias = torch.from_numpy(b_h).cuda()
+    total = args.warmup + args.steps
+
+    def dev_bf16(bits):
+        return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16)
+
+    # inputs resident in HBM before timing
+    xs = [{B: dev_bf16(v).cuda() for B, v in step_inputs(W, s).items()} for s in range(total)]
+    resid = [{B: xs[s][B].float() for B in BATCHES} for s in range(total)]
+    idx = {B: torch.empty((B, W.k), dtype=torch.int32, device="cuda") for B in BATCHES}
+    wts = {B: torch.empty((B, W.k), dtype=torch.float32, device="cuda") for B in BATCHES}
+    out = {B: torch.empty((B, W.H), dtype=torch.float32, device="cuda") for B in BATCHES}
+    torch.cuda.synchronize()
+
+    def step(s):
+        for B in BATCHES:
+            cache.route(0, xs[s][B], Wr, bias, idx[B], wts[B])
+            cache.layer_forward(0, xs[s][B], resid[s][B], out[B], idx[B], wts[B])
+
+    for s in range(args.warmup):
+        step(s)
+    cache.sync()
+    cache.kernel_stats(reset=True)
+    cache.stats(reset=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for s in range(args.warmup, total):
+        step(s)
+    ev1.record(stream)
+    cache.sync()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = ev0.elapsed_time(ev1)
+    ms_max = allreduce_max(ms, world)
+    barrier(world)
+    kst = cache.kernel_stats()
+    st = cache.stats()
+
+    # end to end: inputs in pinned host memory, copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        hx = [{B: dev_bf16(v).pin_memory() for B, v in step_inputs(W, s).items()} for s in range(total)]
+        hr = [{B: hx[s][B].float().pin_memory() for B in BATCHES} for s in range(total)]
+        hout = {B: torch.empty((B, W.H), dtype=torch.float32).pin_memory() for B in BATCHES}
+        dx = {B: torch.empty((B, W.H), dtype=torch.bfloat16, device="cuda") for B in BATCHES}
+        dr = {B: torch.empty((B, W.H), dtype=torch.float32, device="cuda") for B in BATCHES}
+
+        def step_e2e(s):
+            with torch.cuda.stream(stream):
+                for B in BATCHES:
+                    dx[B].copy_(hx[s][B], non_blocking=True)
+                    dr[B].copy_(hr[s][B], non_blocking=True)
+                    cache.route(0, dx[B], Wr, bias, idx[B], wts[B])
+                    cache.layer_forward(0, dx[B], dr[B], out[B], idx[B], wts[B])
+                    hout[B].copy_(out[B], non_blocking=True)
+
+        for s in range(args.warmup):
+            step_e2e(s)
+        cache.sync()
+        torch.cuda.synchronize()
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for s in range(args.warmup, total):
+            step_e2e(s)
+        e1.record(stream)
+        cache.sync()
+        torch.cuda.synchronize()
+        ems = allreduce_max(e0.elapsed_time(e1), world)
+        tokens_e2e = args.steps * sum(BATCHES) * world
+        e2e = {"value": tokens_e2e / (ems / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": sum(B * W.H * (2 + 4) for B in BATCHES),
+               "d2h_bytes_per_step": sum(B * W.H * 4 for B in BATCHES)}
+
+    tokens = args.steps * sum(BATCHES) * world
+    peak, peak_kind = measured_peaks()
+    g = kst["gemv_gateup"]
+    roof = None
+    if g["launches"]:
+        avg_ms = g["total_ms"] / g["launches"]
+        bytes_per_launch = g["bytes"] / g["launches"]
+        achieved = bytes_per_launch / (avg_ms / 1e3) / 1e9
+        roof = {"kernel": "gemv_gateup", "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                "traffic": traffic_from_profile(), "bytes_per_launch": bytes_per_launch,
+                "avg_launch_ms": avg_ms}
+    kernels = {n: {"launches": v["launches"], "avg_us": (1e3 * v["total_ms"] / v["launches"]) if v["launches"] else None,
+                   "GB/s": (v["bytes"] / (v["total_ms"] / 1e3) / 1e9) if v["total_ms"] else None}
+               for n, v in kst.items() if v["launches"]}
+    launches = int(sum(v["launches"] for v in kst.values()))
+
+    result = {
+        "metric": METRIC, "value": round(tokens / (ms_max / 1e3), 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded Philox: N(0,0.02) bf16 weights, N(0,1) activations, Zipf(1.1) router bias)",
+        "config": {"workload": "decode layer: hidden 4096, intermediate 1536, 256 experts top-6, "
+                               "64-entry LRU cache, batches 1+4+16 per step",
+                   "tokens_per_step": sum(BATCHES), "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2: each step streams >= 226 MB of expert weights (L2 126 MB)",
+                   "hit_rate": (st["hits"] / st["expert_reads"]) if st["expert_reads"] else None,
+                   "fills_per_step": st["misses"] / args.steps,
+                   "fill_GBps": (st["fill_bytes"] / (st["fill_ms"] / 1e3) / 1e9) if st["fill_ms"] else None},
+        "clocks": clk, "e2e": e2e, "gpu_launches": launches, "roofline": roof, "kernels": kernels,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(W, Wr_h, b_h)
+    cache.close()
+    return result
+
+
+# ----------------------------------------------------------------------------- reference arm
+def run_reference(args):
+    """The CPU oracle as it stands, on the same workload: every step is one whole benchmark
+    step (batches 1, 4 and 16) computed by the oracle on the host cores."""
+    import numpy as np
+
+    import moe_inputs as mi
+    import oracle
+    W = workload()
+    Wr = mi.router_weights(W.seed, 0, W.E, W.H)
+    b, _ = mi.router_bias(W.seed, 0, W.E, W.zipf_s)
+    entries = make_entries(W)
+    total = args.warmup + args.steps
+    xs_all = [step_inputs(W, s) for s in range(total)]
+    for s in range(total):  # regenerate the routed entries outside the timing
+        for B in BATCHES:
+            idx, _, _, _ = oracle.route(xs_all[s][B], Wr, b, W.k)
+            for e in np.unique(idx):
+                entries(int(e))
+    for s in range(args.warmup):
+        cpu_oracle_step(W, Wr, b, xs_all[s], entries)
+    t0 = time.perf_counter()
+    for s in range(args.warmup, total):
+        cpu_oracle_step(W, Wr, b, xs_all[s], entries)
+    dt = time.perf_counter() - t0
+    tokens = args.steps * sum(BATCHES)
+    v = tokens / dt
+    return {"impl": "reference", "metric": METRIC, "value": round(v, 3), "unit": UNIT, "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * dt / args.steps, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded Philox)",
+            "config": {"workload": "decode layer: hidden 4096, intermediate 1536, 256 experts top-6, "
+                                   "64-entry LRU cache, batches 1+4+16 per step", "tokens_per_step": sum(BATCHES)},
+            "cpu_baseline": {"value": round(v, 3), "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": f"{args.steps} whole benchmark steps ({tokens} tokens)"},
+            "e2e": {"value": round(v, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+# ----------------------------------------------------------------------------- distributed glue
+_pg = False
+
+
+def init_dist(world, local):
+    global _pg
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+        _pg = True
+
+
+def barrier(world):
+    if _pg:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def allreduce_max(v: float, world: int) -> float:
+    if not _pg:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def main():
+    global BATCHES
+    args = parse_args()
+    BATCHES = tuple(int(b) for b in args.batches.split(","))
+    rank, world, local = dist_env()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    init_dist(world, local)
+    res = run_b300(args, rank, world, local)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if _pg:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

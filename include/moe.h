@@ -1,0 +1,258 @@
+/*
+ * moe.h -- C ABI of the B300 (sm_103a) routed Mixture-of-Experts layer served from a
+ * shared VRAM LRU cache of whole (layer, expert) entries, with the complete expert pool
+ * in pinned host memory as the source of truth.
+ *
+ * What the calls implement, by page (title, section):
+ *  - "FreeToken rtx 4090" (freetoken.wiki/hardware), "How the MoE Memory Hierarchy Works":
+ *    the host keeps the complete expert pool; VRAM keeps a cache of complete
+ *    layer-and-expert entries executed through one logical mapping; a router selects a
+ *    few routed experts per token per layer ("six of 256"); decode keeps a shared LRU
+ *    cache across layers and tokens; prefill streams the next layer's experts while the
+ *    current layer computes; startup loads weights directly into the final host layout.
+ *  - "FreeToken benchmark" (freetoken.wiki/performance), "How FreeToken Serves Large MoE
+ *    Models": full-layer double buffering in prefill; shared least-recently-used expert
+ *    cache in decode; misses move experts over the PCIe link into the GPU cache.
+ *  - The per-layer arithmetic, which the pages do not state, is this library's
+ *    specification: logits z = W_r x + b (fp32), top-k by (z desc, id asc), gates
+ *    w_j = softmax of the k chosen logits, SwiGLU experts
+ *    y_e(x) = W_down (silu(W_gate x) * (W_up x)), out = resid + sum_j w_j y_{e_j}(x).
+ *
+ * Conventions for every call:
+ *  - Return 0 on success or a negative MOE_E_* code; moe_last_error() then holds a
+ *    thread-local message. No call aborts or throws across the ABI. A failed call leaves
+ *    the LRU bookkeeping consistent (an entry is only marked resident once its fill is
+ *    enqueued successfully).
+ *  - "device" pointers are CUDA device memory owned by the caller. All device work runs
+ *    in order on the context's compute stream; fills run on its copy stream.
+ *  - A context is used by one host thread at a time.
+ *  - Activations are bf16 (raw 16-bit patterns), row-major [T x hidden].
+ *  - Entry layout (host pool and device slot alike), bf16 row-major, contiguous:
+ *      W_gate [inter x hidden] | W_up [inter x hidden] | W_down [hidden x inter]
+ *    i.e. 3 * hidden * inter * 2 bytes per (layer, expert).
+ *  - Shape limits: hidden % 256 == 0, inter % 128 == 0, 1 <= top_k <= num_experts <= 1024,
+ *    top_k <= 32.
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- error codes ---- */
+#define MOE_OK 0
+#define MOE_E_INVAL (-1)    /* bad argument or shape */
+#define MOE_E_NOMEM (-2)    /* host pinned or device allocation failed */
+#define MOE_E_CUDA (-3)     /* a CUDA runtime call failed (message has the CUDA error) */
+#define MOE_E_TIMEOUT (-4)  /* a host wait on the GPU passed its deadline */
+#define MOE_E_CAPACITY (-5) /* the request needs more cache entries than configured */
+#define MOE_E_DEVICE (-6)   /* a kernel reported an error through the device status word */
+
+/* ---- config flags ---- */
+#define MOE_TRACE 1u      /* keep a ring of LRU events, readable through moe_stats */
+#define MOE_PROFILE 2u    /* time every kernel launch with CUDA events (moe_kernel_stats) */
+#define MOE_PREFILL_DB 4u /* full-layer double buffering is intended: requires capacity >= 2*num_experts */
+
+/* ---- fill modes (moe_cache_fill) ---- */
+#define MOE_FILL_DEMAND 0     /* access the distinct experts of the given top-k indices */
+#define MOE_FILL_FULL_LAYER 1 /* prefetch every expert of the layer (prefill double buffering) */
+
+/* ---- expert-FFN path selection (moe_set_path) ---- */
+#define MOE_PATH_AUTO 0 /* GEMV when every routed expert has <= 32 tokens, else grouped GEMM */
+#define MOE_PATH_GEMV 1 /* HBM-streaming GEMV kernels (decode) */
+#define MOE_PATH_GEMM 2 /* tcgen05 grouped GEMM kernels (prefill) */
+
+/* ---- LRU event kinds ---- */
+#define MOE_EV_HIT 0           /* routed access, entry resident */
+#define MOE_EV_FILL 1          /* routed access, entry copied in (a miss) */
+#define MOE_EV_PREFETCH_FILL 2 /* whole-layer prefetch copied the entry in */
+#define MOE_EV_PREFETCH_HIT 3  /* whole-layer prefetch found the entry resident */
+
+typedef struct moe_ctx moe_ctx; /* opaque: pinned pool, slot arena, LRU, streams, scratch */
+
+typedef struct {
+    int32_t num_layers;  /* L: layers sharing the cache */
+    int32_t num_experts; /* E: routed experts per layer */
+    int32_t hidden;      /* H */
+    int32_t inter;       /* I: expert SwiGLU intermediate size */
+    int32_t top_k;       /* k */
+    int32_t capacity;    /* C: cache slots, in whole entries */
+    int32_t max_tokens;  /* largest T passed to moe_route / moe_layer_forward */
+    uint32_t flags;      /* MOE_TRACE | MOE_PROFILE | MOE_PREFILL_DB */
+    uint64_t trace_capacity; /* events kept by MOE_TRACE (0: 1<<20) */
+} moe_config_t;
+
+typedef struct {
+    uint64_t expert_reads;   /* routed accesses: one per distinct (layer, expert) per forward */
+    uint64_t hits;           /* routed accesses that found the entry resident */
+    uint64_t misses;         /* routed accesses that filled the entry */
+    uint64_t prefetch_fills; /* whole-layer prefetches that filled an entry */
+    uint64_t prefetch_hits;  /* whole-layer prefetches that found the entry resident */
+    uint64_t evictions;      /* fills that replaced a resident entry */
+    uint64_t fill_bytes;     /* bytes copied host -> device by fills */
+    double fill_ms;          /* copy-stream time of completed fill batches (CUDA events) */
+    uint64_t trace_len;      /* events recorded since the last reset (the ring keeps the newest) */
+    uint64_t forwards;       /* moe_layer_forward calls */
+    uint64_t waves;          /* expert waves run (a layer routing to more than C experts runs several) */
+} moe_stats_t;
+
+typedef struct {
+    int32_t kind;      /* MOE_EV_* */
+    int32_t layer;     /* accessed entry */
+    int32_t expert;
+    int32_t slot;      /* cache slot that holds it afterwards */
+    int32_t ev_layer;  /* entry evicted to make room, or -1 */
+    int32_t ev_expert; /* or -1 */
+} moe_event_t;
+
+typedef struct {
+    char name[32];     /* kernel name */
+    uint64_t launches; /* launches timed */
+    double total_ms;   /* summed CUDA-event durations */
+    double bytes;      /* algorithmic HBM bytes of those launches (weights + activations + outputs) */
+    double flops;      /* algorithmic flops of those launches */
+} moe_kernel_stat_t;
+
+/*
+ * Create a context: pinned host pool of L*E entries (zeroed), device arena of C entries,
+ * slot-indirection table slot_of[L][E] (all -1), host LRU, scratch for max_tokens.
+ * stream_compute / stream_copy: cudaStream_t handles to use, or NULL to create private
+ * streams. The caller then writes each entry straight into moe_host_entry(). Ownership:
+ * the context owns everything it allocates; moe_cache_destroy frees it.
+ * Errors: MOE_E_INVAL (shape limits above), MOE_E_CAPACITY (MOE_PREFILL_DB with C < 2E, or
+ * C < 1), MOE_E_NOMEM, MOE_E_CUDA.
+ */
+int moe_cache_init(const moe_config_t* cfg, void* stream_compute, void* stream_copy, moe_ctx** out);
+
+/* Free every resource of the context (waits for its streams first). NULL is a no-op. */
+void moe_cache_destroy(moe_ctx* ctx);
+
+/*
+ * Host pointer (pinned, writable) to entry (layer, expert) of the pool, in the final
+ * layout given above, so loaders write weights in place. NULL if out of range.
+ * Entries must not change while a fill of that entry may be in flight.
+ */
+void* moe_host_entry(moe_ctx* ctx, int layer, int expert);
+
+/* Bytes of one entry: 3 * hidden * inter * 2. */
+uint64_t moe_entry_bytes(const moe_ctx* ctx);
+
+/*
+ * Router for one layer: logits z[t,e] = fp32(sum_h W_r[e,h] x[t,h]) + b[e] in a fixed
+ * order (32 lane partials over h = 256m + 8l + r, m then r ascending, fmaf; pairwise folds
+ * at distances 16,8,4,2,1; bias last), top-k by (z desc, id asc), gates = softmax over the
+ * k chosen logits (fp32).
+ * x_bf16 [T x H], router_w fp32 [E x H], router_b fp32 [E] (NULL: zero), outputs
+ * topk_idx int32 [T x k], topk_w fp32 [T x k], logits_or_null fp32 [T x E] -- all device.
+ * Asynchronous on the compute stream. Errors: MOE_E_INVAL (T < 0 or T > max_tokens, layer
+ * out of range, NULL pointer), MOE_E_CUDA. T == 0 is a no-op.
+ */
+int moe_route(moe_ctx* ctx, int layer, const void* x_bf16, int T, const float* router_w, const float* router_b,
+              int32_t* topk_idx, float* topk_w, float* logits_or_null);
+
+/*
+ * Forced routing: token t uses the k distinct experts forced_sets[t*k .. t*k+k-1] (device
+ * int32). The router logits are computed as in moe_route; the forced experts are ordered
+ * by (z desc, id asc) and gated by the softmax over their k logits. A set with a repeated
+ * or out-of-range id makes the kernel raise the device status (MOE_E_DEVICE at the next
+ * synchronising call) and write expert 0 / gate 0 for that token.
+ */
+int moe_route_forced(moe_ctx* ctx, int layer, const void* x_bf16, int T, const float* router_w,
+                     const float* router_b, const int32_t* forced_sets, int32_t* topk_idx, float* topk_w,
+                     float* logits_or_null);
+
+/*
+ * Cache fill without compute.
+ *  MOE_FILL_DEMAND: topk_idx_host holds n host int32 expert ids (e.g. a T*k top-k block);
+ *    their distinct values are accessed in ascending id. Errors: MOE_E_CAPACITY if more than
+ *    C distinct experts are given (moe_layer_forward runs such layers in waves instead).
+ *  MOE_FILL_FULL_LAYER: every expert 0..E-1 of the layer is accessed as a prefetch; the
+ *    copies are enqueued on the copy stream and the call returns without waiting, so they
+ *    overlap compute already enqueued (prefill double buffering). topk_idx_host/n ignored.
+ *    Errors: MOE_E_CAPACITY if C < E.
+ * Copies into a slot wait (on the GPU) for every enqueued compute that read the slot's
+ * previous entry; compute that reads a filled slot waits (on the GPU) for its copy.
+ */
+int moe_cache_fill(moe_ctx* ctx, int layer, const int32_t* topk_idx_host, int n, int mode);
+
+/*
+ * One MoE layer on T tokens (device pointers): out = resid + sum_j w_j y_{e_j}(x).
+ * x_bf16 [T x H], resid fp32 [T x H] (may equal out), out fp32 [T x H],
+ * topk_idx int32 [T x k], topk_w fp32 [T x k] (as written by moe_route).
+ * Steps: a D2H copy of topk_idx and a host wait (the host LRU needs the routed experts);
+ * the distinct experts D (ascending) are accessed in the LRU in waves of at most C;
+ * missing entries are copied in on the copy stream; per wave the expert FFN runs through
+ * the device slot table; a deterministic combine sums the k contributions in j order.
+ * Returns after enqueuing the last kernel (no wait at the end).
+ * Errors: MOE_E_INVAL, MOE_E_CUDA, MOE_E_TIMEOUT (host wait deadline), MOE_E_DEVICE (a kernel
+ * of an earlier call reported an error).
+ */
+int moe_layer_forward(moe_ctx* ctx, int layer, const void* x_bf16, const float* resid, float* out, int T,
+                      const int32_t* topk_idx, const float* topk_w);
+
+/*
+ * Counters and trace. out may be NULL. trace_or_null receives up to trace_cap of the
+ * newest events, oldest first; the return value is the number written (>= 0), or a
+ * negative error. reset != 0 clears counters and trace after reading.
+ */
+int moe_stats(moe_ctx* ctx, moe_stats_t* out, moe_event_t* trace_or_null, uint64_t trace_cap, int reset);
+
+/* ---- helpers ---- */
+
+/* Thread-local message of the last failing call on this thread ("" if none). */
+const char* moe_last_error(void);
+
+/* Choose the expert-FFN path for later moe_layer_forward calls (MOE_PATH_*). */
+int moe_set_path(moe_ctx* ctx, int path);
+
+/* Wait (with a deadline) until all enqueued work of the context has finished; reports any
+ * device status raised by its kernels (MOE_E_DEVICE). */
+int moe_sync(moe_ctx* ctx);
+
+/* Slot of entry (layer, expert) if resident, else -1 (host bookkeeping, no GPU access). */
+int moe_resident_slot(moe_ctx* ctx, int layer, int expert);
+
+/*
+ * Per-kernel timing gathered under MOE_PROFILE (complete launches only; call moe_sync
+ * first). Writes up to cap records, returns how many kernels there are. reset != 0 clears.
+ */
+int moe_kernel_stats(moe_ctx* ctx, moe_kernel_stat_t* out, int cap, int reset);
+
+/*
+ * Host-only run of this library's LRU policy (no GPU, no context): capacity slots, n
+ * accesses (layer[i], expert[i], kind[i]: 0 routed, 1 prefetch). Writes n events. Lets the
+ * host policy be checked against a reference without a GPU. Returns 0 or MOE_E_INVAL.
+ */
+int moe_lru_simulate(int capacity, int n, const int32_t* layer, const int32_t* expert, const int32_t* kind,
+                     moe_event_t* events);
+
+/*
+ * Host-side fault injection for tests: the next `count` fill copies of this context report
+ * failure before any copy is enqueued (kind 1), or the next `count` host waits report a
+ * timeout (kind 2). kind 0 clears. No GPU fault is ever produced.
+ */
+int moe_debug_inject(moe_ctx* ctx, int kind, int count);
+
+/*
+ * Copy an internal device buffer of the last moe_layer_forward to host memory, for tests.
+ * Waits (with the deadline) for the compute stream first. bytes must not exceed the
+ * buffer's size for the last call; returns MOE_E_INVAL otherwise.
+ */
+#define MOE_DBG_OFFSETS 0    /* int32 [E+1]: first permuted position of each expert */
+#define MOE_DBG_PERM 1       /* int32 [T*k]: pair id t*k+j at each permuted position */
+#define MOE_DBG_INV_PERM 2   /* int32 [T*k]: permuted position of each pair id */
+#define MOE_DBG_ACTIVE 3     /* int32 [E]: experts with >= 1 pair, ascending (first n_active valid) */
+#define MOE_DBG_N_ACTIVE 4   /* int32 [1] */
+#define MOE_DBG_SLOT_TABLE 5 /* int32 [L*E]: device slot table */
+#define MOE_DBG_H_PERM 6     /* bf16 [T*k x inter]: SwiGLU activations per permuted position */
+int moe_debug_read(moe_ctx* ctx, int what, void* host_dst, uint64_t bytes);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H */

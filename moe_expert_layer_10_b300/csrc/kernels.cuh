@@ -1,0 +1,73 @@
+// Kernel launchers of the routed-MoE hot path (sm_103a). Each launcher enqueues on the
+// given stream and returns the launch's cudaError_t. Pointers are device pointers.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+// --- router: logits in the fixed fp32 order, then top-k + softmax gates ---
+cudaError_t launch_router_logits(const uint16_t* x, const float* Wr, const float* b, int T, int H, int E, float* z,
+                                 cudaStream_t st);
+// forced == nullptr: top-k by (z desc, id asc); else order the forced sets the same way.
+cudaError_t launch_router_topk(const float* z, int T, int E, int k, const int32_t* forced, int32_t* idx, float* w,
+                               int* status, cudaStream_t st);
+
+// --- permutation: stable grouping of the T*k pairs by expert (one CTA) ---
+cudaError_t launch_permute(const int32_t* idx, const float* w, int P, int E, int32_t* offsets, int32_t* perm,
+                           int32_t* inv_perm, float* w_perm, int32_t* active, int32_t* n_active, int* status,
+                           cudaStream_t st);
+// x_perm[pos] = x[perm[pos] / k]  (bf16 rows of H)
+cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* perm, int P, int k, int H, uint16_t* x_perm,
+                               cudaStream_t st);
+
+// --- decode expert FFN: HBM-streaming GEMV through the slot table ---
+struct GemvWork {
+    int expert;      // expert id
+    int tok_off;     // first permuted position of its tokens
+    int n_tok;       // tokens routed to it
+    int unit_begin;  // first work unit of this expert (entry n_work holds the total)
+};
+
+struct GemvMaps {
+    CUtensorMap w_gu[2];  // arena viewed as [C*3I rows x H], boxes for 4 and 2 rows per warp
+    CUtensorMap w_d[2];   // arena viewed as [C*3H rows x I]
+    CUtensorMap xperm;    // [P_max x H], box 8 rows
+    CUtensorMap hperm;    // [P_max x I], box 8 rows
+    int ks_down;          // slab width of the down projection (256 or 128)
+};
+
+int gemv_nt_bucket(int max_tokens_per_expert);  // 8, 16 or 32 (tokens per pass)
+int gemv_units_per_chunk(bool gateup, int nt_bucket, int H, int I);
+
+// h_perm[pos, i] = bf16( silu(W_gate[i] . x) * (W_up[i] . x) ) for the wave's experts
+cudaError_t launch_gemv_gateup(const GemvMaps& maps, int nt_bucket, const GemvWork* work, int n_work, int n_units,
+                               const int32_t* slot_row, int H, int I, uint16_t* h_perm, int* status, int num_sms,
+                               cudaStream_t st);
+// pair_out[pos, n] = w_perm[pos] * (W_down[n] . h[pos])
+cudaError_t launch_gemv_down(const GemvMaps& maps, int nt_bucket, const GemvWork* work, int n_work, int n_units,
+                             const int32_t* slot_row, int H, int I, const float* w_perm, float* pair_out,
+                             int* status, int num_sms, cudaStream_t st);
+
+// --- combine: out[t] = resid[t] + sum_j pair_out[inv_perm[t*k+j]] (j order) ---
+cudaError_t launch_combine(const float* pair_out, const int32_t* inv_perm, const float* resid, float* out, int T,
+                           int k, int H, cudaStream_t st);
+
+// --- prefill expert FFN: tcgen05 grouped GEMM ---
+struct GemmMaps {
+    CUtensorMap a_x;    // x_perm [P_max x H], box 64 x 128, 128B swizzle
+    CUtensorMap b_gu;   // arena [C*3I rows x H], box 64 x 128, 128B swizzle
+    CUtensorMap a_h;    // h_perm [P_max x I], box 64 x 128
+    CUtensorMap b_d;    // arena [C*3H rows x I], box 64 x 128
+};
+int gemm_tiles(bool gateup, const int* counts, int n, int H, int I);  // grid bound for a wave
+cudaError_t launch_gemm_gateup(const GemmMaps& maps, const int32_t* offsets, const int32_t* active, int a_begin,
+                               int a_end, int total_tiles, const int32_t* slot_row, int H, int I, uint16_t* h_perm,
+                               int* status, int num_sms, cudaStream_t st);
+cudaError_t launch_gemm_down(const GemmMaps& maps, const int32_t* offsets, const int32_t* active, int a_begin,
+                             int a_end, int total_tiles, const int32_t* slot_row, int H, int I, const float* w_perm,
+                             float* pair_out, int* status, int num_sms, cudaStream_t st);
+
+}  // namespace moe

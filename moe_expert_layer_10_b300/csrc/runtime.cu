@@ -1,0 +1,873 @@
+// Host runtime and C ABI of the routed-MoE layer (see include/moe.h for the contract).
+//
+// Sources (page title, section):
+//  * "FreeToken rtx 4090" (freetoken.wiki/hardware), "How the MoE Memory Hierarchy Works":
+//    the complete expert pool stays in host memory as the source of truth; VRAM holds a
+//    cache of complete (layer, expert) entries; decode follows routing with a shared LRU;
+//    prefill loads the next layer's experts while the current layer computes; startup
+//    writes weights straight into the final host layout (moe_host_entry).
+//  * "FreeToken benchmark" (freetoken.wiki/performance), "How FreeToken Serves Large MoE
+//    Models": full-layer double buffering; the PCIe link moves selected experts into the
+//    GPU cache; the runtime console reports cache activity (moe_stats).
+//
+// B300 design: one context owns a pinned pool (cudaHostAlloc), a device arena of C whole
+// entries, a device slot table slot_of[L][E], a compute stream and a copy stream. Fills are
+// single cudaMemcpyAsync copies of a contiguous entry on the copy stream. Ordering is by
+// events: a fill into a slot waits for the last compute wave that read the slot; a wave
+// waits for the last fill batch of its slots. Every host wait polls with a deadline.
+#include <algorithm>
+#include <chrono>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <string>
+#include <thread>
+#include <vector>
+
+#include "../../include/moe.h"
+#include "kernels.cuh"
+#include "lru.h"
+
+using moe::ExpertLru;
+using moe::GemvWork;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int code, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return code;
+}
+
+#define CUDA_TRY(call)                                                                                 \
+    do {                                                                                               \
+        cudaError_t e_ = (call);                                                                       \
+        if (e_ != cudaSuccess) return fail(MOE_E_CUDA, "%s: %s (%s:%d)", #call, cudaGetErrorString(e_), \
+                                           __FILE__, __LINE__);                                        \
+    } while (0)
+
+constexpr int kEvRing = 256;     // compute-wave and fill-batch events
+constexpr int kStageRing = 16;   // pinned staging buffers for small H2D copies
+
+enum KernelId { kRouterLogits, kRouterTopk, kPermute, kGather, kGemvGateUp, kGemvDown, kGemmGateUp, kGemmDown,
+                kCombine, kNumKernels };
+const char* kKernelNames[kNumKernels] = {"router_logits", "router_topk", "permute",    "gather_rows",
+                                         "gemv_gateup",   "gemv_down",   "gemm_gateup", "gemm_down",
+                                         "combine"};
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+// bf16 2-D view [rows x cols] (cols contiguous) with a box of [box_rows x box_cols].
+bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_cols, uint32_t box_rows,
+              CUtensorMapSwizzle sw) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+double wait_deadline_s() {
+    static double v = [] {
+        const char* s = getenv("MOE_WAIT_TIMEOUT_S");
+        double d = s ? atof(s) : 120.0;
+        return d > 0 ? d : 120.0;
+    }();
+    return v;
+}
+
+struct ProfRec {
+    int kernel;
+    cudaEvent_t start, stop;
+    double bytes, flops;
+};
+
+struct FillRec {
+    cudaEvent_t start, stop;
+};
+
+}  // namespace
+
+struct moe_ctx {
+    moe_config_t cfg{};
+    int dev = 0, num_sms = 148;
+    int L = 0, E = 0, H = 0, I = 0, k = 0, C = 0, Tmax = 0, Pmax = 0;
+    size_t entry_elems = 0, entry_bytes = 0;
+    int path = MOE_PATH_AUTO;
+
+    uint16_t* pool = nullptr;   // pinned host, L*E entries
+    uint16_t* arena = nullptr;  // device, C entries
+    std::vector<int32_t> slot_host;   // [L*E]
+    int32_t* slot_dev = nullptr;      // [L*E]
+    bool table_dirty = true;
+    ExpertLru lru;
+
+    cudaStream_t s_comp = nullptr, s_copy = nullptr;
+    bool own_comp = false, own_copy = false;
+
+    // scratch (device)
+    float* logits = nullptr;
+    int32_t *offsets = nullptr, *perm = nullptr, *inv_perm = nullptr, *active = nullptr, *n_active = nullptr;
+    float *w_perm = nullptr, *pair_out = nullptr;
+    uint16_t *x_perm = nullptr, *h_perm = nullptr;
+    int* status = nullptr;
+    GemvWork* work_dev = nullptr;
+
+    // pinned host staging
+    int32_t* idx_host = nullptr;   // [Pmax]
+    int* status_host = nullptr;    // [1]
+    int32_t* table_stage = nullptr;        // [kStageRing][L*E]
+    GemvWork* work_stage = nullptr;        // [kStageRing][E+1]
+    cudaEvent_t stage_ev[kStageRing] = {};
+    int stage_next = 0;
+    cudaEvent_t ev_d2h = nullptr;
+
+    // ordering between fills and compute
+    cudaEvent_t comp_ev[kEvRing] = {}, fill_ev[kEvRing] = {};
+    int64_t comp_seq = -1, fill_seq = -1;
+    std::vector<int64_t> slot_last_use, slot_fill;
+
+    moe::GemvMaps gemv_maps{};
+    moe::GemmMaps gemm_maps{};
+
+    // stats and trace
+    moe_stats_t stats{};
+    std::vector<moe_event_t> trace;
+    std::vector<FillRec> fill_pending;
+    std::vector<cudaEvent_t> ev_pool;
+    std::vector<ProfRec> prof_pending;
+    moe_kernel_stat_t kstats[kNumKernels] = {};
+
+    int inject_kind = 0, inject_count = 0;
+};
+
+namespace {
+
+cudaEvent_t pool_event(moe_ctx* c) {
+    if (!c->ev_pool.empty()) {
+        cudaEvent_t e = c->ev_pool.back();
+        c->ev_pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    return e;
+}
+
+// Fold completed timing records into the counters (no waiting).
+void harvest(moe_ctx* c) {
+    size_t keep = 0;
+    for (size_t i = 0; i < c->prof_pending.size(); ++i) {
+        ProfRec& r = c->prof_pending[i];
+        if (cudaEventQuery(r.stop) == cudaSuccess) {
+            float ms = 0.f;
+            cudaEventElapsedTime(&ms, r.start, r.stop);
+            moe_kernel_stat_t& s = c->kstats[r.kernel];
+            s.launches++;
+            s.total_ms += ms;
+            s.bytes += r.bytes;
+            s.flops += r.flops;
+            c->ev_pool.push_back(r.start);
+            c->ev_pool.push_back(r.stop);
+        } else {
+            c->prof_pending[keep++] = r;
+        }
+    }
+    c->prof_pending.resize(keep);
+    keep = 0;
+    for (size_t i = 0; i < c->fill_pending.size(); ++i) {
+        FillRec& r = c->fill_pending[i];
+        if (cudaEventQuery(r.stop) == cudaSuccess) {
+            float ms = 0.f;
+            cudaEventElapsedTime(&ms, r.start, r.stop);
+            c->stats.fill_ms += ms;
+            c->ev_pool.push_back(r.start);
+            c->ev_pool.push_back(r.stop);
+        } else {
+            c->fill_pending[keep++] = r;
+        }
+    }
+    c->fill_pending.resize(keep);
+    cudaGetLastError();  // cudaEventQuery's cudaErrorNotReady is not an error here
+}
+
+struct ProfScope {
+    moe_ctx* c;
+    int kernel;
+    double bytes, flops;
+    cudaEvent_t start = nullptr;
+    ProfScope(moe_ctx* c_, int kid, double b, double f) : c(c_), kernel(kid), bytes(b), flops(f) {
+        if (c->cfg.flags & MOE_PROFILE) {
+            start = pool_event(c);
+            if (start) cudaEventRecord(start, c->s_comp);
+        }
+    }
+    ~ProfScope() {
+        if (start) {
+            cudaEvent_t stop = pool_event(c);
+            if (stop) {
+                cudaEventRecord(stop, c->s_comp);
+                c->prof_pending.push_back(ProfRec{kernel, start, stop, bytes, flops});
+            }
+        }
+    }
+};
+
+int wait_event(moe_ctx* c, cudaEvent_t ev, const char* what) {
+    if (c->inject_kind == 2 && c->inject_count > 0) {
+        c->inject_count--;
+        return fail(MOE_E_TIMEOUT, "%s: injected host wait timeout", what);
+    }
+    const auto t0 = std::chrono::steady_clock::now();
+    for (long it = 0;; ++it) {
+        cudaError_t e = cudaEventQuery(ev);
+        if (e == cudaSuccess) return MOE_OK;
+        if (e != cudaErrorNotReady) return fail(MOE_E_CUDA, "%s: %s", what, cudaGetErrorString(e));
+        if ((it & 255) == 255) {
+            const double dt = std::chrono::duration<double>(std::chrono::steady_clock::now() - t0).count();
+            if (dt > wait_deadline_s()) return fail(MOE_E_TIMEOUT, "%s: no completion after %.0f s", what, dt);
+            std::this_thread::yield();
+        }
+    }
+}
+
+int check_status(moe_ctx* c) {
+    if (*c->status_host != 0) {
+        const int code = *c->status_host;
+        *c->status_host = 0;
+        // clear the device word too, in stream order, so the context stays usable
+        cudaMemsetAsync(c->status, 0, sizeof(int), c->s_comp);
+        return fail(MOE_E_DEVICE, "a kernel raised device status %d (1 wait timeout, 2 bad forced set, 3 bad slot, "
+                                  "4 bad expert index)", code);
+    }
+    return MOE_OK;
+}
+
+// Pinned staging slot for a small H2D copy; waits (bounded) until its previous copy is done.
+int next_stage(moe_ctx* c, int* slot_out) {
+    const int s = c->stage_next;
+    c->stage_next = (s + 1) % kStageRing;
+    int rc = wait_event(c, c->stage_ev[s], "staging buffer reuse");
+    if (rc) return rc;
+    *slot_out = s;
+    return MOE_OK;
+}
+
+int upload_table(moe_ctx* c) {
+    if (!c->table_dirty) return MOE_OK;
+    int s;
+    int rc = next_stage(c, &s);
+    if (rc) return rc;
+    const size_t n = static_cast<size_t>(c->L) * c->E;
+    int32_t* host = c->table_stage + static_cast<size_t>(s) * n;
+    std::memcpy(host, c->slot_host.data(), n * sizeof(int32_t));
+    CUDA_TRY(cudaMemcpyAsync(c->slot_dev, host, n * sizeof(int32_t), cudaMemcpyHostToDevice, c->s_comp));
+    CUDA_TRY(cudaEventRecord(c->stage_ev[s], c->s_comp));
+    c->table_dirty = false;
+    return MOE_OK;
+}
+
+void record_event(moe_ctx* c, int kind, int key, int slot, int victim) {
+    c->stats.trace_len++;
+    if (!(c->cfg.flags & MOE_TRACE) || c->trace.empty()) return;
+    moe_event_t ev;
+    ev.kind = kind;
+    ev.layer = key / c->E;
+    ev.expert = key % c->E;
+    ev.slot = slot;
+    ev.ev_layer = victim >= 0 ? victim / c->E : -1;
+    ev.ev_expert = victim >= 0 ? victim % c->E : -1;
+    c->trace[(c->stats.trace_len - 1) % c->trace.size()] = ev;
+}
+
+// Access the given keys in order (routed or prefetch), enqueue the fills as one batch on
+// the copy stream. Each filled slot remembers the batch, whose event compute waits for.
+// On any failure the batch opened so far is still closed with its event, and the access
+// that failed is not committed, so the policy and the slot table stay consistent.
+int access_keys(moe_ctx* c, const std::vector<int>& keys, bool prefetch) {
+    bool batch_open = false;
+    FillRec fr{nullptr, nullptr};
+    int rc = MOE_OK;
+    for (int key : keys) {
+        ExpertLru::Plan p = c->lru.plan(key, prefetch);
+        const bool fill = p.kind == ExpertLru::kFill || p.kind == ExpertLru::kPrefetchFill;
+        if (fill) {
+            if (c->inject_kind == 1 && c->inject_count > 0) {
+                c->inject_count--;
+                rc = fail(MOE_E_CUDA, "injected fill failure (layer %d expert %d)", key / c->E, key % c->E);
+                break;
+            }
+            if (!batch_open) {
+                fr.start = pool_event(c);
+                if (fr.start) cudaEventRecord(fr.start, c->s_copy);
+                batch_open = true;
+            }
+            // the slot's previous entry may still be read by an enqueued wave
+            const int64_t last = c->slot_last_use[p.slot];
+            cudaError_t e = cudaSuccess;
+            if (last >= 0) e = cudaStreamWaitEvent(c->s_copy, c->comp_ev[last % kEvRing], 0);
+            if (e == cudaSuccess)
+                e = cudaMemcpyAsync(c->arena + static_cast<size_t>(p.slot) * c->entry_elems,
+                                    c->pool + static_cast<size_t>(key) * c->entry_elems, c->entry_bytes,
+                                    cudaMemcpyHostToDevice, c->s_copy);
+            if (e != cudaSuccess) {
+                rc = fail(MOE_E_CUDA, "fill of layer %d expert %d: %s", key / c->E, key % c->E,
+                          cudaGetErrorString(e));
+                break;
+            }
+        }
+        c->lru.commit(p);
+        record_event(c, p.kind, key, p.slot, p.victim);
+        switch (p.kind) {
+            case ExpertLru::kHit: c->stats.expert_reads++; c->stats.hits++; break;
+            case ExpertLru::kFill: c->stats.expert_reads++; c->stats.misses++; break;
+            case ExpertLru::kPrefetchFill: c->stats.prefetch_fills++; break;
+            case ExpertLru::kPrefetchHit: c->stats.prefetch_hits++; break;
+        }
+        if (fill) {
+            c->stats.fill_bytes += c->entry_bytes;
+            if (p.victim >= 0) {
+                c->stats.evictions++;
+                c->slot_host[p.victim] = -1;
+            }
+            c->slot_host[key] = p.slot;
+            c->slot_fill[p.slot] = c->fill_seq + 1;  // the batch event recorded below
+            c->table_dirty = true;
+        }
+    }
+    if (batch_open) {
+        c->fill_seq++;
+        cudaError_t e = cudaEventRecord(c->fill_ev[c->fill_seq % kEvRing], c->s_copy);
+        fr.stop = pool_event(c);
+        if (fr.start && fr.stop) {
+            cudaEventRecord(fr.stop, c->s_copy);
+            c->fill_pending.push_back(fr);
+        }
+        if (e != cudaSuccess && rc == MOE_OK)
+            rc = fail(MOE_E_CUDA, "fill batch event: %s", cudaGetErrorString(e));
+    }
+    return rc;
+}
+
+int validate_layer(moe_ctx* c, int layer) {
+    if (!c) return fail(MOE_E_INVAL, "null context");
+    if (layer < 0 || layer >= c->L) return fail(MOE_E_INVAL, "layer %d outside [0, %d)", layer, c->L);
+    return MOE_OK;
+}
+
+void free_all(moe_ctx* c) {
+    if (c->s_comp) cudaStreamSynchronize(c->s_comp);
+    if (c->s_copy) cudaStreamSynchronize(c->s_copy);
+    harvest(c);
+    for (auto& r : c->prof_pending) {
+        cudaEventDestroy(r.start);
+        cudaEventDestroy(r.stop);
+    }
+    for (auto& r : c->fill_pending) {
+        cudaEventDestroy(r.start);
+        cudaEventDestroy(r.stop);
+    }
+    for (cudaEvent_t e : c->ev_pool) cudaEventDestroy(e);
+    for (int i = 0; i < kEvRing; ++i) {
+        if (c->comp_ev[i]) cudaEventDestroy(c->comp_ev[i]);
+        if (c->fill_ev[i]) cudaEventDestroy(c->fill_ev[i]);
+    }
+    for (int i = 0; i < kStageRing; ++i)
+        if (c->stage_ev[i]) cudaEventDestroy(c->stage_ev[i]);
+    if (c->ev_d2h) cudaEventDestroy(c->ev_d2h);
+    void* dev_ptrs[] = {c->arena, c->slot_dev, c->logits, c->offsets, c->perm, c->inv_perm, c->active,
+                        c->n_active, c->w_perm, c->pair_out, c->x_perm, c->h_perm, c->status, c->work_dev};
+    for (void* p : dev_ptrs)
+        if (p) cudaFree(p);
+    void* host_ptrs[] = {c->pool, c->idx_host, c->status_host, c->table_stage, c->work_stage};
+    for (void* p : host_ptrs)
+        if (p) cudaFreeHost(p);
+    if (c->own_comp && c->s_comp) cudaStreamDestroy(c->s_comp);
+    if (c->own_copy && c->s_copy) cudaStreamDestroy(c->s_copy);
+    delete c;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_last_error(void) { return g_last_error.c_str(); }
+
+uint64_t moe_entry_bytes(const moe_ctx* c) { return c ? c->entry_bytes : 0; }
+
+int moe_cache_init(const moe_config_t* cfg, void* stream_compute, void* stream_copy, moe_ctx** out) {
+    g_last_error.clear();
+    if (!cfg || !out) return fail(MOE_E_INVAL, "null argument");
+    *out = nullptr;
+    const moe_config_t& f = *cfg;
+    if (f.num_layers < 1 || f.num_experts < 1 || f.num_experts > 1024 || f.top_k < 1 || f.top_k > 32 ||
+        f.top_k > f.num_experts || f.hidden < 256 || f.hidden % 256 || f.inter < 128 || f.inter % 128 ||
+        f.max_tokens < 1)
+        return fail(MOE_E_INVAL, "shape outside the limits (hidden %% 256, inter %% 128, 1 <= k <= min(E, 32), "
+                                 "E <= 1024, max_tokens >= 1)");
+    if (f.capacity < 1) return fail(MOE_E_CAPACITY, "capacity must be >= 1");
+    if ((f.flags & MOE_PREFILL_DB) && f.capacity < 2 * f.num_experts)
+        return fail(MOE_E_CAPACITY, "double buffering needs capacity >= 2 * num_experts (%d < %d)", f.capacity,
+                    2 * f.num_experts);
+    const uint64_t keys = static_cast<uint64_t>(f.num_layers) * f.num_experts;
+    const uint64_t entry_elems = 3ull * f.hidden * f.inter;
+    if (static_cast<uint64_t>(f.capacity) * 3ull * f.inter >= (1ull << 31) ||
+        static_cast<uint64_t>(f.capacity) * 3ull * f.hidden >= (1ull << 31) || keys >= (1ull << 31))
+        return fail(MOE_E_INVAL, "arena too large for 32-bit row coordinates");
+    if (!encode_fn()) return fail(MOE_E_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+
+    moe_ctx* c = new moe_ctx();
+    c->cfg = f;
+    c->L = f.num_layers;
+    c->E = f.num_experts;
+    c->H = f.hidden;
+    c->I = f.inter;
+    c->k = f.top_k;
+    c->C = f.capacity;
+    c->Tmax = f.max_tokens;
+    c->Pmax = f.max_tokens * f.top_k;
+    c->entry_elems = entry_elems;
+    c->entry_bytes = entry_elems * 2;
+    c->lru.reset(c->C, static_cast<int>(keys));
+    c->slot_host.assign(keys, -1);
+    c->slot_last_use.assign(c->C, -1);
+    c->slot_fill.assign(c->C, -1);
+    if (f.flags & MOE_TRACE) c->trace.resize(f.trace_capacity ? f.trace_capacity : (1u << 20));
+
+#define INIT_TRY(call)                                                                          \
+    do {                                                                                        \
+        cudaError_t e_ = (call);                                                                \
+        if (e_ != cudaSuccess) {                                                                \
+            int code_ = (e_ == cudaErrorMemoryAllocation) ? MOE_E_NOMEM : MOE_E_CUDA;           \
+            fail(code_, "%s: %s", #call, cudaGetErrorString(e_));                               \
+            std::string msg_ = g_last_error;                                                    \
+            free_all(c);                                                                        \
+            g_last_error = msg_;                                                                \
+            return code_;                                                                       \
+        }                                                                                       \
+    } while (0)
+
+    INIT_TRY(cudaGetDevice(&c->dev));
+    INIT_TRY(cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->dev));
+    if (stream_compute) {
+        c->s_comp = static_cast<cudaStream_t>(stream_compute);
+    } else {
+        INIT_TRY(cudaStreamCreateWithFlags(&c->s_comp, cudaStreamNonBlocking));
+        c->own_comp = true;
+    }
+    if (stream_copy) {
+        c->s_copy = static_cast<cudaStream_t>(stream_copy);
+    } else {
+        INIT_TRY(cudaStreamCreateWithFlags(&c->s_copy, cudaStreamNonBlocking));
+        c->own_copy = true;
+    }
+    const size_t pool_bytes = keys * c->entry_bytes;
+    INIT_TRY(cudaHostAlloc(reinterpret_cast<void**>(&c->pool), pool_bytes, cudaHostAllocPortable));
+    std::memset(c->pool, 0, pool_bytes);
+    INIT_TRY(cudaMalloc(&c->arena, static_cast<size_t>(c->C) * c->entry_bytes));
+    INIT_TRY(cudaMalloc(&c->slot_dev, keys * sizeof(int32_t)));
+    INIT_TRY(cudaMalloc(&c->logits, static_cast<size_t>(c->Tmax) * c->E * sizeof(float)));
+    INIT_TRY(cudaMalloc(&c->offsets, (c->E + 1) * sizeof(int32_t)));
+    INIT_TRY(cudaMalloc(&c->active, c->E * sizeof(int32_t)));
+    INIT_TRY(cudaMalloc(&c->n_active, sizeof(int32_t)));
+    INIT_TRY(cudaMalloc(&c->perm, c->Pmax * sizeof(int32_t)));
+    INIT_TRY(cudaMalloc(&c->inv_perm, c->Pmax * sizeof(int32_t)));
+    INIT_TRY(cudaMalloc(&c->w_perm, c->Pmax * sizeof(float)));
+    INIT_TRY(cudaMalloc(&c->x_perm, static_cast<size_t>(c->Pmax) * c->H * 2));
+    INIT_TRY(cudaMalloc(&c->h_perm, static_cast<size_t>(c->Pmax) * c->I * 2));
+    INIT_TRY(cudaMalloc(&c->pair_out, static_cast<size_t>(c->Pmax) * c->H * sizeof(float)));
+    INIT_TRY(cudaMalloc(&c->status, sizeof(int)));
+    INIT_TRY(cudaMalloc(&c->work_dev, (c->E + 1) * sizeof(GemvWork)));
+    INIT_TRY(cudaMemset(c->status, 0, sizeof(int)));
+    INIT_TRY(cudaMemset(c->x_perm, 0, static_cast<size_t>(c->Pmax) * c->H * 2));
+    INIT_TRY(cudaMemset(c->h_perm, 0, static_cast<size_t>(c->Pmax) * c->I * 2));
+    INIT_TRY(cudaHostAlloc(reinterpret_cast<void**>(&c->idx_host), c->Pmax * sizeof(int32_t), 0));
+    INIT_TRY(cudaHostAlloc(reinterpret_cast<void**>(&c->status_host), sizeof(int), 0));
+    *c->status_host = 0;
+    INIT_TRY(cudaHostAlloc(reinterpret_cast<void**>(&c->table_stage), kStageRing * keys * sizeof(int32_t), 0));
+    INIT_TRY(cudaHostAlloc(reinterpret_cast<void**>(&c->work_stage),
+                           static_cast<size_t>(kStageRing) * (c->E + 1) * sizeof(GemvWork), 0));
+    for (int i = 0; i < kStageRing; ++i) {
+        INIT_TRY(cudaEventCreateWithFlags(&c->stage_ev[i], cudaEventDisableTiming));
+        INIT_TRY(cudaEventRecord(c->stage_ev[i], c->s_comp));
+    }
+    for (int i = 0; i < kEvRing; ++i) {
+        INIT_TRY(cudaEventCreateWithFlags(&c->comp_ev[i], cudaEventDisableTiming));
+        INIT_TRY(cudaEventCreateWithFlags(&c->fill_ev[i], cudaEventDisableTiming));
+    }
+    INIT_TRY(cudaEventCreateWithFlags(&c->ev_d2h, cudaEventDisableTiming));
+
+    // TMA views. Arena rows: [C*3I x H] for gate/up, [C*3H x I] for down.
+    const uint64_t H = c->H, I = c->I, C = c->C, P = c->Pmax;
+    c->gemv_maps.ks_down = (I % 256 == 0) ? 256 : 128;
+    const uint32_t ksd = c->gemv_maps.ks_down;
+    bool ok = make_map(&c->gemv_maps.w_gu[0], c->arena, H, C * 3 * I, 256, 16, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+              make_map(&c->gemv_maps.w_gu[1], c->arena, H, C * 3 * I, 256, 8, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+              make_map(&c->gemv_maps.w_d[0], c->arena, I, C * 3 * H, ksd, 32, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+              make_map(&c->gemv_maps.w_d[1], c->arena, I, C * 3 * H, ksd, 16, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+              make_map(&c->gemv_maps.xperm, c->x_perm, H, P, 256, 8, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+              make_map(&c->gemv_maps.hperm, c->h_perm, I, P, ksd, 8, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+              make_map(&c->gemm_maps.a_x, c->x_perm, H, P, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) &&
+              make_map(&c->gemm_maps.b_gu, c->arena, H, C * 3 * I, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) &&
+              make_map(&c->gemm_maps.a_h, c->h_perm, I, P, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) &&
+              make_map(&c->gemm_maps.b_d, c->arena, I, C * 3 * H, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (!ok) {
+        free_all(c);
+        return fail(MOE_E_CUDA, "cuTensorMapEncodeTiled rejected a tensor view");
+    }
+    if (upload_table(c) != MOE_OK) {
+        std::string msg = g_last_error;
+        free_all(c);
+        g_last_error = msg;
+        return MOE_E_CUDA;
+    }
+    INIT_TRY(cudaStreamSynchronize(c->s_comp));
+#undef INIT_TRY
+    *out = c;
+    return MOE_OK;
+}
+
+void moe_cache_destroy(moe_ctx* c) {
+    if (!c) return;
+    cudaSetDevice(c->dev);
+    free_all(c);
+}
+
+void* moe_host_entry(moe_ctx* c, int layer, int expert) {
+    if (!c || layer < 0 || layer >= c->L || expert < 0 || expert >= c->E) return nullptr;
+    return c->pool + (static_cast<size_t>(layer) * c->E + expert) * c->entry_elems;
+}
+
+int moe_set_path(moe_ctx* c, int path) {
+    if (!c) return fail(MOE_E_INVAL, "null context");
+    if (path != MOE_PATH_AUTO && path != MOE_PATH_GEMV && path != MOE_PATH_GEMM)
+        return fail(MOE_E_INVAL, "unknown path %d", path);
+    c->path = path;
+    return MOE_OK;
+}
+
+int moe_resident_slot(moe_ctx* c, int layer, int expert) {
+    if (!c || layer < 0 || layer >= c->L || expert < 0 || expert >= c->E) return -1;
+    return c->lru.slot_of(layer * c->E + expert);
+}
+
+int moe_debug_inject(moe_ctx* c, int kind, int count) {
+    if (!c) return fail(MOE_E_INVAL, "null context");
+    if (kind < 0 || kind > 2 || count < 0) return fail(MOE_E_INVAL, "bad injection");
+    c->inject_kind = kind;
+    c->inject_count = kind ? count : 0;
+    return MOE_OK;
+}
+
+static int route_impl(moe_ctx* c, int layer, const void* x, int T, const float* Wr, const float* b,
+                      const int32_t* forced, int32_t* idx, float* w, float* logits) {
+    g_last_error.clear();
+    int rc = validate_layer(c, layer);
+    if (rc) return rc;
+    if (T < 0 || T > c->Tmax) return fail(MOE_E_INVAL, "T=%d outside [0, %d]", T, c->Tmax);
+    if (T == 0) return MOE_OK;
+    if (!x || !Wr || !idx || !w) return fail(MOE_E_INVAL, "null device pointer");
+    CUDA_TRY(cudaSetDevice(c->dev));
+    float* z = logits ? logits : c->logits;
+    {
+        ProfScope ps(c, kRouterLogits, 4.0 * c->E * c->H + 2.0 * T * c->H + 4.0 * T * c->E,
+                     2.0 * T * c->E * c->H);
+        CUDA_TRY(moe::launch_router_logits(static_cast<const uint16_t*>(x), Wr, b, T, c->H, c->E, z, c->s_comp));
+    }
+    {
+        ProfScope ps(c, kRouterTopk, 4.0 * T * c->E + 8.0 * T * c->k, 0.0);
+        CUDA_TRY(moe::launch_router_topk(z, T, c->E, c->k, forced, idx, w, c->status, c->s_comp));
+    }
+    return MOE_OK;
+}
+
+int moe_route(moe_ctx* c, int layer, const void* x, int T, const float* Wr, const float* b, int32_t* idx, float* w,
+              float* logits) {
+    return route_impl(c, layer, x, T, Wr, b, nullptr, idx, w, logits);
+}
+
+int moe_route_forced(moe_ctx* c, int layer, const void* x, int T, const float* Wr, const float* b,
+                     const int32_t* forced, int32_t* idx, float* w, float* logits) {
+    if (!forced && T > 0) return fail(MOE_E_INVAL, "null forced sets");
+    return route_impl(c, layer, x, T, Wr, b, forced, idx, w, logits);
+}
+
+int moe_cache_fill(moe_ctx* c, int layer, const int32_t* idx_host, int n, int mode) {
+    g_last_error.clear();
+    int rc = validate_layer(c, layer);
+    if (rc) return rc;
+    CUDA_TRY(cudaSetDevice(c->dev));
+    std::vector<int> keys;
+    if (mode == MOE_FILL_FULL_LAYER) {
+        if (c->C < c->E) return fail(MOE_E_CAPACITY, "a whole layer (%d) does not fit in %d slots", c->E, c->C);
+        for (int e = 0; e < c->E; ++e) keys.push_back(layer * c->E + e);
+        rc = access_keys(c, keys, true);
+        return rc ? rc : upload_table(c);
+    }
+    if (mode != MOE_FILL_DEMAND) return fail(MOE_E_INVAL, "unknown fill mode %d", mode);
+    if (n < 0 || (n > 0 && !idx_host)) return fail(MOE_E_INVAL, "bad index list");
+    std::vector<char> used(c->E, 0);
+    for (int i = 0; i < n; ++i) {
+        if (idx_host[i] < 0 || idx_host[i] >= c->E) return fail(MOE_E_INVAL, "expert id %d out of range", idx_host[i]);
+        used[idx_host[i]] = 1;
+    }
+    for (int e = 0; e < c->E; ++e)
+        if (used[e]) keys.push_back(layer * c->E + e);
+    if (static_cast<int>(keys.size()) > c->C)
+        return fail(MOE_E_CAPACITY, "%zu distinct experts exceed %d slots", keys.size(), c->C);
+    rc = access_keys(c, keys, false);
+    return rc ? rc : upload_table(c);
+}
+
+int moe_layer_forward(moe_ctx* c, int layer, const void* x, const float* resid, float* out, int T,
+                      const int32_t* idx, const float* w) {
+    g_last_error.clear();
+    int rc = validate_layer(c, layer);
+    if (rc) return rc;
+    if (T < 0 || T > c->Tmax) return fail(MOE_E_INVAL, "T=%d outside [0, %d]", T, c->Tmax);
+    if (T == 0) return MOE_OK;
+    if (!x || !resid || !out || !idx || !w) return fail(MOE_E_INVAL, "null device pointer");
+    CUDA_TRY(cudaSetDevice(c->dev));
+    const int P = T * c->k;
+    const int E = c->E, H = c->H, I = c->I;
+    c->stats.forwards++;
+
+    // 1. routed indices to the host (the LRU needs them), plus the device status word
+    CUDA_TRY(cudaMemcpyAsync(c->idx_host, idx, P * sizeof(int32_t), cudaMemcpyDeviceToHost, c->s_comp));
+    CUDA_TRY(cudaMemcpyAsync(c->status_host, c->status, sizeof(int), cudaMemcpyDeviceToHost, c->s_comp));
+    CUDA_TRY(cudaEventRecord(c->ev_d2h, c->s_comp));
+    // 2. permutation and row gather run while the host waits and plans
+    {
+        ProfScope ps(c, kPermute, 8.0 * P + 12.0 * P + 8.0 * E, 0.0);
+        CUDA_TRY(moe::launch_permute(idx, w, P, E, c->offsets, c->perm, c->inv_perm, c->w_perm, c->active,
+                                     c->n_active, c->status, c->s_comp));
+    }
+    {
+        ProfScope ps(c, kGather, 4.0 * P * H, 0.0);
+        CUDA_TRY(moe::launch_gather_rows(static_cast<const uint16_t*>(x), c->perm, P, c->k, H, c->x_perm, c->s_comp));
+    }
+    rc = wait_event(c, c->ev_d2h, "routed indices copy");
+    if (rc) return rc;
+    harvest(c);
+    rc = check_status(c);
+    if (rc) return rc;
+
+    // 3. counts, offsets and the distinct experts in ascending id
+    std::vector<int> count(E, 0);
+    for (int p = 0; p < P; ++p) {
+        const int e = c->idx_host[p];
+        if (e < 0 || e >= E) return fail(MOE_E_INVAL, "routed expert id %d out of range", e);
+        count[e]++;
+    }
+    std::vector<int> offs(E + 1, 0), distinct;
+    int max_n = 0;
+    for (int e = 0; e < E; ++e) {
+        offs[e + 1] = offs[e] + count[e];
+        if (count[e]) {
+            distinct.push_back(e);
+            max_n = std::max(max_n, count[e]);
+        }
+    }
+    const int U = static_cast<int>(distinct.size());
+    int path = c->path;
+    if (path == MOE_PATH_AUTO) path = MOE_PATH_GEMV;  // grouped GEMM selection comes with its kernel
+    if (path == MOE_PATH_GEMM) return fail(MOE_E_INVAL, "the grouped-GEMM path is not built in this library");
+
+    // 4. waves of at most C experts
+    for (int a0 = 0; a0 < U; a0 += c->C) {
+        const int a1 = std::min(U, a0 + c->C);
+        std::vector<int> keys;
+        for (int a = a0; a < a1; ++a) keys.push_back(layer * E + distinct[a]);
+        rc = access_keys(c, keys, false);
+        if (rc) return rc;
+        rc = upload_table(c);
+        if (rc) return rc;
+        int64_t need_fill = -1;
+        for (int a = a0; a < a1; ++a) need_fill = std::max(need_fill, c->slot_fill[c->lru.slot_of(keys[a - a0])]);
+        if (need_fill >= 0) CUDA_TRY(cudaStreamWaitEvent(c->s_comp, c->fill_ev[need_fill % kEvRing], 0));
+
+        // work list for this wave
+        int wmax = 0, pw = 0;
+        for (int a = a0; a < a1; ++a) {
+            wmax = std::max(wmax, count[distinct[a]]);
+            pw += count[distinct[a]];
+        }
+        const int nt = moe::gemv_nt_bucket(wmax);
+        int s;
+        rc = next_stage(c, &s);
+        if (rc) return rc;
+        GemvWork* wk = c->work_stage + static_cast<size_t>(s) * (E + 1);
+        const int upc_gu = moe::gemv_units_per_chunk(true, nt, H, I);
+        const int upc_d = moe::gemv_units_per_chunk(false, nt, H, I);
+        int units_gu = 0, units_d = 0;
+        for (int a = a0; a < a1; ++a) {
+            const int e = distinct[a];
+            const int chunks = (count[e] + nt - 1) / nt;
+            wk[a - a0] = GemvWork{e, offs[e], count[e], units_gu};
+            units_gu += chunks * upc_gu;
+            units_d += chunks * upc_d;
+        }
+        const int nw = a1 - a0;
+        wk[nw] = GemvWork{-1, 0, 0, units_gu};
+        CUDA_TRY(cudaMemcpyAsync(c->work_dev, wk, (nw + 1) * sizeof(GemvWork), cudaMemcpyHostToDevice, c->s_comp));
+        CUDA_TRY(cudaEventRecord(c->stage_ev[s], c->s_comp));
+        const int32_t* slot_row = c->slot_dev + static_cast<size_t>(layer) * E;
+        {
+            ProfScope ps(c, kGemvGateUp, 4.0 * nw * I * H + 2.0 * pw * H + 2.0 * pw * I, 4.0 * pw * I * H);
+            CUDA_TRY(moe::launch_gemv_gateup(c->gemv_maps, nt, c->work_dev, nw, units_gu, slot_row, H, I, c->h_perm,
+                                             c->status, c->num_sms, c->s_comp));
+        }
+        // the down kernel numbers its units with its own chunking; rewrite unit_begin
+        rc = next_stage(c, &s);
+        if (rc) return rc;
+        GemvWork* wk2 = c->work_stage + static_cast<size_t>(s) * (E + 1);
+        int u = 0;
+        for (int a = a0; a < a1; ++a) {
+            const int e = distinct[a];
+            wk2[a - a0] = GemvWork{e, offs[e], count[e], u};
+            u += ((count[e] + nt - 1) / nt) * upc_d;
+        }
+        wk2[nw] = GemvWork{-1, 0, 0, u};
+        // second copy goes right after the first kernel in stream order
+        CUDA_TRY(cudaMemcpyAsync(c->work_dev, wk2, (nw + 1) * sizeof(GemvWork), cudaMemcpyHostToDevice, c->s_comp));
+        CUDA_TRY(cudaEventRecord(c->stage_ev[s], c->s_comp));
+        {
+            ProfScope ps(c, kGemvDown, 2.0 * nw * H * I + 2.0 * pw * I + 4.0 * pw * H + 4.0 * pw, 2.0 * pw * I * H);
+            CUDA_TRY(moe::launch_gemv_down(c->gemv_maps, nt, c->work_dev, nw, units_d, slot_row, H, I, c->w_perm,
+                                           c->pair_out, c->status, c->num_sms, c->s_comp));
+        }
+        c->comp_seq++;
+        CUDA_TRY(cudaEventRecord(c->comp_ev[c->comp_seq % kEvRing], c->s_comp));
+        for (int key : keys) c->slot_last_use[c->lru.slot_of(key)] = c->comp_seq;
+        c->stats.waves++;
+    }
+
+    // 5. combine in j order
+    {
+        ProfScope ps(c, kCombine, 4.0 * P * H + 8.0 * T * H + 4.0 * P, 1.0 * P * H);
+        CUDA_TRY(moe::launch_combine(c->pair_out, c->inv_perm, resid, out, T, c->k, H, c->s_comp));
+    }
+    return MOE_OK;
+}
+
+int moe_sync(moe_ctx* c) {
+    g_last_error.clear();
+    if (!c) return fail(MOE_E_INVAL, "null context");
+    CUDA_TRY(cudaSetDevice(c->dev));
+    CUDA_TRY(cudaMemcpyAsync(c->status_host, c->status, sizeof(int), cudaMemcpyDeviceToHost, c->s_comp));
+    cudaEvent_t e1 = pool_event(c), e2 = pool_event(c);
+    if (!e1 || !e2) return fail(MOE_E_CUDA, "event creation failed");
+    CUDA_TRY(cudaEventRecord(e1, c->s_comp));
+    CUDA_TRY(cudaEventRecord(e2, c->s_copy));
+    int rc = wait_event(c, e1, "compute stream");
+    if (!rc) rc = wait_event(c, e2, "copy stream");
+    c->ev_pool.push_back(e1);
+    c->ev_pool.push_back(e2);
+    if (rc) return rc;
+    harvest(c);
+    return check_status(c);
+}
+
+int moe_stats(moe_ctx* c, moe_stats_t* out, moe_event_t* trace, uint64_t cap, int reset) {
+    g_last_error.clear();
+    if (!c) return fail(MOE_E_INVAL, "null context");
+    harvest(c);
+    if (out) *out = c->stats;
+    int written = 0;
+    if (trace && cap > 0 && !c->trace.empty()) {
+        const uint64_t have = std::min<uint64_t>(c->stats.trace_len, c->trace.size());
+        const uint64_t n = std::min<uint64_t>(have, cap);
+        const uint64_t first = c->stats.trace_len - n;
+        for (uint64_t i = 0; i < n; ++i) trace[i] = c->trace[(first + i) % c->trace.size()];
+        written = static_cast<int>(n);
+    }
+    if (reset) {
+        c->stats = moe_stats_t{};
+    }
+    return written;
+}
+
+int moe_kernel_stats(moe_ctx* c, moe_kernel_stat_t* out, int cap, int reset) {
+    if (!c) return fail(MOE_E_INVAL, "null context");
+    harvest(c);
+    for (int i = 0; i < kNumKernels && i < cap; ++i) {
+        if (!out) break;
+        out[i] = c->kstats[i];
+        std::snprintf(out[i].name, sizeof(out[i].name), "%s", kKernelNames[i]);
+    }
+    if (reset)
+        for (auto& s : c->kstats) s = moe_kernel_stat_t{};
+    return kNumKernels;
+}
+
+int moe_debug_read(moe_ctx* c, int what, void* dst, uint64_t bytes) {
+    g_last_error.clear();
+    if (!c || !dst) return fail(MOE_E_INVAL, "null argument");
+    const void* src = nullptr;
+    uint64_t cap = 0;
+    switch (what) {
+        case MOE_DBG_OFFSETS: src = c->offsets; cap = (c->E + 1) * 4ull; break;
+        case MOE_DBG_PERM: src = c->perm; cap = c->Pmax * 4ull; break;
+        case MOE_DBG_INV_PERM: src = c->inv_perm; cap = c->Pmax * 4ull; break;
+        case MOE_DBG_ACTIVE: src = c->active; cap = c->E * 4ull; break;
+        case MOE_DBG_N_ACTIVE: src = c->n_active; cap = 4; break;
+        case MOE_DBG_SLOT_TABLE: src = c->slot_dev; cap = static_cast<uint64_t>(c->L) * c->E * 4; break;
+        case MOE_DBG_H_PERM: src = c->h_perm; cap = static_cast<uint64_t>(c->Pmax) * c->I * 2; break;
+        default: return fail(MOE_E_INVAL, "unknown buffer %d", what);
+    }
+    if (bytes > cap) return fail(MOE_E_INVAL, "%llu bytes requested, buffer holds %llu",
+                                 static_cast<unsigned long long>(bytes), static_cast<unsigned long long>(cap));
+    int rc = moe_sync(c);
+    if (rc) return rc;
+    CUDA_TRY(cudaMemcpy(dst, src, bytes, cudaMemcpyDeviceToHost));
+    return MOE_OK;
+}
+
+int moe_lru_simulate(int capacity, int n, const int32_t* layer, const int32_t* expert, const int32_t* kind,
+                     moe_event_t* events) {
+    if (capacity < 1 || n < 0 || (n > 0 && (!layer || !expert || !kind || !events)))
+        return fail(MOE_E_INVAL, "bad arguments");
+    int L = 1, E = 1;
+    for (int i = 0; i < n; ++i) {
+        if (layer[i] < 0 || expert[i] < 0) return fail(MOE_E_INVAL, "negative key");
+        L = std::max(L, layer[i] + 1);
+        E = std::max(E, expert[i] + 1);
+    }
+    ExpertLru lru(capacity, L * E);
+    for (int i = 0; i < n; ++i) {
+        const int key = layer[i] * E + expert[i];
+        ExpertLru::Plan p = lru.plan(key, kind[i] == 1);
+        lru.commit(p);
+        events[i] = moe_event_t{p.kind, layer[i], expert[i], p.slot, p.victim >= 0 ? p.victim / E : -1,
+                                p.victim >= 0 ? p.victim % E : -1};
+    }
+    return MOE_OK;
+}
+
+}  // extern "C"
