@@ -251,6 +251,34 @@ int moe_debug_inject(moe_ctx* ctx, int kind, int count);
 #define MOE_DBG_H_PERM 6     /* bf16 [T*k x inter]: SwiGLU activations per permuted position */
 int moe_debug_read(moe_ctx* ctx, int what, void* host_dst, uint64_t bytes);
 
+/*
+ * Router that allocates nothing: moe_route without a context, for callers that cannot call
+ * cudaMalloc -- for example code that runs inside a region where device allocation is not
+ * allowed (a stream being captured into a CUDA graph with allocation forbidden), a process
+ * whose device memory belongs entirely to another allocator (a serving engine's memory
+ * pool), or firmware-style callers that must stay within a fixed, preallocated footprint.
+ * The paper has no counterpart of this call; it is a deployment convenience of this library.
+ *
+ * It computes what moe_route computes, with the same kernels: fp32 logits in the fixed
+ * order, top-k by (z desc, id asc), softmax gates over the k chosen logits.
+ * Arguments: x_bf16 [T x hidden], router_w fp32 [num_experts x hidden], router_b fp32
+ * [num_experts] or NULL, outputs topk_idx int32 [T x top_k] and topk_w fp32 [T x top_k] --
+ * all device pointers owned by the caller; cuda_stream is a cudaStream_t or NULL.
+ * Scratch: the T x num_experts fp32 logits live in one static device array of
+ * MOE_NOALLOC_MAX_LOGITS floats (256 KiB) inside the library; every GPU that loads the
+ * library holds it until the process exits. T * num_experts above that limit returns
+ * MOE_E_INVAL; so do hidden % 256 != 0, num_experts outside [1, 1024], top_k outside
+ * [1, min(num_experts, 32)], T < 0 and NULL pointers. T == 0 is a no-op.
+ * The array is shared by every call and keeps the last call's logits: calls that overlap on
+ * the GPU (other streams, other host threads on the same device) race on it, so issue them
+ * in order on one stream. The first call on each device looks up the array's device address
+ * with that device current (cudaGetSymbolAddress); make that first call before any stream
+ * capture begins. Errors: MOE_E_INVAL, MOE_E_CUDA.
+ */
+#define MOE_NOALLOC_MAX_LOGITS 65536
+int moe_route_noalloc(const void* x_bf16, int T, int hidden, int num_experts, int top_k, const float* router_w,
+                      const float* router_b, int32_t* topk_idx, float* topk_w, void* cuda_stream);
+
 #ifdef __cplusplus
 }
 #endif

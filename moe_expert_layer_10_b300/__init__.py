@@ -28,7 +28,8 @@ EV_HIT, EV_FILL, EV_PREFETCH_FILL, EV_PREFETCH_HIT = 0, 1, 2, 3
 EXPORTS = ["moe_cache_init", "moe_cache_destroy", "moe_host_entry", "moe_entry_bytes", "moe_route",
            "moe_route_forced", "moe_cache_fill", "moe_layer_forward", "moe_stats", "moe_last_error",
            "moe_set_path", "moe_sync", "moe_resident_slot", "moe_kernel_stats", "moe_lru_simulate",
-           "moe_debug_inject", "moe_debug_read"]
+           "moe_debug_inject", "moe_debug_read", "moe_route_noalloc"]
+MOE_NOALLOC_MAX_LOGITS = 65536
 MOE_DBG_OFFSETS, MOE_DBG_PERM, MOE_DBG_INV_PERM, MOE_DBG_ACTIVE, MOE_DBG_N_ACTIVE, MOE_DBG_SLOT_TABLE, \
     MOE_DBG_H_PERM = range(7)
 
@@ -97,6 +98,7 @@ def lib():
     L.moe_lru_simulate.argtypes = [i32, i32, vp, vp, vp, vp]
     L.moe_debug_inject.argtypes = [vp, i32, i32]
     L.moe_debug_read.argtypes = [vp, i32, vp, u64]
+    L.moe_route_noalloc.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp, vp, vp]
     _lib = L
     return L
 
@@ -141,6 +143,13 @@ def lru_simulate(capacity: int, layers, experts, kinds=None):
            "moe_lru_simulate")
     return np.array([[ev[i].kind, ev[i].layer, ev[i].expert, ev[i].slot, ev[i].ev_layer, ev[i].ev_expert]
                      for i in range(n)], dtype=np.int32).reshape(n, 6)
+
+
+def route_noalloc(x, router_w, router_b, topk_idx, topk_w, top_k: int, stream=None, T: Optional[int] = None):
+    """moe_route_noalloc: the router without a context or any allocation (see include/moe.h)."""
+    T = x.shape[0] if T is None else T
+    _check(lib().moe_route_noalloc(_ptr(x), T, x.shape[1], router_w.shape[0], top_k, _ptr(router_w), _ptr(router_b),
+                                   _ptr(topk_idx), _ptr(topk_w), _stream_handle(stream)), "moe_route_noalloc")
 
 
 @dataclass

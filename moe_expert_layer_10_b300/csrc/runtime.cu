@@ -415,6 +415,11 @@ void free_all(moe_ctx* c) {
 
 }  // namespace
 
+namespace moe {
+// Record a thread-local error message for moe_last_error() and return `code`.
+int set_error(int code, const char* msg) { return fail(code, "%s", msg); }
+}  // namespace moe
+
 extern "C" {
 
 const char* moe_last_error(void) { return g_last_error.c_str(); }
