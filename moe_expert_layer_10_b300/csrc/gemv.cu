@@ -69,11 +69,16 @@ struct UnitPos {
     int rb;     // row block
 };
 
-__device__ __forceinline__ UnitPos locate(const GemvWork* work, int n_work, int u, int rbs, int a_hint) {
-    int a = a_hint;
-    while (a + 1 < n_work && u >= work[a + 1].unit_begin) ++a;
-    const int local = u - work[a].unit_begin;
-    return UnitPos{a, local / rbs, local % rbs};
+// Unit u -> (work entry, token chunk, row block): the last entry whose first unit is <= u.
+__device__ __forceinline__ UnitPos locate(const GemvWork* work, int n_work, int u, int rbs) {
+    int lo = 0, hi = n_work - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldg(&work[mid].unit_begin) <= u) lo = mid;
+        else hi = mid - 1;
+    }
+    const int local = u - __ldg(&work[lo].unit_begin);
+    return UnitPos{lo, local / rbs, local % rbs};
 }
 
 template <bool GATEUP, int KS, int RPW, int NTMAX>
@@ -102,10 +107,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int out_rows = GATEUP ? I : H;          // output rows of one expert
     const int slabs = K / KS;
     const int rbs = out_rows / C::UNIT_ROWS;      // row blocks per token chunk
-    const int G = gridDim.x, c = blockIdx.x;
-    const int u_begin = static_cast<int>(static_cast<long long>(n_units) * c / G);
-    const int u_end = static_cast<int>(static_cast<long long>(n_units) * (c + 1) / G);
-    if (u_begin >= u_end) return;
+    // Round-robin units over the CTAs: units of one expert land on different SMs, so the
+    // compute of experts with many tokens is spread evenly.
+    const int G = gridDim.x;
+    if (static_cast<int>(blockIdx.x) >= n_units) return;
 
     if (warp == kConsumerWarps) {
         // ------------------------------------------------------------ producer
@@ -117,11 +122,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t phase = 0;
         uint32_t used = 0, last_phase = 0;  // per-stage bits for the drain
         bool ok = true;
-        int a = 0;
-        for (int u = u_begin; u < u_end && ok; ++u) {
-            const UnitPos up = locate(work, n_work, u, rbs, a);
-            a = up.a;
-            const GemvWork wk = work[a];
+        for (int u = blockIdx.x; u < n_units && ok; u += G) {
+            const UnitPos up = locate(work, n_work, u, rbs);
+            const GemvWork wk = work[up.a];
             int slot = slot_row[wk.expert];
             if (slot < 0) {
                 raise_status(status, kDevBadSlot);
@@ -170,11 +173,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------------- consumers
     int stage = 0;
     uint32_t phase = 0;
-    int a = 0;
-    for (int u = u_begin; u < u_end; ++u) {
-        const UnitPos up = locate(work, n_work, u, rbs, a);
-        a = up.a;
-        const GemvWork wk = work[a];
+    for (int u = blockIdx.x; u < n_units; u += G) {
+        const UnitPos up = locate(work, n_work, u, rbs);
+        const GemvWork wk = work[up.a];
         const int tok0 = wk.tok_off + up.chunk * NTMAX;
         const int nt = min(NTMAX, wk.n_tok - up.chunk * NTMAX);
         float acc[RPW][NTMAX];
@@ -199,26 +200,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                 load_chunk<C::VE>(st + row * KS * 2 + lane * C::VE * 2, wv[r]);
             }
             const uint8_t* xs = st + C::W_BYTES + lane * C::VE * 2;
+            // tokens in pairs: rows up to the next even count are loaded in this stage (whole
+            // 8-row boxes), and results of the padding token are never stored
 #pragma unroll
-            for (int t = 0; t < NTMAX; ++t) {
-                if (t < nt) {
-                    uint32_t xv[C::VE / 2];
-                    load_chunk<C::VE>(xs + t * KS * 2, xv);
-                    float xf[C::VE];
+            for (int tp = 0; tp < NTMAX; tp += 2) {
+                if (tp < nt) {
 #pragma unroll
-                    for (int q = 0; q < C::VE / 2; ++q) {
-                        xf[2 * q] = bf16lo(xv[q]);
-                        xf[2 * q + 1] = bf16hi(xv[q]);
-                    }
-#pragma unroll
-                    for (int r = 0; r < RPW; ++r) {
-                        float s = acc[r][t];
+                    for (int t = tp; t < tp + 2; ++t) {
+                        uint32_t xv[C::VE / 2];
+                        load_chunk<C::VE>(xs + t * KS * 2, xv);
+                        float xf[C::VE];
 #pragma unroll
                         for (int q = 0; q < C::VE / 2; ++q) {
-                            s = __fmaf_rn(bf16lo(wv[r][q]), xf[2 * q], s);
-                            s = __fmaf_rn(bf16hi(wv[r][q]), xf[2 * q + 1], s);
+                            xf[2 * q] = bf16lo(xv[q]);
+                            xf[2 * q + 1] = bf16hi(xv[q]);
                         }
-                        acc[r][t] = s;
+#pragma unroll
+                        for (int r = 0; r < RPW; ++r) {
+                            float sacc = acc[r][t];
+#pragma unroll
+                            for (int q = 0; q < C::VE / 2; ++q) {
+                                sacc = __fmaf_rn(bf16lo(wv[r][q]), xf[2 * q], sacc);
+                                sacc = __fmaf_rn(bf16hi(wv[r][q]), xf[2 * q + 1], sacc);
+                            }
+                            acc[r][t] = sacc;
+                        }
                     }
                 }
             }

@@ -19,7 +19,6 @@
 namespace moe {
 namespace {
 
-constexpr int kWarpsPerBlockSmallT = 2;
 constexpr int kWarpsPerBlockLargeT = 8;
 
 // One warp per expert e, TB tokens per CTA; warps of a CTA take consecutive experts.
@@ -67,6 +66,89 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const uint16_t* __re
             if (lane == 0) z[static_cast<size_t>(t0 + i) * E + e] = __fadd_rn(v, b);
         }
     }
+}
+
+// Small batches (decode): latency-bound, so a CTA first stages its EPB experts' router
+// rows and the whole batch of activations in shared memory, every load in flight at once,
+// then evaluates the same fixed fp32 order from shared memory. Warp w computes expert
+// e0 + w % EPB for tokens t = w / EPB + (8 / EPB) * i.
+template <int EPB, int TPW>
+__global__ void __launch_bounds__(256) router_logits_staged_kernel(const uint16_t* __restrict__ x,
+                                                                   const float* __restrict__ Wr,
+                                                                   const float* __restrict__ bias, int T, int H,
+                                                                   int E, float* __restrict__ z) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    float* wr = reinterpret_cast<float*>(smem);                   // [EPB][H]
+    uint16_t* xs = reinterpret_cast<uint16_t*>(wr + EPB * H);     // [T][H]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int e0 = blockIdx.x * EPB;
+    const int ne = min(EPB, E - e0);
+    {
+        const float4* src = reinterpret_cast<const float4*>(Wr + static_cast<size_t>(e0) * H);
+        float4* dst = reinterpret_cast<float4*>(wr);
+        const int n4 = ne * H / 4;
+        for (int i = threadIdx.x; i < n4; i += 256) dst[i] = __ldg(src + i);
+        const uint4* xsrc = reinterpret_cast<const uint4*>(x);
+        uint4* xdst = reinterpret_cast<uint4*>(xs);
+        const int nx = T * H / 8;
+        for (int i = threadIdx.x; i < nx; i += 256) xdst[i] = __ldg(xsrc + i);
+    }
+    __syncthreads();
+    constexpr int WPE = 8 / EPB;  // warps per expert
+    const int el = warp % EPB;
+    if (el >= ne) return;
+    const int e = e0 + el;
+    const int tw = warp / EPB;
+    float acc[TPW];
+#pragma unroll
+    for (int i = 0; i < TPW; ++i) acc[i] = 0.0f;
+    const float* wrow = wr + el * H + 8 * lane;
+    for (int m = 0; m < H / 256; ++m) {
+        const float4 wa = *reinterpret_cast<const float4*>(wrow + 256 * m);
+        const float4 wb = *reinterpret_cast<const float4*>(wrow + 256 * m + 4);
+        const float wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+        for (int i = 0; i < TPW; ++i) {
+            const int t = tw + WPE * i;
+            if (t < T) {
+                const uint4 xv = *reinterpret_cast<const uint4*>(xs + static_cast<size_t>(t) * H + 256 * m + 8 * lane);
+                const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+                float a = acc[i];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    a = __fmaf_rn(wv[2 * q], bf16lo(xw[q]), a);
+                    a = __fmaf_rn(wv[2 * q + 1], bf16hi(xw[q]), a);
+                }
+                acc[i] = a;
+            }
+        }
+    }
+    const float b = bias ? bias[e] : 0.0f;
+#pragma unroll
+    for (int i = 0; i < TPW; ++i) {
+        const int t = tw + WPE * i;
+        if (t < T) {
+            float v = acc[i];
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
+            if (lane == 0) z[static_cast<size_t>(t) * E + e] = __fadd_rn(v, b);
+        }
+    }
+}
+
+template <int EPB, int TPW>
+cudaError_t launch_staged(const uint16_t* x, const float* Wr, const float* b, int T, int H, int E, float* z,
+                          cudaStream_t st) {
+    auto kern = router_logits_staged_kernel<EPB, TPW>;
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    const size_t smem = static_cast<size_t>(EPB) * H * 4 + static_cast<size_t>(T) * H * 2;
+    kern<<<(E + EPB - 1) / EPB, 256, smem, st>>>(x, Wr, b, T, H, E, z);
+    return cudaGetLastError();
 }
 
 __device__ __forceinline__ bool ranks_before(float za, int ea, float zb, int eb) {
@@ -164,17 +246,14 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float* __restric
 cudaError_t launch_router_logits(const uint16_t* x, const float* Wr, const float* b, int T, int H, int E, float* z,
                                  cudaStream_t st) {
     if (T <= 0) return cudaSuccess;
-    if (T <= 16) {
-        const int wpb = kWarpsPerBlockSmallT;
-        dim3 block(32 * wpb);
-        if (T == 1) {
-            router_logits_kernel<1><<<dim3((E + wpb - 1) / wpb, 1), block, 0, st>>>(x, Wr, b, T, H, E, z);
-        } else if (T <= 4) {
-            router_logits_kernel<4><<<dim3((E + wpb - 1) / wpb, 1), block, 0, st>>>(x, Wr, b, T, H, E, z);
-        } else {
-            router_logits_kernel<16><<<dim3((E + wpb - 1) / wpb, 1), block, 0, st>>>(x, Wr, b, T, H, E, z);
-        }
-    } else {
+    // staged kernel when the experts' rows and the batch fit in shared memory
+    const size_t smem4 = 4ull * H * 4 + static_cast<size_t>(T) * H * 2;
+    if (T <= 2 && 2ull * H * 4 + static_cast<size_t>(T) * H * 2 <= 200 * 1024)
+        return launch_staged<2, 1>(x, Wr, b, T, H, E, z, st);
+    if (T <= 8 && smem4 <= 200 * 1024) return launch_staged<4, 4>(x, Wr, b, T, H, E, z, st);
+    if (T <= 16 && smem4 <= 200 * 1024) return launch_staged<4, 8>(x, Wr, b, T, H, E, z, st);
+    if (T <= 32 && smem4 <= 200 * 1024) return launch_staged<4, 16>(x, Wr, b, T, H, E, z, st);
+    {
         const int wpb = kWarpsPerBlockLargeT;
         router_logits_kernel<16>
             <<<dim3((E + wpb - 1) / wpb, (T + 15) / 16), dim3(32 * wpb), 0, st>>>(x, Wr, b, T, H, E, z);

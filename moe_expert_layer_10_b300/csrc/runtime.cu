@@ -701,8 +701,7 @@ int moe_layer_forward(moe_ctx* c, int layer, const void* x, const float* resid, 
     }
     const int U = static_cast<int>(distinct.size());
     int path = c->path;
-    if (path == MOE_PATH_AUTO) path = MOE_PATH_GEMV;  // grouped GEMM selection comes with its kernel
-    if (path == MOE_PATH_GEMM) return fail(MOE_E_INVAL, "the grouped-GEMM path is not built in this library");
+    if (path == MOE_PATH_AUTO) path = (max_n <= 32) ? MOE_PATH_GEMV : MOE_PATH_GEMM;
 
     // 4. waves of at most C experts
     for (int a0 = 0; a0 < U; a0 += c->C) {
@@ -716,6 +715,35 @@ int moe_layer_forward(moe_ctx* c, int layer, const void* x, const float* resid, 
         int64_t need_fill = -1;
         for (int a = a0; a < a1; ++a) need_fill = std::max(need_fill, c->slot_fill[c->lru.slot_of(keys[a - a0])]);
         if (need_fill >= 0) CUDA_TRY(cudaStreamWaitEvent(c->s_comp, c->fill_ev[need_fill % kEvRing], 0));
+
+        const int32_t* slot_row = c->slot_dev + static_cast<size_t>(layer) * E;
+        if (path == MOE_PATH_GEMM) {
+            std::vector<int> wc;
+            int pw = 0;
+            for (int a = a0; a < a1; ++a) {
+                wc.push_back(count[distinct[a]]);
+                pw += count[distinct[a]];
+            }
+            const int nw = a1 - a0;
+            const int tiles_gu = moe::gemm_tiles(true, wc.data(), nw, H, I);
+            const int tiles_d = moe::gemm_tiles(false, wc.data(), nw, H, I);
+            {
+                ProfScope ps(c, kGemmGateUp, 4.0 * nw * I * H + 2.0 * pw * H + 2.0 * pw * I, 4.0 * pw * I * H);
+                CUDA_TRY(moe::launch_gemm_gateup(c->gemm_maps, c->offsets, c->active, a0, a1, tiles_gu, slot_row, H,
+                                                 I, c->h_perm, c->status, c->num_sms, c->s_comp));
+            }
+            {
+                ProfScope ps(c, kGemmDown, 2.0 * nw * H * I + 2.0 * pw * I + 4.0 * pw * H + 4.0 * pw,
+                             2.0 * pw * I * H);
+                CUDA_TRY(moe::launch_gemm_down(c->gemm_maps, c->offsets, c->active, a0, a1, tiles_d, slot_row, H, I,
+                                               c->w_perm, c->pair_out, c->status, c->num_sms, c->s_comp));
+            }
+            c->comp_seq++;
+            CUDA_TRY(cudaEventRecord(c->comp_ev[c->comp_seq % kEvRing], c->s_comp));
+            for (int key : keys) c->slot_last_use[c->lru.slot_of(key)] = c->comp_seq;
+            c->stats.waves++;
+            continue;
+        }
 
         // work list for this wave
         int wmax = 0, pw = 0;
@@ -742,7 +770,6 @@ int moe_layer_forward(moe_ctx* c, int layer, const void* x, const float* resid, 
         wk[nw] = GemvWork{-1, 0, 0, units_gu};
         CUDA_TRY(cudaMemcpyAsync(c->work_dev, wk, (nw + 1) * sizeof(GemvWork), cudaMemcpyHostToDevice, c->s_comp));
         CUDA_TRY(cudaEventRecord(c->stage_ev[s], c->s_comp));
-        const int32_t* slot_row = c->slot_dev + static_cast<size_t>(layer) * E;
         {
             ProfScope ps(c, kGemvGateUp, 4.0 * nw * I * H + 2.0 * pw * H + 2.0 * pw * I, 4.0 * pw * I * H);
             CUDA_TRY(moe::launch_gemv_gateup(c->gemv_maps, nt, c->work_dev, nw, units_gu, slot_row, H, I, c->h_perm,
