@@ -50,6 +50,10 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batches", default="1,4,16", help="decode batch sizes of one step (profiling cases)")
     ap.add_argument("--capacity", type=int, default=0, help="override the cache capacity (profiling cases)")
+    ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--only-prefill", action="store_true", help="profiling cases: run the prefill leg alone")
+    ap.add_argument("--prefill-tokens", type=int, default=4096)
+    ap.add_argument("--prefill-experts", type=int, default=0, help="fewer experts for profiling cases")
     return ap.parse_args()
 
 
@@ -319,10 +323,114 @@ def run_b300(args, rank, world, local):
                    "fill_GBps": (st["fill_bytes"] / (st["fill_ms"] / 1e3) / 1e9) if st["fill_ms"] else None},
         "clocks": clk, "e2e": e2e, "gpu_launches": launches, "roofline": roof, "kernels": kernels,
     }
+    # per-batch kernel times (an untimed pass after the measurement)
+    by_batch = {}
+    for B in BATCHES:
+        cache.sync()
+        cache.kernel_stats(reset=True)
+        for s in range(args.warmup, min(total, args.warmup + 8)):
+            cache.route(0, xs[s][B], Wr, bias, idx[B], wts[B])
+            cache.layer_forward(0, xs[s][B], resid[s][B], out[B], idx[B], wts[B])
+        cache.sync()
+        kb = cache.kernel_stats()
+        by_batch[f"B{B}"] = {n: {"avg_us": round(1e3 * v["total_ms"] / v["launches"], 2),
+                                 "GB/s": round(v["bytes"] / (v["total_ms"] / 1e3) / 1e9, 1)}
+                             for n, v in kb.items() if v["launches"]}
+    result["kernels_by_batch"] = by_batch
+    cache.close()
+    if not args.no_prefill:
+        result["prefill"] = run_prefill(args)
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(W, Wr_h, b_h)
-    cache.close()
     return result
+
+
+def run_prefill(args, reps: int = 5):
+    """Prefill leg: the 4096-token layer (hidden 4096, intermediate 1536, 256 experts top-6,
+    Zipf(1.1) bias) with every expert resident, on the grouped tcgen05 GEMM path; plus a
+    labelled diagnostic with 24 groups of T/4 tokens (compute-bound)."""
+    import numpy as np
+    import torch
+
+    import moe_expert_layer_10_b300 as moe
+    import moe_inputs as mi
+    W = mi.WORKLOADS["prefill"]
+    T = args.prefill_tokens
+    E = args.prefill_experts or W.E
+    stream = torch.cuda.Stream()
+    cache = moe.MoeCache(moe.LayerShape(1, E, W.H, W.I, W.k, E, T), flags=moe.MOE_PROFILE, stream_compute=stream)
+    for e in range(E):
+        mi.fill_entry_at(cache.host_entry(0, e), W.seed, 0, e, W.H, W.I)
+    cache.cache_fill(0, None, moe.MOE_FILL_FULL_LAYER)
+    Wr = torch.from_numpy(mi.router_weights(W.seed, 0, E, W.H)).cuda()
+    b_h, _ = mi.router_bias(W.seed, 0, E, W.zipf_s)
+    bias = torch.from_numpy(b_h).cuda()
+    x = torch.from_numpy(mi.activations(W.seed, 9000, T, W.H).view(np.int16)).view(torch.bfloat16).cuda()
+    resid = x.float()
+    out = torch.empty((T, W.H), dtype=torch.float32, device="cuda")
+    idx = torch.empty((T, W.k), dtype=torch.int32, device="cuda")
+    wts = torch.empty((T, W.k), dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()
+    pk = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    peaks = json.load(open(pk)) if os.path.exists(pk) else {"bf16_tflops": 1800.0, "hbm_gbs": 6400.0}
+    tc_peak, bw_peak = float(peaks["bf16_tflops"]), float(peaks["hbm_gbs"])
+
+    def measure(forced=None):
+        def fwd():
+            if forced is None:
+                cache.route(0, x, Wr, bias, idx, wts)
+            else:
+                cache.route_forced(0, x, Wr, bias, forced, idx, wts)
+            cache.layer_forward(0, x, resid, out, idx, wts)
+        for _ in range(2):
+            fwd()
+        cache.sync()
+        cache.kernel_stats(reset=True)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            fwd()
+        e1.record(stream)
+        cache.sync()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        ks = cache.kernel_stats()
+        res = {"ms_per_layer": round(ms, 4), "tok_s": round(T / (ms / 1e3), 1)}
+        for n in ("gemm_gateup", "gemm_down", "router_logits", "router_topk", "permute", "gather_rows", "combine"):
+            v = ks.get(n)
+            if v and v["launches"]:
+                t = v["total_ms"] / v["launches"] / 1e3
+                tf = v["flops"] / v["launches"] / t / 1e12
+                gbs = v["bytes"] / v["launches"] / t / 1e9
+                res[n] = {"avg_us": round(t * 1e6, 1), "TFLOP/s": round(tf, 1), "frac_tensor": round(tf / tc_peak, 4),
+                          "GB/s": round(gbs, 1), "frac_hbm": round(gbs / bw_peak, 4)}
+        # per-expert roofline bound sum_e max(flops_e / TC, bytes_e / BW) of the two GEMMs
+        counts = np.bincount(idx.cpu().numpy().ravel(), minlength=E)
+        bound = 0.0
+        for n_e in counts[counts > 0]:
+            fl = 2.0 * n_e * 3 * W.H * W.I
+            by = 3.0 * W.H * W.I * 2 + n_e * (W.H * 2 + W.I * 2 * 2 + W.H * 4)
+            bound += max(fl / (tc_peak * 1e12), by / (bw_peak * 1e9))
+        gemm_s = sum(res[n]["avg_us"] for n in ("gemm_gateup", "gemm_down") if n in res) / 1e6
+        res["gemm_roofline_bound_us"] = round(bound * 1e6, 1)
+        res["gemm_frac_of_bound"] = round(bound / gemm_s, 4) if gemm_s else None
+        res["max_tokens_per_expert"] = int(counts.max())
+        return res
+
+    out_res = {"workload": f"prefill layer: {T} tokens, hidden 4096, intermediate 1536, {E} experts top-6, "
+                           "Zipf(1.1) bias, every expert resident", "peak_tflops": tc_peak,
+               "peak_kind": "measured burst"}
+    out_res.update(measure())
+    if E >= 24:
+        # token t uses experts 6*(t%4) .. 6*(t%4)+5 -> 24 groups of T/4 tokens
+        sets = torch.tensor([[6 * (t % 4) + j for j in range(W.k)] for t in range(T)], dtype=torch.int32,
+                            device="cuda")
+        torch.cuda.synchronize()
+        diag = measure(forced=sets)
+        diag["label"] = f"diagnostic, not the prefill workload: 24 experts x {T // 4} tokens (forced routing)"
+        out_res["diagnostic_large_groups"] = diag
+    cache.close()
+    return out_res
 
 
 # ----------------------------------------------------------------------------- reference arm
@@ -405,6 +513,11 @@ def main():
             print(json.dumps(run_reference(args)), flush=True)
         return
     init_dist(world, local)
+    if args.only_prefill:
+        import torch
+        torch.cuda.set_device(local)
+        print(json.dumps({"prefill": run_prefill(args)}), flush=True)
+        return
     res = run_b300(args, rank, world, local)
     if rank == 0:
         print(json.dumps(res), flush=True)

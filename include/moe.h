@@ -26,6 +26,8 @@
  *  - "device" pointers are CUDA device memory owned by the caller. All device work runs
  *    in order on the context's compute stream; fills run on its copy stream.
  *  - A context is used by one host thread at a time.
+ *  - Device buffers passed to a call must stay valid until that call's work has finished on
+ *    the compute stream (moe_sync, or any later synchronising call).
  *  - Activations are bf16 (raw 16-bit patterns), row-major [T x hidden].
  *  - Entry layout (host pool and device slot alike), bf16 row-major, contiguous:
  *      W_gate [inter x hidden] | W_up [inter x hidden] | W_down [hidden x inter]

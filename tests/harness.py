@@ -22,9 +22,15 @@ def f32_dev(a: np.ndarray):
 
 def make_cache(W: mi.Workload, max_tokens: int, L: int | None = None, capacity: int | None = None,
                flags: int = moe.MOE_TRACE) -> moe.MoeCache:
+    import torch
     L = W.L if L is None else L
+    # one stream for torch's work (inputs, resid = x.float(), ...) and the library's compute,
+    # so everything the tests enqueue is ordered
+    stream = torch.cuda.Stream()
+    torch.cuda.set_stream(stream)
     cache = moe.MoeCache(moe.LayerShape(L, W.E, W.H, W.I, W.k, W.C if capacity is None else capacity, max_tokens),
-                         flags=flags)
+                         flags=flags, stream_compute=stream)
+    cache.torch_stream = stream
     for l in range(L):
         for e in range(W.E):
             mi.fill_entry_at(cache.host_entry(l, e), W.seed, l, e, W.H, W.I)
