@@ -74,13 +74,13 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def traffic_from_profile():
-    """dram bytes per launch of the gate/up GEMV from the committed ncu summary, or None if
-    the summary is missing or was taken on a different kernel source."""
+def traffic_ratio_from_profile():
+    """DRAM bytes / algorithmic bytes of the gate/up GEMV launch captured in the committed ncu
+    summary, or None if the summary is missing or was taken on a different kernel source."""
     if not os.path.exists(PROFILE_SUMMARY):
         return None
     text = open(PROFILE_SUMMARY).read()
-    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    m = re.search(r"traffic_ratio:\s*([0-9.eE+]+)", text)
     h = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
     if not m or not h:
         return None
@@ -302,8 +302,14 @@ def run_b300(args, rank, world, local):
         achieved = bytes_per_launch / (avg_ms / 1e3) / 1e9
         roof = {"kernel": "gemv_gateup", "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                 "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                "traffic": traffic_from_profile(), "bytes_per_launch": bytes_per_launch,
+                "traffic": None, "bytes_per_launch": bytes_per_launch,
                 "avg_launch_ms": avg_ms}
+        ratio = traffic_ratio_from_profile()
+        if ratio is not None:
+            # the captured launch's DRAM bytes per algorithmic byte, applied to this run's
+            # average launch (the capture is one batch-16 launch, not this run's mix)
+            roof["traffic"] = round(ratio * bytes_per_launch)
+            roof["traffic_note"] = "ncu dram bytes/algorithmic bytes of one captured launch x bytes_per_launch"
     kernels = {n: {"launches": v["launches"], "avg_us": (1e3 * v["total_ms"] / v["launches"]) if v["launches"] else None,
                    "GB/s": (v["bytes"] / (v["total_ms"] / 1e3) / 1e9) if v["total_ms"] else None}
                for n, v in kst.items() if v["launches"]}

@@ -255,10 +255,10 @@ int moe_debug_read(moe_ctx* ctx, int what, void* host_dst, uint64_t bytes);
 
 /*
  * Router that allocates nothing: moe_route without a context, for callers that cannot call
- * cudaMalloc -- for example code that runs inside a region where device allocation is not
- * allowed (a stream being captured into a CUDA graph with allocation forbidden), a process
- * whose device memory belongs entirely to another allocator (a serving engine's memory
- * pool), or firmware-style callers that must stay within a fixed, preallocated footprint.
+ * cudaMalloc -- for example a process whose device memory belongs entirely to another
+ * allocator (a serving engine's memory pool, where a stray cudaMalloc would break its
+ * accounting), or a caller that must stay within a fixed, preallocated footprint and may not
+ * grow the device heap at run time.
  * The paper has no counterpart of this call; it is a deployment convenience of this library.
  *
  * It computes what moe_route computes, with the same kernels: fp32 logits in the fixed
