@@ -19,51 +19,108 @@
 namespace moe {
 namespace {
 
-constexpr int kWarpsPerBlockLargeT = 8;
+// Large batches (prefill): a register-tiled evaluation of the same order. A CTA of 8 warps
+// owns a tile of 32 tokens x 16 experts and walks H in chunks of 256 columns, staged in
+// shared memory with cp.async (double-buffered). Warp w owns the 8 x 8 sub-tile of tokens
+// 8*(w/2).. and experts 8*(w%2)..; its lane l keeps the 64 partials s_l(t, e), each
+// accumulated with fmaf over exactly the columns 256m + 8l + r (m, then r = 0..7) that the
+// one-warp-per-dot-product kernels give lane l, so the fold yields the same bits.
+constexpr int kTT = 32, kTE = 16;
+constexpr int kXBytes = kTT * 512;   // 32 rows x 256 bf16
+constexpr int kWBytes = kTE * 1024;  // 16 rows x 256 fp32
+constexpr int kTiledStage = kXBytes + kWBytes;
+constexpr int kTiledSmem = 2 * kTiledStage;
 
-// One warp per expert e, TB tokens per CTA; warps of a CTA take consecutive experts.
-template <int TB>
-__global__ void __launch_bounds__(256) router_logits_kernel(const uint16_t* __restrict__ x,
-                                                            const float* __restrict__ Wr,
-                                                            const float* __restrict__ bias, int T, int H, int E,
-                                                            float* __restrict__ z) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int e = blockIdx.x * (blockDim.x >> 5) + warp;
-    const int t0 = blockIdx.y * TB;
-    if (e >= E || t0 >= T) return;
-    const int nt = min(TB, T - t0);
-    float acc[TB];
-#pragma unroll
-    for (int i = 0; i < TB; ++i) acc[i] = 0.0f;
-    const float* wrow = Wr + static_cast<size_t>(e) * H + 8 * lane;
-    const uint16_t* xrow = x + static_cast<size_t>(t0) * H + 8 * lane;
-    for (int m = 0; m < H / 256; ++m) {
-        const float4 wa = __ldg(reinterpret_cast<const float4*>(wrow + 256 * m));
-        const float4 wb = __ldg(reinterpret_cast<const float4*>(wrow + 256 * m + 4));
-        const float wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
-#pragma unroll
-        for (int i = 0; i < TB; ++i) {
-            if (i < nt) {
-                const uint4 xv = __ldg(reinterpret_cast<const uint4*>(xrow + static_cast<size_t>(i) * H + 256 * m));
-                const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-                float a = acc[i];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    a = __fmaf_rn(wv[2 * q], bf16lo(xw[q]), a);
-                    a = __fmaf_rn(wv[2 * q + 1], bf16hi(xw[q]), a);
-                }
-                acc[i] = a;
-            }
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// Stage columns [256m, 256m+256) of the tile. x rows keep their order (lane l reads the 16
+// bytes at 16l). A W_r row's 8-float run of lane l is split into its halves, stored at
+// 16l and 512 + 16l, so the lanes' 16-byte reads of one half are contiguous.
+__device__ __forceinline__ void router_stage(uint8_t* buf, const uint16_t* x, const float* Wr, int t0, int e0, int T,
+                                             int E, int H, int m) {
+    for (int i = threadIdx.x; i < 2048; i += 256) {
+        if (i < 1024) {
+            const int row = i >> 5, c = i & 31;
+            const int t = min(t0 + row, T - 1);
+            cp_async16(buf + row * 512 + c * 16, x + static_cast<size_t>(t) * H + 256 * m + 8 * c);
+        } else {
+            const int j = i - 1024;
+            const int row = j >> 6, c = j & 63;
+            const int e = min(e0 + row, E - 1);
+            const int l = c >> 1, h = c & 1;
+            cp_async16(buf + kXBytes + row * 1024 + h * 512 + l * 16, Wr + static_cast<size_t>(e) * H + 256 * m + 4 * c);
         }
     }
-    const float b = bias ? bias[e] : 0.0f;
+}
+
+__global__ void __launch_bounds__(256, 1) router_logits_tiled_kernel(const uint16_t* __restrict__ x,
+                                                                     const float* __restrict__ Wr,
+                                                                     const float* __restrict__ bias, int T, int H,
+                                                                     int E, float* __restrict__ z) {
+    extern __shared__ __align__(16) uint8_t rsm[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t0 = blockIdx.y * kTT, e0 = blockIdx.x * kTE;
+    const int tw = (warp >> 1) * 8, ew = (warp & 1) * 8;
+    float acc[8][8];
 #pragma unroll
-    for (int i = 0; i < TB; ++i) {
-        if (i < nt) {
-            float v = acc[i];
+    for (int t = 0; t < 8; ++t)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[t][e] = 0.0f;
+    const int M = H / 256;
+    router_stage(rsm, x, Wr, t0, e0, T, E, H, 0);
+    cp_async_commit();
+    for (int m = 0; m < M; ++m) {
+        if (m + 1 < M) {
+            router_stage(rsm + ((m + 1) & 1) * kTiledStage, x, Wr, t0, e0, T, E, H, m + 1);
+            cp_async_commit();
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
+        }
+        __syncthreads();
+        const uint8_t* xs = rsm + (m & 1) * kTiledStage;
+        const uint8_t* ws = xs + kXBytes;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            uint2 xv[8];
+#pragma unroll
+            for (int t = 0; t < 8; ++t)
+                xv[t] = *reinterpret_cast<const uint2*>(xs + (tw + t) * 512 + lane * 16 + h * 8);
+            float4 wv[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                wv[e] = *reinterpret_cast<const float4*>(ws + (ew + e) * 1024 + h * 512 + lane * 16);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+#pragma unroll
+                for (int t = 0; t < 8; ++t) {
+                    const uint32_t word = (q < 2) ? xv[t].x : xv[t].y;
+                    const float xf = (q & 1) ? bf16hi(word) : bf16lo(word);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float wf = q == 0 ? wv[e].x : q == 1 ? wv[e].y : q == 2 ? wv[e].z : wv[e].w;
+                        acc[t][e] = __fmaf_rn(wf, xf, acc[t][e]);
+                    }
+                }
+            }
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            float v = acc[t][e];
 #pragma unroll
             for (int o = 16; o >= 1; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
-            if (lane == 0) z[static_cast<size_t>(t0 + i) * E + e] = __fadd_rn(v, b);
+            const int tt = t0 + tw + t, ee = e0 + ew + e;
+            if (lane == ((t * 8 + e) & 31) && tt < T && ee < E)
+                z[static_cast<size_t>(tt) * E + ee] = __fadd_rn(v, bias ? __ldg(bias + ee) : 0.0f);
         }
     }
 }
@@ -253,11 +310,15 @@ cudaError_t launch_router_logits(const uint16_t* x, const float* Wr, const float
     if (T <= 8 && smem4 <= 200 * 1024) return launch_staged<4, 4>(x, Wr, b, T, H, E, z, st);
     if (T <= 16 && smem4 <= 200 * 1024) return launch_staged<4, 8>(x, Wr, b, T, H, E, z, st);
     if (T <= 32 && smem4 <= 200 * 1024) return launch_staged<4, 16>(x, Wr, b, T, H, E, z, st);
-    {
-        const int wpb = kWarpsPerBlockLargeT;
-        router_logits_kernel<16>
-            <<<dim3((E + wpb - 1) / wpb, (T + 15) / 16), dim3(32 * wpb), 0, st>>>(x, Wr, b, T, H, E, z);
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(router_logits_tiled_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             kTiledSmem);
+        if (e != cudaSuccess) return e;
+        attr = true;
     }
+    router_logits_tiled_kernel<<<dim3((E + kTE - 1) / kTE, (T + kTT - 1) / kTT), 256, kTiledSmem, st>>>(x, Wr, b, T,
+                                                                                                      H, E, z);
     return cudaGetLastError();
 }
 
