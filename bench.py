@@ -5,14 +5,14 @@ Workload (the decode-layer shape): hidden 4096, expert SwiGLU intermediate 1536,
 experts (36 MiB bf16 each, 9.66 GB pool in pinned host memory), top-6, router bias from
 Zipf(1.1), LRU cache of 64 entries, fresh N(0,1) activations every step. One benchmark step
 = one decode step at batch 1, one at batch 4 and one at batch 16 (21 tokens): router GEMV,
-top-k, host LRU, fills of missing experts over PCIe, permutation, gate/up and down GEMVs
+top-k, host LRU, fills of missing experts over PCIe, permutation, gate/up and down expert kernels
 through the slot table, combine.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl b300|reference]
 
 Prints one JSON line (rank 0). `value` is device-timed tok/s with inputs resident in HBM;
 `e2e` repeats the measurement through the same C-ABI calls with inputs in pinned host memory
-and the host<->device copies inside the timed region. `roofline` is the gate/up GEMV (the
+and the host<->device copies inside the timed region. `roofline` is the decode gate/up kernel (the
 dominant kernel) against the measured HBM copy bandwidth. `--impl reference` times the CPU
 oracle on the same workload (bounded per step). Multi-GPU runs are independent replicas.
 """
@@ -36,8 +36,8 @@ METRIC = "MoE-layer decode tok/s (batch 1/4/16, 256 experts top-6, 64-entry LRU 
 UNIT = "tok/s"
 BATCHES = (1, 4, 16)  # replaced by --batches
 FALLBACK_HBM_GBS = 6400.0
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "gemv_gateup_decode.md")
-GEMV_SOURCE = os.path.join(ROOT, "moe_expert_layer_10_b300", "csrc", "gemv.cu")
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_gateup.md")
+DECODE_SOURCE = os.path.join(ROOT, "moe_expert_layer_10_b300", "csrc", "decode_mma.cu")
 
 
 def parse_args():
@@ -75,7 +75,7 @@ def measured_peaks():
 
 
 def traffic_ratio_from_profile():
-    """DRAM bytes / algorithmic bytes of the gate/up GEMV launch captured in the committed ncu
+    """DRAM bytes / algorithmic bytes of the decode gate/up launch captured in the committed ncu
     summary, or None if the summary is missing or was taken on a different kernel source."""
     if not os.path.exists(PROFILE_SUMMARY):
         return None
@@ -84,7 +84,7 @@ def traffic_ratio_from_profile():
     h = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
     if not m or not h:
         return None
-    cur = hashlib.sha256(open(GEMV_SOURCE, "rb").read()).hexdigest()
+    cur = hashlib.sha256(open(DECODE_SOURCE, "rb").read()).hexdigest()
     return float(m.group(1)) if h.group(1) == cur else None
 
 
@@ -294,13 +294,13 @@ def run_b300(args, rank, world, local):
 
     tokens = args.steps * sum(BATCHES) * world
     peak, peak_kind = measured_peaks()
-    g = kst["gemv_gateup"]
+    g = kst["decode_gateup"]
     roof = None
     if g["launches"]:
         avg_ms = g["total_ms"] / g["launches"]
         bytes_per_launch = g["bytes"] / g["launches"]
         achieved = bytes_per_launch / (avg_ms / 1e3) / 1e9
-        roof = {"kernel": "gemv_gateup", "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+        roof = {"kernel": "decode_gateup", "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                 "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
                 "traffic": None, "bytes_per_launch": bytes_per_launch,
                 "avg_launch_ms": avg_ms}

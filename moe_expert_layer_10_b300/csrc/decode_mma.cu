@@ -1,0 +1,421 @@
+// Decode expert FFN on the tensor cores: every weight byte streams from HBM once, the few
+// tokens of each expert ride along as the narrow side of the product.
+//
+// Source: "FreeToken rtx 4090" (freetoken.wiki/hardware), "How the MoE Memory Hierarchy
+// Works" -- an expert is a complete cached (layer, expert) entry executed through one
+// logical mapping; here the mapping is slot_of[layer][expert] -> arena slot. The SwiGLU
+// expert form y = W_down (silu(W_gate x) * (W_up x)) is this library's specification.
+//
+// In decode an expert sees a handful of tokens, so the work is a skinny product whose cost
+// is reading the expert's weights. Doing the products on the SM's fp32 pipes makes a kernel
+// issue-bound once an expert has more than a few tokens; here the weight rows are the M side
+// of tcgen05.mma (M = 128) and the expert's tokens the N side (N = 16, 32, 48 or 64), so the
+// tensor cores take the arithmetic and the SMs only move bytes:
+//   gate/up: A tile = gate rows i0..i0+63 and the up rows of the same i (two 64-row TMA
+//            boxes), B tile = the chunk's x_perm rows; accumulator lanes 0-63 hold gate,
+//            lanes 64-127 up. The epilogue pairs them through shared memory and writes
+//            h = bf16(silu(g) * u).
+//   down:    A tile = W_down rows n0..n0+127, B tile = the chunk's h_perm rows; the epilogue
+//            writes pair_out = w_p * y in fp32.
+// Work units (work entry, token chunk of <= 64, row tile, K split) are dealt round-robin to
+// one persistent CTA per SM. A launch with too few tiles to fill the SMs evenly splits K
+// S ways (S <= 4): each split writes its fp32 partial tile to a workspace, and the split that
+// finishes last (a per-tile arrival counter) adds the S partials in split order -- a fixed
+// order, so results do not depend on timing -- and runs the epilogue.
+// Roles (6 warps): warp 0 TMA producer, warp 1 MMA issuer (and TMEM owner), warps 2-5
+// epilogue (warp w reads TMEM lanes 32*(w%4)..). Two accumulator buffers of 64 columns
+// let the epilogue of one unit overlap the MMAs of the next.
+// Every mbarrier wait is bounded (2 s); the epilogue's wait is taken by one thread and its
+// outcome shared through a named barrier, so the four warps always leave together. On a
+// timeout the kernel raises the device status, drains its copies and MMAs (bounded) and frees
+// its TMEM before returning.
+#include <algorithm>
+
+#include "kernels.cuh"
+#include "ptx.cuh"
+#include "umma.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int BK = 64;                       // K per stage (one 128-byte swizzle row)
+constexpr int kNMax = 64;                    // tokens per chunk (MMA N <= 64)
+constexpr int A_BYTES = 128 * BK * 2;        // 16 KB of weights per stage
+constexpr int B_BYTES = kNMax * BK * 2;      // up to 8 KB of tokens per stage
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int kStages = 7;
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 128;          // 2 accumulators x 64 columns
+constexpr int kXchgFloats = kNMax * 64;      // up values of one unit: [token][64 rows]
+
+struct __align__(8) Shared {
+    uint64_t full[kStages], empty[kStages], acc_full[2], acc_empty[2];
+    uint32_t tmem_base;
+    int ok[2];
+    int last[2];
+};
+constexpr int SMEM_BYTES = kStages * STAGE_BYTES + 2 * kXchgFloats * 4 + static_cast<int>(sizeof(Shared)) + 1024;
+
+struct Unit {
+    int a;       // work entry
+    int chunk;   // token chunk
+    int tile;    // row tile
+    int split;   // K split
+};
+
+__device__ __forceinline__ Unit locate_unit(const GemvWork* work, int n_work, int u, int R, int S) {
+    int lo = 0, hi = n_work - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldg(&work[mid].unit_begin) <= u) lo = mid;
+        else hi = mid - 1;
+    }
+    const int local = u - __ldg(&work[lo].unit_begin);
+    const int rest = local / S;
+    return Unit{lo, rest / R, rest % R, local % S};
+}
+
+__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
+
+template <bool GATEUP>
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_mma_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                      const GemvWork* __restrict__ work, int n_work, int n_units, int S,
+                      const int32_t* __restrict__ slot_row, int H, int I, uint16_t* __restrict__ h_out,
+                      const float* __restrict__ w_perm, float* __restrict__ pair_out, float* __restrict__ ws,
+                      int* __restrict__ cnt, int* status) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    float* xchg = reinterpret_cast<float*>(tiles + kStages * STAGE_BYTES);
+    Shared& sh = *reinterpret_cast<Shared*>(xchg + 2 * kXchgFloats);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int K = GATEUP ? H : I;
+    const int KB = K / BK;
+    const int R = GATEUP ? I / 64 : H / 128;  // row tiles per token chunk
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&sh.full[s], 1);
+            mbar_init(&sh.empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&sh.acc_full[b], 1);
+            mbar_init(&sh.acc_empty[b], 4);
+        }
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&sh.tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sh.tmem_base;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            prefetch_tmap(&tm_a);
+            prefetch_tmap(&tm_b);
+            const uint64_t pol_w = policy_evict_first();
+            int stage = 0;
+            uint32_t phase = 0, used = 0, last_phase = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+                const Unit un = locate_unit(work, n_work, u, R, S);
+                const GemvWork wk = work[un.a];
+                int slot = slot_row[wk.expert];
+                if (slot < 0) {
+                    raise_status(status, kDevBadSlot);
+                    slot = 0;  // keep every copy inside the arena; results are discarded
+                }
+                const int tok0 = wk.tok_off + un.chunk * kNMax;
+                const int nt = min(kNMax, wk.n_tok - un.chunk * kNMax);
+                const int nb = (nt + 15) >> 4;  // 16-row token boxes
+                const int kb0 = un.split * KB / S, kb1 = (un.split + 1) * KB / S;
+                const uint32_t tx = A_BYTES + nb * 16 * BK * 2;
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if (!mbar_wait(&sh.empty[stage], phase ^ 1u)) {
+                        raise_status(status, kDevWaitTimeout);
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* sa = tiles + stage * STAGE_BYTES;
+                    mbar_arrive_expect_tx(&sh.full[stage], tx);
+                    if (GATEUP) {
+                        const int row = slot * 3 * I + un.tile * 64;
+                        tma_load_2d_hint(sa, &tm_a, &sh.full[stage], kb * BK, row, pol_w);
+                        tma_load_2d_hint(sa + A_BYTES / 2, &tm_a, &sh.full[stage], kb * BK, row + I, pol_w);
+                    } else {
+                        const int row = slot * 3 * H + 2 * H + un.tile * 128;
+                        tma_load_2d_hint(sa, &tm_a, &sh.full[stage], kb * BK, row, pol_w);
+                    }
+                    for (int b = 0; b < nb; ++b)
+                        tma_load_2d(sa + A_BYTES + b * 16 * BK * 2, &tm_b, &sh.full[stage], kb * BK, tok0 + 16 * b);
+                    used |= 1u << stage;
+                    last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            // every issued copy must land before the CTA exits
+            for (int s = 0; s < kStages; ++s)
+                if ((used >> s) & 1u)
+                    if (!mbar_wait(&sh.full[s], (last_phase >> s) & 1u)) raise_status(status, kDevWaitTimeout);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int stage = 0, acc = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            int last_acc = -1;
+            uint32_t last_acc_phase = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+                const Unit un = locate_unit(work, n_work, u, R, S);
+                const GemvWork wk = work[un.a];
+                const int nt = min(kNMax, wk.n_tok - un.chunk * kNMax);
+                const uint32_t idesc = idesc_bf16_f32(128, ((nt + 15) >> 4) * 16);
+                const int kb0 = un.split * KB / S, kb1 = (un.split + 1) * KB / S;
+                if (!mbar_wait(&sh.acc_empty[acc], acc_phase ^ 1u)) {
+                    raise_status(status, kDevWaitTimeout);
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d = tmem + static_cast<uint32_t>(acc * kNMax);
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if (!mbar_wait(&sh.full[stage], phase)) {
+                        raise_status(status, kDevWaitTimeout);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint8_t* sa = tiles + stage * STAGE_BYTES;
+                    const uint64_t da = sw128_kmajor_desc(smem_u32(sa));
+                    const uint64_t db = sw128_kmajor_desc(smem_u32(sa + A_BYTES));
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k)  // +32 bytes per K=16 step inside the swizzle row
+                        umma_bf16(d, da + 2 * k, db + 2 * k, idesc, (kb != kb0 || k != 0) ? 1u : 0u);
+                    umma_commit(&sh.empty[stage]);
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                umma_commit(&sh.acc_full[acc]);
+                last_acc = acc;
+                last_acc_phase = acc_phase;
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1u;
+            }
+            // every issued MMA has finished once the last commit has arrived
+            if (last_acc >= 0 && !mbar_wait(&sh.acc_full[last_acc], last_acc_phase))
+                raise_status(status, kDevWaitTimeout);
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue (128 threads)
+        const int q = warp & 3;         // TMEM lanes 32q .. 32q+31
+        const int row = q * 32 + lane;  // accumulator row of this thread
+        const bool leader = threadIdx.x == 64;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+            const Unit un = locate_unit(work, n_work, u, R, S);
+            const GemvWork wk = work[un.a];
+            const int tok0 = wk.tok_off + un.chunk * kNMax;
+            const int nt = min(kNMax, wk.n_tok - un.chunk * kNMax);
+            const int nc = (nt + 15) >> 4;  // 16-column chunks of the accumulator
+            if (leader) sh.ok[acc] = mbar_wait(&sh.acc_full[acc], acc_phase) ? 1 : 0;
+            named_bar(1, 128);
+            if (!sh.ok[acc]) {
+                if (leader) raise_status(status, kDevWaitTimeout);
+                break;
+            }
+            tc_fence_after();
+            const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kNMax);
+            const size_t tile_floats = static_cast<size_t>(kNMax) * 128;
+            bool from_ws = false;
+            if (S > 1) {
+                // partial of this split -> workspace [unit][token][row], coalesced over rows
+                float* wsu = ws + static_cast<size_t>(u) * tile_floats;
+                for (int c = 0; c < nc; ++c) {
+                    uint32_t v[16];
+                    tmem_ld16(taddr + 16 * c, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) __stcg(wsu + (16 * c + j) * 128 + row, __uint_as_float(v[j]));
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sh.acc_empty[acc]);
+                __threadfence();
+                named_bar(1, 128);
+                if (leader) {
+                    const int tile_id = u / S;
+                    const int old = atomicAdd(cnt + tile_id, 1);
+                    const int is_last = (old == S - 1) ? 1 : 0;
+                    if (is_last) {
+                        cnt[tile_id] = 0;  // ready for the next launch
+                        __threadfence();
+                    }
+                    sh.last[acc] = is_last;
+                }
+                named_bar(1, 128);
+                const bool is_last = sh.last[acc] != 0;
+                if (!is_last) {
+                    acc ^= 1;
+                    if (acc == 0) acc_phase ^= 1u;
+                    continue;
+                }
+                __threadfence();
+                from_ws = true;
+            }
+            const float* ws0 = ws + static_cast<size_t>(u - un.split) * tile_floats;
+            // 16 accumulator columns of this thread's row: TMEM, or the sum of the S partials
+            auto fetch = [&](int c, float (&v)[16]) {
+                if (from_ws) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) v[j] = __ldcg(ws0 + (16 * c + j) * 128 + row);
+                    for (int s = 1; s < S; ++s) {
+                        const float* p = ws0 + static_cast<size_t>(s) * tile_floats;
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) v[j] += __ldcg(p + (16 * c + j) * 128 + row);
+                    }
+                } else {
+                    uint32_t r[16];
+                    tmem_ld16(taddr + 16 * c, r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+                }
+            };
+            auto release = [&]() {
+                if (!from_ws) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&sh.acc_empty[acc]);
+                }
+            };
+            if (GATEUP) {
+                float* xc = xchg + acc * kXchgFloats;
+                const int i0 = un.tile * 64;
+                if (q >= 2) {  // up rows: hand them to the gate warps
+                    for (int c = 0; c < nc; ++c) {
+                        float v[16];
+                        fetch(c, v);
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) xc[(16 * c + j) * 64 + row - 64] = v[j];
+                    }
+                    release();
+                }
+                named_bar(1, 128);
+                if (q < 2) {  // gate rows: h = silu(g) * u for the chunk's tokens
+                    for (int c = 0; c < nc; ++c) {
+                        float v[16];
+                        fetch(c, v);
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const int n = 16 * c + j;
+                            if (n < nt) {
+                                const float h = silu_mul(v[j], xc[n * 64 + row]);
+                                reinterpret_cast<__nv_bfloat16*>(h_out)[static_cast<size_t>(tok0 + n) * I + i0 + row] =
+                                    __float2bfloat16_rn(h);
+                            }
+                        }
+                    }
+                    release();
+                }
+            } else {
+                const int n0 = un.tile * 128;
+                for (int c = 0; c < nc; ++c) {
+                    float v[16];
+                    fetch(c, v);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int n = 16 * c + j;
+                        if (n < nt) {
+                            const size_t pos = static_cast<size_t>(tok0 + n);
+                            pair_out[pos * H + n0 + row] = __ldg(w_perm + pos) * v[j];
+                        }
+                    }
+                }
+                release();
+            }
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+template <bool GATEUP>
+cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const GemvWork* work, int n_work, int n_units,
+                   int S, const int32_t* slot_row, int H, int I, uint16_t* h_out, const float* w_perm,
+                   float* pair_out, float* ws, int* cnt, int* status, int num_sms, cudaStream_t st) {
+    if (n_units <= 0 || n_work <= 0) return cudaSuccess;
+    if (S < 1 || S > kDecodeMaxSplit) return cudaErrorInvalidValue;
+    if (S > 1 && n_units > kDecodeSplitUnits) return cudaErrorInvalidValue;
+    auto kern = decode_mma_kernel<GATEUP>;
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    const int grid = std::min(n_units, num_sms);
+    kern<<<grid, kThreads, SMEM_BYTES, st>>>(ta, tb, work, n_work, n_units, S, slot_row, H, I, h_out, w_perm,
+                                             pair_out, ws, cnt, status);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int decode_row_tiles(bool gateup, int H, int I) { return gateup ? I / 64 : H / 128; }
+
+int decode_token_chunks(int n_tok) { return (n_tok + kNMax - 1) / kNMax; }
+
+int decode_choose_split(int n_tiles, bool gateup, int H, int I, int num_sms) {
+    const int KB = (gateup ? H : I) / BK;
+    auto eff = [&](int s) {
+        const long long n = static_cast<long long>(n_tiles) * s;
+        const long long waves = (n + num_sms - 1) / num_sms;
+        return static_cast<double>(n) / static_cast<double>(waves * num_sms);
+    };
+    if (n_tiles <= 0 || eff(1) >= 0.85) return 1;
+    int best = 1;
+    double best_eff = eff(1);
+    for (int s = 2; s <= kDecodeMaxSplit; ++s) {
+        if (static_cast<long long>(n_tiles) * s > kDecodeSplitUnits || KB / s < 4) break;
+        const double e = eff(s) - 0.02 * (s - 1);  // each split adds a partial write and read
+        if (e > best_eff + 1e-9) {
+            best = s;
+            best_eff = e;
+        }
+    }
+    return best;
+}
+
+cudaError_t launch_decode_gateup(const DecodeMaps& m, const GemvWork* work, int n_work, int n_units, int S,
+                                 const int32_t* slot_row, int H, int I, uint16_t* h_perm, float* ws, int* cnt,
+                                 int* status, int num_sms, cudaStream_t st) {
+    return launch<true>(m.a_gu, m.b_x, work, n_work, n_units, S, slot_row, H, I, h_perm, nullptr, nullptr, ws, cnt,
+                        status, num_sms, st);
+}
+
+cudaError_t launch_decode_down(const DecodeMaps& m, const GemvWork* work, int n_work, int n_units, int S,
+                               const int32_t* slot_row, int H, int I, const float* w_perm, float* pair_out, float* ws,
+                               int* cnt, int* status, int num_sms, cudaStream_t st) {
+    return launch<false>(m.a_d, m.b_h, work, n_work, n_units, S, slot_row, H, I, nullptr, w_perm, pair_out, ws, cnt,
+                         status, num_sms, st);
+}
+
+}  // namespace moe

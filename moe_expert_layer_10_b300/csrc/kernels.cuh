@@ -23,7 +23,7 @@ cudaError_t launch_permute(const int32_t* idx, const float* w, int P, int E, int
 cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* perm, int P, int k, int H, uint16_t* x_perm,
                                cudaStream_t st);
 
-// --- decode expert FFN: HBM-streaming GEMV through the slot table ---
+// --- decode expert FFN: work list of one wave (one entry per routed expert) ---
 struct GemvWork {
     int expert;      // expert id
     int tok_off;     // first permuted position of its tokens
@@ -31,25 +31,30 @@ struct GemvWork {
     int unit_begin;  // first work unit of this expert (entry n_work holds the total)
 };
 
-struct GemvMaps {
-    CUtensorMap w_gu[2];  // arena viewed as [C*3I rows x H], boxes for 4 and 2 rows per warp
-    CUtensorMap w_d[2];   // arena viewed as [C*3H rows x I]
-    CUtensorMap xperm;    // [P_max x H], box 8 rows
-    CUtensorMap hperm;    // [P_max x I], box 8 rows
-    int ks_down;          // slab width of the down projection (256 or 128)
+// --- decode expert FFN on the tensor cores (weights as M = 128, tokens as N <= 64) ---
+constexpr int kDecodeMaxSplit = 4;       // largest K split of one launch
+constexpr int kDecodeSplitUnits = 1024;  // most units of a split launch (workspace tiles)
+constexpr int kDecodeTileFloats = 64 * 128;  // fp32 partial tile: [64 tokens][128 rows]
+
+struct DecodeMaps {
+    CUtensorMap a_gu;  // arena [C*3I rows x H], box 64 x 64 rows, 128B swizzle
+    CUtensorMap a_d;   // arena [C*3H rows x I], box 64 x 128 rows
+    CUtensorMap b_x;   // x_perm [P_max x H], box 64 x 16 rows
+    CUtensorMap b_h;   // h_perm [P_max x I], box 64 x 16 rows
 };
 
-int gemv_nt_bucket(int max_tokens_per_expert);  // 8, 16 or 32 (tokens per pass)
-int gemv_units_per_chunk(bool gateup, int nt_bucket, int H, int I);
-
-// h_perm[pos, i] = bf16( silu(W_gate[i] . x) * (W_up[i] . x) ) for the wave's experts
-cudaError_t launch_gemv_gateup(const GemvMaps& maps, int nt_bucket, const GemvWork* work, int n_work, int n_units,
-                               const int32_t* slot_row, int H, int I, uint16_t* h_perm, int* status, int num_sms,
-                               cudaStream_t st);
+int decode_row_tiles(bool gateup, int H, int I);   // row tiles per token chunk
+int decode_token_chunks(int n_tok);                // chunks of <= 64 tokens
+int decode_choose_split(int n_tiles, bool gateup, int H, int I, int num_sms);  // K split S of a launch
+// h_perm[pos, i] = bf16( silu(W_gate[i] . x) * (W_up[i] . x) ) for the wave's experts.
+// work[a].unit_begin counts units = chunks * row tiles * S per entry (entry n_work: total).
+cudaError_t launch_decode_gateup(const DecodeMaps& maps, const GemvWork* work, int n_work, int n_units, int S,
+                                 const int32_t* slot_row, int H, int I, uint16_t* h_perm, float* ws, int* cnt,
+                                 int* status, int num_sms, cudaStream_t st);
 // pair_out[pos, n] = w_perm[pos] * (W_down[n] . h[pos])
-cudaError_t launch_gemv_down(const GemvMaps& maps, int nt_bucket, const GemvWork* work, int n_work, int n_units,
-                             const int32_t* slot_row, int H, int I, const float* w_perm, float* pair_out,
-                             int* status, int num_sms, cudaStream_t st);
+cudaError_t launch_decode_down(const DecodeMaps& maps, const GemvWork* work, int n_work, int n_units, int S,
+                               const int32_t* slot_row, int H, int I, const float* w_perm, float* pair_out, float* ws,
+                               int* cnt, int* status, int num_sms, cudaStream_t st);
 
 // --- combine: out[t] = resid[t] + sum_j pair_out[inv_perm[t*k+j]] (j order) ---
 cudaError_t launch_combine(const float* pair_out, const int32_t* inv_perm, const float* resid, float* out, int T,

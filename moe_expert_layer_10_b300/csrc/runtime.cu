@@ -55,11 +55,12 @@ int fail(int code, const char* fmt, ...) {
 
 constexpr int kEvRing = 256;     // compute-wave and fill-batch events
 constexpr int kStageRing = 16;   // pinned staging buffers for small H2D copies
+constexpr int kDecodeMaxTokens = 64;  // AUTO path: tensor-core decode kernels up to this many tokens per expert
 
-enum KernelId { kRouterLogits, kRouterTopk, kPermute, kGather, kGemvGateUp, kGemvDown, kGemmGateUp, kGemmDown,
+enum KernelId { kRouterLogits, kRouterTopk, kPermute, kGather, kDecodeGateUp, kDecodeDown, kGemmGateUp, kGemmDown,
                 kCombine, kNumKernels };
-const char* kKernelNames[kNumKernels] = {"router_logits", "router_topk", "permute",    "gather_rows",
-                                         "gemv_gateup",   "gemv_down",   "gemm_gateup", "gemm_down",
+const char* kKernelNames[kNumKernels] = {"router_logits", "router_topk",  "permute",     "gather_rows",
+                                         "decode_gateup", "decode_down",  "gemm_gateup", "gemm_down",
                                          "combine"};
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -153,7 +154,9 @@ struct moe_ctx {
     int64_t comp_seq = -1, fill_seq = -1;
     std::vector<int64_t> slot_last_use, slot_fill;
 
-    moe::GemvMaps gemv_maps{};
+    moe::DecodeMaps dec_maps{};
+    float* dec_ws = nullptr;  // split-K partial tiles of the decode kernels
+    int* dec_cnt = nullptr;   // per-tile arrival counters (zero between launches)
     moe::GemmMaps gemm_maps{};
 
     // stats and trace
@@ -263,6 +266,8 @@ int check_status(moe_ctx* c) {
         *c->status_host = 0;
         // clear the device word too, in stream order, so the context stays usable
         cudaMemsetAsync(c->status, 0, sizeof(int), c->s_comp);
+        // a kernel that stopped early may have left split-K arrival counters behind
+        cudaMemsetAsync(c->dec_cnt, 0, moe::kDecodeSplitUnits * sizeof(int), c->s_comp);
         return fail(MOE_E_DEVICE, "a kernel raised device status %d (1 wait timeout, 2 bad forced set, 3 bad slot, "
                                   "4 bad expert index)", code);
     }
@@ -402,7 +407,8 @@ void free_all(moe_ctx* c) {
         if (c->stage_ev[i]) cudaEventDestroy(c->stage_ev[i]);
     if (c->ev_d2h) cudaEventDestroy(c->ev_d2h);
     void* dev_ptrs[] = {c->arena, c->slot_dev, c->logits, c->offsets, c->perm, c->inv_perm, c->active,
-                        c->n_active, c->w_perm, c->pair_out, c->x_perm, c->h_perm, c->status, c->work_dev};
+                        c->n_active, c->w_perm, c->pair_out, c->x_perm, c->h_perm, c->status, c->work_dev,
+                        c->dec_ws,   c->dec_cnt};
     for (void* p : dev_ptrs)
         if (p) cudaFree(p);
     void* host_ptrs[] = {c->pool, c->idx_host, c->status_host, c->table_stage, c->work_stage};
@@ -508,7 +514,10 @@ int moe_cache_init(const moe_config_t* cfg, void* stream_compute, void* stream_c
     INIT_TRY(cudaMalloc(&c->h_perm, static_cast<size_t>(c->Pmax) * c->I * 2));
     INIT_TRY(cudaMalloc(&c->pair_out, static_cast<size_t>(c->Pmax) * c->H * sizeof(float)));
     INIT_TRY(cudaMalloc(&c->status, sizeof(int)));
-    INIT_TRY(cudaMalloc(&c->work_dev, (c->E + 1) * sizeof(GemvWork)));
+    INIT_TRY(cudaMalloc(&c->work_dev, 2 * (c->E + 1) * sizeof(GemvWork)));
+    INIT_TRY(cudaMalloc(&c->dec_ws, static_cast<size_t>(moe::kDecodeSplitUnits) * moe::kDecodeTileFloats * sizeof(float)));
+    INIT_TRY(cudaMalloc(&c->dec_cnt, moe::kDecodeSplitUnits * sizeof(int)));
+    INIT_TRY(cudaMemset(c->dec_cnt, 0, moe::kDecodeSplitUnits * sizeof(int)));
     INIT_TRY(cudaMemset(c->status, 0, sizeof(int)));
     INIT_TRY(cudaMemset(c->x_perm, 0, static_cast<size_t>(c->Pmax) * c->H * 2));
     INIT_TRY(cudaMemset(c->h_perm, 0, static_cast<size_t>(c->Pmax) * c->I * 2));
@@ -517,7 +526,7 @@ int moe_cache_init(const moe_config_t* cfg, void* stream_compute, void* stream_c
     *c->status_host = 0;
     INIT_TRY(cudaHostAlloc(reinterpret_cast<void**>(&c->table_stage), kStageRing * keys * sizeof(int32_t), 0));
     INIT_TRY(cudaHostAlloc(reinterpret_cast<void**>(&c->work_stage),
-                           static_cast<size_t>(kStageRing) * (c->E + 1) * sizeof(GemvWork), 0));
+                           static_cast<size_t>(kStageRing) * 2 * (c->E + 1) * sizeof(GemvWork), 0));
     for (int i = 0; i < kStageRing; ++i) {
         INIT_TRY(cudaEventCreateWithFlags(&c->stage_ev[i], cudaEventDisableTiming));
         INIT_TRY(cudaEventRecord(c->stage_ev[i], c->s_comp));
@@ -530,14 +539,10 @@ int moe_cache_init(const moe_config_t* cfg, void* stream_compute, void* stream_c
 
     // TMA views. Arena rows: [C*3I x H] for gate/up, [C*3H x I] for down.
     const uint64_t H = c->H, I = c->I, C = c->C, P = c->Pmax;
-    c->gemv_maps.ks_down = (I % 256 == 0) ? 256 : 128;
-    const uint32_t ksd = c->gemv_maps.ks_down;
-    bool ok = make_map(&c->gemv_maps.w_gu[0], c->arena, H, C * 3 * I, 256, 16, CU_TENSOR_MAP_SWIZZLE_NONE) &&
-              make_map(&c->gemv_maps.w_gu[1], c->arena, H, C * 3 * I, 256, 8, CU_TENSOR_MAP_SWIZZLE_NONE) &&
-              make_map(&c->gemv_maps.w_d[0], c->arena, I, C * 3 * H, ksd, 32, CU_TENSOR_MAP_SWIZZLE_NONE) &&
-              make_map(&c->gemv_maps.w_d[1], c->arena, I, C * 3 * H, ksd, 16, CU_TENSOR_MAP_SWIZZLE_NONE) &&
-              make_map(&c->gemv_maps.xperm, c->x_perm, H, P, 256, 8, CU_TENSOR_MAP_SWIZZLE_NONE) &&
-              make_map(&c->gemv_maps.hperm, c->h_perm, I, P, ksd, 8, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+    bool ok = make_map(&c->dec_maps.a_gu, c->arena, H, C * 3 * I, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
+              make_map(&c->dec_maps.a_d, c->arena, I, C * 3 * H, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) &&
+              make_map(&c->dec_maps.b_x, c->x_perm, H, P, 64, 16, CU_TENSOR_MAP_SWIZZLE_128B) &&
+              make_map(&c->dec_maps.b_h, c->h_perm, I, P, 64, 16, CU_TENSOR_MAP_SWIZZLE_128B) &&
               make_map(&c->gemm_maps.a_x, c->x_perm, H, P, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) &&
               make_map(&c->gemm_maps.b_gu, c->arena, H, C * 3 * I, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) &&
               make_map(&c->gemm_maps.a_h, c->h_perm, I, P, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) &&
@@ -701,7 +706,7 @@ int moe_layer_forward(moe_ctx* c, int layer, const void* x, const float* resid, 
     }
     const int U = static_cast<int>(distinct.size());
     int path = c->path;
-    if (path == MOE_PATH_AUTO) path = (max_n <= 32) ? MOE_PATH_GEMV : MOE_PATH_GEMM;
+    if (path == MOE_PATH_AUTO) path = (max_n <= kDecodeMaxTokens) ? MOE_PATH_GEMV : MOE_PATH_GEMM;
 
     // 4. waves of at most C experts
     for (int a0 = 0; a0 < U; a0 += c->C) {
@@ -745,54 +750,46 @@ int moe_layer_forward(moe_ctx* c, int layer, const void* x, const float* resid, 
             continue;
         }
 
-        // work list for this wave
-        int wmax = 0, pw = 0;
+        // work lists for this wave: one entry per expert, units = token chunks x row tiles x
+        // K splits (the split of each kernel is chosen so its units fill the SMs evenly)
+        int pw = 0, chunks = 0;
         for (int a = a0; a < a1; ++a) {
-            wmax = std::max(wmax, count[distinct[a]]);
             pw += count[distinct[a]];
+            chunks += moe::decode_token_chunks(count[distinct[a]]);
         }
-        const int nt = moe::gemv_nt_bucket(wmax);
+        const int nw = a1 - a0;
+        const int Rg = moe::decode_row_tiles(true, H, I), Rd = moe::decode_row_tiles(false, H, I);
+        const int Sg = moe::decode_choose_split(chunks * Rg, true, H, I, c->num_sms);
+        const int Sd = moe::decode_choose_split(chunks * Rd, false, H, I, c->num_sms);
         int s;
         rc = next_stage(c, &s);
         if (rc) return rc;
-        GemvWork* wk = c->work_stage + static_cast<size_t>(s) * (E + 1);
-        const int upc_gu = moe::gemv_units_per_chunk(true, nt, H, I);
-        const int upc_d = moe::gemv_units_per_chunk(false, nt, H, I);
+        GemvWork* wk = c->work_stage + static_cast<size_t>(s) * 2 * (E + 1);
+        GemvWork* wk2 = wk + (E + 1);
         int units_gu = 0, units_d = 0;
         for (int a = a0; a < a1; ++a) {
             const int e = distinct[a];
-            const int chunks = (count[e] + nt - 1) / nt;
+            const int ch = moe::decode_token_chunks(count[e]);
             wk[a - a0] = GemvWork{e, offs[e], count[e], units_gu};
-            units_gu += chunks * upc_gu;
-            units_d += chunks * upc_d;
+            wk2[a - a0] = GemvWork{e, offs[e], count[e], units_d};
+            units_gu += ch * Rg * Sg;
+            units_d += ch * Rd * Sd;
         }
-        const int nw = a1 - a0;
         wk[nw] = GemvWork{-1, 0, 0, units_gu};
-        CUDA_TRY(cudaMemcpyAsync(c->work_dev, wk, (nw + 1) * sizeof(GemvWork), cudaMemcpyHostToDevice, c->s_comp));
+        wk2[nw] = GemvWork{-1, 0, 0, units_d};
+        // both lists in one copy: gate/up at work_dev, down at work_dev + E + 1
+        CUDA_TRY(cudaMemcpyAsync(c->work_dev, wk, 2 * (E + 1) * sizeof(GemvWork), cudaMemcpyHostToDevice, c->s_comp));
         CUDA_TRY(cudaEventRecord(c->stage_ev[s], c->s_comp));
         {
-            ProfScope ps(c, kGemvGateUp, 4.0 * nw * I * H + 2.0 * pw * H + 2.0 * pw * I, 4.0 * pw * I * H);
-            CUDA_TRY(moe::launch_gemv_gateup(c->gemv_maps, nt, c->work_dev, nw, units_gu, slot_row, H, I, c->h_perm,
-                                             c->status, c->num_sms, c->s_comp));
+            ProfScope ps(c, kDecodeGateUp, 4.0 * nw * I * H + 2.0 * pw * H + 2.0 * pw * I, 4.0 * pw * I * H);
+            CUDA_TRY(moe::launch_decode_gateup(c->dec_maps, c->work_dev, nw, units_gu, Sg, slot_row, H, I, c->h_perm,
+                                               c->dec_ws, c->dec_cnt, c->status, c->num_sms, c->s_comp));
         }
-        // the down kernel numbers its units with its own chunking; rewrite unit_begin
-        rc = next_stage(c, &s);
-        if (rc) return rc;
-        GemvWork* wk2 = c->work_stage + static_cast<size_t>(s) * (E + 1);
-        int u = 0;
-        for (int a = a0; a < a1; ++a) {
-            const int e = distinct[a];
-            wk2[a - a0] = GemvWork{e, offs[e], count[e], u};
-            u += ((count[e] + nt - 1) / nt) * upc_d;
-        }
-        wk2[nw] = GemvWork{-1, 0, 0, u};
-        // second copy goes right after the first kernel in stream order
-        CUDA_TRY(cudaMemcpyAsync(c->work_dev, wk2, (nw + 1) * sizeof(GemvWork), cudaMemcpyHostToDevice, c->s_comp));
-        CUDA_TRY(cudaEventRecord(c->stage_ev[s], c->s_comp));
         {
-            ProfScope ps(c, kGemvDown, 2.0 * nw * H * I + 2.0 * pw * I + 4.0 * pw * H + 4.0 * pw, 2.0 * pw * I * H);
-            CUDA_TRY(moe::launch_gemv_down(c->gemv_maps, nt, c->work_dev, nw, units_d, slot_row, H, I, c->w_perm,
-                                           c->pair_out, c->status, c->num_sms, c->s_comp));
+            ProfScope ps(c, kDecodeDown, 2.0 * nw * H * I + 2.0 * pw * I + 4.0 * pw * H + 4.0 * pw, 2.0 * pw * I * H);
+            CUDA_TRY(moe::launch_decode_down(c->dec_maps, c->work_dev + (E + 1), nw, units_d, Sd, slot_row, H, I,
+                                             c->w_perm, c->pair_out, c->dec_ws, c->dec_cnt, c->status, c->num_sms,
+                                             c->s_comp));
         }
         c->comp_seq++;
         CUDA_TRY(cudaEventRecord(c->comp_ev[c->comp_seq % kEvRing], c->s_comp));
