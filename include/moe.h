@@ -64,8 +64,8 @@ extern "C" {
 #define MOE_FILL_FULL_LAYER 1 /* prefetch every expert of the layer (prefill double buffering) */
 
 /* ---- expert-FFN path selection (moe_set_path) ---- */
-#define MOE_PATH_AUTO 0 /* GEMV when every routed expert has <= 32 tokens, else grouped GEMM */
-#define MOE_PATH_GEMV 1 /* HBM-streaming GEMV kernels (decode) */
+#define MOE_PATH_AUTO 0 /* decode kernels when every routed expert has <= 64 tokens, else grouped GEMM */
+#define MOE_PATH_GEMV 1 /* decode kernels: weight-streaming tcgen05 products, tokens as the narrow side */
 #define MOE_PATH_GEMM 2 /* tcgen05 grouped GEMM kernels (prefill) */
 
 /* ---- LRU event kinds ---- */
@@ -189,6 +189,10 @@ int moe_cache_fill(moe_ctx* ctx, int layer, const int32_t* topk_idx_host, int n,
  * the distinct experts D (ascending) are accessed in the LRU in waves of at most C;
  * missing entries are copied in on the copy stream; per wave the expert FFN runs through
  * the device slot table; a deterministic combine sums the k contributions in j order.
+ * On the decode path each fill is followed, on the copy stream, by a write of the slot's
+ * fill generation to a device flag, and the expert kernels stream a filled entry only once
+ * its flag shows the copy has landed: resident experts compute while the fills cross the
+ * link. Results do not depend on which entries had to be filled.
  * Returns after enqueuing the last kernel (no wait at the end).
  * Errors: MOE_E_INVAL, MOE_E_CUDA, MOE_E_TIMEOUT (host wait deadline), MOE_E_DEVICE (a kernel
  * of an earlier call reported an error).
@@ -210,6 +214,10 @@ const char* moe_last_error(void);
 
 /* Choose the expert-FFN path for later moe_layer_forward calls (MOE_PATH_*). */
 int moe_set_path(moe_ctx* ctx, int path);
+
+/* Turn the per-launch CUDA-event timing of MOE_PROFILE on (on != 0) or off for later calls,
+ * e.g. to time a region without the events and then profile a separate pass. */
+int moe_set_profile(moe_ctx* ctx, int on);
 
 /* Wait (with a deadline) until all enqueued work of the context has finished; reports any
  * device status raised by its kernels (MOE_E_DEVICE). */
@@ -235,7 +243,11 @@ int moe_lru_simulate(int capacity, int n, const int32_t* layer, const int32_t* e
 /*
  * Host-side fault injection for tests: the next `count` fill copies of this context report
  * failure before any copy is enqueued (kind 1), or the next `count` host waits report a
- * timeout (kind 2). kind 0 clears. No GPU fault is ever produced.
+ * timeout (kind 2), or the next `count` decode waves that fill entries tell their kernels to
+ * wait for a fill generation that the copy stream does not write, with a 0.2 s device-side
+ * deadline (kind 3): the kernels give up, raise device status 5 (MOE_E_DEVICE at the next
+ * synchronising call) and the context stays usable. kind 0 clears. No GPU fault is ever
+ * produced.
  */
 int moe_debug_inject(moe_ctx* ctx, int kind, int count);
 

@@ -27,7 +27,7 @@ EV_HIT, EV_FILL, EV_PREFETCH_FILL, EV_PREFETCH_HIT = 0, 1, 2, 3
 # every symbol include/moe.h declares
 EXPORTS = ["moe_cache_init", "moe_cache_destroy", "moe_host_entry", "moe_entry_bytes", "moe_route",
            "moe_route_forced", "moe_cache_fill", "moe_layer_forward", "moe_stats", "moe_last_error",
-           "moe_set_path", "moe_sync", "moe_resident_slot", "moe_kernel_stats", "moe_lru_simulate",
+           "moe_set_path", "moe_set_profile", "moe_sync", "moe_resident_slot", "moe_kernel_stats", "moe_lru_simulate",
            "moe_debug_inject", "moe_debug_read", "moe_route_noalloc"]
 MOE_NOALLOC_MAX_LOGITS = 65536
 MOE_DBG_OFFSETS, MOE_DBG_PERM, MOE_DBG_INV_PERM, MOE_DBG_ACTIVE, MOE_DBG_N_ACTIVE, MOE_DBG_SLOT_TABLE, \
@@ -92,6 +92,7 @@ def lib():
     L.moe_stats.argtypes = [vp, ctypes.POINTER(Stats), vp, u64, i32]
     L.moe_last_error.restype = ctypes.c_char_p
     L.moe_set_path.argtypes = [vp, i32]
+    L.moe_set_profile.argtypes = [vp, i32]
     L.moe_sync.argtypes = [vp]
     L.moe_resident_slot.argtypes = [vp, i32, i32]
     L.moe_kernel_stats.argtypes = [vp, vp, i32, i32]
@@ -236,6 +237,9 @@ class MoeCache:
 
     def set_path(self, path: int):
         _check(lib().moe_set_path(self._h, path), "moe_set_path")
+
+    def set_profile(self, on: bool):
+        _check(lib().moe_set_profile(self._h, 1 if on else 0), "moe_set_profile")
 
     def sync(self):
         _check(lib().moe_sync(self._h), "moe_sync")

@@ -18,7 +18,11 @@
 //   down:    A tile = W_down rows n0..n0+127, B tile = the chunk's h_perm rows; the epilogue
 //            writes pair_out = w_p * y in fp32.
 // Work units (work entry, token chunk of <= 64, row tile, K split) are dealt round-robin to
-// one persistent CTA per SM. A launch with too few tiles to fill the SMs evenly splits K
+// one persistent CTA per SM. Entries whose cache fill was enqueued by the same forward come
+// last in the list and carry the slot and fill generation to wait for: the producer polls the
+// slot's fill flag (bumped by the copy stream after the copy) before streaming that expert, so
+// resident experts compute while the fills cross the link and each filled expert starts as
+// soon as its own bytes have landed -- one launch per wave, no host round trip. A launch with too few tiles to fill the SMs evenly splits K
 // S ways (S <= 4): each split writes its fp32 partial tile to a workspace, and the split that
 // finishes last (a per-tile arrival counter) adds the S partials in split order -- a fixed
 // order, so results do not depend on timing -- and runs the epilogue.
@@ -43,18 +47,36 @@ constexpr int kNMax = 64;                    // tokens per chunk (MMA N <= 64)
 constexpr int A_BYTES = 128 * BK * 2;        // 16 KB of weights per stage
 constexpr int B_BYTES = kNMax * BK * 2;      // up to 8 KB of tokens per stage
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int kStages = 7;
+constexpr int kMaxStages = 9;
 constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 128;          // 2 accumulators x 64 columns
 constexpr int kXchgFloats = kNMax * 64;      // up values of one unit: [token][64 rows]
 
 struct __align__(8) Shared {
-    uint64_t full[kStages], empty[kStages], acc_full[2], acc_empty[2];
+    uint64_t full[kMaxStages], empty[kMaxStages], acc_full[2], acc_empty[2];
     uint32_t tmem_base;
     int ok[2];
     int last[2];
 };
-constexpr int SMEM_BYTES = kStages * STAGE_BYTES + 2 * kXchgFloats * 4 + static_cast<int>(sizeof(Shared)) + 1024;
+
+// gate/up keeps a 16 KB exchange buffer for the up values, so it has one stage fewer
+template <bool GATEUP>
+struct Layout {
+    static constexpr int STAGES = GATEUP ? 8 : 9;
+    static constexpr int XCHG_BYTES = GATEUP ? kXchgFloats * 4 : 0;
+    static constexpr int SMEM = STAGES * STAGE_BYTES + XCHG_BYTES + static_cast<int>(sizeof(Shared)) + 1024;
+    static_assert(STAGES <= kMaxStages, "stage count");
+    static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
+};
+
+// Arrival on a split tile's counter: a gpu-scope acquire-release add. The barrier before it
+// orders the other epilogue threads' partial stores ahead of this release (cumulativity), and
+// the barrier after it orders their partial loads behind this acquire.
+__device__ __forceinline__ int atomic_add_acq_rel_gpu(int* p, int v) {
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
 
 struct Unit {
     int a;       // work entry
@@ -81,13 +103,18 @@ template <bool GATEUP>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_mma_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                       const GemvWork* __restrict__ work, int n_work, int n_units, int S,
-                      const int32_t* __restrict__ slot_row, int H, int I, uint16_t* __restrict__ h_out,
+                      const int32_t* __restrict__ slot_row, const uint32_t* __restrict__ fill_flag, int H, int I,
+                      uint16_t* __restrict__ h_out,
                       const float* __restrict__ w_perm, float* __restrict__ pair_out, float* __restrict__ ws,
-                      int* __restrict__ cnt, int* status) {
+                      int* __restrict__ cnt, int* status, uint64_t fill_wait_ns) {
+    using Lay = Layout<GATEUP>;
+    // the MMA and epilogue roles may legitimately wait as long as the producer waits for a fill
+    const uint64_t consumer_wait_ns = fill_wait_ns + kWaitDeadlineNs;
+    constexpr int kStages = Lay::STAGES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float* xchg = reinterpret_cast<float*>(tiles + kStages * STAGE_BYTES);
-    Shared& sh = *reinterpret_cast<Shared*>(xchg + 2 * kXchgFloats);
+    Shared& sh = *reinterpret_cast<Shared*>(tiles + kStages * STAGE_BYTES + Lay::XCHG_BYTES);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int K = GATEUP ? H : I;
     const int KB = K / BK;
@@ -122,9 +149,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             int stage = 0;
             uint32_t phase = 0, used = 0, last_phase = 0;
             bool ok = true;
+            int ready_a = -1;  // last work entry whose fill was seen (a CTA visits entries in order)
             for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
                 const Unit un = locate_unit(work, n_work, u, R, S);
                 const GemvWork wk = work[un.a];
+                if (wk.wait_slot >= 0 && un.a != ready_a) {
+                    // an entry filled by this wave: stream it once its copy has landed
+                    if (!wait_fill_flag(fill_flag + wk.wait_slot, wk.gen, fill_wait_ns)) {
+                        raise_status(status, kDevFillTimeout);
+                        break;
+                    }
+                    ready_a = un.a;
+                }
                 int slot = slot_row[wk.expert];
                 if (slot < 0) {
                     raise_status(status, kDevBadSlot);
@@ -180,14 +216,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int nt = min(kNMax, wk.n_tok - un.chunk * kNMax);
                 const uint32_t idesc = idesc_bf16_f32(128, ((nt + 15) >> 4) * 16);
                 const int kb0 = un.split * KB / S, kb1 = (un.split + 1) * KB / S;
-                if (!mbar_wait(&sh.acc_empty[acc], acc_phase ^ 1u)) {
+                if (!mbar_wait(&sh.acc_empty[acc], acc_phase ^ 1u, consumer_wait_ns)) {
                     raise_status(status, kDevWaitTimeout);
                     break;
                 }
                 tc_fence_after();
                 const uint32_t d = tmem + static_cast<uint32_t>(acc * kNMax);
                 for (int kb = kb0; kb < kb1; ++kb) {
-                    if (!mbar_wait(&sh.full[stage], phase)) {
+                    if (!mbar_wait(&sh.full[stage], phase, consumer_wait_ns)) {
                         raise_status(status, kDevWaitTimeout);
                         ok = false;
                         break;
@@ -229,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int tok0 = wk.tok_off + un.chunk * kNMax;
             const int nt = min(kNMax, wk.n_tok - un.chunk * kNMax);
             const int nc = (nt + 15) >> 4;  // 16-column chunks of the accumulator
-            if (leader) sh.ok[acc] = mbar_wait(&sh.acc_full[acc], acc_phase) ? 1 : 0;
+            if (leader) sh.ok[acc] = mbar_wait(&sh.acc_full[acc], acc_phase, consumer_wait_ns) ? 1 : 0;
             named_bar(1, 128);
             if (!sh.ok[acc]) {
                 if (leader) raise_status(status, kDevWaitTimeout);
@@ -252,16 +288,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sh.acc_empty[acc]);
-                __threadfence();
                 named_bar(1, 128);
                 if (leader) {
                     const int tile_id = u / S;
-                    const int old = atomicAdd(cnt + tile_id, 1);
+                    const int old = atomic_add_acq_rel_gpu(cnt + tile_id, 1);
                     const int is_last = (old == S - 1) ? 1 : 0;
-                    if (is_last) {
-                        cnt[tile_id] = 0;  // ready for the next launch
-                        __threadfence();
-                    }
+                    if (is_last) cnt[tile_id] = 0;  // every split has arrived; ready for the next launch
                     sh.last[acc] = is_last;
                 }
                 named_bar(1, 128);
@@ -271,7 +303,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (acc == 0) acc_phase ^= 1u;
                     continue;
                 }
-                __threadfence();
                 from_ws = true;
             }
             const float* ws0 = ws + static_cast<size_t>(u - un.split) * tile_floats;
@@ -301,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             };
             if (GATEUP) {
-                float* xc = xchg + acc * kXchgFloats;
+                float* xc = xchg;
                 const int i0 = un.tile * 64;
                 if (q >= 2) {  // up rows: hand them to the gate warps
                     for (int c = 0; c < nc; ++c) {
@@ -329,6 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     release();
                 }
+                named_bar(1, 128);  // the exchange buffer is free for the next unit
             } else {
                 const int n0 = un.tile * 128;
                 for (int c = 0; c < nc; ++c) {
@@ -359,21 +391,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <bool GATEUP>
 cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const GemvWork* work, int n_work, int n_units,
-                   int S, const int32_t* slot_row, int H, int I, uint16_t* h_out, const float* w_perm,
-                   float* pair_out, float* ws, int* cnt, int* status, int num_sms, cudaStream_t st) {
+                   int S, const int32_t* slot_row, const uint32_t* fill_flag, int H, int I, uint16_t* h_out,
+                   const float* w_perm, float* pair_out, float* ws, int* cnt, int* status, uint64_t fill_wait_ns,
+                   int num_sms, cudaStream_t st) {
     if (n_units <= 0 || n_work <= 0) return cudaSuccess;
     if (S < 1 || S > kDecodeMaxSplit) return cudaErrorInvalidValue;
     if (S > 1 && n_units > kDecodeSplitUnits) return cudaErrorInvalidValue;
     auto kern = decode_mma_kernel<GATEUP>;
+    constexpr int smem = Layout<GATEUP>::SMEM;
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         attr = true;
     }
     const int grid = std::min(n_units, num_sms);
-    kern<<<grid, kThreads, SMEM_BYTES, st>>>(ta, tb, work, n_work, n_units, S, slot_row, H, I, h_out, w_perm,
-                                             pair_out, ws, cnt, status);
+    kern<<<grid, kThreads, smem, st>>>(ta, tb, work, n_work, n_units, S, slot_row, fill_flag, H, I, h_out, w_perm,
+                                       pair_out, ws, cnt, status, fill_wait_ns);
     return cudaGetLastError();
 }
 
@@ -405,17 +439,19 @@ int decode_choose_split(int n_tiles, bool gateup, int H, int I, int num_sms) {
 }
 
 cudaError_t launch_decode_gateup(const DecodeMaps& m, const GemvWork* work, int n_work, int n_units, int S,
-                                 const int32_t* slot_row, int H, int I, uint16_t* h_perm, float* ws, int* cnt,
-                                 int* status, int num_sms, cudaStream_t st) {
-    return launch<true>(m.a_gu, m.b_x, work, n_work, n_units, S, slot_row, H, I, h_perm, nullptr, nullptr, ws, cnt,
-                        status, num_sms, st);
+                                 const int32_t* slot_row, const uint32_t* fill_flag, int H, int I, uint16_t* h_perm,
+                                 float* ws, int* cnt, int* status, uint64_t fill_wait_ns, int num_sms,
+                                 cudaStream_t st) {
+    return launch<true>(m.a_gu, m.b_x, work, n_work, n_units, S, slot_row, fill_flag, H, I, h_perm, nullptr, nullptr,
+                        ws, cnt, status, fill_wait_ns, num_sms, st);
 }
 
 cudaError_t launch_decode_down(const DecodeMaps& m, const GemvWork* work, int n_work, int n_units, int S,
-                               const int32_t* slot_row, int H, int I, const float* w_perm, float* pair_out, float* ws,
-                               int* cnt, int* status, int num_sms, cudaStream_t st) {
-    return launch<false>(m.a_d, m.b_h, work, n_work, n_units, S, slot_row, H, I, nullptr, w_perm, pair_out, ws, cnt,
-                         status, num_sms, st);
+                               const int32_t* slot_row, const uint32_t* fill_flag, int H, int I, const float* w_perm,
+                               float* pair_out, float* ws, int* cnt, int* status, uint64_t fill_wait_ns, int num_sms,
+                               cudaStream_t st) {
+    return launch<false>(m.a_d, m.b_h, work, n_work, n_units, S, slot_row, fill_flag, H, I, nullptr, w_perm, pair_out,
+                         ws, cnt, status, fill_wait_ns, num_sms, st);
 }
 
 }  // namespace moe

@@ -29,6 +29,9 @@ struct GemvWork {
     int tok_off;     // first permuted position of its tokens
     int n_tok;       // tokens routed to it
     int unit_begin;  // first work unit of this expert (entry n_work holds the total)
+    int wait_slot;   // slot whose fill flag must reach `gen` before its weights are read, or -1
+    uint32_t gen;    // fill generation of that slot (written by the copy stream after the copy)
+    int pad0, pad1;
 };
 
 // --- decode expert FFN on the tensor cores (weights as M = 128, tokens as N <= 64) ---
@@ -48,13 +51,16 @@ int decode_token_chunks(int n_tok);                // chunks of <= 64 tokens
 int decode_choose_split(int n_tiles, bool gateup, int H, int I, int num_sms);  // K split S of a launch
 // h_perm[pos, i] = bf16( silu(W_gate[i] . x) * (W_up[i] . x) ) for the wave's experts.
 // work[a].unit_begin counts units = chunks * row tiles * S per entry (entry n_work: total).
+// fill_flag[slot] is the device word the copy stream bumps after each fill of the slot.
 cudaError_t launch_decode_gateup(const DecodeMaps& maps, const GemvWork* work, int n_work, int n_units, int S,
-                                 const int32_t* slot_row, int H, int I, uint16_t* h_perm, float* ws, int* cnt,
-                                 int* status, int num_sms, cudaStream_t st);
+                                 const int32_t* slot_row, const uint32_t* fill_flag, int H, int I, uint16_t* h_perm,
+                                 float* ws, int* cnt, int* status, uint64_t fill_wait_ns, int num_sms,
+                                 cudaStream_t st);
 // pair_out[pos, n] = w_perm[pos] * (W_down[n] . h[pos])
 cudaError_t launch_decode_down(const DecodeMaps& maps, const GemvWork* work, int n_work, int n_units, int S,
-                               const int32_t* slot_row, int H, int I, const float* w_perm, float* pair_out, float* ws,
-                               int* cnt, int* status, int num_sms, cudaStream_t st);
+                               const int32_t* slot_row, const uint32_t* fill_flag, int H, int I, const float* w_perm,
+                               float* pair_out, float* ws, int* cnt, int* status, uint64_t fill_wait_ns, int num_sms,
+                               cudaStream_t st);
 
 // --- combine: out[t] = resid[t] + sum_j pair_out[inv_perm[t*k+j]] (j order) ---
 cudaError_t launch_combine(const float* pair_out, const int32_t* inv_perm, const float* resid, float* out, int T,

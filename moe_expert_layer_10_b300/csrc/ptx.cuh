@@ -15,6 +15,7 @@ enum : int {
     kDevBadForcedSet = 2,  // forced routing set with a repeated / out-of-range id
     kDevBadSlot = 3,       // slot table held -1 for an expert being computed
     kDevBadIndex = 4,      // a routed expert id outside [0, E)
+    kDevFillTimeout = 5,   // a fill flag did not reach its generation before the deadline
 };
 
 // Deadline for any single spin-wait inside a kernel (nanoseconds of %globaltimer).
@@ -69,14 +70,36 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 
 // Wait until the phase with the given parity has completed, or until the deadline.
 // Returns false on timeout (the caller raises the status and stops).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t deadline_ns = kWaitDeadlineNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (;;) {
         for (int i = 0; i < 64; ++i)
             if (mbar_try_wait(bar, parity)) return true;
-        if (globaltimer_ns() - t0 > kWaitDeadlineNs) return false;
+        if (globaltimer_ns() - t0 > deadline_ns) return false;
     }
+}
+
+// Wait until the fill flag of a slot has reached generation `gen` (wrap-safe compare), then
+// order the following TMA (async-proxy) reads of the slot after the observed copy. Returns
+// false after deadline_ns.
+__device__ __forceinline__ bool wait_fill_flag(const uint32_t* flag, uint32_t gen, uint64_t deadline_ns) {
+    auto reached = [&]() {
+        uint32_t v;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+        return static_cast<int32_t>(v - gen) >= 0;
+    };
+    bool ok = reached();
+    if (!ok) {
+        const uint64_t t0 = globaltimer_ns();
+        for (;;) {
+            __nanosleep(200);
+            if ((ok = reached())) break;
+            if (globaltimer_ns() - t0 > deadline_ns) return false;
+        }
+    }
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    return true;
 }
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {

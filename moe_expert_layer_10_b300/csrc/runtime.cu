@@ -55,7 +55,11 @@ int fail(int code, const char* fmt, ...) {
 
 constexpr int kEvRing = 256;     // compute-wave and fill-batch events
 constexpr int kStageRing = 16;   // pinned staging buffers for small H2D copies
+constexpr uint64_t kFillWaitNs = 20000000000ull;  // 20 s: a wave's own fills must land by then
+constexpr uint64_t kInjectedFillWaitNs = 200000000ull;  // 0.2 s under injection kind 3
 constexpr int kDecodeMaxTokens = 64;  // AUTO path: tensor-core decode kernels up to this many tokens per expert
+// work-list entries of one wave: a gate/up and a down list, each closed by a total entry
+constexpr size_t kWorkEntries(int E) { return 2 * (static_cast<size_t>(E) + 1); }
 
 enum KernelId { kRouterLogits, kRouterTopk, kPermute, kGather, kDecodeGateUp, kDecodeDown, kGemmGateUp, kGemmDown,
                 kCombine, kNumKernels };
@@ -76,6 +80,23 @@ EncodeTiledFn encode_fn() {
                 cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
             fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+typedef CUresult (*WriteValue32Fn)(CUstream, CUdeviceptr, cuuint32_t, unsigned int);
+
+// cuStreamWriteValue32: a stream memory operation that writes a 32-bit word in stream order
+// (with a memory barrier before the write, so the stream's earlier copies are visible first).
+WriteValue32Fn write_value_fn() {
+    static WriteValue32Fn fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuStreamWriteValue32", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<WriteValue32Fn>(p);
     }
     return fn;
 }
@@ -144,7 +165,7 @@ struct moe_ctx {
     int32_t* idx_host = nullptr;   // [Pmax]
     int* status_host = nullptr;    // [1]
     int32_t* table_stage = nullptr;        // [kStageRing][L*E]
-    GemvWork* work_stage = nullptr;        // [kStageRing][E+1]
+    GemvWork* work_stage = nullptr;        // [kStageRing][kWorkEntries(E)]
     cudaEvent_t stage_ev[kStageRing] = {};
     int stage_next = 0;
     cudaEvent_t ev_d2h = nullptr;
@@ -153,6 +174,10 @@ struct moe_ctx {
     cudaEvent_t comp_ev[kEvRing] = {}, fill_ev[kEvRing] = {};
     int64_t comp_seq = -1, fill_seq = -1;
     std::vector<int64_t> slot_last_use, slot_fill;
+    // per-slot fill generation: the copy stream writes fill_gen[slot] to fill_flag[slot] after
+    // each fill, and the decode kernels poll it before streaming a freshly filled slot
+    uint32_t* fill_flag = nullptr;     // device [C]
+    std::vector<uint32_t> fill_gen;    // host [C], the generation of the last enqueued fill
 
     moe::DecodeMaps dec_maps{};
     float* dec_ws = nullptr;  // split-K partial tiles of the decode kernels
@@ -168,6 +193,7 @@ struct moe_ctx {
     moe_kernel_stat_t kstats[kNumKernels] = {};
 
     int inject_kind = 0, inject_count = 0;
+    uint64_t fill_wait_ns = kFillWaitNs;  // device-side deadline of a wait for a fill
 };
 
 namespace {
@@ -269,7 +295,7 @@ int check_status(moe_ctx* c) {
         // a kernel that stopped early may have left split-K arrival counters behind
         cudaMemsetAsync(c->dec_cnt, 0, moe::kDecodeSplitUnits * sizeof(int), c->s_comp);
         return fail(MOE_E_DEVICE, "a kernel raised device status %d (1 wait timeout, 2 bad forced set, 3 bad slot, "
-                                  "4 bad expert index)", code);
+                                  "4 bad expert index, 5 fill wait timeout)", code);
     }
     return MOE_OK;
 }
@@ -346,6 +372,15 @@ int access_keys(moe_ctx* c, const std::vector<int>& keys, bool prefetch) {
                           cudaGetErrorString(e));
                 break;
             }
+            const uint32_t gen = c->fill_gen[p.slot] + 1;
+            const CUresult r = write_value_fn()(reinterpret_cast<CUstream>(c->s_copy),
+                                                reinterpret_cast<CUdeviceptr>(c->fill_flag + p.slot), gen, 0);
+            if (r != CUDA_SUCCESS) {
+                rc = fail(MOE_E_CUDA, "fill flag write for layer %d expert %d: driver error %d", key / c->E,
+                          key % c->E, static_cast<int>(r));
+                break;
+            }
+            c->fill_gen[p.slot] = gen;
         }
         c->lru.commit(p);
         record_event(c, p.kind, key, p.slot, p.victim);
@@ -362,20 +397,24 @@ int access_keys(moe_ctx* c, const std::vector<int>& keys, bool prefetch) {
                 c->slot_host[p.victim] = -1;
             }
             c->slot_host[key] = p.slot;
-            c->slot_fill[p.slot] = c->fill_seq + 1;  // the batch event recorded below
+            // each fill gets its own completion event, so compute can start on the entries
+            // that have landed while later copies are still crossing the link
+            c->fill_seq++;
+            c->slot_fill[p.slot] = c->fill_seq;
             c->table_dirty = true;
+            cudaError_t e = cudaEventRecord(c->fill_ev[c->fill_seq % kEvRing], c->s_copy);
+            if (e != cudaSuccess) {
+                rc = fail(MOE_E_CUDA, "fill event: %s", cudaGetErrorString(e));
+                break;
+            }
         }
     }
     if (batch_open) {
-        c->fill_seq++;
-        cudaError_t e = cudaEventRecord(c->fill_ev[c->fill_seq % kEvRing], c->s_copy);
         fr.stop = pool_event(c);
         if (fr.start && fr.stop) {
             cudaEventRecord(fr.stop, c->s_copy);
             c->fill_pending.push_back(fr);
         }
-        if (e != cudaSuccess && rc == MOE_OK)
-            rc = fail(MOE_E_CUDA, "fill batch event: %s", cudaGetErrorString(e));
     }
     return rc;
 }
@@ -408,7 +447,7 @@ void free_all(moe_ctx* c) {
     if (c->ev_d2h) cudaEventDestroy(c->ev_d2h);
     void* dev_ptrs[] = {c->arena, c->slot_dev, c->logits, c->offsets, c->perm, c->inv_perm, c->active,
                         c->n_active, c->w_perm, c->pair_out, c->x_perm, c->h_perm, c->status, c->work_dev,
-                        c->dec_ws,   c->dec_cnt};
+                        c->dec_ws,   c->dec_cnt, c->fill_flag};
     for (void* p : dev_ptrs)
         if (p) cudaFree(p);
     void* host_ptrs[] = {c->pool, c->idx_host, c->status_host, c->table_stage, c->work_stage};
@@ -452,6 +491,7 @@ int moe_cache_init(const moe_config_t* cfg, void* stream_compute, void* stream_c
         static_cast<uint64_t>(f.capacity) * 3ull * f.hidden >= (1ull << 31) || keys >= (1ull << 31))
         return fail(MOE_E_INVAL, "arena too large for 32-bit row coordinates");
     if (!encode_fn()) return fail(MOE_E_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    if (!write_value_fn()) return fail(MOE_E_CUDA, "cuStreamWriteValue32 is not available from the driver");
 
     moe_ctx* c = new moe_ctx();
     c->cfg = f;
@@ -469,6 +509,7 @@ int moe_cache_init(const moe_config_t* cfg, void* stream_compute, void* stream_c
     c->slot_host.assign(keys, -1);
     c->slot_last_use.assign(c->C, -1);
     c->slot_fill.assign(c->C, -1);
+    c->fill_gen.assign(c->C, 0);
     if (f.flags & MOE_TRACE) c->trace.resize(f.trace_capacity ? f.trace_capacity : (1u << 20));
 
 #define INIT_TRY(call)                                                                          \
@@ -514,9 +555,11 @@ int moe_cache_init(const moe_config_t* cfg, void* stream_compute, void* stream_c
     INIT_TRY(cudaMalloc(&c->h_perm, static_cast<size_t>(c->Pmax) * c->I * 2));
     INIT_TRY(cudaMalloc(&c->pair_out, static_cast<size_t>(c->Pmax) * c->H * sizeof(float)));
     INIT_TRY(cudaMalloc(&c->status, sizeof(int)));
-    INIT_TRY(cudaMalloc(&c->work_dev, 2 * (c->E + 1) * sizeof(GemvWork)));
+    INIT_TRY(cudaMalloc(&c->work_dev, kWorkEntries(c->E) * sizeof(GemvWork)));
     INIT_TRY(cudaMalloc(&c->dec_ws, static_cast<size_t>(moe::kDecodeSplitUnits) * moe::kDecodeTileFloats * sizeof(float)));
     INIT_TRY(cudaMalloc(&c->dec_cnt, moe::kDecodeSplitUnits * sizeof(int)));
+    INIT_TRY(cudaMalloc(&c->fill_flag, static_cast<size_t>(c->C) * sizeof(uint32_t)));
+    INIT_TRY(cudaMemset(c->fill_flag, 0, static_cast<size_t>(c->C) * sizeof(uint32_t)));
     INIT_TRY(cudaMemset(c->dec_cnt, 0, moe::kDecodeSplitUnits * sizeof(int)));
     INIT_TRY(cudaMemset(c->status, 0, sizeof(int)));
     INIT_TRY(cudaMemset(c->x_perm, 0, static_cast<size_t>(c->Pmax) * c->H * 2));
@@ -526,7 +569,7 @@ int moe_cache_init(const moe_config_t* cfg, void* stream_compute, void* stream_c
     *c->status_host = 0;
     INIT_TRY(cudaHostAlloc(reinterpret_cast<void**>(&c->table_stage), kStageRing * keys * sizeof(int32_t), 0));
     INIT_TRY(cudaHostAlloc(reinterpret_cast<void**>(&c->work_stage),
-                           static_cast<size_t>(kStageRing) * 2 * (c->E + 1) * sizeof(GemvWork), 0));
+                           static_cast<size_t>(kStageRing) * kWorkEntries(c->E) * sizeof(GemvWork), 0));
     for (int i = 0; i < kStageRing; ++i) {
         INIT_TRY(cudaEventCreateWithFlags(&c->stage_ev[i], cudaEventDisableTiming));
         INIT_TRY(cudaEventRecord(c->stage_ev[i], c->s_comp));
@@ -582,6 +625,13 @@ int moe_set_path(moe_ctx* c, int path) {
     return MOE_OK;
 }
 
+int moe_set_profile(moe_ctx* c, int on) {
+    if (!c) return fail(MOE_E_INVAL, "null context");
+    if (on) c->cfg.flags |= MOE_PROFILE;
+    else c->cfg.flags &= ~MOE_PROFILE;
+    return MOE_OK;
+}
+
 int moe_resident_slot(moe_ctx* c, int layer, int expert) {
     if (!c || layer < 0 || layer >= c->L || expert < 0 || expert >= c->E) return -1;
     return c->lru.slot_of(layer * c->E + expert);
@@ -589,7 +639,7 @@ int moe_resident_slot(moe_ctx* c, int layer, int expert) {
 
 int moe_debug_inject(moe_ctx* c, int kind, int count) {
     if (!c) return fail(MOE_E_INVAL, "null context");
-    if (kind < 0 || kind > 2 || count < 0) return fail(MOE_E_INVAL, "bad injection");
+    if (kind < 0 || kind > 3 || count < 0) return fail(MOE_E_INVAL, "bad injection");
     c->inject_kind = kind;
     c->inject_count = kind ? count : 0;
     return MOE_OK;
@@ -713,16 +763,17 @@ int moe_layer_forward(moe_ctx* c, int layer, const void* x, const float* resid, 
         const int a1 = std::min(U, a0 + c->C);
         std::vector<int> keys;
         for (int a = a0; a < a1; ++a) keys.push_back(layer * E + distinct[a]);
+        const int64_t seq_before = c->fill_seq;
         rc = access_keys(c, keys, false);
         if (rc) return rc;
         rc = upload_table(c);
         if (rc) return rc;
-        int64_t need_fill = -1;
-        for (int a = a0; a < a1; ++a) need_fill = std::max(need_fill, c->slot_fill[c->lru.slot_of(keys[a - a0])]);
-        if (need_fill >= 0) CUDA_TRY(cudaStreamWaitEvent(c->s_comp, c->fill_ev[need_fill % kEvRing], 0));
 
         const int32_t* slot_row = c->slot_dev + static_cast<size_t>(layer) * E;
         if (path == MOE_PATH_GEMM) {
+            int64_t need_fill = -1;
+            for (int key : keys) need_fill = std::max(need_fill, c->slot_fill[c->lru.slot_of(key)]);
+            if (need_fill >= 0) CUDA_TRY(cudaStreamWaitEvent(c->s_comp, c->fill_ev[need_fill % kEvRing], 0));
             std::vector<int> wc;
             int pw = 0;
             for (int a = a0; a < a1; ++a) {
@@ -750,8 +801,32 @@ int moe_layer_forward(moe_ctx* c, int layer, const void* x, const float* resid, 
             continue;
         }
 
-        // work lists for this wave: one entry per expert, units = token chunks x row tiles x
-        // K splits (the split of each kernel is chosen so its units fill the SMs evenly)
+        // One launch per kernel for the whole wave. The work list holds the resident experts
+        // first and then the ones this wave filled, in fill order; those carry their slot and
+        // fill generation, and the kernel waits on the slot's fill flag before streaming them.
+        // So resident experts compute while the copies cross the link, and each filled expert
+        // starts as soon as its own copy has landed. Fills enqueued before this wave (a
+        // prefetch still in flight) are waited for here, on the stream. Each expert writes only
+        // its own pair_out rows, and every unit is computed the same way whatever the order, so
+        // results do not depend on which entries had to be filled.
+        bool inject_wave = false;
+        std::vector<int> order;          // indices a into distinct[]: hits, then misses
+        std::vector<char> filled_now(a1 - a0, 0);
+        int64_t older_fill = -1;
+        for (int a = a0; a < a1; ++a) {
+            const int64_t f = c->slot_fill[c->lru.slot_of(keys[a - a0])];
+            if (f > seq_before) filled_now[a - a0] = 1;
+            else older_fill = std::max(older_fill, f);
+        }
+        for (int a = a0; a < a1; ++a)
+            if (!filled_now[a - a0]) order.push_back(a);
+        for (int a = a0; a < a1; ++a)
+            if (filled_now[a - a0]) order.push_back(a);
+        if (older_fill >= 0) CUDA_TRY(cudaStreamWaitEvent(c->s_comp, c->fill_ev[older_fill % kEvRing], 0));
+
+        // Work lists (gate/up, then down), each closed by an entry holding the unit total.
+        // Units are token chunks x row tiles x K splits; the split of each kernel fills the SMs
+        // evenly and depends only on the wave's routed set.
         int pw = 0, chunks = 0;
         for (int a = a0; a < a1; ++a) {
             pw += count[distinct[a]];
@@ -764,32 +839,43 @@ int moe_layer_forward(moe_ctx* c, int layer, const void* x, const float* resid, 
         int s;
         rc = next_stage(c, &s);
         if (rc) return rc;
-        GemvWork* wk = c->work_stage + static_cast<size_t>(s) * 2 * (E + 1);
+        GemvWork* wk = c->work_stage + static_cast<size_t>(s) * kWorkEntries(E);
         GemvWork* wk2 = wk + (E + 1);
         int units_gu = 0, units_d = 0;
-        for (int a = a0; a < a1; ++a) {
+        for (int i = 0; i < nw; ++i) {
+            const int a = order[i];
             const int e = distinct[a];
             const int ch = moe::decode_token_chunks(count[e]);
-            wk[a - a0] = GemvWork{e, offs[e], count[e], units_gu};
-            wk2[a - a0] = GemvWork{e, offs[e], count[e], units_d};
+            const int slot = c->lru.slot_of(keys[a - a0]);
+            const int wait_slot = filled_now[a - a0] ? slot : -1;
+            uint32_t gen = c->fill_gen[slot];
+            if (wait_slot >= 0 && c->inject_kind == 3 && c->inject_count > 0) {
+                gen += 1000;  // injected: a generation the copy stream will not write for a long time
+                inject_wave = true;
+            }
+            wk[i] = GemvWork{e, offs[e], count[e], units_gu, wait_slot, gen, 0, 0};
+            wk2[i] = GemvWork{e, offs[e], count[e], units_d, wait_slot, gen, 0, 0};
             units_gu += ch * Rg * Sg;
             units_d += ch * Rd * Sd;
         }
-        wk[nw] = GemvWork{-1, 0, 0, units_gu};
-        wk2[nw] = GemvWork{-1, 0, 0, units_d};
+        const uint64_t fill_wait_ns = inject_wave ? kInjectedFillWaitNs : c->fill_wait_ns;
+        if (inject_wave) c->inject_count--;
+        wk[nw] = GemvWork{-1, 0, 0, units_gu, -1, 0, 0, 0};
+        wk2[nw] = GemvWork{-1, 0, 0, units_d, -1, 0, 0, 0};
         // both lists in one copy: gate/up at work_dev, down at work_dev + E + 1
         CUDA_TRY(cudaMemcpyAsync(c->work_dev, wk, 2 * (E + 1) * sizeof(GemvWork), cudaMemcpyHostToDevice, c->s_comp));
         CUDA_TRY(cudaEventRecord(c->stage_ev[s], c->s_comp));
         {
             ProfScope ps(c, kDecodeGateUp, 4.0 * nw * I * H + 2.0 * pw * H + 2.0 * pw * I, 4.0 * pw * I * H);
-            CUDA_TRY(moe::launch_decode_gateup(c->dec_maps, c->work_dev, nw, units_gu, Sg, slot_row, H, I, c->h_perm,
-                                               c->dec_ws, c->dec_cnt, c->status, c->num_sms, c->s_comp));
+            CUDA_TRY(moe::launch_decode_gateup(c->dec_maps, c->work_dev, nw, units_gu, Sg, slot_row, c->fill_flag, H,
+                                               I, c->h_perm, c->dec_ws, c->dec_cnt, c->status, fill_wait_ns,
+                                               c->num_sms, c->s_comp));
         }
         {
             ProfScope ps(c, kDecodeDown, 2.0 * nw * H * I + 2.0 * pw * I + 4.0 * pw * H + 4.0 * pw, 2.0 * pw * I * H);
-            CUDA_TRY(moe::launch_decode_down(c->dec_maps, c->work_dev + (E + 1), nw, units_d, Sd, slot_row, H, I,
-                                             c->w_perm, c->pair_out, c->dec_ws, c->dec_cnt, c->status, c->num_sms,
-                                             c->s_comp));
+            CUDA_TRY(moe::launch_decode_down(c->dec_maps, c->work_dev + (E + 1), nw, units_d, Sd, slot_row,
+                                             c->fill_flag, H, I, c->w_perm, c->pair_out, c->dec_ws, c->dec_cnt,
+                                             c->status, fill_wait_ns, c->num_sms, c->s_comp));
         }
         c->comp_seq++;
         CUDA_TRY(cudaEventRecord(c->comp_ev[c->comp_seq % kEvRing], c->s_comp));

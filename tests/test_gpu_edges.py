@@ -133,3 +133,23 @@ def test_deterministic_outputs():
         o1 = _layer(c, x, 8)[2]
         o2 = _layer(c, x, 8)[2]
     assert np.array_equal(o1.view(np.uint32), o2.view(np.uint32))
+
+
+def test_device_fill_wait_deadline_reports_and_recovers():
+    """A decode wave whose kernels wait for a fill generation that is never written (injected
+    on the host) gives up after its device-side deadline, raises the device status, and
+    leaves the context usable: the next forward matches the oracle."""
+    ents = hz.OracleEntries(W)
+    with hz.make_cache(W, max_tokens=8) as c:
+        x = mi.activations(0, 5, 8, W.H)
+        c.debug_inject(3, 1)
+        with pytest.raises(moe.MoeError) as e:
+            _layer(c, x, 8)  # 8 tokens top-2 over 16 experts with 4 empty slots: fills happen
+        assert e.value.code == moe.MOE_E_DEVICE
+        assert "5" in str(e.value)
+        x2 = mi.activations(0, 6, 8, W.H)
+        idx, w, out, resid, Wr, b = _layer(c, x2, 8)
+        idx_o, w_o, _, _ = oracle.route(x2, Wr, b, W.k)
+        assert np.array_equal(idx, idx_o)
+        ref = oracle.moe_layer([ents(0, e_) for e_ in range(W.E)], W.H, W.I, x2, resid, idx_o, w_o)
+        hz.assert_out_close(out, ref, resid)
