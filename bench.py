@@ -136,6 +136,14 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------- workload
+def fill_pool(cache, W, L: int, E: int):
+    """Seeded entries into the context's pinned pool, generated on the GPU (the same bits as
+    the CPU generator that the oracle uses)."""
+    import moe_inputs as mi
+    keys = [(l, e) for l in range(L) for e in range(E)]
+    mi.gpu_fill_entries(W.seed, keys, W.H, W.I, [cache.host_entry(l, e) for l, e in keys])
+
+
 def workload():
     import moe_inputs as mi
     return mi.WORKLOADS["decode"]
@@ -209,8 +217,7 @@ def run_b300(args, rank, world, local):
     C = args.capacity or W.C
     # per-launch event timing stays off in the timed regions; a separate pass profiles
     cache = moe.MoeCache(moe.LayerShape(1, W.E, W.H, W.I, W.k, C, max(BATCHES)), flags=0, stream_compute=stream)
-    for e in range(W.E):
-        mi.fill_entry_at(cache.host_entry(0, e), W.seed, 0, e, W.H, W.I)
+    fill_pool(cache, W, 1, W.E)
     Wr_h = mi.router_weights(W.seed, 0, W.E, W.H)
     b_h, _ = mi.router_bias(W.seed, 0, W.E, W.zipf_s)
     Wr = torch.from_numpy(Wr_h).cuda()
@@ -394,8 +401,7 @@ def resident_context(args, W, E=None):
     E = E or args.prefill_experts or W.E
     stream = torch.cuda.Stream()
     cache = moe.MoeCache(moe.LayerShape(1, E, W.H, W.I, W.k, E, T), flags=0, stream_compute=stream)
-    for e in range(E):
-        mi.fill_entry_at(cache.host_entry(0, e), W.seed, 0, e, W.H, W.I)
+    fill_pool(cache, W, 1, E)
     cache.cache_fill(0, None, moe.MOE_FILL_FULL_LAYER)
     cache.sync()
     return {"cache": cache, "stream": stream, "E": E, "T": T}

@@ -28,12 +28,46 @@ _SRC = os.path.join(_HERE, "gen.c")
 KIND_EXPERT, KIND_ROUTER, KIND_X, KIND_PERM, KIND_TRACE = 1, 2, 3, 4, 5
 
 
+_CORE = os.path.join(_HERE, "normal_core.h")
+_SO_FMA = os.path.join(_HERE, "libmoe_inputs_fma.so")
+
+
+def _cpu_has_fma() -> bool:
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("flags"):
+                    return " fma " in line + " "
+    except OSError:
+        pass
+    return False
+_GPU_SRC = os.path.join(_HERE, "gen_gpu.cu")
+_GPU_SO = os.path.join(_HERE, "libmoe_inputs_gpu.so")
+_NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
+
+
+def _stale(out: str, *srcs: str) -> bool:
+    return not os.path.exists(out) or os.path.getmtime(out) < max(os.path.getmtime(s) for s in srcs)
+
+
 def build(force: bool = False) -> str:
-    """Compile gen.c into libmoe_inputs.so next to it (gcc, OpenMP)."""
-    if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(_SRC):
-        tmp = _SO + f".tmp{os.getpid()}"
-        subprocess.check_call(["gcc", "-O2", "-fopenmp", "-shared", "-fPIC", "-std=c11", _SRC, "-o", tmp, "-lm"])
-        os.replace(tmp, _SO)
+    """Compile gen.c into libmoe_inputs.so (gcc, OpenMP) and gen_gpu.cu into
+    libmoe_inputs_gpu.so (nvcc, sm_103a) next to them. Neither build contracts a*b+c."""
+    # two CPU builds: one that calls fma() from libm, and one that uses the FMA instruction
+    # (loaded only on CPUs that have it); fused multiply-add rounds once either way, so the
+    # bits are the same
+    for so, extra in ((_SO, []), (_SO_FMA, ["-mfma"])):
+        if force or _stale(so, _SRC, _CORE):
+            tmp = so + f".tmp{os.getpid()}"
+            subprocess.check_call(["gcc", "-O2", "-ffp-contract=off", "-fopenmp", "-shared", "-fPIC", "-std=c11"] +
+                                  extra + [_SRC, "-o", tmp, "-lm"])
+            os.replace(tmp, so)
+    if os.path.exists(_NVCC) and (force or _stale(_GPU_SO, _GPU_SRC, _CORE)):
+        tmp = _GPU_SO + f".tmp{os.getpid()}"
+        subprocess.check_call([_NVCC, "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-fmad=false",
+                               "-std=c++17", "-shared", "-Xcompiler", "-fPIC", "-Xcompiler", "-ffp-contract=off",
+                               "-cudart", "shared", _GPU_SRC, "-o", tmp])
+        os.replace(tmp, _GPU_SO)
     return _SO
 
 
@@ -44,7 +78,7 @@ def lib():
     global _lib
     if _lib is None:
         build()
-        L = ctypes.CDLL(_SO)
+        L = ctypes.CDLL(_SO_FMA if _cpu_has_fma() else _SO)
         u64, i32, dbl, vp = ctypes.c_uint64, ctypes.c_int, ctypes.c_double, ctypes.c_void_p
         L.mi_philox4x32_10.argtypes = [vp, vp, vp]
         L.mi_normal_bf16.argtypes = [u64, u64, u64, u64, dbl, vp]
@@ -55,8 +89,38 @@ def lib():
         L.mi_trace_reuse.restype = i32
         L.mi_f32_to_bf16.argtypes = [ctypes.c_float]
         L.mi_f32_to_bf16.restype = ctypes.c_uint16
+        L.mi_log_unit.argtypes = [dbl]
+        L.mi_log_unit.restype = dbl
+        L.mi_sincos_2pi.argtypes = [dbl, vp, vp]
         _lib = L
     return _lib
+
+
+_gpu_lib = None
+
+
+def gpu_lib():
+    """The GPU build of the generator (needs a CUDA device at call time)."""
+    global _gpu_lib
+    if _gpu_lib is None:
+        build()
+        L = ctypes.CDLL(_GPU_SO)
+        L.mi_gpu_normal_bf16_to_host.argtypes = [ctypes.c_uint64, ctypes.c_int, ctypes.c_void_p, ctypes.c_uint64,
+                                                 ctypes.c_double, ctypes.c_void_p, ctypes.c_char_p, ctypes.c_int]
+        _gpu_lib = L
+    return _gpu_lib
+
+
+def log_unit(x: float) -> float:
+    """The generator's own series logarithm (the one its normal transform uses)."""
+    return float(lib().mi_log_unit(float(x)))
+
+
+def sincos_turn(u: float):
+    """(sin, cos) of 2*pi*u by the generator's own series (u in [0, 1))."""
+    s, c = ctypes.c_double(), ctypes.c_double()
+    lib().mi_sincos_2pi(float(u), ctypes.byref(s), ctypes.byref(c))
+    return s.value, c.value
 
 
 def stream_id(kind: int, a: int = 0, b: int = 0) -> int:
@@ -114,6 +178,20 @@ def expert_entry(seed: int, layer: int, expert: int, H: int, I: int) -> np.ndarr
 def fill_entry_at(ptr: int, seed: int, layer: int, expert: int, H: int, I: int) -> None:
     """Write entry (layer, expert) straight into host memory at `ptr` (3*H*I bf16)."""
     lib().mi_normal_bf16(seed, stream_id(KIND_EXPERT, layer, expert), 0, 3 * H * I, 0.02, ptr)
+
+
+def gpu_fill_entries(seed: int, keys, H: int, I: int, ptrs) -> None:
+    """Write entries keys[i] = (layer, expert) into host memory at ptrs[i] using the GPU build
+    of this generator (same bits as fill_entry_at; the current CUDA device does the work)."""
+    keys = list(keys)
+    if not keys:
+        return
+    streams = (ctypes.c_uint64 * len(keys))(*[stream_id(KIND_EXPERT, l, e) for l, e in keys])
+    dsts = (ctypes.c_void_p * len(keys))(*[int(p) for p in ptrs])
+    err = ctypes.create_string_buffer(256)
+    rc = gpu_lib().mi_gpu_normal_bf16_to_host(seed, len(keys), streams, 3 * H * I, 0.02, dsts, err, 256)
+    if rc != 0:
+        raise RuntimeError("GPU input generator: " + err.value.decode(errors="replace"))
 
 
 def router_weights(seed: int, layer: int, E: int, H: int) -> np.ndarray:

@@ -9,74 +9,32 @@
  * Dror and Shaw, "Parallel random numbers: as easy as 1, 2, 3" (SC'11),
  * written here from its published definition. Each 64-bit "stream" names one
  * tensor. Element i of a stream takes word i%4 of the block with counter
- * (i/4, stream). Normals use the Box-Muller transform on pairs of words.
+ * (i/4, stream). Normals use the Box-Muller transform on pairs of words; the
+ * arithmetic core lives in normal_core.h, shared with the GPU build gen_gpu.cu
+ * so both give the same bits.
  */
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
 
-#define PHILOX_M0 0xD2511F53u
-#define PHILOX_M1 0xCD9E8D57u
-#define PHILOX_W0 0x9E3779B9u
-#define PHILOX_W1 0xBB67AE85u
+#include "normal_core.h"
 
-static inline void philox_round(uint32_t c[4], const uint32_t k[2]) {
-    uint64_t p0 = (uint64_t)PHILOX_M0 * c[0];
-    uint64_t p1 = (uint64_t)PHILOX_M1 * c[2];
-    uint32_t hi0 = (uint32_t)(p0 >> 32), lo0 = (uint32_t)p0;
-    uint32_t hi1 = (uint32_t)(p1 >> 32), lo1 = (uint32_t)p1;
-    uint32_t n0 = hi1 ^ c[1] ^ k[0];
-    uint32_t n2 = hi0 ^ c[3] ^ k[1];
-    c[0] = n0;
-    c[1] = lo1;
-    c[2] = n2;
-    c[3] = lo0;
-}
-
-void mi_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]) {
-    uint32_t c[4] = {ctr[0], ctr[1], ctr[2], ctr[3]};
-    uint32_t k[2] = {key[0], key[1]};
-    for (int r = 0; r < 10; ++r) {
-        if (r > 0) {
-            k[0] += PHILOX_W0;
-            k[1] += PHILOX_W1;
-        }
-        philox_round(c, k);
-    }
-    memcpy(out, c, sizeof(c));
-}
+void mi_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]) { mi_philox_10(ctr, key, out); }
 
 static inline void block_of(uint64_t seed, uint64_t stream, uint64_t q, uint32_t out[4]) {
-    uint32_t ctr[4] = {(uint32_t)q, (uint32_t)(q >> 32), (uint32_t)stream, (uint32_t)(stream >> 32)};
-    uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
-    mi_philox4x32_10(ctr, key, out);
+    mi_block(seed, stream, q, out);
 }
 
-/* (0,1): the word plus one half, scaled by 2^-32 */
-static inline double unit_open(uint32_t r) { return ((double)r + 0.5) * (1.0 / 4294967296.0); }
-
-/* four standard normals from one Philox block (two Box-Muller pairs) */
 static inline void normals4(uint64_t seed, uint64_t stream, uint64_t q, double z[4]) {
-    uint32_t r[4];
-    block_of(seed, stream, q, r);
-    const double two_pi = 6.283185307179586476925286766559;
-    for (int h = 0; h < 2; ++h) {
-        double u1 = unit_open(r[2 * h]), u2 = unit_open(r[2 * h + 1]);
-        double rad = sqrt(-2.0 * log(u1));
-        z[2 * h] = rad * cos(two_pi * u2);
-        z[2 * h + 1] = rad * sin(two_pi * u2);
-    }
+    mi_normals4(seed, stream, q, z);
 }
 
-/* fp32 -> bf16 bits, round to nearest even; NaN maps to a quiet NaN */
-static inline uint16_t f32_to_bf16_rne(float f) {
-    uint32_t u;
-    memcpy(&u, &f, 4);
-    if ((u & 0x7f800000u) == 0x7f800000u && (u & 0x007fffffu)) return 0x7fc0;
-    u += 0x7fffu + ((u >> 16) & 1u);
-    return (uint16_t)(u >> 16);
-}
+static inline uint16_t f32_to_bf16_rne(float f) { return mi_bf16_rne(f); }
+
+/* The series logarithm and turn sine/cosine of the normal transform, for the pins. */
+double mi_log_unit(double x) { return mi_log(x); }
+void mi_sincos_2pi(double u, double* sn, double* cs) { mi_sincos_turn(u, sn, cs); }
 
 uint16_t mi_f32_to_bf16(float f) { return f32_to_bf16_rne(f); }
 
@@ -164,7 +122,7 @@ void mi_zipf_bias(uint64_t seed, uint64_t stream, int E, double s, int32_t* perm
 
 /* draw a rank from Zipf(s) by inverse CDF on a (0,1) uniform */
 static int zipf_draw(const double* cdf, int E, word_src* src) {
-    double u = unit_open(next_word(src));
+    double u = mi_unit_open(next_word(src));
     int lo = 0, hi = E - 1;
     while (lo < hi) {
         int mid = (lo + hi) / 2;

@@ -1,0 +1,70 @@
+/*
+ * GPU build of the seeded input generator: fills host buffers (normally the library's pinned
+ * expert pool) with exactly the bits gen.c produces for the same (seed, stream, element), so
+ * large pools are written at GPU speed instead of host speed. The arithmetic is the shared
+ * core in normal_core.h; this file only schedules it (one thread per Philox block of four
+ * elements) and copies the result to the host. It holds no arithmetic of the MoE method.
+ * Built with -fmad=false so that no a*b+c outside the core's explicit fma is fused.
+ */
+#include <cuda_runtime.h>
+#include <stdio.h>
+
+#include "normal_core.h"
+
+__global__ void mi_normal_bf16_kernel(uint64_t seed, uint64_t stream, uint64_t n, double stddev, uint16_t* out) {
+    const uint64_t nq = (n + 3) / 4;
+    for (uint64_t q = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; q < nq; q += (uint64_t)gridDim.x * blockDim.x) {
+        double z[4];
+        mi_normals4(seed, stream, q, z);
+        for (int w = 0; w < 4; ++w) {
+            const uint64_t i = q * 4 + w;
+            if (i < n) out[i] = mi_bf16_rne((float)(z[w] * stddev));
+        }
+    }
+}
+
+static int report(cudaError_t e, const char* what, char* err, int err_len) {
+    if (err && err_len > 0) snprintf(err, err_len, "%s: %s", what, cudaGetErrorString(e));
+    return -1;
+}
+
+/*
+ * For each i < n_streams: host_dst[i][0 .. n) = elements [0, n) of stream streams[i], each
+ * N(0, stddev) rounded to fp32 and then to bf16 -- the same bits as mi_normal_bf16 of gen.c.
+ * Runs on the current device with two device staging buffers (generation of one stream
+ * overlaps the copy-out of the previous). Returns 0, or -1 with a message in err.
+ */
+extern "C" int mi_gpu_normal_bf16_to_host(uint64_t seed, int n_streams, const uint64_t* streams, uint64_t n,
+                                          double stddev, void* const* host_dst, char* err, int err_len) {
+    if (n_streams <= 0 || n == 0) return 0;
+    uint16_t* buf[2] = {nullptr, nullptr};
+    cudaEvent_t done[2] = {nullptr, nullptr};
+    cudaStream_t st = nullptr;
+    cudaError_t e = cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking);
+    if (e != cudaSuccess) return report(e, "stream", err, err_len);
+    int rc = 0;
+    for (int b = 0; b < 2 && rc == 0; ++b) {
+        if ((e = cudaMalloc(&buf[b], n * sizeof(uint16_t))) != cudaSuccess) rc = report(e, "cudaMalloc", err, err_len);
+        else if ((e = cudaEventCreateWithFlags(&done[b], cudaEventDisableTiming)) != cudaSuccess)
+            rc = report(e, "event", err, err_len);
+        else if ((e = cudaEventRecord(done[b], st)) != cudaSuccess) rc = report(e, "event record", err, err_len);
+    }
+    const uint64_t nq = (n + 3) / 4;
+    const unsigned grid = (unsigned)((nq + 255) / 256 < 148 * 16 ? (nq + 255) / 256 : 148 * 16);
+    for (int i = 0; i < n_streams && rc == 0; ++i) {
+        const int b = i & 1;
+        // the buffer's previous copy-out must be done before it is overwritten (stream order)
+        mi_normal_bf16_kernel<<<grid, 256, 0, st>>>(seed, streams[i], n, stddev, buf[b]);
+        if ((e = cudaGetLastError()) != cudaSuccess) rc = report(e, "generator launch", err, err_len);
+        else if ((e = cudaMemcpyAsync(host_dst[i], buf[b], n * sizeof(uint16_t), cudaMemcpyDeviceToHost, st)) !=
+                 cudaSuccess)
+            rc = report(e, "copy to host", err, err_len);
+    }
+    if (rc == 0 && (e = cudaStreamSynchronize(st)) != cudaSuccess) rc = report(e, "synchronize", err, err_len);
+    for (int b = 0; b < 2; ++b) {
+        if (buf[b]) cudaFree(buf[b]);
+        if (done[b]) cudaEventDestroy(done[b]);
+    }
+    cudaStreamDestroy(st);
+    return rc;
+}

@@ -31,10 +31,15 @@ def make_cache(W: mi.Workload, max_tokens: int, L: int | None = None, capacity: 
     cache = moe.MoeCache(moe.LayerShape(L, W.E, W.H, W.I, W.k, W.C if capacity is None else capacity, max_tokens),
                          flags=flags, stream_compute=stream)
     cache.torch_stream = stream
-    for l in range(L):
-        for e in range(W.E):
-            mi.fill_entry_at(cache.host_entry(l, e), W.seed, l, e, W.H, W.I)
+    fill_pool(cache, W, L)
     return cache
+
+
+def fill_pool(cache: moe.MoeCache, W: mi.Workload, L: int):
+    """Write every seeded entry into the context's pinned pool, with the GPU build of the input
+    generator (the same bits as the CPU build, which the oracle uses for its own copy)."""
+    keys = [(l, e) for l in range(L) for e in range(W.E)]
+    mi.gpu_fill_entries(W.seed, keys, W.H, W.I, [cache.host_entry(l, e) for l, e in keys])
 
 
 class OracleEntries:

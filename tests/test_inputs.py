@@ -52,3 +52,43 @@ def test_reuse_trace_properties():
     reuse = np.mean([len(set(tr[s, l, b]) & set(tr[s - 1, l, b])) / k
                      for s in range(1, steps) for l in range(L) for b in range(B)])
     assert reuse > 0.7  # at least the forced 70% plus chance repeats of Zipf draws
+
+
+def test_series_log_matches_the_logarithm():
+    """The generator's own logarithm agrees with the exact one within a few ulps over (0, 1],
+    including the special points 1 and powers of two."""
+    import math
+    rng = np.random.default_rng(3)
+    xs = np.concatenate([rng.random(20000), np.array([2.0 ** -32, 0.5, 0.25, 0.70710678118654752, 0.9999999999])])
+    xs = xs[xs > 0]
+    for x in xs:
+        got, ref = mi.log_unit(float(x)), math.log(float(x))
+        assert abs(got - ref) <= 4e-16 * max(1.0, abs(ref)), (x, got, ref)
+    assert mi.log_unit(1.0) == 0.0
+    assert abs(mi.log_unit(0.5) + math.log(2.0)) <= 2.3e-16
+
+
+def test_series_sincos_matches_the_circle():
+    import math
+    rng = np.random.default_rng(4)
+    for u in np.concatenate([rng.random(20000), np.array([0.0, 0.125, 0.25, 0.5, 0.75, 0.999999])]):
+        s, c = mi.sincos_turn(float(u))
+        assert abs(s - math.sin(2 * math.pi * u)) <= 2e-15 and abs(c - math.cos(2 * math.pi * u)) <= 2e-15, u
+    assert mi.sincos_turn(0.0) == (0.0, 1.0)
+    assert mi.sincos_turn(0.25)[0] == 1.0 and mi.sincos_turn(0.5)[1] == -1.0
+
+
+def test_cpu_builds_with_and_without_fma_instructions_agree():
+    """The generator is built once with libm's fma() and once with the FMA instruction; fused
+    multiply-add rounds once in both, so the two builds give the same bits."""
+    import ctypes
+    mi.build()
+    n = 3 * 256 * 128 + 3
+    outs = []
+    for so in (mi._SO, mi._SO_FMA):
+        L = ctypes.CDLL(so)
+        L.mi_normal_bf16.argtypes = [ctypes.c_uint64] * 4 + [ctypes.c_double, ctypes.c_void_p]
+        b = np.empty(n, np.uint16)
+        L.mi_normal_bf16(0, mi.stream_id(mi.KIND_EXPERT, 1, 2), 5, n, 0.02, b.ctypes.data)
+        outs.append(b)
+    assert np.array_equal(outs[0], outs[1])
