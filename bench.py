@@ -54,6 +54,9 @@ def parse_args():
     ap.add_argument("--only-prefill", action="store_true", help="profiling cases: run the prefill leg alone")
     ap.add_argument("--prefill-tokens", type=int, default=4096)
     ap.add_argument("--prefill-experts", type=int, default=0, help="fewer experts for profiling cases")
+    ap.add_argument("--workload", choices=["decode", "stream8", "stack48"], default="decode",
+                    help="decode: the default decode layer; stream8: the 8-layer decode stream with a shared "
+                         "30%% cache; stack48: the 48-layer stack (double-buffered prefill, then decode)")
     return ap.parse_args()
 
 
@@ -502,6 +505,175 @@ def run_prefill(args, res=None, reps: int = 5):
     return out_res
 
 
+# ----------------------------------------------------------------------------- multi-layer legs
+def _stats_summary(st, ms):
+    return {"hit_rate": (st["hits"] / st["expert_reads"]) if st["expert_reads"] else None,
+            "expert_reads": st["expert_reads"], "misses": st["misses"], "prefetch_fills": st["prefetch_fills"],
+            "fill_GB": st["fill_bytes"] / 1e9,
+            "fill_GBps": (st["fill_bytes"] / (st["fill_ms"] / 1e3) / 1e9) if st["fill_ms"] else None,
+            "fill_share": (st["fill_ms"] / ms) if ms else None}
+
+
+def run_stream8(args):
+    """The 8-layer decode stream at full size: hidden 4096, intermediate 1536, 256 experts top-6
+    per layer, batch 8, routing forced by the reuse trace (each token re-picks an expert of its
+    previous step with p = 0.7, else Zipf(1.1)), one LRU cache of 30% of the 2048 entries
+    (614), 77 GB expert pool in pinned host memory. A step runs the 8 tokens through all 8
+    layers; value = tokens/s."""
+    import numpy as np
+    import torch
+
+    import moe_expert_layer_10_b300 as moe
+    import moe_inputs as mi
+    W = mi.WORKLOADS["stream8"]
+    B = 8
+    steps = args.steps if args.steps != 64 else 512
+    total = args.warmup + steps
+    t0 = time.time()
+    stream = torch.cuda.Stream()
+    cache = moe.MoeCache(moe.LayerShape(W.L, W.E, W.H, W.I, W.k, W.C, B), flags=0, stream_compute=stream)
+    fill_pool(cache, W, W.L, W.E)
+    setup_s = time.time() - t0
+    Wr = [torch.from_numpy(mi.router_weights(W.seed, l, W.E, W.H)).cuda() for l in range(W.L)]
+    bp = [mi.router_bias(W.seed, l, W.E, W.zipf_s) for l in range(W.L)]
+    bias = [torch.from_numpy(b).cuda() for b, _ in bp]
+    trace = mi.trace_reuse(W.seed, W.L, total, B, W.E, W.k, W.zipf_s, 0.7, np.stack([p for _, p in bp]))
+    sets = torch.from_numpy(np.ascontiguousarray(trace)).cuda()
+    xs = torch.from_numpy(np.stack([mi.activations(W.seed, 100000 + s * W.L + l, B, W.H)
+                                    for s in range(total) for l in range(W.L)]).view(np.int16)).view(torch.bfloat16)
+    xs = xs.cuda().reshape(total, W.L, B, W.H)
+    resid = xs.float()
+    idx = torch.empty((B, W.k), dtype=torch.int32, device="cuda")
+    wts = torch.empty((B, W.k), dtype=torch.float32, device="cuda")
+    out = torch.empty((B, W.H), dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()
+
+    def step(s):
+        for l in range(W.L):
+            cache.route_forced(l, xs[s, l], Wr[l], bias[l], sets[s, l], idx, wts)
+            cache.layer_forward(l, xs[s, l], resid[s, l], out, idx, wts)
+
+    for s in range(args.warmup):
+        step(s)
+    cache.sync()
+    cache.stats(reset=True)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(0)
+    clocks.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for s in range(args.warmup, total):
+        step(s)
+    e1.record(stream)
+    cache.sync()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1)
+    st = cache.stats()
+    cache.close()
+    tokens = steps * B
+    return {"metric": "8-layer MoE decode stream tok/s (256 experts top-6 per layer, batch 8, shared LRU of 30%)",
+            "value": round(tokens / (ms / 1e3), 2), "unit": "tok/s", "n_gpus": 1, "steps": steps,
+            "warmup": args.warmup, "ms_per_step": round(ms / steps, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded Philox)",
+            "config": {"workload": "8-layer decode stream: hidden 4096, intermediate 1536, 256 experts top-6, "
+                                   "batch 8, reuse trace p=0.7, 614-entry LRU over 2048 (layer, expert) entries",
+                       "pool_GB": W.L * W.E * 3 * W.H * W.I * 2 / 1e9, "setup_s": round(setup_s, 1),
+                       **_stats_summary(st, ms)},
+            "clocks": clk, "gpu_launches": int(steps * W.L * 5 + 2 * st["waves"])}
+
+
+def run_stack48(args):
+    """The 48-layer stack at full size: hidden 2048, intermediate 768, 128 experts top-8 per layer
+    (58 GB pool in pinned host memory), LRU cache of 25% of the 6144 entries (1536). A
+    2048-token prefill runs layer by layer with full-layer double buffering (layer l+1's experts
+    are prefetched on the copy stream while layer l computes), then decode steps at batch 32
+    through all 48 layers. value = decode tok/s; the prefill is reported beside it."""
+    import numpy as np
+    import torch
+
+    import moe_expert_layer_10_b300 as moe
+    import moe_inputs as mi
+    W = mi.WORKLOADS["stack48"]
+    T, B = 2048, 32
+    steps = args.steps if args.steps != 64 else 32
+    t0 = time.time()
+    stream = torch.cuda.Stream()
+    cache = moe.MoeCache(moe.LayerShape(W.L, W.E, W.H, W.I, W.k, W.C, T), flags=moe.MOE_PREFILL_DB,
+                         stream_compute=stream)
+    fill_pool(cache, W, W.L, W.E)
+    setup_s = time.time() - t0
+    Wr = [torch.from_numpy(mi.router_weights(W.seed, l, W.E, W.H)).cuda() for l in range(W.L)]
+    bias = [torch.from_numpy(mi.router_bias(W.seed, l, W.E, W.zipf_s)[0]).cuda() for l in range(W.L)]
+
+    def dev_x(step, n):
+        return [torch.from_numpy(mi.activations(W.seed, step * W.L + l, n, W.H).view(np.int16))
+                .view(torch.bfloat16).cuda() for l in range(W.L)]
+    xp = dev_x(200000, T)
+    rp = [x.float() for x in xp]
+    idx = torch.empty((T, W.k), dtype=torch.int32, device="cuda")
+    wts = torch.empty((T, W.k), dtype=torch.float32, device="cuda")
+    out = torch.empty((T, W.H), dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()
+    # prefill: prefetch layer 0, then per layer: route, forward, prefetch the next layer
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    cache.cache_fill(0, None, moe.MOE_FILL_FULL_LAYER)
+    for l in range(W.L):
+        cache.route(l, xp[l], Wr[l], bias[l], idx, wts)
+        cache.layer_forward(l, xp[l], rp[l], out, idx, wts)
+        if l + 1 < W.L:
+            cache.cache_fill(l + 1, None, moe.MOE_FILL_FULL_LAYER)
+    e1.record(stream)
+    cache.sync()
+    torch.cuda.synchronize()
+    ms_pre = e0.elapsed_time(e1)
+    st_pre = cache.stats(reset=True)
+    del xp, rp
+    # decode at batch 32 through every layer
+    xd = [dev_x(300000 + s, B) for s in range(args.warmup + steps)]
+    rd = [[x.float() for x in xs] for xs in xd]
+    idx_d = idx[:B]
+    wts_d = wts[:B]
+    out_d = out[:B]
+    torch.cuda.synchronize()
+
+    def step(s):
+        for l in range(W.L):
+            cache.route(l, xd[s][l], Wr[l], bias[l], idx_d, wts_d)
+            cache.layer_forward(l, xd[s][l], rd[s][l], out_d, idx_d, wts_d)
+
+    for s in range(args.warmup):
+        step(s)
+    cache.sync()
+    cache.stats(reset=True)
+    clocks = ClockSampler(0)
+    clocks.start()
+    d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    d0.record(stream)
+    for s in range(args.warmup, args.warmup + steps):
+        step(s)
+    d1.record(stream)
+    cache.sync()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = d0.elapsed_time(d1)
+    st = cache.stats()
+    cache.close()
+    return {"metric": "48-layer MoE stack decode tok/s (128 experts top-8 per layer, batch 32, LRU of 25%)",
+            "value": round(steps * B / (ms / 1e3), 2), "unit": "tok/s", "n_gpus": 1, "steps": steps,
+            "warmup": args.warmup, "ms_per_step": round(ms / steps, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded Philox)",
+            "config": {"workload": "48-layer stack: hidden 2048, intermediate 768, 128 experts top-8, 1536-entry "
+                                   "LRU over 6144 (layer, expert) entries; 2048-token double-buffered prefill, "
+                                   "then decode at batch 32",
+                       "pool_GB": W.L * W.E * 3 * W.H * W.I * 2 / 1e9, "setup_s": round(setup_s, 1),
+                       **_stats_summary(st, ms)},
+            "prefill": {"tokens": T, "ms": round(ms_pre, 2), "tok_s": round(T / (ms_pre / 1e3), 1),
+                        **_stats_summary(st_pre, ms_pre)},
+            "clocks": clk, "gpu_launches": int(steps * W.L * 5 + 2 * st["waves"])}
+
+
 # ----------------------------------------------------------------------------- reference arm
 def run_reference(args):
     """The CPU oracle as it stands, on the same workload: every step is one whole benchmark
@@ -582,6 +754,13 @@ def main():
             print(json.dumps(run_reference(args)), flush=True)
         return
     init_dist(world, local)
+    if args.workload != "decode":
+        import torch
+        torch.cuda.set_device(local)
+        res = run_stream8(args) if args.workload == "stream8" else run_stack48(args)
+        if rank == 0:
+            print(json.dumps(res), flush=True)
+        return
     if args.only_prefill:
         import torch
         torch.cuda.set_device(local)
