@@ -317,10 +317,19 @@ def run_b300(args, rank, world, local):
     # decode kernels' time is their own weight streaming -- the roofline pass
     res = resident_context(args, W, E=W.E)
     rc = res["cache"]
-    rc.set_profile(True)
     for s in range(args.warmup):
         step(rc, s)
     rc.sync()
+    # timed without events first: the step time when nothing has to be filled
+    r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    r0.record(res["stream"])
+    for s in range(args.warmup, total):
+        step(rc, s)
+    r1.record(res["stream"])
+    rc.sync()
+    torch.cuda.synchronize()
+    ms_resident = r0.elapsed_time(r1) / args.steps
+    rc.set_profile(True)
     rc.kernel_stats(reset=True)
     for s in range(args.warmup, total):
         step(rc, s)
@@ -382,6 +391,9 @@ def run_b300(args, rank, world, local):
                    "fill_share_of_step": ((st["fill_ms"] / args.steps) / (ms_max / args.steps))
                    if st["fill_ms"] else None},
         "clocks": clk, "e2e": e2e, "gpu_launches": int(launches), "roofline": roof,
+        "resident_pass": {"ms_per_step": round(ms_resident, 4),
+                          "tok_s": round(sum(BATCHES) / (ms_resident / 1e3), 1),
+                          "note": "the same steps with every expert resident (no fills), timed without events"},
         "kernels_resident_pass": table(kst), "kernels_by_batch_resident": by_batch,
         "kernels_lru_pass": table(kst_lru),
     }

@@ -58,6 +58,14 @@ extern "C" {
 #define MOE_TRACE 1u      /* keep a ring of LRU events, readable through moe_stats */
 #define MOE_PROFILE 2u    /* time every kernel launch with CUDA events (moe_kernel_stats) */
 #define MOE_PREFILL_DB 4u /* full-layer double buffering is intended: requires capacity >= 2*num_experts */
+/* Keep the LRU policy, the slot table, the counters and the trace on the GPU, and issue the
+ * fills from a kernel that reads the pinned pool through its device mapping: moe_layer_forward
+ * then never waits on the host, and a decode step (moe_route + moe_layer_forward per layer) can
+ * be captured into a CUDA graph on the compute stream. Same policy and traces as the host
+ * policy. Decode kernels only (MOE_PATH_GEMM is refused); moe_cache_fill joins its fills
+ * back into the compute stream (no prefill overlap); moe_stats reports fill_ms = 0. Run one
+ * call of each shape before capturing, and keep MOE_PROFILE timing off while capturing. */
+#define MOE_DEVICE_POLICY 8u
 
 /* ---- fill modes (moe_cache_fill) ---- */
 #define MOE_FILL_DEMAND 0     /* access the distinct experts of the given top-k indices */
@@ -84,7 +92,7 @@ typedef struct {
     int32_t top_k;       /* k */
     int32_t capacity;    /* C: cache slots, in whole entries */
     int32_t max_tokens;  /* largest T passed to moe_route / moe_layer_forward */
-    uint32_t flags;      /* MOE_TRACE | MOE_PROFILE | MOE_PREFILL_DB */
+    uint32_t flags;      /* MOE_TRACE | MOE_PROFILE | MOE_PREFILL_DB | MOE_DEVICE_POLICY */
     uint64_t trace_capacity; /* events kept by MOE_TRACE (0: 1<<20) */
 } moe_config_t;
 

@@ -106,8 +106,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const int32_t* __restrict__ slot_row, const uint32_t* __restrict__ fill_flag, int H, int I,
                       uint16_t* __restrict__ h_out,
                       const float* __restrict__ w_perm, float* __restrict__ pair_out, float* __restrict__ ws,
-                      int* __restrict__ cnt, int* status, uint64_t fill_wait_ns) {
+                      int* __restrict__ cnt, int* status, uint64_t fill_wait_ns, const int* __restrict__ dyn) {
     using Lay = Layout<GATEUP>;
+    if (dyn) {  // work size written on the device (device-resident policy)
+        n_work = dyn[0];
+        n_units = dyn[1];
+        S = dyn[2];
+    }
     // the MMA and epilogue roles may legitimately wait as long as the producer waits for a fill
     const uint64_t consumer_wait_ns = fill_wait_ns + kWaitDeadlineNs;
     constexpr int kStages = Lay::STAGES;
@@ -393,10 +398,12 @@ template <bool GATEUP>
 cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const GemvWork* work, int n_work, int n_units,
                    int S, const int32_t* slot_row, const uint32_t* fill_flag, int H, int I, uint16_t* h_out,
                    const float* w_perm, float* pair_out, float* ws, int* cnt, int* status, uint64_t fill_wait_ns,
-                   int num_sms, cudaStream_t st) {
-    if (n_units <= 0 || n_work <= 0) return cudaSuccess;
-    if (S < 1 || S > kDecodeMaxSplit) return cudaErrorInvalidValue;
-    if (S > 1 && n_units > kDecodeSplitUnits) return cudaErrorInvalidValue;
+                   int num_sms, cudaStream_t st, const int* dyn = nullptr) {
+    if (!dyn) {
+        if (n_units <= 0 || n_work <= 0) return cudaSuccess;
+        if (S < 1 || S > kDecodeMaxSplit) return cudaErrorInvalidValue;
+        if (S > 1 && n_units > kDecodeSplitUnits) return cudaErrorInvalidValue;
+    }
     auto kern = decode_mma_kernel<GATEUP>;
     constexpr int smem = Layout<GATEUP>::SMEM;
     static bool attr = false;
@@ -405,9 +412,9 @@ cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const GemvWork*
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    const int grid = std::min(n_units, num_sms);
+    const int grid = dyn ? num_sms : std::min(n_units, num_sms);
     kern<<<grid, kThreads, smem, st>>>(ta, tb, work, n_work, n_units, S, slot_row, fill_flag, H, I, h_out, w_perm,
-                                       pair_out, ws, cnt, status, fill_wait_ns);
+                                       pair_out, ws, cnt, status, fill_wait_ns, dyn);
     return cudaGetLastError();
 }
 
@@ -444,6 +451,20 @@ cudaError_t launch_decode_gateup(const DecodeMaps& m, const GemvWork* work, int 
                                  cudaStream_t st) {
     return launch<true>(m.a_gu, m.b_x, work, n_work, n_units, S, slot_row, fill_flag, H, I, h_perm, nullptr, nullptr,
                         ws, cnt, status, fill_wait_ns, num_sms, st);
+}
+
+cudaError_t launch_decode_gateup_dyn(const DecodeMaps& m, const GemvWork* work, const int* dyn,
+                                     const int32_t* slot_row, int H, int I, uint16_t* h_perm, float* ws, int* cnt,
+                                     int* status, int num_sms, cudaStream_t st) {
+    return launch<true>(m.a_gu, m.b_x, work, 0, 0, 1, slot_row, nullptr, H, I, h_perm, nullptr, nullptr, ws, cnt, status,
+                        0, num_sms, st, dyn);
+}
+
+cudaError_t launch_decode_down_dyn(const DecodeMaps& m, const GemvWork* work, const int* dyn,
+                                   const int32_t* slot_row, int H, int I, const float* w_perm, float* pair_out,
+                                   float* ws, int* cnt, int* status, int num_sms, cudaStream_t st) {
+    return launch<false>(m.a_d, m.b_h, work, 0, 0, 1, slot_row, nullptr, H, I, nullptr, w_perm, pair_out, ws, cnt,
+                         status, 0, num_sms, st, dyn);
 }
 
 cudaError_t launch_decode_down(const DecodeMaps& m, const GemvWork* work, int n_work, int n_units, int S,

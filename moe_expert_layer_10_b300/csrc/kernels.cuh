@@ -56,11 +56,64 @@ cudaError_t launch_decode_gateup(const DecodeMaps& maps, const GemvWork* work, i
                                  const int32_t* slot_row, const uint32_t* fill_flag, int H, int I, uint16_t* h_perm,
                                  float* ws, int* cnt, int* status, uint64_t fill_wait_ns, int num_sms,
                                  cudaStream_t st);
+// Same kernels with the work size read on the device: dyn = {n_work, n_units, S} (written by
+// the policy kernel); the grid is one CTA per SM.
+cudaError_t launch_decode_gateup_dyn(const DecodeMaps& maps, const GemvWork* work, const int* dyn,
+                                     const int32_t* slot_row, int H, int I, uint16_t* h_perm, float* ws, int* cnt,
+                                     int* status, int num_sms, cudaStream_t st);
+cudaError_t launch_decode_down_dyn(const DecodeMaps& maps, const GemvWork* work, const int* dyn,
+                                   const int32_t* slot_row, int H, int I, const float* w_perm, float* pair_out,
+                                   float* ws, int* cnt, int* status, int num_sms, cudaStream_t st);
 // pair_out[pos, n] = w_perm[pos] * (W_down[n] . h[pos])
 cudaError_t launch_decode_down(const DecodeMaps& maps, const GemvWork* work, int n_work, int n_units, int S,
                                const int32_t* slot_row, const uint32_t* fill_flag, int H, int I, const float* w_perm,
                                float* pair_out, float* ws, int* cnt, int* status, uint64_t fill_wait_ns, int num_sms,
                                cudaStream_t st);
+
+// --- device-resident cache policy (decode forward with no host round trip) ---
+enum : int { kEvHit = 0, kEvFill = 1, kEvPrefetchFill = 2, kEvPrefetchHit = 3 };
+
+struct DevLruState {
+    int head, tail, n_used, pad;  // most / least recently used slot, slots handed out so far
+};
+struct DevStats {  // the fields of moe_stats_t that the device policy counts
+    unsigned long long expert_reads, hits, misses, prefetch_fills, prefetch_hits, evictions, fill_bytes, trace_len,
+        forwards, waves;
+};
+struct DevEvent {
+    int kind, layer, expert, slot, ev_layer, ev_expert;
+};
+struct WaveHdr {  // written by the policy kernel, read by the fill and decode kernels
+    int n_fill;
+    int hit_gu[3], hit_d[3], miss_gu[3], miss_d[3];  // {n_work, n_units, S} per decode launch
+};
+struct DevPolicyArgs {
+    DevLruState* state;
+    int *lru_prev, *lru_next, *lru_key;  // [C]
+    int32_t* slot_of;                    // [L*E] device slot table
+    int C, E, H, I, layer, num_sms;
+    int prefetch;                        // accesses are prefetches (no compute)
+    // keys: the routed wave (active list of the permutation) or an explicit expert list
+    const int32_t* active;
+    const int32_t* n_active;
+    int wave;
+    const int32_t* keys;
+    int n_keys;
+    const int32_t* offsets;              // expert offsets of the permutation (for work lists)
+    int2* fill_list;                     // [C] (key, slot)
+    GemvWork* work_hit;                  // [2*(E+1)]: gate/up list, then down list (or null)
+    GemvWork* work_miss;                 // [2*(E+1)]
+    int* order;                          // [2*C] scratch: hit experts, then filled experts
+    WaveHdr* hdr;
+    DevStats* stats;
+    DevEvent* trace;                     // ring of trace_cap events (or null)
+    unsigned long long trace_cap;
+    unsigned long long entry_bytes;
+};
+cudaError_t launch_policy(const DevPolicyArgs& a, cudaStream_t st);
+// copy the fill list's entries from the host pool (device-mapped) into their slots
+cudaError_t launch_fill(const void* pool_dev, void* arena, const int2* fill_list, const int* n_fill,
+                        size_t entry_bytes, int num_sms, cudaStream_t st);
 
 // --- combine: out[t] = resid[t] + sum_j pair_out[inv_perm[t*k+j]] (j order) ---
 cudaError_t launch_combine(const float* pair_out, const int32_t* inv_perm, const float* resid, float* out, int T,

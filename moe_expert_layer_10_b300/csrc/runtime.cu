@@ -62,10 +62,10 @@ constexpr int kDecodeMaxTokens = 64;  // AUTO path: tensor-core decode kernels u
 constexpr size_t kWorkEntries(int E) { return 2 * (static_cast<size_t>(E) + 1); }
 
 enum KernelId { kRouterLogits, kRouterTopk, kPermute, kGather, kDecodeGateUp, kDecodeDown, kGemmGateUp, kGemmDown,
-                kCombine, kNumKernels };
+                kCombine, kPolicy, kFill, kNumKernels };
 const char* kKernelNames[kNumKernels] = {"router_logits", "router_topk",  "permute",     "gather_rows",
                                          "decode_gateup", "decode_down",  "gemm_gateup", "gemm_down",
-                                         "combine"};
+                                         "combine",       "device_policy", "device_fill"};
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -194,6 +194,22 @@ struct moe_ctx {
 
     int inject_kind = 0, inject_count = 0;
     uint64_t fill_wait_ns = kFillWaitNs;  // device-side deadline of a wait for a fill
+
+    // device-resident policy (MOE_DEVICE_POLICY): LRU, stats, trace and fills on the GPU
+    bool dev_policy = false;
+    void* pool_dev = nullptr;              // the pinned pool's device-mapped address
+    moe::DevLruState* d_lru = nullptr;
+    int *d_prev = nullptr, *d_next = nullptr, *d_key = nullptr;  // [C]
+    moe::DevStats* d_stats = nullptr;
+    moe::DevEvent* d_trace = nullptr;
+    uint64_t d_trace_cap = 0;
+    int2* d_fill_list = nullptr;           // [C]
+    GemvWork* d_work = nullptr;            // [4*(E+1)]: hit lists, then miss lists
+    int* d_order = nullptr;                // [2*C]
+    moe::WaveHdr* d_hdr = nullptr;
+    int32_t* d_keys = nullptr;             // [E]: explicit key lists of moe_cache_fill
+    int32_t* d_iota = nullptr;             // [E]: 0..E-1
+    cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
 };
 
 namespace {
@@ -252,7 +268,9 @@ struct ProfScope {
     double bytes, flops;
     cudaEvent_t start = nullptr;
     ProfScope(moe_ctx* c_, int kid, double b, double f) : c(c_), kernel(kid), bytes(b), flops(f) {
-        if (c->cfg.flags & MOE_PROFILE) {
+        cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+        cudaStreamIsCapturing(c->s_comp, &cap);
+        if ((c->cfg.flags & MOE_PROFILE) && cap == cudaStreamCaptureStatusNone) {
             start = pool_event(c);
             if (start) cudaEventRecord(start, c->s_comp);
         }
@@ -445,9 +463,13 @@ void free_all(moe_ctx* c) {
     for (int i = 0; i < kStageRing; ++i)
         if (c->stage_ev[i]) cudaEventDestroy(c->stage_ev[i]);
     if (c->ev_d2h) cudaEventDestroy(c->ev_d2h);
+    if (c->ev_fork) cudaEventDestroy(c->ev_fork);
+    if (c->ev_join) cudaEventDestroy(c->ev_join);
     void* dev_ptrs[] = {c->arena, c->slot_dev, c->logits, c->offsets, c->perm, c->inv_perm, c->active,
                         c->n_active, c->w_perm, c->pair_out, c->x_perm, c->h_perm, c->status, c->work_dev,
-                        c->dec_ws,   c->dec_cnt, c->fill_flag};
+                        c->dec_ws,   c->dec_cnt, c->fill_flag, c->d_lru,   c->d_prev, c->d_next,  c->d_key,
+                        c->d_stats,  c->d_trace, c->d_fill_list, c->d_work, c->d_order, c->d_hdr, c->d_keys,
+                        c->d_iota};
     for (void* p : dev_ptrs)
         if (p) cudaFree(p);
     void* host_ptrs[] = {c->pool, c->idx_host, c->status_host, c->table_stage, c->work_stage};
@@ -456,6 +478,119 @@ void free_all(moe_ctx* c) {
     if (c->own_comp && c->s_comp) cudaStreamDestroy(c->s_comp);
     if (c->own_copy && c->s_copy) cudaStreamDestroy(c->s_copy);
     delete c;
+}
+
+}  // namespace
+
+namespace {
+
+// The device policy on one key set, then the fills it chose on the copy stream (forked from
+// and, when `join`, joined back into the compute stream). No host wait: capturable.
+int dev_policy_run(moe_ctx* c, moe::DevPolicyArgs a, bool join) {
+    a.state = c->d_lru;
+    a.lru_prev = c->d_prev;
+    a.lru_next = c->d_next;
+    a.lru_key = c->d_key;
+    a.slot_of = c->slot_dev;
+    a.C = c->C;
+    a.E = c->E;
+    a.H = c->H;
+    a.I = c->I;
+    a.num_sms = c->num_sms;
+    a.fill_list = c->d_fill_list;
+    a.order = c->d_order;
+    a.hdr = c->d_hdr;
+    a.stats = c->d_stats;
+    a.trace = c->d_trace;
+    a.trace_cap = c->d_trace_cap;
+    a.entry_bytes = c->entry_bytes;
+    {
+        ProfScope ps(c, kPolicy, 0.0, 0.0);
+        CUDA_TRY(moe::launch_policy(a, c->s_comp));
+    }
+    CUDA_TRY(cudaEventRecord(c->ev_fork, c->s_comp));
+    CUDA_TRY(cudaStreamWaitEvent(c->s_copy, c->ev_fork, 0));
+    CUDA_TRY(moe::launch_fill(c->pool_dev, c->arena, c->d_fill_list, &c->d_hdr->n_fill, c->entry_bytes, c->num_sms,
+                              c->s_copy));
+    CUDA_TRY(cudaEventRecord(c->ev_join, c->s_copy));
+    if (join) CUDA_TRY(cudaStreamWaitEvent(c->s_comp, c->ev_join, 0));
+    return MOE_OK;
+}
+
+// Decode forward with the device-resident policy: permutation, then per wave the policy,
+// the fills (copy stream) alongside the resident experts' kernels, the filled experts'
+// kernels after the fills, then the combine. Enqueues only; never waits on the host.
+int forward_device(moe_ctx* c, int layer, const void* x, const float* resid, float* out, int T, const int32_t* idx,
+                   const float* w) {
+    const int P = T * c->k, E = c->E, H = c->H, I = c->I;
+    if (c->path == MOE_PATH_GEMM)
+        return fail(MOE_E_INVAL, "the device-resident policy runs the decode kernels only (MOE_PATH_GEMM unsupported)");
+    {
+        ProfScope ps(c, kPermute, 8.0 * P + 12.0 * P + 8.0 * E, 0.0);
+        CUDA_TRY(moe::launch_permute(idx, w, P, E, c->offsets, c->perm, c->inv_perm, c->w_perm, c->active,
+                                     c->n_active, c->status, c->s_comp));
+    }
+    {
+        ProfScope ps(c, kGather, 4.0 * P * H, 0.0);
+        CUDA_TRY(moe::launch_gather_rows(static_cast<const uint16_t*>(x), c->perm, P, c->k, H, c->x_perm, c->s_comp));
+    }
+    const int32_t* slot_row = c->slot_dev + static_cast<size_t>(layer) * E;
+    GemvWork* wh = c->d_work;
+    GemvWork* wm = c->d_work + 2 * (E + 1);
+    const int waves = (std::min(P, E) + c->C - 1) / c->C;  // the most the routed set can need
+    for (int wv = 0; wv < waves; ++wv) {
+        moe::DevPolicyArgs a{};
+        a.layer = layer;
+        a.active = c->active;
+        a.n_active = c->n_active;
+        a.wave = wv;
+        a.offsets = c->offsets;
+        a.work_hit = wh;
+        a.work_miss = wm;
+        int rc = dev_policy_run(c, a, false);
+        if (rc) return rc;
+        {
+            ProfScope ps(c, kDecodeGateUp, 0.0, 0.0);
+            CUDA_TRY(moe::launch_decode_gateup_dyn(c->dec_maps, wh, c->d_hdr->hit_gu, slot_row, H, I, c->h_perm,
+                                                   c->dec_ws, c->dec_cnt, c->status, c->num_sms, c->s_comp));
+        }
+        {
+            ProfScope ps(c, kDecodeDown, 0.0, 0.0);
+            CUDA_TRY(moe::launch_decode_down_dyn(c->dec_maps, wh + (E + 1), c->d_hdr->hit_d, slot_row, H, I,
+                                                 c->w_perm, c->pair_out, c->dec_ws, c->dec_cnt, c->status, c->num_sms,
+                                                 c->s_comp));
+        }
+        CUDA_TRY(cudaStreamWaitEvent(c->s_comp, c->ev_join, 0));
+        {
+            ProfScope ps(c, kDecodeGateUp, 0.0, 0.0);
+            CUDA_TRY(moe::launch_decode_gateup_dyn(c->dec_maps, wm, c->d_hdr->miss_gu, slot_row, H, I, c->h_perm,
+                                                   c->dec_ws, c->dec_cnt, c->status, c->num_sms, c->s_comp));
+        }
+        {
+            ProfScope ps(c, kDecodeDown, 0.0, 0.0);
+            CUDA_TRY(moe::launch_decode_down_dyn(c->dec_maps, wm + (E + 1), c->d_hdr->miss_d, slot_row, H, I,
+                                                 c->w_perm, c->pair_out, c->dec_ws, c->dec_cnt, c->status, c->num_sms,
+                                                 c->s_comp));
+        }
+    }
+    {
+        ProfScope ps(c, kCombine, 4.0 * P * H + 8.0 * T * H + 4.0 * P, 1.0 * P * H);
+        CUDA_TRY(moe::launch_combine(c->pair_out, c->inv_perm, resid, out, T, c->k, H, c->s_comp));
+    }
+    return MOE_OK;
+}
+
+// Wait for both streams (bounded) without touching the device status.
+int drain(moe_ctx* c) {
+    cudaEvent_t e1 = pool_event(c), e2 = pool_event(c);
+    if (!e1 || !e2) return fail(MOE_E_CUDA, "event creation failed");
+    CUDA_TRY(cudaEventRecord(e1, c->s_comp));
+    CUDA_TRY(cudaEventRecord(e2, c->s_copy));
+    int rc = wait_event(c, e1, "compute stream");
+    if (!rc) rc = wait_event(c, e2, "copy stream");
+    c->ev_pool.push_back(e1);
+    c->ev_pool.push_back(e2);
+    return rc;
 }
 
 }  // namespace
@@ -540,7 +675,10 @@ int moe_cache_init(const moe_config_t* cfg, void* stream_compute, void* stream_c
         c->own_copy = true;
     }
     const size_t pool_bytes = keys * c->entry_bytes;
-    INIT_TRY(cudaHostAlloc(reinterpret_cast<void**>(&c->pool), pool_bytes, cudaHostAllocPortable));
+    c->dev_policy = (f.flags & MOE_DEVICE_POLICY) != 0;
+    INIT_TRY(cudaHostAlloc(reinterpret_cast<void**>(&c->pool), pool_bytes,
+                           cudaHostAllocPortable | (c->dev_policy ? cudaHostAllocMapped : 0)));
+    if (c->dev_policy) INIT_TRY(cudaHostGetDevicePointer(&c->pool_dev, c->pool, 0));
     std::memset(c->pool, 0, pool_bytes);
     INIT_TRY(cudaMalloc(&c->arena, static_cast<size_t>(c->C) * c->entry_bytes));
     INIT_TRY(cudaMalloc(&c->slot_dev, keys * sizeof(int32_t)));
@@ -579,6 +717,34 @@ int moe_cache_init(const moe_config_t* cfg, void* stream_compute, void* stream_c
         INIT_TRY(cudaEventCreateWithFlags(&c->fill_ev[i], cudaEventDisableTiming));
     }
     INIT_TRY(cudaEventCreateWithFlags(&c->ev_d2h, cudaEventDisableTiming));
+    if (c->dev_policy) {
+        const size_t Cn = static_cast<size_t>(c->C);
+        INIT_TRY(cudaMalloc(&c->d_lru, sizeof(moe::DevLruState)));
+        INIT_TRY(cudaMalloc(&c->d_prev, Cn * sizeof(int)));
+        INIT_TRY(cudaMalloc(&c->d_next, Cn * sizeof(int)));
+        INIT_TRY(cudaMalloc(&c->d_key, Cn * sizeof(int)));
+        INIT_TRY(cudaMalloc(&c->d_stats, sizeof(moe::DevStats)));
+        c->d_trace_cap = (f.flags & MOE_TRACE) ? (f.trace_capacity ? f.trace_capacity : (1u << 20)) : 0;
+        if (c->d_trace_cap) INIT_TRY(cudaMalloc(&c->d_trace, c->d_trace_cap * sizeof(moe::DevEvent)));
+        INIT_TRY(cudaMalloc(&c->d_fill_list, Cn * sizeof(int2)));
+        INIT_TRY(cudaMalloc(&c->d_work, 4 * (static_cast<size_t>(c->E) + 1) * sizeof(GemvWork)));
+        INIT_TRY(cudaMalloc(&c->d_order, 2 * Cn * sizeof(int)));
+        INIT_TRY(cudaMalloc(&c->d_hdr, sizeof(moe::WaveHdr)));
+        INIT_TRY(cudaMalloc(&c->d_keys, c->E * sizeof(int32_t)));
+        INIT_TRY(cudaMalloc(&c->d_iota, c->E * sizeof(int32_t)));
+        std::vector<int32_t> iota(c->E);
+        for (int e = 0; e < c->E; ++e) iota[e] = e;
+        INIT_TRY(cudaMemcpy(c->d_iota, iota.data(), c->E * sizeof(int32_t), cudaMemcpyHostToDevice));
+        const moe::DevLruState st0{-1, -1, 0, 0};
+        INIT_TRY(cudaMemcpy(c->d_lru, &st0, sizeof(st0), cudaMemcpyHostToDevice));
+        INIT_TRY(cudaMemset(c->d_prev, 0xff, Cn * sizeof(int)));
+        INIT_TRY(cudaMemset(c->d_next, 0xff, Cn * sizeof(int)));
+        INIT_TRY(cudaMemset(c->d_key, 0xff, Cn * sizeof(int)));
+        INIT_TRY(cudaMemset(c->d_stats, 0, sizeof(moe::DevStats)));
+        INIT_TRY(cudaMemset(c->d_hdr, 0, sizeof(moe::WaveHdr)));
+        INIT_TRY(cudaEventCreateWithFlags(&c->ev_fork, cudaEventDisableTiming));
+        INIT_TRY(cudaEventCreateWithFlags(&c->ev_join, cudaEventDisableTiming));
+    }
 
     // TMA views. Arena rows: [C*3I x H] for gate/up, [C*3H x I] for down.
     const uint64_t H = c->H, I = c->I, C = c->C, P = c->Pmax;
@@ -634,6 +800,14 @@ int moe_set_profile(moe_ctx* c, int on) {
 
 int moe_resident_slot(moe_ctx* c, int layer, int expert) {
     if (!c || layer < 0 || layer >= c->L || expert < 0 || expert >= c->E) return -1;
+    if (c->dev_policy) {
+        int32_t s = -1;
+        if (cudaSetDevice(c->dev) != cudaSuccess || drain(c) != MOE_OK ||
+            cudaMemcpy(&s, c->slot_dev + static_cast<size_t>(layer) * c->E + expert, sizeof(s),
+                       cudaMemcpyDeviceToHost) != cudaSuccess)
+            return -1;
+        return s;
+    }
     return c->lru.slot_of(layer * c->E + expert);
 }
 
@@ -683,6 +857,38 @@ int moe_cache_fill(moe_ctx* c, int layer, const int32_t* idx_host, int n, int mo
     int rc = validate_layer(c, layer);
     if (rc) return rc;
     CUDA_TRY(cudaSetDevice(c->dev));
+    if (c->dev_policy) {
+        moe::DevPolicyArgs a{};
+        a.layer = layer;
+        if (mode == MOE_FILL_FULL_LAYER) {
+            if (c->C < c->E) return fail(MOE_E_CAPACITY, "a whole layer (%d) does not fit in %d slots", c->E, c->C);
+            a.keys = c->d_iota;
+            a.n_keys = c->E;
+            a.prefetch = 1;
+        } else if (mode == MOE_FILL_DEMAND) {
+            if (n < 0 || (n > 0 && !idx_host)) return fail(MOE_E_INVAL, "bad index list");
+            std::vector<char> used(c->E, 0);
+            for (int i = 0; i < n; ++i) {
+                if (idx_host[i] < 0 || idx_host[i] >= c->E)
+                    return fail(MOE_E_INVAL, "expert id %d out of range", idx_host[i]);
+                used[idx_host[i]] = 1;
+            }
+            std::vector<int32_t> ids;
+            for (int e = 0; e < c->E; ++e)
+                if (used[e]) ids.push_back(e);
+            if (static_cast<int>(ids.size()) > c->C)
+                return fail(MOE_E_CAPACITY, "%zu distinct experts exceed %d slots", ids.size(), c->C);
+            if (ids.empty()) return MOE_OK;
+            CUDA_TRY(cudaMemcpyAsync(c->d_keys, ids.data(), ids.size() * sizeof(int32_t), cudaMemcpyHostToDevice,
+                                     c->s_comp));
+            CUDA_TRY(cudaStreamSynchronize(c->s_comp));  // the host list goes out of scope
+            a.keys = c->d_keys;
+            a.n_keys = static_cast<int>(ids.size());
+        } else {
+            return fail(MOE_E_INVAL, "unknown fill mode %d", mode);
+        }
+        return dev_policy_run(c, a, true);
+    }
     std::vector<int> keys;
     if (mode == MOE_FILL_FULL_LAYER) {
         if (c->C < c->E) return fail(MOE_E_CAPACITY, "a whole layer (%d) does not fit in %d slots", c->E, c->C);
@@ -714,6 +920,7 @@ int moe_layer_forward(moe_ctx* c, int layer, const void* x, const float* resid, 
     if (T == 0) return MOE_OK;
     if (!x || !resid || !out || !idx || !w) return fail(MOE_E_INVAL, "null device pointer");
     CUDA_TRY(cudaSetDevice(c->dev));
+    if (c->dev_policy) return forward_device(c, layer, x, resid, out, T, idx, w);
     const int P = T * c->k;
     const int E = c->E, H = c->H, I = c->I;
     c->stats.forwards++;
@@ -912,6 +1119,43 @@ int moe_sync(moe_ctx* c) {
 int moe_stats(moe_ctx* c, moe_stats_t* out, moe_event_t* trace, uint64_t cap, int reset) {
     g_last_error.clear();
     if (!c) return fail(MOE_E_INVAL, "null context");
+    if (c->dev_policy) {
+        CUDA_TRY(cudaSetDevice(c->dev));
+        int rc = drain(c);
+        if (rc) return rc;
+        moe::DevStats d{};
+        CUDA_TRY(cudaMemcpy(&d, c->d_stats, sizeof(d), cudaMemcpyDeviceToHost));
+        if (out) {
+            *out = moe_stats_t{};
+            out->expert_reads = d.expert_reads;
+            out->hits = d.hits;
+            out->misses = d.misses;
+            out->prefetch_fills = d.prefetch_fills;
+            out->prefetch_hits = d.prefetch_hits;
+            out->evictions = d.evictions;
+            out->fill_bytes = d.fill_bytes;
+            out->fill_ms = 0.0;  // fills run inside kernels here; no per-batch copy timing
+            out->trace_len = d.trace_len;
+            out->forwards = d.forwards;
+            out->waves = d.waves;
+        }
+        int written = 0;
+        if (trace && cap > 0 && c->d_trace_cap) {
+            const uint64_t have = std::min<uint64_t>(d.trace_len, c->d_trace_cap);
+            const uint64_t n = std::min<uint64_t>(have, cap);
+            for (uint64_t i = 0; i < n;) {
+                const uint64_t pos = (d.trace_len - n + i) % c->d_trace_cap;
+                const uint64_t run = std::min<uint64_t>(n - i, c->d_trace_cap - pos);
+                static_assert(sizeof(moe::DevEvent) == sizeof(moe_event_t), "event layout");
+                CUDA_TRY(cudaMemcpy(trace + i, c->d_trace + pos, run * sizeof(moe_event_t), cudaMemcpyDeviceToHost));
+                i += run;
+            }
+            written = static_cast<int>(n);
+        }
+        if (reset) CUDA_TRY(cudaMemset(c->d_stats, 0, sizeof(moe::DevStats)));
+        harvest(c);
+        return written;
+    }
     harvest(c);
     if (out) *out = c->stats;
     int written = 0;
