@@ -51,9 +51,15 @@ def parse_args():
     ap.add_argument("--batches", default="1,4,16", help="decode batch sizes of one step (profiling cases)")
     ap.add_argument("--capacity", type=int, default=0, help="override the cache capacity (profiling cases)")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--prefetch-all", action="store_true",
+                    help="comparison case: prefetch every expert before timing (needs --capacity >= 256), so every "
+                         "routed access hits and the step time is compute plus control")
     ap.add_argument("--only-prefill", action="store_true", help="profiling cases: run the prefill leg alone")
     ap.add_argument("--prefill-tokens", type=int, default=4096)
     ap.add_argument("--prefill-experts", type=int, default=0, help="fewer experts for profiling cases")
+    ap.add_argument("--policy", choices=["host", "device"], default="host",
+                    help="host: LRU on the host (one sync per forward); device: LRU and fills on the GPU, the "
+                         "whole decode step captured in a CUDA graph and replayed")
     ap.add_argument("--workload", choices=["decode", "stream8", "stack48"], default="decode",
                     help="decode: the default decode layer; stream8: the 8-layer decode stream with a shared "
                          "30%% cache; stack48: the 48-layer stack (double-buffered prefill, then decode)")
@@ -219,8 +225,13 @@ def run_b300(args, rank, world, local):
     stream = torch.cuda.Stream()
     C = args.capacity or W.C
     # per-launch event timing stays off in the timed regions; a separate pass profiles
-    cache = moe.MoeCache(moe.LayerShape(1, W.E, W.H, W.I, W.k, C, max(BATCHES)), flags=0, stream_compute=stream)
+    device = args.policy == "device"
+    cache = moe.MoeCache(moe.LayerShape(1, W.E, W.H, W.I, W.k, C, max(BATCHES)),
+                         flags=moe.MOE_DEVICE_POLICY if device else 0, stream_compute=stream)
     fill_pool(cache, W, 1, W.E)
+    if args.prefetch_all:
+        cache.cache_fill(0, None, moe.MOE_FILL_FULL_LAYER)
+        cache.sync()
     Wr_h = mi.router_weights(W.seed, 0, W.E, W.H)
     b_h, _ = mi.router_bias(W.seed, 0, W.E, W.zipf_s)
     Wr = torch.from_numpy(Wr_h).cuda()
@@ -243,7 +254,37 @@ def run_b300(args, rank, world, local):
             c.route(0, xs[s][B], Wr, bias, idx[B], wts[B])
             c.layer_forward(0, xs[s][B], resid[s][B], out[B], idx[B], wts[B])
 
-    for s in range(args.warmup):
+    graph = None
+    if device:
+        # the whole step in one CUDA graph over static input buffers; a step copies its
+        # inputs in and replays the graph (the LRU and the fills run on the GPU)
+        xin = {B: torch.empty((B, W.H), dtype=torch.bfloat16, device="cuda") for B in BATCHES}
+        rin = {B: torch.empty((B, W.H), dtype=torch.float32, device="cuda") for B in BATCHES}
+
+        def static_step(c):
+            for B in BATCHES:
+                c.route(0, xin[B], Wr, bias, idx[B], wts[B])
+                c.layer_forward(0, xin[B], rin[B], out[B], idx[B], wts[B])
+
+        def load(s):
+            for B in BATCHES:
+                xin[B].copy_(xs[s][B], non_blocking=True)
+                rin[B].copy_(resid[s][B], non_blocking=True)
+
+        with torch.cuda.stream(stream):
+            load(0)
+            static_step(cache)  # eager once: kernel attributes are set outside the capture
+        cache.sync()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            static_step(cache)
+
+        def step(c, s):  # noqa: F811 -- the device-policy step
+            with torch.cuda.stream(stream):
+                load(s)
+                graph.replay()
+
+    for s in range(1 if device else 0, args.warmup):
         step(cache, s)
     cache.sync()
     cache.stats(reset=True)
@@ -275,6 +316,14 @@ def run_b300(args, rank, world, local):
 
         def step_e2e(s):
             with torch.cuda.stream(stream):
+                if device:
+                    for B in BATCHES:
+                        xin[B].copy_(hx[s][B], non_blocking=True)
+                        rin[B].copy_(hr[s][B], non_blocking=True)
+                    graph.replay()
+                    for B in BATCHES:
+                        hout[B].copy_(out[B], non_blocking=True)
+                    return
                 for B in BATCHES:
                     dx[B].copy_(hx[s][B], non_blocking=True)
                     dr[B].copy_(hr[s][B], non_blocking=True)
@@ -306,15 +355,23 @@ def run_b300(args, rank, world, local):
     cache.set_profile(True)
     cache.kernel_stats(reset=True)
     for s in range(args.warmup, min(total, args.warmup + 16)):
-        step(cache, s)
+        for B in BATCHES:  # eager calls (graph replays are not profiled per launch)
+            cache.route(0, xs[s][B], Wr, bias, idx[B], wts[B])
+            cache.layer_forward(0, xs[s][B], resid[s][B], out[B], idx[B], wts[B])
     cache.sync()
     kst_lru = cache.kernel_stats()
+    del graph
     cache.close()
     del cache
     torch.cuda.synchronize()
 
     # every expert resident (the prefill leg's context): the same decode batches again, so the
     # decode kernels' time is their own weight streaming -- the roofline pass
+    def step(c, s):  # noqa: F811 -- eager steps for the resident context
+        for B in BATCHES:
+            c.route(0, xs[s][B], Wr, bias, idx[B], wts[B])
+            c.layer_forward(0, xs[s][B], resid[s][B], out[B], idx[B], wts[B])
+
     res = resident_context(args, W, E=W.E)
     rc = res["cache"]
     for s in range(args.warmup):
@@ -375,6 +432,8 @@ def run_b300(args, rank, world, local):
     # launches of this library's kernels in the timed region: route (2) + permute, gather,
     # combine (3) per forward, and two expert kernels per wave
     launches = args.steps * (5 * len(BATCHES)) + 2 * st["waves"]
+    if device:  # per forward: policy, fill and 4 decode launches for each possible wave
+        launches = args.steps * sum(5 + 6 * ((min(B * W.k, W.E) + C - 1) // C) for B in BATCHES)
 
     result = {
         "metric": METRIC, "value": round(tokens / (ms_max / 1e3), 2), "unit": UNIT, "n_gpus": world,
@@ -383,13 +442,15 @@ def run_b300(args, rank, world, local):
         "data": "synthetic (seeded Philox: N(0,0.02) bf16 weights, N(0,1) activations, Zipf(1.1) router bias)",
         "config": {"workload": "decode layer: hidden 4096, intermediate 1536, 256 experts top-6, "
                                "64-entry LRU cache, batches 1+4+16 per step",
+                   "policy": "device (CUDA graph per step)" if device else "host",
                    "tokens_per_step": sum(BATCHES), "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2: each step streams >= 226 MB of expert weights (L2 126 MB)",
                    "hit_rate": (st["hits"] / st["expert_reads"]) if st["expert_reads"] else None,
                    "fills_per_step": st["misses"] / args.steps,
                    "fill_GBps": (st["fill_bytes"] / (st["fill_ms"] / 1e3) / 1e9) if st["fill_ms"] else None,
                    "fill_share_of_step": ((st["fill_ms"] / args.steps) / (ms_max / args.steps))
-                   if st["fill_ms"] else None},
+                   if st["fill_ms"] else None,
+                   "fill_GB_per_step": st["fill_bytes"] / args.steps / 1e9},
         "clocks": clk, "e2e": e2e, "gpu_launches": int(launches), "roofline": roof,
         "resident_pass": {"ms_per_step": round(ms_resident, 4),
                           "tok_s": round(sum(BATCHES) / (ms_resident / 1e3), 1),
@@ -543,7 +604,9 @@ def run_stream8(args):
     total = args.warmup + steps
     t0 = time.time()
     stream = torch.cuda.Stream()
-    cache = moe.MoeCache(moe.LayerShape(W.L, W.E, W.H, W.I, W.k, W.C, B), flags=0, stream_compute=stream)
+    device = args.policy == "device"
+    cache = moe.MoeCache(moe.LayerShape(W.L, W.E, W.H, W.I, W.k, W.C, B),
+                         flags=moe.MOE_DEVICE_POLICY if device else 0, stream_compute=stream)
     fill_pool(cache, W, W.L, W.E)
     setup_s = time.time() - t0
     Wr = [torch.from_numpy(mi.router_weights(W.seed, l, W.E, W.H)).cuda() for l in range(W.L)]
@@ -565,7 +628,36 @@ def run_stream8(args):
             cache.route_forced(l, xs[s, l], Wr[l], bias[l], sets[s, l], idx, wts)
             cache.layer_forward(l, xs[s, l], resid[s, l], out, idx, wts)
 
-    for s in range(args.warmup):
+    if device:
+        # the 8-layer step in one CUDA graph over static inputs, replayed per step
+        xin = torch.empty_like(xs[0])
+        rin = torch.empty_like(resid[0])
+        sin = torch.empty_like(sets[0])
+
+        def static_step():
+            for l in range(W.L):
+                cache.route_forced(l, xin[l], Wr[l], bias[l], sin[l], idx, wts)
+                cache.layer_forward(l, xin[l], rin[l], out, idx, wts)
+
+        def load(s):
+            xin.copy_(xs[s], non_blocking=True)
+            rin.copy_(resid[s], non_blocking=True)
+            sin.copy_(sets[s], non_blocking=True)
+
+        with torch.cuda.stream(stream):
+            load(0)
+            static_step()
+        cache.sync()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            static_step()
+
+        def step(s):  # noqa: F811 -- the device-policy step
+            with torch.cuda.stream(stream):
+                load(s)
+                graph.replay()
+
+    for s in range(1 if device else 0, args.warmup):
         step(s)
     cache.sync()
     cache.stats(reset=True)
@@ -590,6 +682,7 @@ def run_stream8(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded Philox)",
             "config": {"workload": "8-layer decode stream: hidden 4096, intermediate 1536, 256 experts top-6, "
                                    "batch 8, reuse trace p=0.7, 614-entry LRU over 2048 (layer, expert) entries",
+                       "policy": "device (CUDA graph per step)" if device else "host",
                        "pool_GB": W.L * W.E * 3 * W.H * W.I * 2 / 1e9, "setup_s": round(setup_s, 1),
                        **_stats_summary(st, ms)},
             "clocks": clk, "gpu_launches": int(steps * W.L * 5 + 2 * st["waves"])}
