@@ -818,17 +818,21 @@ def run_reference(args):
 
 
 # ----------------------------------------------------------------------------- distributed glue
+# Replicas only: ranks share no data; the glue is a barrier around the timed region and the
+# max of the ranks' times (the job is as slow as its slowest replica).
 _pg = False
+_backend = None
 
 
-def init_dist(world, local):
-    global _pg
+def init_dist(world, local, backend: str = "nccl"):
+    global _pg, _backend
     if world > 1:
         import torch
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
-        _pg = True
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+        _pg, _backend = True, backend
 
 
 def barrier(world):
@@ -842,9 +846,17 @@ def allreduce_max(v: float, world: int) -> float:
         return v
     import torch
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if _backend == "nccl" else "cpu")
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def close_dist():
+    global _pg
+    if _pg:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+        _pg = False
 
 
 def main():
@@ -874,9 +886,7 @@ def main():
     res = run_b300(args, rank, world, local)
     if rank == 0:
         print(json.dumps(res), flush=True)
-    if _pg:
-        import torch.distributed as dist
-        dist.destroy_process_group()
+    close_dist()
 
 
 if __name__ == "__main__":
