@@ -55,7 +55,7 @@ def lib():
         L.orc_moe_dense.argtypes = [vp, i32, i32, i32, vp, vp, i32, i32, vp, vp, vp]
         L.orc_layer_accesses.argtypes = [vp, i32, i32, i32, vp]
         L.orc_layer_accesses.restype = i32
-        L.orc_lru_run.argtypes = [i32, i32, vp, vp, vp, vp, vp, vp, vp]
+        L.orc_lru_run.argtypes = [i32, i32, vp, vp, vp, i32, vp, vp, vp, vp, vp, vp]
         L.orc_lru_run.restype = i32
         _lib = L
     return _lib
@@ -197,19 +197,21 @@ def layer_accesses(idx: np.ndarray, E: int) -> np.ndarray:
 
 
 def lru_run(capacity: int, layers, experts, kinds=None) -> np.ndarray:
-    """Run the LRU over an access sequence. Returns events as an int32 array (n, 6):
-    (kind, layer, expert, slot, evicted_layer, evicted_expert)."""
+    """Run the LRU over an operation sequence (kind 0 routed access, 1 prefetch, 2 capacity
+    change to `experts[i]` slots). Returns events as an int32 array (n_events, 6):
+    (kind, layer, expert, slot, evicted_layer, evicted_expert); kind 4 = evicted by a
+    capacity change."""
     l = _c(layers, np.int32)
     e = _c(experts, np.int32)
     n = len(l)
     kd = _c(np.zeros(n) if kinds is None else kinds, np.int32)
-    k_out = np.empty(n, np.int32)
-    s_out = np.empty(n, np.int32)
-    vl = np.empty(n, np.int32)
-    ve = np.empty(n, np.int32)
-    if lib().orc_lru_run(capacity, n, _p(l), _p(e), _p(kd), _p(k_out), _p(s_out), _p(vl), _p(ve)) != 0:
+    cap_max = int(max([capacity] + [int(x) for x, k in zip(e, kd) if k == 2]))
+    m = n + cap_max * int(np.sum(kd == 2)) + 1
+    outs = [np.empty(m, np.int32) for _ in range(6)]
+    got = lib().orc_lru_run(capacity, n, _p(l), _p(e), _p(kd), m, *[_p(o) for o in outs])
+    if got < 0:
         raise ValueError("capacity must be >= 1")
-    return np.stack([k_out, l, e, s_out, vl, ve], axis=1)
+    return np.stack([o[:got] for o in outs], axis=1)
 
 
 def route(x_bf16, Wr, b, k):

@@ -266,33 +266,70 @@ int orc_layer_accesses(const int32_t* idx, int T, int k, int E, int32_t* experts
 }
 
 // Shared LRU over whole (layer, expert) entries with `capacity` slots, run on a sequence
-// of accesses; kind_in[i] = 0 for a routed access, 1 for a prefetch of the whole next layer.
+// of operations; kind_in[i] = 0 for a routed access, 1 for a prefetch of the whole next
+// layer, 2 for a change of capacity to expert[i] slots (layer[i] ignored).
 // Brute force: a recency list scanned linearly, MRU first.
 // A present key is a hit and becomes MRU. An absent key takes the lowest free slot; if
 // none is free, the LRU entry is evicted and its slot reused; the key becomes MRU.
-// Event kinds out: 0 HIT, 1 FILL (routed miss), 2 PREFETCH_FILL, 3 PREFETCH_HIT.
-// ev_vl/ev_ve = evicted (layer, expert), or -1/-1. Returns 0, or -1 for capacity < 1.
+// A capacity change keeps the min(n, new) most recently used entries and evicts the others,
+// least recent first; the survivors are renumbered 0, 1, ... in the order of their old
+// slots, and the slots from the number of survivors up to the new capacity are free.
+// Events out, one per access and one per entry evicted by a capacity change:
+//   kind 0 HIT, 1 FILL (routed miss), 2 PREFETCH_FILL, 3 PREFETCH_HIT, 4 RESIZE_EVICT;
+//   (layer, expert) of the access or of the evicted entry; slot = the entry's slot
+//   (for RESIZE_EVICT the slot it held); ev_vl/ev_ve = evicted (layer, expert) or -1/-1.
+// Returns the number of events (at most max_events), or -1 for a capacity < 1 or too many
+// events.
 int orc_lru_run(int capacity, int n, const int32_t* layer, const int32_t* expert, const int32_t* kind_in,
-                int32_t* ev_kind, int32_t* ev_slot, int32_t* ev_vl, int32_t* ev_ve) {
+                int max_events, int32_t* ev_kind, int32_t* ev_l, int32_t* ev_e, int32_t* ev_slot, int32_t* ev_vl,
+                int32_t* ev_ve) {
     if (capacity < 1) return -1;
     std::vector<std::pair<int, int>> recency;  // front = most recently used
     std::map<std::pair<int, int>, int> slot_of;
     std::set<int> free_slots;
     for (int s = 0; s < capacity; ++s) free_slots.insert(s);
+    int m = 0;
+    auto emit = [&](int kind, int l, int e, int slot, int vl, int ve) {
+        if (m >= max_events) return false;
+        ev_kind[m] = kind;
+        ev_l[m] = l;
+        ev_e[m] = e;
+        ev_slot[m] = slot;
+        ev_vl[m] = vl;
+        ev_ve[m] = ve;
+        ++m;
+        return true;
+    };
     for (int i = 0; i < n; ++i) {
+        if (kind_in[i] == 2) {
+            const int cap2 = expert[i];
+            if (cap2 < 1) return -1;
+            while (static_cast<int>(recency.size()) > cap2) {
+                std::pair<int, int> victim = recency.back();
+                recency.pop_back();
+                if (!emit(4, victim.first, victim.second, slot_of[victim], -1, -1)) return -1;
+                slot_of.erase(victim);
+            }
+            // renumber the survivors in the order of their old slots
+            std::vector<std::pair<int, std::pair<int, int>>> by_slot;
+            for (const auto& kv : slot_of) by_slot.push_back({kv.second, kv.first});
+            std::sort(by_slot.begin(), by_slot.end());
+            for (size_t r = 0; r < by_slot.size(); ++r) slot_of[by_slot[r].second] = static_cast<int>(r);
+            free_slots.clear();
+            for (int s = static_cast<int>(by_slot.size()); s < cap2; ++s) free_slots.insert(s);
+            capacity = cap2;
+            continue;
+        }
         std::pair<int, int> key(layer[i], expert[i]);
         bool prefetch = kind_in[i] == 1;
         auto it = std::find(recency.begin(), recency.end(), key);
-        ev_vl[i] = -1;
-        ev_ve[i] = -1;
         if (it != recency.end()) {
             recency.erase(it);
             recency.insert(recency.begin(), key);
-            ev_kind[i] = prefetch ? 3 : 0;
-            ev_slot[i] = slot_of[key];
+            if (!emit(prefetch ? 3 : 0, key.first, key.second, slot_of[key], -1, -1)) return -1;
             continue;
         }
-        int slot;
+        int slot, vl = -1, ve = -1;
         if (!free_slots.empty()) {
             slot = *free_slots.begin();
             free_slots.erase(free_slots.begin());
@@ -301,15 +338,14 @@ int orc_lru_run(int capacity, int n, const int32_t* layer, const int32_t* expert
             recency.pop_back();
             slot = slot_of[victim];
             slot_of.erase(victim);
-            ev_vl[i] = victim.first;
-            ev_ve[i] = victim.second;
+            vl = victim.first;
+            ve = victim.second;
         }
         recency.insert(recency.begin(), key);
         slot_of[key] = slot;
-        ev_kind[i] = prefetch ? 2 : 1;
-        ev_slot[i] = slot;
+        if (!emit(prefetch ? 2 : 1, key.first, key.second, slot, vl, ve)) return -1;
     }
-    return 0;
+    return m;
 }
 
 }  // extern "C"

@@ -1,7 +1,8 @@
 """Pins for the oracle's shared LRU over whole (layer, expert) entries (CPU).
 
-Hand-traced sequences (tests/golden/lru_hand_traces.txt), LRU's inclusion property (a
-stack algorithm: with one more slot the hit set can only grow), and closed-form counts.
+Hand-traced sequences (tests/golden/lru_hand_traces.txt), hand-traced capacity changes
+(tests/golden/lru_resize_traces.txt), LRU's inclusion property (a stack algorithm: with one
+more slot the hit set can only grow), and closed-form counts.
 """
 import os
 
@@ -11,12 +12,12 @@ import pytest
 import oracle
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
-KIND = {"HIT": 0, "FILL": 1, "PFILL": 2, "PHIT": 3}
+KIND = {"HIT": 0, "FILL": 1, "PFILL": 2, "PHIT": 3, "REVICT": 4}
 
 
-def load_cases():
+def load_cases(name="lru_hand_traces.txt"):
     cases, cur = [], None
-    for line in open(os.path.join(GOLDEN, "lru_hand_traces.txt")):
+    for line in open(os.path.join(GOLDEN, name)):
         line = line.strip()
         if not line or line.startswith("#"):
             continue
@@ -25,6 +26,13 @@ def load_cases():
             cur = {"name": name, "cap": int(cap), "acc": [], "ev": []}
         elif line == "end":
             cases.append(cur)
+        elif line.startswith("C "):
+            lhs, rhs = line.split("->")
+            cur["acc"].append((2, 0, int(lhs.split()[1])))
+            if rhs.strip() != "none":
+                for part in rhs.split(";"):
+                    kind, l, e, slot = part.split()
+                    cur["ev"].append((KIND[kind], int(l), int(e), int(slot), -1, -1))
         else:
             lhs, rhs = line.split("->")
             a, l, e = lhs.split()
@@ -39,6 +47,28 @@ def test_lru_hand_traces(case):
     acc = np.array(case["acc"], np.int32)
     ev = oracle.lru_run(case["cap"], acc[:, 1], acc[:, 2], acc[:, 0])
     assert [tuple(r) for r in ev.tolist()] == case["ev"]
+
+
+@pytest.mark.parametrize("case", load_cases("lru_resize_traces.txt"), ids=lambda c: c["name"])
+def test_lru_resize_hand_traces(case):
+    acc = np.array(case["acc"], np.int32)
+    ev = oracle.lru_run(case["cap"], acc[:, 1], acc[:, 2], acc[:, 0])
+    assert [tuple(r) for r in ev.tolist()] == case["ev"]
+
+
+def test_lru_resize_to_the_same_size_changes_nothing():
+    """A capacity change to the current capacity with every slot in use evicts nothing and
+    renumbers nothing: the run continues exactly as without it."""
+    rng = np.random.default_rng(9)
+    n, cap = 3000, 7
+    e = rng.integers(0, 20, n)
+    base = oracle.lru_run(cap, np.zeros(n), e)
+    ins = 1500
+    assert len(np.unique(e[:ins])) >= cap  # every slot is in use at the change
+    l2 = np.concatenate([np.zeros(ins), [0], np.zeros(n - ins)])
+    e2 = np.concatenate([e[:ins], [cap], e[ins:]])
+    k2 = np.concatenate([np.zeros(ins), [2], np.zeros(n - ins)])
+    assert np.array_equal(oracle.lru_run(cap, l2, e2, k2), base)
 
 
 def test_lru_inclusion_property():
