@@ -81,6 +81,7 @@ extern "C" {
 #define MOE_EV_FILL 1          /* routed access, entry copied in (a miss) */
 #define MOE_EV_PREFETCH_FILL 2 /* whole-layer prefetch copied the entry in */
 #define MOE_EV_PREFETCH_HIT 3  /* whole-layer prefetch found the entry resident */
+#define MOE_EV_RESIZE_EVICT 4  /* moe_cache_resize evicted the entry (slot = the slot it held) */
 
 typedef struct moe_ctx moe_ctx; /* opaque: pinned pool, slot arena, LRU, streams, scratch */
 
@@ -108,6 +109,7 @@ typedef struct {
     uint64_t trace_len;      /* events recorded since the last reset (the ring keeps the newest) */
     uint64_t forwards;       /* moe_layer_forward calls */
     uint64_t waves;          /* expert waves run (a layer routing to more than C experts runs several) */
+    uint64_t resize_evictions; /* entries evicted by moe_cache_resize */
 } moe_stats_t;
 
 typedef struct {
@@ -147,6 +149,22 @@ void moe_cache_destroy(moe_ctx* ctx);
  * Entries must not change while a fill of that entry may be in flight.
  */
 void* moe_host_entry(moe_ctx* ctx, int layer, int expert);
+
+/*
+ * Elastic cache: change the capacity to new_capacity entries at a safe point. The call waits
+ * (with the deadline) until the context's enqueued work has finished, then:
+ *  - keeps the min(n_resident, new_capacity) most recently used entries and evicts the
+ *    others, least recent first (trace events MOE_EV_RESIZE_EVICT, counter resize_evictions);
+ *  - moves the survivors into a new device arena of new_capacity slots, renumbered 0, 1, ...
+ *    in the order of their old slots (growing moves nothing); the slots above are free;
+ *  - keeps the recency order, the host pool and every counter.
+ * Later misses take the lowest free slot, then the least recently used entry, as before. The
+ * old arena is freed after the copy, so the device holds both for the duration of the call.
+ * Errors: MOE_E_INVAL (new_capacity < 1, or arena too large), MOE_E_CAPACITY (MOE_PREFILL_DB
+ * with new_capacity < 2*num_experts), MOE_E_NOMEM (the new arena could not be allocated; the
+ * cache is unchanged), MOE_E_TIMEOUT, MOE_E_CUDA.
+ */
+int moe_cache_resize(moe_ctx* ctx, int new_capacity);
 
 /* Bytes of one entry: 3 * hidden * inter * 2. */
 uint64_t moe_entry_bytes(const moe_ctx* ctx);
@@ -242,11 +260,14 @@ int moe_kernel_stats(moe_ctx* ctx, moe_kernel_stat_t* out, int cap, int reset);
 
 /*
  * Host-only run of this library's LRU policy (no GPU, no context): capacity slots, n
- * accesses (layer[i], expert[i], kind[i]: 0 routed, 1 prefetch). Writes n events. Lets the
- * host policy be checked against a reference without a GPU. Returns 0 or MOE_E_INVAL.
+ * operations (layer[i], expert[i], kind[i]: 0 routed access, 1 prefetch, 2 capacity change to
+ * expert[i] slots as moe_cache_resize does it). Writes one event per access and one
+ * MOE_EV_RESIZE_EVICT event per entry a capacity change evicts, at most events_cap. Lets the
+ * host policy be checked against a reference without a GPU. Returns the number of events
+ * written, or MOE_E_INVAL (bad arguments, or more events than events_cap).
  */
 int moe_lru_simulate(int capacity, int n, const int32_t* layer, const int32_t* expert, const int32_t* kind,
-                     moe_event_t* events);
+                     moe_event_t* events, uint64_t events_cap);
 
 /*
  * Host-side fault injection for tests: the next `count` fill copies of this context report

@@ -22,13 +22,13 @@ MOE_OK, MOE_E_INVAL, MOE_E_NOMEM, MOE_E_CUDA, MOE_E_TIMEOUT, MOE_E_CAPACITY, MOE
 MOE_TRACE, MOE_PROFILE, MOE_PREFILL_DB, MOE_DEVICE_POLICY = 1, 2, 4, 8
 MOE_FILL_DEMAND, MOE_FILL_FULL_LAYER = 0, 1
 MOE_PATH_AUTO, MOE_PATH_GEMV, MOE_PATH_GEMM = 0, 1, 2
-EV_HIT, EV_FILL, EV_PREFETCH_FILL, EV_PREFETCH_HIT = 0, 1, 2, 3
+EV_HIT, EV_FILL, EV_PREFETCH_FILL, EV_PREFETCH_HIT, EV_RESIZE_EVICT = 0, 1, 2, 3, 4
 
 # every symbol include/moe.h declares
 EXPORTS = ["moe_cache_init", "moe_cache_destroy", "moe_host_entry", "moe_entry_bytes", "moe_route",
            "moe_route_forced", "moe_cache_fill", "moe_layer_forward", "moe_stats", "moe_last_error",
            "moe_set_path", "moe_set_profile", "moe_sync", "moe_resident_slot", "moe_kernel_stats", "moe_lru_simulate",
-           "moe_debug_inject", "moe_debug_read", "moe_route_noalloc"]
+           "moe_debug_inject", "moe_debug_read", "moe_route_noalloc", "moe_cache_resize"]
 MOE_NOALLOC_MAX_LOGITS = 65536
 MOE_DBG_OFFSETS, MOE_DBG_PERM, MOE_DBG_INV_PERM, MOE_DBG_ACTIVE, MOE_DBG_N_ACTIVE, MOE_DBG_SLOT_TABLE, \
     MOE_DBG_H_PERM = range(7)
@@ -50,7 +50,8 @@ class Stats(ctypes.Structure):
     _fields_ = [("expert_reads", ctypes.c_uint64), ("hits", ctypes.c_uint64), ("misses", ctypes.c_uint64),
                 ("prefetch_fills", ctypes.c_uint64), ("prefetch_hits", ctypes.c_uint64),
                 ("evictions", ctypes.c_uint64), ("fill_bytes", ctypes.c_uint64), ("fill_ms", ctypes.c_double),
-                ("trace_len", ctypes.c_uint64), ("forwards", ctypes.c_uint64), ("waves", ctypes.c_uint64)]
+                ("trace_len", ctypes.c_uint64), ("forwards", ctypes.c_uint64), ("waves", ctypes.c_uint64),
+                ("resize_evictions", ctypes.c_uint64)]
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}
@@ -96,7 +97,8 @@ def lib():
     L.moe_sync.argtypes = [vp]
     L.moe_resident_slot.argtypes = [vp, i32, i32]
     L.moe_kernel_stats.argtypes = [vp, vp, i32, i32]
-    L.moe_lru_simulate.argtypes = [i32, i32, vp, vp, vp, vp]
+    L.moe_lru_simulate.argtypes = [i32, i32, vp, vp, vp, vp, u64]
+    L.moe_cache_resize.argtypes = [vp, i32]
     L.moe_debug_inject.argtypes = [vp, i32, i32]
     L.moe_debug_read.argtypes = [vp, i32, vp, u64]
     L.moe_route_noalloc.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp, vp, vp]
@@ -132,18 +134,22 @@ def _stream_handle(stream) -> int:
 
 
 def lru_simulate(capacity: int, layers, experts, kinds=None):
-    """Run the library's host LRU policy on an access sequence (no GPU). Returns rows
-    (kind, layer, expert, slot, evicted_layer, evicted_expert)."""
+    """Run the library's host LRU policy on an operation sequence (no GPU): kind 0 routed
+    access, 1 prefetch, 2 capacity change to experts[i] slots. Returns rows (kind, layer,
+    expert, slot, evicted_layer, evicted_expert), one per access and one per entry evicted by
+    a capacity change (kind 4)."""
     import numpy as np
     l = np.ascontiguousarray(layers, dtype=np.int32)
     e = np.ascontiguousarray(experts, dtype=np.int32)
     n = len(l)
     k = np.ascontiguousarray(np.zeros(n) if kinds is None else kinds, dtype=np.int32)
-    ev = (Event * max(n, 1))()
-    _check(lib().moe_lru_simulate(capacity, n, l.ctypes.data, e.ctypes.data, k.ctypes.data, ctypes.addressof(ev)),
-           "moe_lru_simulate")
+    cap_max = int(max([capacity] + [int(x) for x, kk in zip(e, k) if kk == 2]))
+    m = n + cap_max * int(np.sum(k == 2)) + 1
+    ev = (Event * m)()
+    got = _check(lib().moe_lru_simulate(capacity, n, l.ctypes.data, e.ctypes.data, k.ctypes.data,
+                                        ctypes.addressof(ev), m), "moe_lru_simulate")
     return np.array([[ev[i].kind, ev[i].layer, ev[i].expert, ev[i].slot, ev[i].ev_layer, ev[i].ev_expert]
-                     for i in range(n)], dtype=np.int32).reshape(n, 6)
+                     for i in range(got)], dtype=np.int32).reshape(got, 6)
 
 
 def route_noalloc(x, router_w, router_b, topk_idx, topk_w, top_k: int, stream=None, T: Optional[int] = None):
@@ -234,6 +240,10 @@ class MoeCache:
         T = x.shape[0] if T is None else T
         _check(lib().moe_layer_forward(self._h, layer, _ptr(x), _ptr(resid), _ptr(out), T, _ptr(topk_idx),
                                        _ptr(topk_w)), "moe_layer_forward")
+
+    def resize(self, capacity: int):
+        """Elastic cache: change the capacity at a safe point (waits for enqueued work)."""
+        _check(lib().moe_cache_resize(self._h, capacity), "moe_cache_resize")
 
     def set_path(self, path: int):
         _check(lib().moe_set_path(self._h, path), "moe_set_path")

@@ -78,7 +78,7 @@ struct DevLruState {
 };
 struct DevStats {  // the fields of moe_stats_t that the device policy counts
     unsigned long long expert_reads, hits, misses, prefetch_fills, prefetch_hits, evictions, fill_bytes, trace_len,
-        forwards, waves;
+        forwards, waves, resize_evictions;
 };
 struct DevEvent {
     int kind, layer, expert, slot, ev_layer, ev_expert;

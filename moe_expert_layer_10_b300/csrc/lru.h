@@ -7,14 +7,19 @@
 // Large MoE Models" -- recently routed experts stay in VRAM, misses are filled over PCIe.
 //
 // Slot rule (the pages are silent): a miss takes the lowest free slot; when none is free
-// it takes the slot of the least recently used entry. O(1) touch and evict: an intrusive
+// it takes the slot of the least recently used entry. A capacity change (elastic cache)
+// keeps the most recently used entries that fit, evicts the others least recent first, and
+// renumbers the survivors 0, 1, ... in the order of their old slots, so the used slots are
+// always 0 .. n_used-1. O(1) touch and evict: an intrusive
 // doubly-linked recency list over slots plus a key -> slot array. Decisions are planned
 // first and committed only after the fill copy was enqueued, so a failed fill leaves the
 // policy exactly as it was.
 #pragma once
 
+#include <algorithm>
 #include <cstdint>
 #include <set>
+#include <utility>
 #include <vector>
 
 namespace moe {
@@ -45,6 +50,66 @@ class ExpertLru {
     }
 
     int capacity() const { return cap_; }
+    int used() const { return cap_ - static_cast<int>(free_.size()); }
+
+    // Change the capacity. evicted receives (key, old slot) of each evicted entry, least
+    // recent first; moved receives (old slot, new slot) of each survivor whose slot changes.
+    void resize(int new_cap, std::vector<std::pair<int, int>>* evicted, std::vector<std::pair<int, int>>* moved) {
+        std::vector<int> rec;  // used slots, most recent first
+        for (int s = head_; s >= 0; s = next_[s]) rec.push_back(s);
+        const int keep = std::min(static_cast<int>(rec.size()), new_cap);
+        for (int i = static_cast<int>(rec.size()) - 1; i >= keep; --i) {
+            evicted->push_back({key_in_[rec[i]], rec[i]});
+            slot_of_[key_in_[rec[i]]] = -1;
+        }
+        std::vector<int> by_slot(rec.begin(), rec.begin() + keep);
+        std::sort(by_slot.begin(), by_slot.end());
+        std::vector<int> new_of(cap_, -1);
+        for (int r = 0; r < keep; ++r) {
+            new_of[by_slot[r]] = r;
+            if (by_slot[r] != r) moved->push_back({by_slot[r], r});
+        }
+        std::vector<int> key2(new_cap, -1), prev2(new_cap, -1), next2(new_cap, -1);
+        for (int r = 0; r < keep; ++r) key2[r] = key_in_[by_slot[r]];
+        for (int i = 0; i < keep; ++i) {
+            const int s = new_of[rec[i]];
+            prev2[s] = i > 0 ? new_of[rec[i - 1]] : -1;
+            next2[s] = i + 1 < keep ? new_of[rec[i + 1]] : -1;
+        }
+        head_ = keep > 0 ? new_of[rec[0]] : -1;
+        tail_ = keep > 0 ? new_of[rec[keep - 1]] : -1;
+        for (int r = 0; r < keep; ++r) slot_of_[key2[r]] = r;
+        key_in_.swap(key2);
+        prev_.swap(prev2);
+        next_.swap(next2);
+        cap_ = new_cap;
+        free_.clear();
+        for (int s2 = keep; s2 < new_cap; ++s2) free_.insert(s2);
+    }
+
+    // The recency list and slot contents, for a policy that runs elsewhere (the GPU).
+    void export_state(std::vector<int>* prev, std::vector<int>* next, std::vector<int>* key, int* head, int* tail,
+                      int* n_used) const {
+        *prev = prev_;
+        *next = next_;
+        *key = key_in_;
+        *head = head_;
+        *tail = tail_;
+        *n_used = used();
+    }
+    void import_state(const std::vector<int>& prev, const std::vector<int>& next, const std::vector<int>& key,
+                      int head, int tail, int n_used) {
+        prev_ = prev;
+        next_ = next;
+        key_in_ = key;
+        head_ = head;
+        tail_ = tail;
+        std::fill(slot_of_.begin(), slot_of_.end(), -1);
+        for (int s = 0; s < cap_; ++s)
+            if (key_in_[s] >= 0) slot_of_[key_in_[s]] = s;
+        free_.clear();
+        for (int s = n_used; s < cap_; ++s) free_.insert(s);
+    }
     int slot_of(int key) const { return slot_of_[key]; }
     int key_in(int slot) const { return key_in_[slot]; }
 

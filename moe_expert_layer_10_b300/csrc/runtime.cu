@@ -437,6 +437,15 @@ int access_keys(moe_ctx* c, const std::vector<int>& keys, bool prefetch) {
     return rc;
 }
 
+// TMA views of the slot arena (they change when the arena is reallocated).
+bool make_arena_maps(moe_ctx* c) {
+    const uint64_t H = c->H, I = c->I, C = c->C;
+    return make_map(&c->dec_maps.a_gu, c->arena, H, C * 3 * I, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
+           make_map(&c->dec_maps.a_d, c->arena, I, C * 3 * H, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) &&
+           make_map(&c->gemm_maps.b_gu, c->arena, H, C * 3 * I, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) &&
+           make_map(&c->gemm_maps.b_d, c->arena, I, C * 3 * H, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
 int validate_layer(moe_ctx* c, int layer) {
     if (!c) return fail(MOE_E_INVAL, "null context");
     if (layer < 0 || layer >= c->L) return fail(MOE_E_INVAL, "layer %d outside [0, %d)", layer, c->L);
@@ -593,6 +602,29 @@ int drain(moe_ctx* c) {
     return rc;
 }
 
+// The device policy's recency list into the host LRU (the device owns it between calls).
+int dev_state_pull(moe_ctx* c) {
+    std::vector<int> prev(c->C), next(c->C), key(c->C);
+    moe::DevLruState st{};
+    CUDA_TRY(cudaMemcpy(prev.data(), c->d_prev, c->C * sizeof(int), cudaMemcpyDeviceToHost));
+    CUDA_TRY(cudaMemcpy(next.data(), c->d_next, c->C * sizeof(int), cudaMemcpyDeviceToHost));
+    CUDA_TRY(cudaMemcpy(key.data(), c->d_key, c->C * sizeof(int), cudaMemcpyDeviceToHost));
+    CUDA_TRY(cudaMemcpy(&st, c->d_lru, sizeof(st), cudaMemcpyDeviceToHost));
+    c->lru.import_state(prev, next, key, st.head, st.tail, st.n_used);
+    return MOE_OK;
+}
+
+int dev_state_push(moe_ctx* c) {
+    std::vector<int> prev, next, key;
+    moe::DevLruState st{};
+    c->lru.export_state(&prev, &next, &key, &st.head, &st.tail, &st.n_used);
+    CUDA_TRY(cudaMemcpy(c->d_prev, prev.data(), c->C * sizeof(int), cudaMemcpyHostToDevice));
+    CUDA_TRY(cudaMemcpy(c->d_next, next.data(), c->C * sizeof(int), cudaMemcpyHostToDevice));
+    CUDA_TRY(cudaMemcpy(c->d_key, key.data(), c->C * sizeof(int), cudaMemcpyHostToDevice));
+    CUDA_TRY(cudaMemcpy(c->d_lru, &st, sizeof(st), cudaMemcpyHostToDevice));
+    return MOE_OK;
+}
+
 }  // namespace
 
 namespace moe {
@@ -747,15 +779,12 @@ int moe_cache_init(const moe_config_t* cfg, void* stream_compute, void* stream_c
     }
 
     // TMA views. Arena rows: [C*3I x H] for gate/up, [C*3H x I] for down.
-    const uint64_t H = c->H, I = c->I, C = c->C, P = c->Pmax;
-    bool ok = make_map(&c->dec_maps.a_gu, c->arena, H, C * 3 * I, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
-              make_map(&c->dec_maps.a_d, c->arena, I, C * 3 * H, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) &&
+    const uint64_t H = c->H, I = c->I, P = c->Pmax;
+    bool ok = make_arena_maps(c) &&
               make_map(&c->dec_maps.b_x, c->x_perm, H, P, 64, 16, CU_TENSOR_MAP_SWIZZLE_128B) &&
               make_map(&c->dec_maps.b_h, c->h_perm, I, P, 64, 16, CU_TENSOR_MAP_SWIZZLE_128B) &&
               make_map(&c->gemm_maps.a_x, c->x_perm, H, P, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) &&
-              make_map(&c->gemm_maps.b_gu, c->arena, H, C * 3 * I, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) &&
-              make_map(&c->gemm_maps.a_h, c->h_perm, I, P, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) &&
-              make_map(&c->gemm_maps.b_d, c->arena, I, C * 3 * H, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+              make_map(&c->gemm_maps.a_h, c->h_perm, I, P, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
     if (!ok) {
         free_all(c);
         return fail(MOE_E_CUDA, "cuTensorMapEncodeTiled rejected a tensor view");
@@ -788,6 +817,117 @@ int moe_set_path(moe_ctx* c, int path) {
     if (path != MOE_PATH_AUTO && path != MOE_PATH_GEMV && path != MOE_PATH_GEMM)
         return fail(MOE_E_INVAL, "unknown path %d", path);
     c->path = path;
+    return MOE_OK;
+}
+
+int moe_cache_resize(moe_ctx* c, int new_C) {
+    g_last_error.clear();
+    if (!c) return fail(MOE_E_INVAL, "null context");
+    if (new_C < 1) return fail(MOE_E_INVAL, "capacity %d < 1", new_C);
+    if ((c->cfg.flags & MOE_PREFILL_DB) && new_C < 2 * c->E)
+        return fail(MOE_E_CAPACITY, "double buffering needs capacity >= 2 * num_experts (%d < %d)", new_C, 2 * c->E);
+    if (static_cast<uint64_t>(new_C) * 3ull * c->I >= (1ull << 31) ||
+        static_cast<uint64_t>(new_C) * 3ull * c->H >= (1ull << 31))
+        return fail(MOE_E_INVAL, "arena too large for 32-bit row coordinates");
+    CUDA_TRY(cudaSetDevice(c->dev));
+    int rc = drain(c);  // the safe point: nothing enqueued reads or writes the arena any more
+    if (rc) return rc;
+    harvest(c);
+    if (c->dev_policy && (rc = dev_state_pull(c))) return rc;
+
+    ExpertLru next = c->lru;
+    std::vector<std::pair<int, int>> evicted, moved;
+    next.resize(new_C, &evicted, &moved);
+
+    // every new buffer first, so a failed allocation leaves the cache as it was
+    uint16_t* arena2 = nullptr;
+    uint32_t* flag2 = nullptr;
+    int *prev2 = nullptr, *next2 = nullptr, *key2 = nullptr, *order2 = nullptr;
+    int2* fl2 = nullptr;
+    auto release = [&]() {
+        void* ps[] = {arena2, flag2, prev2, next2, key2, order2, fl2};
+        for (void* p : ps)
+            if (p) cudaFree(p);
+    };
+    const size_t Cn = static_cast<size_t>(new_C);
+    bool ok = cudaMalloc(&arena2, Cn * c->entry_bytes) == cudaSuccess &&
+              cudaMalloc(&flag2, Cn * sizeof(uint32_t)) == cudaSuccess;
+    if (ok && c->dev_policy)
+        ok = cudaMalloc(&prev2, Cn * sizeof(int)) == cudaSuccess && cudaMalloc(&next2, Cn * sizeof(int)) == cudaSuccess &&
+             cudaMalloc(&key2, Cn * sizeof(int)) == cudaSuccess &&
+             cudaMalloc(&order2, 2 * Cn * sizeof(int)) == cudaSuccess &&
+             cudaMalloc(&fl2, Cn * sizeof(int2)) == cudaSuccess;
+    if (!ok) {
+        cudaGetLastError();
+        release();
+        return fail(MOE_E_NOMEM, "could not allocate a %d-entry arena", new_C);
+    }
+    // survivors into their new slots (slot r of the new arena holds next.key_in(r))
+    for (int r = 0; r < next.used(); ++r) {
+        const int old = c->lru.slot_of(next.key_in(r));
+        cudaError_t e = cudaMemcpyAsync(arena2 + static_cast<size_t>(r) * c->entry_elems,
+                                        c->arena + static_cast<size_t>(old) * c->entry_elems, c->entry_bytes,
+                                        cudaMemcpyDeviceToDevice, c->s_comp);
+        if (e != cudaSuccess) {
+            release();
+            return fail(MOE_E_CUDA, "moving a cache entry: %s", cudaGetErrorString(e));
+        }
+    }
+    cudaError_t e = cudaMemsetAsync(flag2, 0, Cn * sizeof(uint32_t), c->s_comp);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(c->s_comp);
+    if (e != cudaSuccess) {
+        release();
+        return fail(MOE_E_CUDA, "resize copies: %s", cudaGetErrorString(e));
+    }
+    // commit
+    cudaFree(c->arena);
+    cudaFree(c->fill_flag);
+    c->arena = arena2;
+    c->fill_flag = flag2;
+    c->lru = next;
+    c->C = new_C;
+    c->cfg.capacity = new_C;
+    c->fill_gen.assign(new_C, 0);
+    c->slot_last_use.assign(new_C, -1);
+    c->slot_fill.assign(new_C, -1);
+    for (size_t k = 0; k < c->slot_host.size(); ++k) c->slot_host[k] = c->lru.slot_of(static_cast<int>(k));
+    c->table_dirty = true;
+    if (c->dev_policy) {
+        cudaFree(c->d_prev);
+        cudaFree(c->d_next);
+        cudaFree(c->d_key);
+        cudaFree(c->d_order);
+        cudaFree(c->d_fill_list);
+        c->d_prev = prev2;
+        c->d_next = next2;
+        c->d_key = key2;
+        c->d_order = order2;
+        c->d_fill_list = fl2;
+        if ((rc = dev_state_push(c))) return rc;
+    }
+    if (!make_arena_maps(c)) return fail(MOE_E_CUDA, "cuTensorMapEncodeTiled rejected the resized arena");
+    if ((rc = upload_table(c))) return rc;
+    // trace and counters
+    if (c->dev_policy) {
+        moe::DevStats d{};
+        CUDA_TRY(cudaMemcpy(&d, c->d_stats, sizeof(d), cudaMemcpyDeviceToHost));
+        for (const auto& kv : evicted) {
+            if (c->d_trace_cap) {
+                const moe::DevEvent ev{MOE_EV_RESIZE_EVICT, kv.first / c->E, kv.first % c->E, kv.second, -1, -1};
+                CUDA_TRY(cudaMemcpy(c->d_trace + d.trace_len % c->d_trace_cap, &ev, sizeof(ev),
+                                    cudaMemcpyHostToDevice));
+            }
+            d.trace_len++;
+            d.resize_evictions++;
+        }
+        CUDA_TRY(cudaMemcpy(c->d_stats, &d, sizeof(d), cudaMemcpyHostToDevice));
+    } else {
+        for (const auto& kv : evicted) {
+            record_event(c, MOE_EV_RESIZE_EVICT, kv.first, kv.second, -1);
+            c->stats.resize_evictions++;
+        }
+    }
+    CUDA_TRY(cudaStreamSynchronize(c->s_comp));
     return MOE_OK;
 }
 
@@ -1138,6 +1278,7 @@ int moe_stats(moe_ctx* c, moe_stats_t* out, moe_event_t* trace, uint64_t cap, in
             out->trace_len = d.trace_len;
             out->forwards = d.forwards;
             out->waves = d.waves;
+            out->resize_evictions = d.resize_evictions;
         }
         int written = 0;
         if (trace && cap > 0 && c->d_trace_cap) {
@@ -1209,24 +1350,39 @@ int moe_debug_read(moe_ctx* c, int what, void* dst, uint64_t bytes) {
 }
 
 int moe_lru_simulate(int capacity, int n, const int32_t* layer, const int32_t* expert, const int32_t* kind,
-                     moe_event_t* events) {
+                     moe_event_t* events, uint64_t events_cap) {
     if (capacity < 1 || n < 0 || (n > 0 && (!layer || !expert || !kind || !events)))
         return fail(MOE_E_INVAL, "bad arguments");
     int L = 1, E = 1;
     for (int i = 0; i < n; ++i) {
+        if (kind[i] == 2) {
+            if (expert[i] < 1) return fail(MOE_E_INVAL, "capacity change to %d", expert[i]);
+            continue;
+        }
         if (layer[i] < 0 || expert[i] < 0) return fail(MOE_E_INVAL, "negative key");
         L = std::max(L, layer[i] + 1);
         E = std::max(E, expert[i] + 1);
     }
     ExpertLru lru(capacity, L * E);
+    uint64_t m = 0;
     for (int i = 0; i < n; ++i) {
+        if (kind[i] == 2) {
+            std::vector<std::pair<int, int>> evicted, moved;
+            lru.resize(expert[i], &evicted, &moved);
+            for (const auto& kv : evicted) {
+                if (m >= events_cap) return fail(MOE_E_INVAL, "more events than events_cap");
+                events[m++] = moe_event_t{MOE_EV_RESIZE_EVICT, kv.first / E, kv.first % E, kv.second, -1, -1};
+            }
+            continue;
+        }
+        if (m >= events_cap) return fail(MOE_E_INVAL, "more events than events_cap");
         const int key = layer[i] * E + expert[i];
         ExpertLru::Plan p = lru.plan(key, kind[i] == 1);
         lru.commit(p);
-        events[i] = moe_event_t{p.kind, layer[i], expert[i], p.slot, p.victim >= 0 ? p.victim / E : -1,
-                                p.victim >= 0 ? p.victim % E : -1};
+        events[m++] = moe_event_t{p.kind, layer[i], expert[i], p.slot, p.victim >= 0 ? p.victim / E : -1,
+                                  p.victim >= 0 ? p.victim % E : -1};
     }
-    return MOE_OK;
+    return static_cast<int>(m);
 }
 
 }  // extern "C"

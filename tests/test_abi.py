@@ -63,3 +63,29 @@ def test_init_without_gpu_fails_cleanly():
         pytest.skip("a GPU is present")
     with pytest.raises(moe.MoeError):
         moe.MoeCache(moe.LayerShape(1, 16, 256, 128, 2, 4, 8))
+
+
+def test_lru_simulate_with_capacity_changes_matches_oracle():
+    """The library's host policy and the oracle agree event for event on random sequences
+    with capacity changes (kind 2: grow and shrink) mixed into the accesses."""
+    rng = np.random.default_rng(21)
+    for cap in (1, 3, 8, 30):
+        n = 3000
+        layers = rng.integers(0, 3, n)
+        experts = (rng.zipf(1.3, n) - 1) % 25
+        kinds = (rng.random(n) < 0.05).astype(np.int32)
+        resize = rng.random(n) < 0.01
+        kinds[resize] = 2
+        experts[resize] = rng.integers(1, 40, int(resize.sum()))
+        a = moe.lru_simulate(cap, layers, experts, kinds)
+        b = oracle.lru_run(cap, layers, experts, kinds)
+        assert np.array_equal(a, b)
+        assert (a[:, 0] == moe.EV_RESIZE_EVICT).any() or cap == 1
+
+
+def test_lru_simulate_resize_hand_traces():
+    from tests.test_oracle_lru import load_cases
+    for case in load_cases("lru_resize_traces.txt"):
+        acc = np.array(case["acc"], np.int32)
+        ev = moe.lru_simulate(case["cap"], acc[:, 1], acc[:, 2], acc[:, 0])
+        assert [tuple(r) for r in ev.tolist()] == case["ev"], case["name"]
