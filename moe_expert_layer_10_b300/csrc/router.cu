@@ -19,17 +19,20 @@
 namespace moe {
 namespace {
 
-// Large batches (prefill): a register-tiled evaluation of the same order. A CTA of 8 warps
+// Large batches (prefill): a register-tiled evaluation of the same order. A CTA of 16 warps
 // owns a tile of 32 tokens x 16 experts and walks H in chunks of 256 columns, staged in
-// shared memory with cp.async (double-buffered). Warp w owns the 8 x 8 sub-tile of tokens
-// 8*(w/2).. and experts 8*(w%2)..; its lane l keeps the 64 partials s_l(t, e), each
-// accumulated with fmaf over exactly the columns 256m + 8l + r (m, then r = 0..7) that the
-// one-warp-per-dot-product kernels give lane l, so the fold yields the same bits.
+// shared memory with cp.async (a ring of 4 chunks). Warp w owns the 8 x 4 sub-tile of tokens
+// 8*(w/4).. and experts 4*(w%4)..; its lane l keeps the 32 partials s_l(t, e), each
+// accumulated with fused multiply-adds over exactly the columns 256m + 8l + r (m, then
+// r = 0..7) that the one-warp-per-dot-product kernels give lane l, so the fold yields the
+// same bits. Partials of two tokens share one packed f32x2 instruction (two independent
+// round-to-nearest fused multiply-adds).
 constexpr int kTT = 32, kTE = 16;
 constexpr int kXBytes = kTT * 512;   // 32 rows x 256 bf16
 constexpr int kWBytes = kTE * 1024;  // 16 rows x 256 fp32
 constexpr int kTiledStage = kXBytes + kWBytes;
-constexpr int kTiledSmem = 2 * kTiledStage;
+constexpr int kTiledStages = 4;  // chunks in flight: the next three load while one is used
+constexpr int kTiledSmem = kTiledStages * kTiledStage;
 
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
@@ -41,9 +44,11 @@ __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_gr
 // Stage columns [256m, 256m+256) of the tile. x rows keep their order (lane l reads the 16
 // bytes at 16l). A W_r row's 8-float run of lane l is split into its halves, stored at
 // 16l and 512 + 16l, so the lanes' 16-byte reads of one half are contiguous.
+constexpr int kTiledThreads = 512;
+
 __device__ __forceinline__ void router_stage(uint8_t* buf, const uint16_t* x, const float* Wr, int t0, int e0, int T,
                                              int E, int H, int m) {
-    for (int i = threadIdx.x; i < 2048; i += 256) {
+    for (int i = threadIdx.x; i < 2048; i += kTiledThreads) {
         if (i < 1024) {
             const int row = i >> 5, c = i & 31;
             const int t = min(t0 + row, T - 1);
@@ -58,68 +63,92 @@ __device__ __forceinline__ void router_stage(uint8_t* buf, const uint16_t* x, co
     }
 }
 
-__global__ void __launch_bounds__(256, 1) router_logits_tiled_kernel(const uint16_t* __restrict__ x,
+// Two independent fp32 fused multiply-adds in one instruction (round to nearest each), on
+// register pairs: d = (a.lo * b.lo + c.lo, a.hi * b.hi + c.hi) -- the same two fmaf results.
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+    return d;
+}
+__device__ __forceinline__ float lo_of(uint64_t v) { return __uint_as_float(static_cast<uint32_t>(v)); }
+__device__ __forceinline__ float hi_of(uint64_t v) { return __uint_as_float(static_cast<uint32_t>(v >> 32)); }
+
+__global__ void __launch_bounds__(kTiledThreads, 1) router_logits_tiled_kernel(const uint16_t* __restrict__ x,
                                                                      const float* __restrict__ Wr,
                                                                      const float* __restrict__ bias, int T, int H,
                                                                      int E, float* __restrict__ z) {
     extern __shared__ __align__(16) uint8_t rsm[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t0 = blockIdx.y * kTT, e0 = blockIdx.x * kTE;
-    const int tw = (warp >> 1) * 8, ew = (warp & 1) * 8;
-    float acc[8][8];
+    const int tw = (warp >> 2) * 8, ew = (warp & 3) * 4;
+    // acc[e][p] holds the partials of tokens 2p and 2p+1 for expert e (one f32x2 pair)
+    uint64_t acc[4][4];
 #pragma unroll
-    for (int t = 0; t < 8; ++t)
+    for (int e = 0; e < 4; ++e)
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[t][e] = 0.0f;
+        for (int p = 0; p < 4; ++p) acc[e][p] = 0ull;
     const int M = H / 256;
-    router_stage(rsm, x, Wr, t0, e0, T, E, H, 0);
-    cp_async_commit();
+    // ring of kTiledStages chunks; one commit group per chunk (empty groups past the end keep
+    // the count uniform)
+#pragma unroll
+    for (int m = 0; m < kTiledStages - 1; ++m) {
+        if (m < M) router_stage(rsm + m * kTiledStage, x, Wr, t0, e0, T, E, H, m);
+        cp_async_commit();
+    }
     for (int m = 0; m < M; ++m) {
-        if (m + 1 < M) {
-            router_stage(rsm + ((m + 1) & 1) * kTiledStage, x, Wr, t0, e0, T, E, H, m + 1);
-            cp_async_commit();
-            cp_async_wait<1>();
-        } else {
-            cp_async_wait<0>();
-        }
-        __syncthreads();
-        const uint8_t* xs = rsm + (m & 1) * kTiledStage;
+        cp_async_wait<kTiledStages - 2>();  // chunk m has landed (this thread's copies)
+        __syncthreads();                    // ... everyone's; and chunk m-1's buffer is free
+        if (m + kTiledStages - 1 < M)
+            router_stage(rsm + ((m + kTiledStages - 1) % kTiledStages) * kTiledStage, x, Wr, t0, e0, T, E, H,
+                         m + kTiledStages - 1);
+        cp_async_commit();
+        const uint8_t* xs = rsm + (m % kTiledStages) * kTiledStage;
         const uint8_t* ws = xs + kXBytes;
+        // x: the lane's 8 columns of each of 8 tokens (16 bytes each)
+        uint4 xv[8];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) xv[t] = *reinterpret_cast<const uint4*>(xs + (tw + t) * 512 + lane * 16);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            uint2 xv[8];
+            float4 wv[4];
 #pragma unroll
-            for (int t = 0; t < 8; ++t)
-                xv[t] = *reinterpret_cast<const uint2*>(xs + (tw + t) * 512 + lane * 16 + h * 8);
-            float4 wv[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
+            for (int e = 0; e < 4; ++e)
                 wv[e] = *reinterpret_cast<const float4*>(ws + (ew + e) * 1024 + h * 512 + lane * 16);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
+            for (int q = 0; q < 4; ++q) {  // column r = 4h + q, in order
+                uint64_t xp[4];
 #pragma unroll
-                for (int t = 0; t < 8; ++t) {
-                    const uint32_t word = (q < 2) ? xv[t].x : xv[t].y;
-                    const float xf = (q & 1) ? bf16hi(word) : bf16lo(word);
+                for (int p = 0; p < 4; ++p) {
+                    const uint32_t w0 = (h == 0) ? ((q < 2) ? xv[2 * p].x : xv[2 * p].y)
+                                                 : ((q < 2) ? xv[2 * p].z : xv[2 * p].w);
+                    const uint32_t w1 = (h == 0) ? ((q < 2) ? xv[2 * p + 1].x : xv[2 * p + 1].y)
+                                                 : ((q < 2) ? xv[2 * p + 1].z : xv[2 * p + 1].w);
+                    xp[p] = pack2((q & 1) ? bf16hi(w0) : bf16lo(w0), (q & 1) ? bf16hi(w1) : bf16lo(w1));
+                }
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const float wf = q == 0 ? wv[e].x : q == 1 ? wv[e].y : q == 2 ? wv[e].z : wv[e].w;
-                        acc[t][e] = __fmaf_rn(wf, xf, acc[t][e]);
-                    }
+                for (int e = 0; e < 4; ++e) {
+                    const float wf = q == 0 ? wv[e].x : q == 1 ? wv[e].y : q == 2 ? wv[e].z : wv[e].w;
+                    const uint64_t wd = pack2(wf, wf);
+#pragma unroll
+                    for (int p = 0; p < 4; ++p) acc[e][p] = fma2(wd, xp[p], acc[e][p]);
                 }
             }
         }
-        __syncthreads();
     }
 #pragma unroll
-    for (int t = 0; t < 8; ++t) {
+    for (int e = 0; e < 4; ++e) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            float v = acc[t][e];
+        for (int t = 0; t < 8; ++t) {
+            float v = (t & 1) ? hi_of(acc[e][t >> 1]) : lo_of(acc[e][t >> 1]);
 #pragma unroll
             for (int o = 16; o >= 1; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
             const int tt = t0 + tw + t, ee = e0 + ew + e;
-            if (lane == ((t * 8 + e) & 31) && tt < T && ee < E)
+            if (lane == t * 4 + e && tt < T && ee < E)
                 z[static_cast<size_t>(tt) * E + ee] = __fadd_rn(v, bias ? __ldg(bias + ee) : 0.0f);
         }
     }
@@ -317,8 +346,8 @@ cudaError_t launch_router_logits(const uint16_t* x, const float* Wr, const float
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    router_logits_tiled_kernel<<<dim3((E + kTE - 1) / kTE, (T + kTT - 1) / kTT), 256, kTiledSmem, st>>>(x, Wr, b, T,
-                                                                                                      H, E, z);
+    router_logits_tiled_kernel<<<dim3((E + kTE - 1) / kTE, (T + kTT - 1) / kTT), kTiledThreads, kTiledSmem, st>>>(
+        x, Wr, b, T, H, E, z);
     return cudaGetLastError();
 }
 
