@@ -29,6 +29,7 @@ KIND_EXPERT, KIND_ROUTER, KIND_X, KIND_PERM, KIND_TRACE = 1, 2, 3, 4, 5
 
 
 _CORE = os.path.join(_HERE, "normal_core.h")
+_CORE_FP4 = os.path.join(_HERE, "mxfp4_core.h")
 _SO_FMA = os.path.join(_HERE, "libmoe_inputs_fma.so")
 
 
@@ -57,12 +58,12 @@ def build(force: bool = False) -> str:
     # (loaded only on CPUs that have it); fused multiply-add rounds once either way, so the
     # bits are the same
     for so, extra in ((_SO, []), (_SO_FMA, ["-mfma"])):
-        if force or _stale(so, _SRC, _CORE):
+        if force or _stale(so, _SRC, _CORE, _CORE_FP4):
             tmp = so + f".tmp{os.getpid()}"
             subprocess.check_call(["gcc", "-O2", "-ffp-contract=off", "-fopenmp", "-shared", "-fPIC", "-std=c11"] +
                                   extra + [_SRC, "-o", tmp, "-lm"])
             os.replace(tmp, so)
-    if os.path.exists(_NVCC) and (force or _stale(_GPU_SO, _GPU_SRC, _CORE)):
+    if os.path.exists(_NVCC) and (force or _stale(_GPU_SO, _GPU_SRC, _CORE, _CORE_FP4)):
         tmp = _GPU_SO + f".tmp{os.getpid()}"
         subprocess.check_call([_NVCC, "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-fmad=false",
                                "-std=c++17", "-shared", "-Xcompiler", "-fPIC", "-Xcompiler", "-ffp-contract=off",
@@ -89,6 +90,8 @@ def lib():
         L.mi_trace_reuse.restype = i32
         L.mi_f32_to_bf16.argtypes = [ctypes.c_float]
         L.mi_f32_to_bf16.restype = ctypes.c_uint16
+        L.mi_mxfp4_entry.argtypes = [u64, u64, i32, i32, vp]
+        L.mi_mxfp4_block32.argtypes = [vp, vp, vp]
         L.mi_log_unit.argtypes = [dbl]
         L.mi_log_unit.restype = dbl
         L.mi_sincos_2pi.argtypes = [dbl, vp, vp]
@@ -173,6 +176,33 @@ def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
 def expert_entry(seed: int, layer: int, expert: int, H: int, I: int) -> np.ndarray:
     """Entry (layer, expert): bf16 bits [W_gate (I,H) | W_up (I,H) | W_down (H,I)], N(0, 0.02)."""
     return normal_bf16(seed, stream_id(KIND_EXPERT, layer, expert), 3 * H * I, 0.02)
+
+
+def mxfp4_entry_bytes(H: int, I: int) -> int:
+    """Bytes of one MXFP4 entry: E2M1 pairs (3*H*I/2) then E8M0 scales (3*H*I/32)."""
+    return 3 * H * I // 2 + 3 * H * I // 32
+
+
+def mxfp4_entry(seed: int, layer: int, expert: int, H: int, I: int) -> np.ndarray:
+    """Entry (layer, expert) quantized to MXFP4 (uint8 bytes; layout in gen.c)."""
+    out = np.empty(mxfp4_entry_bytes(H, I), np.uint8)
+    lib().mi_mxfp4_entry(seed, stream_id(KIND_EXPERT, layer, expert), H, I, _ptr(out))
+    return out
+
+
+def mxfp4_block(x_bf16_bits: np.ndarray):
+    """Quantize one block of 32 bf16 values: (16 bytes of E2M1 pairs, E8M0 scale byte)."""
+    x = np.ascontiguousarray(x_bf16_bits, dtype=np.uint16)
+    assert x.size == 32
+    q = np.empty(16, np.uint8)
+    s = np.empty(1, np.uint8)
+    lib().mi_mxfp4_block32(_ptr(x), _ptr(q), _ptr(s))
+    return q, int(s[0])
+
+
+def fill_mxfp4_entry_at(ptr: int, seed: int, layer: int, expert: int, H: int, I: int) -> None:
+    """Write the MXFP4 entry (layer, expert) straight into host memory at `ptr`."""
+    lib().mi_mxfp4_entry(seed, stream_id(KIND_EXPERT, layer, expert), H, I, ptr)
 
 
 def fill_entry_at(ptr: int, seed: int, layer: int, expert: int, H: int, I: int) -> None:

@@ -53,6 +53,8 @@ def lib():
         L.orc_expert_ffn.argtypes = [vp, i32, i32, vp, vp]
         L.orc_moe_layer.argtypes = [vp, i32, i32, vp, vp, i32, i32, vp, vp, vp]
         L.orc_moe_dense.argtypes = [vp, i32, i32, i32, vp, vp, i32, i32, vp, vp, vp]
+        L.orc_mxfp4_dequant.argtypes = [vp, vp, ctypes.c_int64, vp]
+        L.orc_mxfp4_dequant.restype = ctypes.c_int64
         L.orc_layer_accesses.argtypes = [vp, i32, i32, i32, vp]
         L.orc_layer_accesses.restype = i32
         L.orc_lru_run.argtypes = [i32, i32, vp, vp, vp, i32, vp, vp, vp, vp, vp, vp]
@@ -186,6 +188,35 @@ def moe_dense(entries, H: int, I: int, x_bf16, resid, idx, w) -> np.ndarray:
                         _p(_c(w, np.float64)), _p(out))
     del keep
     return out
+
+
+def mxfp4_dequant(q: np.ndarray, s: np.ndarray, n: int) -> np.ndarray:
+    """MXFP4 elements (E2M1 bytes q, E8M0 scales s per 32) -> exact bf16 bit patterns."""
+    qq, ss = _c(q, np.uint8), _c(s, np.uint8)
+    out = np.empty(n, np.uint16)
+    bad = lib().orc_mxfp4_dequant(_p(qq), _p(ss), n, _p(out))
+    if bad:
+        raise ValueError(f"{bad} MXFP4 values are not exact in bf16")
+    return out
+
+
+def mxfp4_entry_as_bf16(entry: np.ndarray, H: int, I: int) -> np.ndarray:
+    """An MXFP4 expert entry as the bf16 entry of the same values, for the bf16 expert FFN.
+    Entry layout: E2M1 bytes of W_gate [I x H], W_up [I x H], W_down [H x I] (row-major), then
+    their E8M0 scales, each matrix as [K/64][rows][2] (every 64 columns, each row's two block
+    scales)."""
+    n = 3 * H * I
+    q = entry[: n // 2]
+    s_all = entry[n // 2:]
+    mats = [(I, H), (I, H), (H, I)]
+    s_rows = []
+    off = 0
+    for rows, K in mats:
+        blk = s_all[off: off + rows * K // 32].reshape(K // 64, rows, 2)
+        s_rows.append(blk.transpose(1, 0, 2).reshape(rows, K // 32))  # back to [rows][K/32]
+        off += rows * K // 32
+    s = np.concatenate([a.ravel() for a in s_rows])
+    return mxfp4_dequant(q, s, n)
 
 
 def layer_accesses(idx: np.ndarray, E: int) -> np.ndarray:

@@ -254,6 +254,28 @@ void orc_moe_dense(const uint16_t* const* entries, int H, int I, int E, const ui
     }
 }
 
+// MXFP4 weights (OCP Microscaling): element i of a tensor is the E2M1 code in nibble i%2 of
+// byte i/2 (low nibble first) -- bit 3 the sign, bits 0-2 the magnitude 0, 0.5, 1, 1.5, 2, 3,
+// 4, 6 -- times 2^(s - 127), s the E8M0 byte of its block of 32. Every such value has at most
+// two significant bits, so it is written here as an exact bf16 (the caller's entries then
+// run through the same bf16 expert FFN). Returns the number of elements that were not
+// exactly representable (0 for any scale in the normal bf16 range).
+int64_t orc_mxfp4_dequant(const uint8_t* q, const uint8_t* s, int64_t n, uint16_t* out) {
+    static const double kMag[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+    int64_t inexact = 0;
+    for (int64_t i = 0; i < n; ++i) {
+        const int code = (q[i / 2] >> (4 * (i % 2))) & 15;
+        double v = std::ldexp(kMag[code & 7], static_cast<int>(s[i / 32]) - 127);
+        if (code & 8) v = -v;
+        const float f = static_cast<float>(v);
+        uint32_t u;
+        std::memcpy(&u, &f, 4);
+        if ((u & 0xffffu) != 0 || static_cast<double>(f) != v) ++inexact;
+        out[i] = static_cast<uint16_t>(u >> 16);
+    }
+    return inexact;
+}
+
 // R5: the distinct experts routed in one layer invocation, in ascending id (the order in
 // which the LRU sees them). Returns their number.
 int orc_layer_accesses(const int32_t* idx, int T, int k, int E, int32_t* experts) {

@@ -92,3 +92,52 @@ def test_cpu_builds_with_and_without_fma_instructions_agree():
         L.mi_normal_bf16(0, mi.stream_id(mi.KIND_EXPERT, 1, 2), 5, n, 0.02, b.ctypes.data)
         outs.append(b)
     assert np.array_equal(outs[0], outs[1])
+
+
+def _mxfp4_golden():
+    import os
+    cases, cur = [], None
+    for line in open(os.path.join(os.path.dirname(__file__), "golden", "mxfp4_blocks.txt")):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        key, *rest = line.split()
+        if key == "block":
+            cur = {"name": rest[0]}
+        elif key == "x":
+            cur["x"] = [float(v) for v in rest]
+        elif key == "scale":
+            cur["scale"] = int(rest[0])
+        elif key == "bytes":
+            cur["bytes"] = [int(v) for v in rest]
+        elif key == "end":
+            cases.append(cur)
+    return cases
+
+
+def test_mxfp4_quantizer_hand_worked_blocks():
+    for c in _mxfp4_golden():
+        x = np.array([mi.f32_to_bf16_bits(v) for v in c["x"]], np.uint16)
+        if c["x"][0] == 0.0 and str(c["x"][0]).startswith("-"):
+            x[0] = 0x8000
+        q, s = mi.mxfp4_block(x)
+        assert s == c["scale"], c["name"]
+        assert q.tolist() == c["bytes"], c["name"]
+
+
+def test_mxfp4_entry_is_the_blocks_of_the_bf16_entry():
+    """An MXFP4 entry is the seeded bf16 entry quantized block by block: the E2M1 bytes of
+    gate, up, down row-major, then each matrix's scales as [K/64][rows][2]."""
+    H, I = 256, 128
+    w = mi.expert_entry(0, 2, 5, H, I)
+    e = mi.mxfp4_entry(0, 2, 5, H, I)
+    n = 3 * H * I
+    assert e.size == mi.mxfp4_entry_bytes(H, I) == n // 2 + n // 32
+    # (matrix, row, 32-block) -> element offset, and the scale's place in the layout
+    for mat, row, b in [(0, 0, 0), (0, 3, 5), (1, 127, 7), (2, 0, 0), (2, 255, 3), (1, 64, 6)]:
+        rows, K = ((I, H), (I, H), (H, I))[mat]
+        elem0 = mat * I * H + row * K + 32 * b
+        q, s = mi.mxfp4_block(w[elem0: elem0 + 32])
+        assert e[elem0 // 2: elem0 // 2 + 16].tolist() == q.tolist()
+        s_off = n // 2 + mat * (I * H // 32) + ((b // 2) * rows + row) * 2 + b % 2
+        assert e[s_off] == s, (mat, row, b)

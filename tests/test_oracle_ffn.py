@@ -150,3 +150,60 @@ def test_permute_invariants_prefill_shape():
         seg = perm[offsets[e]:offsets[e + 1]]
         assert np.all(flat[seg] == e)
         assert np.all(np.diff(seg) > 0)                                      # stable
+
+
+def test_mxfp4_dequant_hand_worked_blocks():
+    """The oracle's MXFP4 reading of the hand-worked blocks (tests/golden/mxfp4_blocks.txt):
+    each code's magnitude times 2^(scale - 127), signs from bit 3."""
+    from tests.test_inputs import _mxfp4_golden
+    expect = {
+        "ties": [0, 1, 1, 2, 2, 4, 4, 6, 6, 0.5, 1.5, 3, -0.0, -1, -6, 0.5, 0.5, 1] + [0] * 14,
+        "small": [6 * 2 ** -7, -3 * 2 ** -7, 0, 2 ** -7] + [0] * 28,
+        "zeros": [-0.0] + [0] * 31,
+    }
+    for c in _mxfp4_golden():
+        got = oracle.mxfp4_dequant(np.array(c["bytes"], np.uint8), np.array([c["scale"]], np.uint8), 32)
+        f = mi.bf16_bits_to_f32(got)
+        assert f.tolist() == expect[c["name"]], c["name"]
+        assert (np.signbit(f) == np.signbit(np.array(expect[c["name"]]))).all()
+
+
+def test_mxfp4_round_trip_error_is_within_half_a_grid_step():
+    """dequant(quant(x)) differs from x by at most half the E2M1 grid step at x's magnitude
+    (0.25, 0.5 or 1 times the block scale), or by the clamp for |x| > 6 * scale; values on the
+    grid come back exactly."""
+    rng = np.random.default_rng(5)
+    for trial in range(200):
+        x = (rng.standard_normal(32) * 10.0 ** rng.uniform(-4, 1)).astype(np.float32)
+        bits = np.array([mi.f32_to_bf16_bits(v) for v in x], np.uint16)
+        xb = mi.bf16_bits_to_f32(bits).astype(np.float64)
+        q, s = mi.mxfp4_block(bits)
+        y = mi.bf16_bits_to_f32(oracle.mxfp4_dequant(q, np.array([s], np.uint8), 32)).astype(np.float64)
+        scale = 2.0 ** (s - 127)
+        a = np.abs(xb) / scale
+        half_step = np.where(a < 2, 0.25, np.where(a < 4, 0.5, 1.0)) * scale
+        bound = np.where(a <= 6, half_step, (a - 6) * scale + 1e-30)
+        assert (np.abs(y - xb) <= bound * (1 + 1e-12)).all(), trial
+        assert np.abs(xb).max() >= 4 * scale  # the scale puts the largest element in [4, 8)
+    grid = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6, -0.5, -1, -1.5, -2, -3, -4, -6, 6] * 2) * 2.0 ** -5
+    bits = np.array([mi.f32_to_bf16_bits(v) for v in grid], np.uint16)
+    q, s = mi.mxfp4_block(bits)
+    y = mi.bf16_bits_to_f32(oracle.mxfp4_dequant(q, np.array([s], np.uint8), 32))
+    assert np.array_equal(y, grid.astype(np.float32))
+
+
+def test_mxfp4_entry_reads_back_within_the_block_bounds():
+    """The oracle's reading of a whole MXFP4 entry (its scale layout included) gives, for every
+    element, a value within the round-trip bound of the seeded bf16 weight it came from, and
+    exactly the dequantized value of that element's own block."""
+    H, I = 256, 128
+    w = mi.bf16_bits_to_f32(mi.expert_entry(0, 1, 2, H, I)).astype(np.float64)
+    y = mi.bf16_bits_to_f32(oracle.mxfp4_entry_as_bf16(mi.mxfp4_entry(0, 1, 2, H, I), H, I)).astype(np.float64)
+    wb = mi.expert_entry(0, 1, 2, H, I)
+    for blk in range(0, w.size // 32, 97):
+        q, s = mi.mxfp4_block(wb[32 * blk: 32 * blk + 32])
+        ref = mi.bf16_bits_to_f32(oracle.mxfp4_dequant(q, np.array([s], np.uint8), 32))
+        assert np.array_equal(y[32 * blk: 32 * blk + 32], ref.astype(np.float64)), blk
+    assert np.abs(y - w).max() <= 0.5 * np.abs(w).max()  # coarse: 4-bit weights
+    rel = np.linalg.norm(y - w) / np.linalg.norm(w)
+    assert 0.05 < rel < 0.2  # MXFP4's relative rms error on Gaussian weights is about 0.1
