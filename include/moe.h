@@ -66,6 +66,13 @@ extern "C" {
  * back into the compute stream (no prefill overlap); moe_stats reports fill_ms = 0. Run one
  * call of each shape before capturing, and keep MOE_PROFILE timing off while capturing. */
 #define MOE_DEVICE_POLICY 8u
+/* Expert entries in MXFP4 (OCP Microscaling: E2M1 weights, one E8M0 scale per 32 along each
+ * row): 3*hidden*inter/2 bytes of E2M1 pairs (W_gate, W_up, W_down row-major, the even element
+ * in the low nibble) followed by 3*hidden*inter/32 scale bytes (each matrix as [K/64][rows][2]).
+ * An entry is 17/64 of its bf16 size, so fills move 3.8x fewer bytes. The kernels expand the
+ * weights to bf16 on chip -- every MXFP4 value is exact in bf16 -- and run the decode kernels
+ * (MOE_PATH_GEMM is refused); activations stay bf16. */
+#define MOE_MXFP4 16u
 
 /* ---- fill modes (moe_cache_fill) ---- */
 #define MOE_FILL_DEMAND 0     /* access the distinct experts of the given top-k indices */
@@ -93,7 +100,7 @@ typedef struct {
     int32_t top_k;       /* k */
     int32_t capacity;    /* C: cache slots, in whole entries */
     int32_t max_tokens;  /* largest T passed to moe_route / moe_layer_forward */
-    uint32_t flags;      /* MOE_TRACE | MOE_PROFILE | MOE_PREFILL_DB | MOE_DEVICE_POLICY */
+    uint32_t flags;      /* MOE_TRACE | MOE_PROFILE | MOE_PREFILL_DB | MOE_DEVICE_POLICY | MOE_MXFP4 */
     uint64_t trace_capacity; /* events kept by MOE_TRACE (0: 1<<20) */
 } moe_config_t;
 
@@ -166,7 +173,7 @@ void* moe_host_entry(moe_ctx* ctx, int layer, int expert);
  */
 int moe_cache_resize(moe_ctx* ctx, int new_capacity);
 
-/* Bytes of one entry: 3 * hidden * inter * 2. */
+/* Bytes of one entry: 3 * hidden * inter * 2 (bf16), or 3 * hidden * inter * 17/32 (MOE_MXFP4). */
 uint64_t moe_entry_bytes(const moe_ctx* ctx);
 
 /*

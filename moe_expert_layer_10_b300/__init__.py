@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(PKG, "libmoe_b300.so")
 HEADER = os.path.join(os.path.dirname(PKG), "include", "moe.h")
 
 MOE_OK, MOE_E_INVAL, MOE_E_NOMEM, MOE_E_CUDA, MOE_E_TIMEOUT, MOE_E_CAPACITY, MOE_E_DEVICE = 0, -1, -2, -3, -4, -5, -6
-MOE_TRACE, MOE_PROFILE, MOE_PREFILL_DB, MOE_DEVICE_POLICY = 1, 2, 4, 8
+MOE_TRACE, MOE_PROFILE, MOE_PREFILL_DB, MOE_DEVICE_POLICY, MOE_MXFP4 = 1, 2, 4, 8, 16
 MOE_FILL_DEMAND, MOE_FILL_FULL_LAYER = 0, 1
 MOE_PATH_AUTO, MOE_PATH_GEMV, MOE_PATH_GEMM = 0, 1, 2
 EV_HIT, EV_FILL, EV_PREFETCH_FILL, EV_PREFETCH_HIT, EV_RESIZE_EVICT = 0, 1, 2, 3, 4
@@ -176,6 +176,7 @@ class MoeCache:
     def __init__(self, shape: LayerShape, flags: int = 0, trace_capacity: int = 0, stream_compute=None,
                  stream_copy=None):
         self.shape = shape
+        self.shape_flags = flags
         cfg = Config(shape.num_layers, shape.num_experts, shape.hidden, shape.inter, shape.top_k, shape.capacity,
                      shape.max_tokens, flags, trace_capacity)
         h = ctypes.c_void_p()
@@ -208,6 +209,11 @@ class MoeCache:
         if not p:
             raise MoeError(MOE_E_INVAL, "moe_host_entry", f"({layer}, {expert}) out of range")
         return p
+
+    def host_entry_bytes(self, layer: int, expert: int):
+        """The pinned pool's entry (layer, expert) as a writable uint8 numpy view."""
+        import numpy as np
+        return np.ctypeslib.as_array((ctypes.c_uint8 * self.entry_bytes).from_address(self.host_entry(layer, expert)))
 
     def host_entry_array(self, layer: int, expert: int):
         """numpy uint16 view of entry (layer, expert) in the pinned pool (writable in place)."""

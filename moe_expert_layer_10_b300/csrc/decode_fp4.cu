@@ -1,0 +1,385 @@
+// Decode expert FFN with MXFP4 expert weights: the 4-bit entries stream from HBM (and cross
+// PCIe on a fill) at a quarter of the bf16 bytes, and are expanded to bf16 on chip.
+//
+// Source: "FreeToken benchmark" (freetoken.wiki/performance) -- the routed experts are
+// evaluated in MXFP4 and NVFP4 as well as BF16 ("Results" tables); "FreeToken rtx 4090"
+// (freetoken.wiki/hardware), "How the MoE Memory Hierarchy Works" -- an expert is a complete
+// cached (layer, expert) entry executed through the slot table.
+//
+// An MXFP4 value is an E2M1 code (magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6) times its block's
+// power-of-two scale, so it is exact in bf16: the kernel expands the weights to bf16 in shared
+// memory and runs the same tcgen05 kind::f16 products as the bf16 kernel (decode_mma.cu),
+// with the tokens as the N side; the epilogue is the shared one (decode_common.cuh).
+// Entry layout: E2M1 bytes of W_gate [I x H], W_up [I x H], W_down [H x I] row-major, then the
+// E8M0 scales of each matrix as [K/64][rows][2].
+// Roles (14 warps):
+//  * warp 0, one lane: producer -- per 64-column slab of a unit, the tile's E2M1 bytes (128 rows
+//    x 32 bytes, a 3-D TMA over (bytes, rows, slot)) and its 256 scale bytes (a bulk copy), into
+//    a 16-deep raw ring, so about 68 KB of weights are in flight per SM;
+//  * warps 6-13 (256 threads): converters -- thread (row, half) expands 32 codes of one row with
+//    one scale into bf16 inside the 128-byte-swizzled A tile of an MMA stage, with byte-permute
+//    lookups (two 4-byte tables per scale for the high and the low byte of the bf16 pattern);
+//    converter 0 also loads the stage's token tile (TMA);
+//  * warp 1, one lane: MMA issuer, as in the bf16 kernel; warps 2-5: epilogue.
+// Waits are bounded; the fill-flag wait and the split-K scheme are those of the bf16 kernel.
+#include <algorithm>
+
+#include "decode_common.cuh"
+
+namespace moe {
+namespace {
+
+using dec::BK;
+using dec::decode_epilogue;
+using dec::kNMax;
+using dec::kXchgFloats;
+using dec::locate_unit;
+using dec::Unit;
+
+constexpr int kRawA = 128 * 32;                // E2M1 bytes of a 128-row tile slab
+constexpr int kRawScales = 256;                // its E8M0 scales: 128 rows x 2
+constexpr int kRawStage = kRawA + kRawScales;  // 4352 bytes (34 x 128)
+constexpr int kRawStages = 16;
+constexpr int kA16 = 128 * BK * 2;             // bf16 A tile: 16 KB
+constexpr int kB16 = kNMax * BK * 2;           // token tile: up to 8 KB
+constexpr int kMmaStage = kA16 + kB16;         // 24 KB
+constexpr int kMaxMmaStages = 6;
+constexpr int kConvWarps = 8;
+constexpr int kConvBase = 192;                 // first converter thread
+constexpr int kThreads = kConvBase + 32 * kConvWarps;
+constexpr uint32_t kTmemCols = 128;
+
+struct __align__(8) Shared {
+    uint64_t raw_full[kRawStages], raw_empty[kRawStages];
+    uint64_t mma_full[kMaxMmaStages], mma_empty[kMaxMmaStages];
+    uint64_t acc_full[2], acc_empty[2];
+    uint32_t tmem_base;
+    int ok[2], last[2];
+};
+
+template <bool GATEUP>
+struct Layout {
+    static constexpr int MMA_STAGES = GATEUP ? 5 : 6;
+    static constexpr int XCHG_BYTES = GATEUP ? kXchgFloats * 4 : 0;
+    static constexpr int SMEM =
+        MMA_STAGES * kMmaStage + kRawStages * kRawStage + XCHG_BYTES + static_cast<int>(sizeof(Shared)) + 1024;
+    static_assert(MMA_STAGES <= kMaxMmaStages, "stages");
+    static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
+};
+
+// bf16 patterns of the 8 E2M1 magnitudes times 2^(s-127): 0, then exponent field
+// s + {-1, 0, 0, 1, 1, 2, 2} with the top mantissa bit set for 1.5, 3, 6. Returned as four
+// byte tables for prmt: high bytes of codes 0-3 / 4-7, low bytes of codes 0-3 / 4-7.
+__device__ __forceinline__ void scale_tables(uint32_t s, uint32_t& h_lo, uint32_t& h_hi, uint32_t& l_lo,
+                                             uint32_t& l_hi) {
+    const uint32_t b = s << 7;
+    const uint32_t p1 = b - 128, p2 = b, p3 = b + 64, p4 = b + 128, p5 = b + 192, p6 = b + 256, p7 = b + 320;
+    const uint32_t q01 = prmt(0u, p1, 0x5410);  // [p0 (= 0), p1] as two 16-bit halves
+    const uint32_t q23 = prmt(p2, p3, 0x5410);
+    const uint32_t q45 = prmt(p4, p5, 0x5410);
+    const uint32_t q67 = prmt(p6, p7, 0x5410);
+    h_lo = prmt(q01, q23, 0x7531);
+    h_hi = prmt(q45, q67, 0x7531);
+    l_lo = prmt(q01, q23, 0x6420);
+    l_hi = prmt(q45, q67, 0x6420);
+}
+
+// 8 E2M1 codes (one word, element k in nibble k) -> 4 words of bf16 pairs (element 2j low).
+__device__ __forceinline__ void expand8(uint32_t v, uint32_t h_lo, uint32_t h_hi, uint32_t l_lo, uint32_t l_hi,
+                                        uint32_t (&w)[4]) {
+    const uint32_t mags = v & 0x77777777u;
+    const uint32_t ha = prmt(h_lo, h_hi, mags), la = prmt(l_lo, l_hi, mags);
+    const uint32_t mh = mags >> 16;
+    const uint32_t hb = prmt(h_lo, h_hi, mh), lb = prmt(l_lo, l_hi, mh);
+    w[0] = prmt(la, ha, 0x5140);
+    w[1] = prmt(la, ha, 0x7362);
+    w[2] = prmt(lb, hb, 0x5140);
+    w[3] = prmt(lb, hb, 0x7362);
+    // signs: bit 3 of nibble 2j -> bit 15 of word j, bit 3 of nibble 2j+1 -> bit 31
+    const uint32_t t = v & 0x88888888u, t4 = t << 4;
+    w[0] = or_and(w[0], prmt(t4, t, 0x4000), 0x80008000u);
+    w[1] = or_and(w[1], prmt(t4, t, 0x5010), 0x80008000u);
+    w[2] = or_and(w[2], prmt(t4, t, 0x6020), 0x80008000u);
+    w[3] = or_and(w[3], prmt(t4, t, 0x7030), 0x80008000u);
+}
+
+template <bool GATEUP>
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_fp4_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                      const uint8_t* __restrict__ arena, uint64_t entry_bytes, const GemvWork* __restrict__ work,
+                      int n_work, int n_units, int S, const int32_t* __restrict__ slot_row,
+                      const uint32_t* __restrict__ fill_flag, int H, int I, uint16_t* __restrict__ h_out,
+                      const float* __restrict__ w_perm, float* __restrict__ pair_out, float* __restrict__ ws,
+                      int* __restrict__ cnt, int* status, uint64_t fill_wait_ns, const int* __restrict__ dyn) {
+    using Lay = Layout<GATEUP>;
+    constexpr int kMma = Lay::MMA_STAGES;
+    if (dyn) {
+        n_work = dyn[0];
+        n_units = dyn[1];
+        S = dyn[2];
+    }
+    const uint64_t consumer_wait_ns = fill_wait_ns + kWaitDeadlineNs;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* mma_tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* raw_tiles = mma_tiles + kMma * kMmaStage;
+    float* xchg = reinterpret_cast<float*>(raw_tiles + kRawStages * kRawStage);
+    Shared& sh = *reinterpret_cast<Shared*>(raw_tiles + kRawStages * kRawStage + Lay::XCHG_BYTES);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int K = GATEUP ? H : I;
+    const int KB = K / BK;
+    const int R = GATEUP ? I / 64 : H / 128;
+    const uint64_t q_bytes = 3ull * H * I / 2;        // the E2M1 part of an entry
+    const uint64_t s_mat = static_cast<uint64_t>(H) * I / 32;  // scale bytes of one matrix
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kRawStages; ++s) {
+            mbar_init(&sh.raw_full[s], 1);
+            mbar_init(&sh.raw_empty[s], kConvWarps);
+        }
+        for (int s = 0; s < kMma; ++s) {
+            mbar_init(&sh.mma_full[s], kConvWarps + 1);  // the converter warps + the token-tile arrival
+            mbar_init(&sh.mma_empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&sh.acc_full[b], 1);
+            mbar_init(&sh.acc_empty[b], 4);
+        }
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&sh.tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sh.tmem_base;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer (weights)
+        if (lane == 0) {
+            prefetch_tmap(&tm_a);
+            const uint64_t pol = policy_evict_first();
+            int stage = 0;
+            uint32_t phase = 0, used = 0, last_phase = 0;
+            bool ok = true;
+            int ready_a = -1;
+            for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+                const Unit un = locate_unit(work, n_work, u, R, S);
+                const GemvWork wk = work[un.a];
+                if (wk.wait_slot >= 0 && un.a != ready_a) {
+                    if (!wait_fill_flag(fill_flag + wk.wait_slot, wk.gen, fill_wait_ns)) {
+                        raise_status(status, kDevFillTimeout);
+                        break;
+                    }
+                    ready_a = un.a;
+                }
+                int slot = slot_row[wk.expert];
+                if (slot < 0) {
+                    raise_status(status, kDevBadSlot);
+                    slot = 0;
+                }
+                const uint8_t* sc = arena + static_cast<uint64_t>(slot) * entry_bytes + q_bytes;
+                const int kb0 = un.split * KB / S, kb1 = (un.split + 1) * KB / S;
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if (!mbar_wait(&sh.raw_empty[stage], phase ^ 1u, consumer_wait_ns)) {
+                        raise_status(status, kDevWaitTimeout);
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* dst = raw_tiles + stage * kRawStage;
+                    mbar_arrive_expect_tx(&sh.raw_full[stage], kRawStage);
+                    if (GATEUP) {
+                        const int r0 = un.tile * 64;
+                        tma_load_3d_hint(dst, &tm_a, &sh.raw_full[stage], kb * 32, r0, slot, pol);
+                        tma_load_3d_hint(dst + kRawA / 2, &tm_a, &sh.raw_full[stage], kb * 32, I + r0, slot, pol);
+                        // scales [K/64][rows][2]: this slab's pairs for rows r0.. of gate, then of up
+                        bulk_load(dst + kRawA, sc + (static_cast<uint64_t>(kb) * I + r0) * 2, 128, &sh.raw_full[stage]);
+                        bulk_load(dst + kRawA + 128, sc + s_mat + (static_cast<uint64_t>(kb) * I + r0) * 2, 128,
+                                  &sh.raw_full[stage]);
+                    } else {
+                        const int r0 = un.tile * 128;
+                        tma_load_3d_hint(dst, &tm_a, &sh.raw_full[stage], kb * 32, 2 * H + r0, slot, pol);
+                        bulk_load(dst + kRawA, sc + 2 * s_mat + (static_cast<uint64_t>(kb) * H + r0) * 2, 256,
+                                  &sh.raw_full[stage]);
+                    }
+                    used |= 1u << stage;
+                    last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
+                    if (++stage == kRawStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            for (int s = 0; s < kRawStages; ++s)
+                if ((used >> s) & 1u)
+                    if (!mbar_wait(&sh.raw_full[s], (last_phase >> s) & 1u)) raise_status(status, kDevWaitTimeout);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int stage = 0, acc = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            int last_acc = -1;
+            uint32_t last_acc_phase = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+                const Unit un = locate_unit(work, n_work, u, R, S);
+                const GemvWork wk = work[un.a];
+                const int nt = min(kNMax, wk.n_tok - un.chunk * kNMax);
+                const uint32_t idesc = idesc_bf16_f32(128, ((nt + 15) >> 4) * 16);
+                const int kb0 = un.split * KB / S, kb1 = (un.split + 1) * KB / S;
+                if (!mbar_wait(&sh.acc_empty[acc], acc_phase ^ 1u, consumer_wait_ns)) {
+                    raise_status(status, kDevWaitTimeout);
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d = tmem + static_cast<uint32_t>(acc * kNMax);
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if (!mbar_wait(&sh.mma_full[stage], phase, consumer_wait_ns)) {
+                        raise_status(status, kDevWaitTimeout);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint8_t* sa = mma_tiles + stage * kMmaStage;
+                    const uint64_t da = sw128_kmajor_desc(smem_u32(sa));
+                    const uint64_t db = sw128_kmajor_desc(smem_u32(sa + kA16));
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k)
+                        umma_bf16(d, da + 2 * k, db + 2 * k, idesc, (kb != kb0 || k != 0) ? 1u : 0u);
+                    umma_commit(&sh.mma_empty[stage]);
+                    if (++stage == kMma) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                umma_commit(&sh.acc_full[acc]);
+                last_acc = acc;
+                last_acc_phase = acc_phase;
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1u;
+            }
+            if (last_acc >= 0 && !mbar_wait(&sh.acc_full[last_acc], last_acc_phase))
+                raise_status(status, kDevWaitTimeout);
+        }
+    } else if (warp < 6) {
+        // ------------------------------------------------------------ epilogue (warps 2-5)
+        decode_epilogue<GATEUP>(sh.acc_full, sh.acc_empty, sh.ok, sh.last, tmem, xchg, work, n_work, n_units, S, R, H,
+                                I, h_out, w_perm, pair_out, ws, cnt, status, consumer_wait_ns, 64);
+    } else {
+        // ------------------------------------------------------------ converters (warps 6-13)
+        const int c = threadIdx.x - kConvBase;
+        const int row = c >> 1, half = c & 1;
+        const bool token_loader = c == 0;
+        if (token_loader) prefetch_tmap(&tm_b);
+        int rs = 0, ms = 0;
+        uint32_t rphase = 0, mphase = 0, used = 0, last_phase = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+            const Unit un = locate_unit(work, n_work, u, R, S);
+            const GemvWork wk = work[un.a];
+            const int tok0 = wk.tok_off + un.chunk * kNMax;
+            const int nt = min(kNMax, wk.n_tok - un.chunk * kNMax);
+            const int nb = (nt + 15) >> 4;
+            const int kb0 = un.split * KB / S, kb1 = (un.split + 1) * KB / S;
+            for (int kb = kb0; kb < kb1; ++kb) {
+                if (!mbar_wait(&sh.raw_full[rs], rphase, consumer_wait_ns) ||
+                    !mbar_wait(&sh.mma_empty[ms], mphase ^ 1u, consumer_wait_ns)) {
+                    raise_status(status, kDevWaitTimeout);
+                    ok = false;
+                    break;
+                }
+                uint8_t* sm = mma_tiles + ms * kMmaStage;
+                if (token_loader) {
+                    mbar_arrive_expect_tx(&sh.mma_full[ms], nb * 16 * BK * 2);
+                    for (int b = 0; b < nb; ++b)
+                        tma_load_2d(sm + kA16 + b * 16 * BK * 2, &tm_b, &sh.mma_full[ms], kb * BK, tok0 + 16 * b);
+                    used |= 1u << ms;
+                    last_phase = (last_phase & ~(1u << ms)) | (mphase << ms);
+                }
+                const uint8_t* raw = raw_tiles + rs * kRawStage;
+                const uint4 codes = *reinterpret_cast<const uint4*>(raw + row * 32 + half * 16);
+                const uint32_t sc = raw[kRawA + row * 2 + half];
+                uint32_t h_lo, h_hi, l_lo, l_hi;
+                scale_tables(sc, h_lo, h_hi, l_lo, l_hi);
+                const uint32_t words[4] = {codes.x, codes.y, codes.z, codes.w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    uint32_t w[4];
+                    expand8(words[q], h_lo, h_hi, l_lo, l_hi, w);
+                    const int chunk = half * 4 + q;  // 16-byte chunk of the 128-byte row
+                    *reinterpret_cast<uint4*>(sm + row * 128 + ((chunk ^ (row & 7)) << 4)) =
+                        make_uint4(w[0], w[1], w[2], w[3]);
+                }
+                fence_proxy_async_shared();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&sh.mma_full[ms]);
+                    mbar_arrive(&sh.raw_empty[rs]);
+                }
+                if (++rs == kRawStages) {
+                    rs = 0;
+                    rphase ^= 1u;
+                }
+                if (++ms == kMma) {
+                    ms = 0;
+                    mphase ^= 1u;
+                }
+            }
+        }
+        // the token tiles this thread issued must land before the CTA exits
+        if (token_loader)
+            for (int s = 0; s < kMma; ++s)
+                if ((used >> s) & 1u)
+                    if (!mbar_wait(&sh.mma_full[s], (last_phase >> s) & 1u)) raise_status(status, kDevWaitTimeout);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+template <bool GATEUP>
+cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const uint8_t* arena, uint64_t entry_bytes,
+                   const GemvWork* work, int n_work, int n_units, int S, const int32_t* slot_row,
+                   const uint32_t* fill_flag, int H, int I, uint16_t* h_out, const float* w_perm, float* pair_out,
+                   float* ws, int* cnt, int* status, uint64_t fill_wait_ns, int num_sms, cudaStream_t st,
+                   const int* dyn) {
+    if (!dyn) {
+        if (n_units <= 0 || n_work <= 0) return cudaSuccess;
+        if (S < 1 || S > kDecodeMaxSplit) return cudaErrorInvalidValue;
+        if (S > 1 && n_units > kDecodeSplitUnits) return cudaErrorInvalidValue;
+    }
+    auto kern = decode_fp4_kernel<GATEUP>;
+    constexpr int smem = Layout<GATEUP>::SMEM;
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    const int grid = dyn ? num_sms : std::min(n_units, num_sms);
+    kern<<<grid, kThreads, smem, st>>>(ta, tb, arena, entry_bytes, work, n_work, n_units, S, slot_row, fill_flag, H, I,
+                                       h_out, w_perm, pair_out, ws, cnt, status, fill_wait_ns, dyn);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode_fp4(bool gateup, const DecodeMaps& m, const uint8_t* arena, uint64_t entry_bytes,
+                              const GemvWork* work, int n_work, int n_units, int S, const int* dyn,
+                              const int32_t* slot_row, const uint32_t* fill_flag, int H, int I, uint16_t* h_perm,
+                              const float* w_perm, float* pair_out, float* ws, int* cnt, int* status,
+                              uint64_t fill_wait_ns, int num_sms, cudaStream_t st) {
+    if (gateup)
+        return launch<true>(m.a_gu4, m.b_x, arena, entry_bytes, work, n_work, n_units, S, slot_row, fill_flag, H, I,
+                            h_perm, nullptr, nullptr, ws, cnt, status, fill_wait_ns, num_sms, st, dyn);
+    return launch<false>(m.a_d4, m.b_h, arena, entry_bytes, work, n_work, n_units, S, slot_row, fill_flag, H, I,
+                         nullptr, w_perm, pair_out, ws, cnt, status, fill_wait_ns, num_sms, st, dyn);
+}
+
+}  // namespace moe

@@ -35,22 +35,24 @@
 // its TMEM before returning.
 #include <algorithm>
 
-#include "kernels.cuh"
-#include "ptx.cuh"
-#include "umma.cuh"
+#include "decode_common.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int BK = 64;                       // K per stage (one 128-byte swizzle row)
-constexpr int kNMax = 64;                    // tokens per chunk (MMA N <= 64)
+using dec::BK;
+using dec::kNMax;
+using dec::kXchgFloats;
+using dec::Unit;
+using dec::locate_unit;
+using dec::decode_epilogue;
+
 constexpr int A_BYTES = 128 * BK * 2;        // 16 KB of weights per stage
 constexpr int B_BYTES = kNMax * BK * 2;      // up to 8 KB of tokens per stage
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int kMaxStages = 9;
 constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 128;          // 2 accumulators x 64 columns
-constexpr int kXchgFloats = kNMax * 64;      // up values of one unit: [token][64 rows]
 
 struct __align__(8) Shared {
     uint64_t full[kMaxStages], empty[kMaxStages], acc_full[2], acc_empty[2];
@@ -69,35 +71,7 @@ struct Layout {
     static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
 };
 
-// Arrival on a split tile's counter: a gpu-scope acquire-release add. The barrier before it
-// orders the other epilogue threads' partial stores ahead of this release (cumulativity), and
-// the barrier after it orders their partial loads behind this acquire.
-__device__ __forceinline__ int atomic_add_acq_rel_gpu(int* p, int v) {
-    int old;
-    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-    return old;
-}
 
-struct Unit {
-    int a;       // work entry
-    int chunk;   // token chunk
-    int tile;    // row tile
-    int split;   // K split
-};
-
-__device__ __forceinline__ Unit locate_unit(const GemvWork* work, int n_work, int u, int R, int S) {
-    int lo = 0, hi = n_work - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (__ldg(&work[mid].unit_begin) <= u) lo = mid;
-        else hi = mid - 1;
-    }
-    const int local = u - __ldg(&work[lo].unit_begin);
-    const int rest = local / S;
-    return Unit{lo, rest / R, rest % R, local % S};
-}
-
-__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
 
 template <bool GATEUP>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -258,133 +232,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 raise_status(status, kDevWaitTimeout);
         }
     } else {
-        // ------------------------------------------------------------ epilogue (128 threads)
-        const int q = warp & 3;         // TMEM lanes 32q .. 32q+31
-        const int row = q * 32 + lane;  // accumulator row of this thread
-        const bool leader = threadIdx.x == 64;
-        int acc = 0;
-        uint32_t acc_phase = 0;
-        for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
-            const Unit un = locate_unit(work, n_work, u, R, S);
-            const GemvWork wk = work[un.a];
-            const int tok0 = wk.tok_off + un.chunk * kNMax;
-            const int nt = min(kNMax, wk.n_tok - un.chunk * kNMax);
-            const int nc = (nt + 15) >> 4;  // 16-column chunks of the accumulator
-            if (leader) sh.ok[acc] = mbar_wait(&sh.acc_full[acc], acc_phase, consumer_wait_ns) ? 1 : 0;
-            named_bar(1, 128);
-            if (!sh.ok[acc]) {
-                if (leader) raise_status(status, kDevWaitTimeout);
-                break;
-            }
-            tc_fence_after();
-            const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kNMax);
-            const size_t tile_floats = static_cast<size_t>(kNMax) * 128;
-            bool from_ws = false;
-            if (S > 1) {
-                // partial of this split -> workspace [unit][token][row], coalesced over rows
-                float* wsu = ws + static_cast<size_t>(u) * tile_floats;
-                for (int c = 0; c < nc; ++c) {
-                    uint32_t v[16];
-                    tmem_ld16(taddr + 16 * c, v);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) __stcg(wsu + (16 * c + j) * 128 + row, __uint_as_float(v[j]));
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&sh.acc_empty[acc]);
-                named_bar(1, 128);
-                if (leader) {
-                    const int tile_id = u / S;
-                    const int old = atomic_add_acq_rel_gpu(cnt + tile_id, 1);
-                    const int is_last = (old == S - 1) ? 1 : 0;
-                    if (is_last) cnt[tile_id] = 0;  // every split has arrived; ready for the next launch
-                    sh.last[acc] = is_last;
-                }
-                named_bar(1, 128);
-                const bool is_last = sh.last[acc] != 0;
-                if (!is_last) {
-                    acc ^= 1;
-                    if (acc == 0) acc_phase ^= 1u;
-                    continue;
-                }
-                from_ws = true;
-            }
-            const float* ws0 = ws + static_cast<size_t>(u - un.split) * tile_floats;
-            // 16 accumulator columns of this thread's row: TMEM, or the sum of the S partials
-            auto fetch = [&](int c, float (&v)[16]) {
-                if (from_ws) {
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) v[j] = __ldcg(ws0 + (16 * c + j) * 128 + row);
-                    for (int s = 1; s < S; ++s) {
-                        const float* p = ws0 + static_cast<size_t>(s) * tile_floats;
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) v[j] += __ldcg(p + (16 * c + j) * 128 + row);
-                    }
-                } else {
-                    uint32_t r[16];
-                    tmem_ld16(taddr + 16 * c, r);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
-                }
-            };
-            auto release = [&]() {
-                if (!from_ws) {
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&sh.acc_empty[acc]);
-                }
-            };
-            if (GATEUP) {
-                float* xc = xchg;
-                const int i0 = un.tile * 64;
-                if (q >= 2) {  // up rows: hand them to the gate warps
-                    for (int c = 0; c < nc; ++c) {
-                        float v[16];
-                        fetch(c, v);
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) xc[(16 * c + j) * 64 + row - 64] = v[j];
-                    }
-                    release();
-                }
-                named_bar(1, 128);
-                if (q < 2) {  // gate rows: h = silu(g) * u for the chunk's tokens
-                    for (int c = 0; c < nc; ++c) {
-                        float v[16];
-                        fetch(c, v);
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const int n = 16 * c + j;
-                            if (n < nt) {
-                                const float h = silu_mul(v[j], xc[n * 64 + row]);
-                                reinterpret_cast<__nv_bfloat16*>(h_out)[static_cast<size_t>(tok0 + n) * I + i0 + row] =
-                                    __float2bfloat16_rn(h);
-                            }
-                        }
-                    }
-                    release();
-                }
-                named_bar(1, 128);  // the exchange buffer is free for the next unit
-            } else {
-                const int n0 = un.tile * 128;
-                for (int c = 0; c < nc; ++c) {
-                    float v[16];
-                    fetch(c, v);
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int n = 16 * c + j;
-                        if (n < nt) {
-                            const size_t pos = static_cast<size_t>(tok0 + n);
-                            pair_out[pos * H + n0 + row] = __ldg(w_perm + pos) * v[j];
-                        }
-                    }
-                }
-                release();
-            }
-            acc ^= 1;
-            if (acc == 0) acc_phase ^= 1u;
-        }
+        decode_epilogue<GATEUP>(sh.acc_full, sh.acc_empty, sh.ok, sh.last, tmem, xchg, work, n_work, n_units, S, R, H,
+                                I, h_out, w_perm, pair_out, ws, cnt, status, consumer_wait_ns, 64);
     }
     tc_fence_before();
     __syncthreads();

@@ -44,6 +44,10 @@ struct DecodeMaps {
     CUtensorMap a_d;   // arena [C*3H rows x I], box 64 x 128 rows
     CUtensorMap b_x;   // x_perm [P_max x H], box 64 x 16 rows
     CUtensorMap b_h;   // h_perm [P_max x I], box 64 x 16 rows
+    // MXFP4 entries: bytes [H/2 x 3I rows x C slots] (box 32 x 64 x 1) and [I/2 x 3H x C]
+    // (box 32 x 128 x 1) over the E2M1 part of each slot
+    CUtensorMap a_gu4;
+    CUtensorMap a_d4;
 };
 
 int decode_row_tiles(bool gateup, int H, int I);   // row tiles per token chunk
@@ -69,6 +73,14 @@ cudaError_t launch_decode_down(const DecodeMaps& maps, const GemvWork* work, int
                                const int32_t* slot_row, const uint32_t* fill_flag, int H, int I, const float* w_perm,
                                float* pair_out, float* ws, int* cnt, int* status, uint64_t fill_wait_ns, int num_sms,
                                cudaStream_t st);
+
+// --- decode expert FFN with MXFP4 entries (expanded to bf16 on chip; decode_fp4.cu) ---
+// Same work lists, splits and epilogues as the bf16 kernels; dyn as for the _dyn launchers.
+cudaError_t launch_decode_fp4(bool gateup, const DecodeMaps& maps, const uint8_t* arena, uint64_t entry_bytes,
+                              const GemvWork* work, int n_work, int n_units, int S, const int* dyn,
+                              const int32_t* slot_row, const uint32_t* fill_flag, int H, int I, uint16_t* h_perm,
+                              const float* w_perm, float* pair_out, float* ws, int* cnt, int* status,
+                              uint64_t fill_wait_ns, int num_sms, cudaStream_t st);
 
 // --- device-resident cache policy (decode forward with no host round trip) ---
 enum : int { kEvHit = 0, kEvFill = 1, kEvPrefetchFill = 2, kEvPrefetchHit = 3 };

@@ -142,6 +142,7 @@ struct moe_ctx {
     int L = 0, E = 0, H = 0, I = 0, k = 0, C = 0, Tmax = 0, Pmax = 0;
     size_t entry_elems = 0, entry_bytes = 0;
     int path = MOE_PATH_AUTO;
+    bool fp4 = false;  // MXFP4 entries (MOE_MXFP4)
 
     uint16_t* pool = nullptr;   // pinned host, L*E entries
     uint16_t* arena = nullptr;  // device, C entries
@@ -437,9 +438,27 @@ int access_keys(moe_ctx* c, const std::vector<int>& keys, bool prefetch) {
     return rc;
 }
 
+// 3-D byte view [d0 x d1 x d2] with strides (bytes) s1 between d1 rows and s2 between d2
+// planes, box [b0 x b1 x 1], no swizzle.
+bool make_map3_u8(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1, uint64_t s2,
+                  uint32_t b0, uint32_t b1) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {d0, d1, d2};
+    cuuint64_t strides[2] = {s1, s2};
+    cuuint32_t box[3] = {b0, b1, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // TMA views of the slot arena (they change when the arena is reallocated).
 bool make_arena_maps(moe_ctx* c) {
     const uint64_t H = c->H, I = c->I, C = c->C;
+    if (c->fp4)  // the E2M1 part of each slot, viewed as rows of H/2 (gate/up) or I/2 (down) bytes
+        return make_map3_u8(&c->dec_maps.a_gu4, c->arena, H / 2, 3 * I, C, H / 2, c->entry_bytes, 32, 64) &&
+               make_map3_u8(&c->dec_maps.a_d4, c->arena, I / 2, 3 * H, C, I / 2, c->entry_bytes, 32, 128);
     return make_map(&c->dec_maps.a_gu, c->arena, H, C * 3 * I, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
            make_map(&c->dec_maps.a_d, c->arena, I, C * 3 * H, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) &&
            make_map(&c->gemm_maps.b_gu, c->arena, H, C * 3 * I, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) &&
@@ -492,6 +511,40 @@ void free_all(moe_ctx* c) {
 }  // namespace
 
 namespace {
+
+// The decode expert kernels for the context's weight format: a work list with its size given
+// here (n_work, n_units, S) or read on the device from dyn = {n_work, n_units, S}.
+cudaError_t run_gateup(moe_ctx* c, const GemvWork* work, int n_work, int n_units, int S, const int* dyn,
+                       const int32_t* slot_row, uint64_t fill_wait_ns) {
+    if (c->fp4)
+        return moe::launch_decode_fp4(true, c->dec_maps, reinterpret_cast<const uint8_t*>(c->arena), c->entry_bytes,
+                                      work, n_work, n_units, S, dyn, slot_row, c->fill_flag, c->H, c->I, c->h_perm,
+                                      nullptr, nullptr, c->dec_ws, c->dec_cnt, c->status, fill_wait_ns, c->num_sms,
+                                      c->s_comp);
+    if (dyn)
+        return moe::launch_decode_gateup_dyn(c->dec_maps, work, dyn, slot_row, c->H, c->I, c->h_perm, c->dec_ws,
+                                             c->dec_cnt, c->status, c->num_sms, c->s_comp);
+    return moe::launch_decode_gateup(c->dec_maps, work, n_work, n_units, S, slot_row, c->fill_flag, c->H, c->I,
+                                     c->h_perm, c->dec_ws, c->dec_cnt, c->status, fill_wait_ns, c->num_sms, c->s_comp);
+}
+
+cudaError_t run_down(moe_ctx* c, const GemvWork* work, int n_work, int n_units, int S, const int* dyn,
+                     const int32_t* slot_row, uint64_t fill_wait_ns) {
+    if (c->fp4)
+        return moe::launch_decode_fp4(false, c->dec_maps, reinterpret_cast<const uint8_t*>(c->arena), c->entry_bytes,
+                                      work, n_work, n_units, S, dyn, slot_row, c->fill_flag, c->H, c->I, nullptr,
+                                      c->w_perm, c->pair_out, c->dec_ws, c->dec_cnt, c->status, fill_wait_ns,
+                                      c->num_sms, c->s_comp);
+    if (dyn)
+        return moe::launch_decode_down_dyn(c->dec_maps, work, dyn, slot_row, c->H, c->I, c->w_perm, c->pair_out,
+                                           c->dec_ws, c->dec_cnt, c->status, c->num_sms, c->s_comp);
+    return moe::launch_decode_down(c->dec_maps, work, n_work, n_units, S, slot_row, c->fill_flag, c->H, c->I,
+                                   c->w_perm, c->pair_out, c->dec_ws, c->dec_cnt, c->status, fill_wait_ns, c->num_sms,
+                                   c->s_comp);
+}
+
+// Bytes of one weight as stored: 2 (bf16) or 17/32 (E2M1 half byte plus a scale per 32).
+double weight_bytes(const moe_ctx* c) { return c->fp4 ? 17.0 / 32.0 : 2.0; }
 
 // The device policy on one key set, then the fills it chose on the copy stream (forked from
 // and, when `join`, joined back into the compute stream). No host wait: capturable.
@@ -560,26 +613,20 @@ int forward_device(moe_ctx* c, int layer, const void* x, const float* resid, flo
         if (rc) return rc;
         {
             ProfScope ps(c, kDecodeGateUp, 0.0, 0.0);
-            CUDA_TRY(moe::launch_decode_gateup_dyn(c->dec_maps, wh, c->d_hdr->hit_gu, slot_row, H, I, c->h_perm,
-                                                   c->dec_ws, c->dec_cnt, c->status, c->num_sms, c->s_comp));
+            CUDA_TRY(run_gateup(c, wh, 0, 0, 1, c->d_hdr->hit_gu, slot_row, 0));
         }
         {
             ProfScope ps(c, kDecodeDown, 0.0, 0.0);
-            CUDA_TRY(moe::launch_decode_down_dyn(c->dec_maps, wh + (E + 1), c->d_hdr->hit_d, slot_row, H, I,
-                                                 c->w_perm, c->pair_out, c->dec_ws, c->dec_cnt, c->status, c->num_sms,
-                                                 c->s_comp));
+            CUDA_TRY(run_down(c, wh + (E + 1), 0, 0, 1, c->d_hdr->hit_d, slot_row, 0));
         }
         CUDA_TRY(cudaStreamWaitEvent(c->s_comp, c->ev_join, 0));
         {
             ProfScope ps(c, kDecodeGateUp, 0.0, 0.0);
-            CUDA_TRY(moe::launch_decode_gateup_dyn(c->dec_maps, wm, c->d_hdr->miss_gu, slot_row, H, I, c->h_perm,
-                                                   c->dec_ws, c->dec_cnt, c->status, c->num_sms, c->s_comp));
+            CUDA_TRY(run_gateup(c, wm, 0, 0, 1, c->d_hdr->miss_gu, slot_row, 0));
         }
         {
             ProfScope ps(c, kDecodeDown, 0.0, 0.0);
-            CUDA_TRY(moe::launch_decode_down_dyn(c->dec_maps, wm + (E + 1), c->d_hdr->miss_d, slot_row, H, I,
-                                                 c->w_perm, c->pair_out, c->dec_ws, c->dec_cnt, c->status, c->num_sms,
-                                                 c->s_comp));
+            CUDA_TRY(run_down(c, wm + (E + 1), 0, 0, 1, c->d_hdr->miss_d, slot_row, 0));
         }
     }
     {
@@ -670,8 +717,10 @@ int moe_cache_init(const moe_config_t* cfg, void* stream_compute, void* stream_c
     c->C = f.capacity;
     c->Tmax = f.max_tokens;
     c->Pmax = f.max_tokens * f.top_k;
-    c->entry_elems = entry_elems;
-    c->entry_bytes = entry_elems * 2;
+    c->fp4 = (f.flags & MOE_MXFP4) != 0;
+    // bf16: 2 bytes per weight; MXFP4: E2M1 halves plus one scale byte per 32 weights
+    c->entry_bytes = c->fp4 ? entry_elems / 2 + entry_elems / 32 : entry_elems * 2;
+    c->entry_elems = c->entry_bytes / 2;  // 16-bit units (pool and arena pointers are uint16_t)
     c->lru.reset(c->C, static_cast<int>(keys));
     c->slot_host.assign(keys, -1);
     c->slot_last_use.assign(c->C, -1);
@@ -1103,7 +1152,9 @@ int moe_layer_forward(moe_ctx* c, int layer, const void* x, const float* resid, 
     }
     const int U = static_cast<int>(distinct.size());
     int path = c->path;
-    if (path == MOE_PATH_AUTO) path = (max_n <= kDecodeMaxTokens) ? MOE_PATH_GEMV : MOE_PATH_GEMM;
+    if (c->fp4 && path == MOE_PATH_GEMM)
+        return fail(MOE_E_INVAL, "MXFP4 entries run on the decode kernels only (MOE_PATH_GEMM unsupported)");
+    if (path == MOE_PATH_AUTO) path = (c->fp4 || max_n <= kDecodeMaxTokens) ? MOE_PATH_GEMV : MOE_PATH_GEMM;
 
     // 4. waves of at most C experts
     for (int a0 = 0; a0 < U; a0 += c->C) {
@@ -1213,16 +1264,14 @@ int moe_layer_forward(moe_ctx* c, int layer, const void* x, const float* resid, 
         CUDA_TRY(cudaMemcpyAsync(c->work_dev, wk, 2 * (E + 1) * sizeof(GemvWork), cudaMemcpyHostToDevice, c->s_comp));
         CUDA_TRY(cudaEventRecord(c->stage_ev[s], c->s_comp));
         {
-            ProfScope ps(c, kDecodeGateUp, 4.0 * nw * I * H + 2.0 * pw * H + 2.0 * pw * I, 4.0 * pw * I * H);
-            CUDA_TRY(moe::launch_decode_gateup(c->dec_maps, c->work_dev, nw, units_gu, Sg, slot_row, c->fill_flag, H,
-                                               I, c->h_perm, c->dec_ws, c->dec_cnt, c->status, fill_wait_ns,
-                                               c->num_sms, c->s_comp));
+            ProfScope ps(c, kDecodeGateUp, 2.0 * nw * I * H * weight_bytes(c) + 2.0 * pw * H + 2.0 * pw * I,
+                         4.0 * pw * I * H);
+            CUDA_TRY(run_gateup(c, c->work_dev, nw, units_gu, Sg, nullptr, slot_row, fill_wait_ns));
         }
         {
-            ProfScope ps(c, kDecodeDown, 2.0 * nw * H * I + 2.0 * pw * I + 4.0 * pw * H + 4.0 * pw, 2.0 * pw * I * H);
-            CUDA_TRY(moe::launch_decode_down(c->dec_maps, c->work_dev + (E + 1), nw, units_d, Sd, slot_row,
-                                             c->fill_flag, H, I, c->w_perm, c->pair_out, c->dec_ws, c->dec_cnt,
-                                             c->status, fill_wait_ns, c->num_sms, c->s_comp));
+            ProfScope ps(c, kDecodeDown, 1.0 * nw * H * I * weight_bytes(c) + 2.0 * pw * I + 4.0 * pw * H + 4.0 * pw,
+                         2.0 * pw * I * H);
+            CUDA_TRY(run_down(c, c->work_dev + (E + 1), nw, units_d, Sd, nullptr, slot_row, fill_wait_ns));
         }
         c->comp_seq++;
         CUDA_TRY(cudaEventRecord(c->comp_ev[c->comp_seq % kEvRing], c->s_comp));

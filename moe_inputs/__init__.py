@@ -110,6 +110,9 @@ def gpu_lib():
         L = ctypes.CDLL(_GPU_SO)
         L.mi_gpu_normal_bf16_to_host.argtypes = [ctypes.c_uint64, ctypes.c_int, ctypes.c_void_p, ctypes.c_uint64,
                                                  ctypes.c_double, ctypes.c_void_p, ctypes.c_char_p, ctypes.c_int]
+        L.mi_gpu_mxfp4_entries_to_host.argtypes = [ctypes.c_uint64, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
+                                                   ctypes.c_int, ctypes.c_double, ctypes.c_void_p, ctypes.c_char_p,
+                                                   ctypes.c_int]
         _gpu_lib = L
     return _gpu_lib
 
@@ -220,6 +223,20 @@ def gpu_fill_entries(seed: int, keys, H: int, I: int, ptrs) -> None:
     dsts = (ctypes.c_void_p * len(keys))(*[int(p) for p in ptrs])
     err = ctypes.create_string_buffer(256)
     rc = gpu_lib().mi_gpu_normal_bf16_to_host(seed, len(keys), streams, 3 * H * I, 0.02, dsts, err, 256)
+    if rc != 0:
+        raise RuntimeError("GPU input generator: " + err.value.decode(errors="replace"))
+
+
+def gpu_fill_mxfp4_entries(seed: int, keys, H: int, I: int, ptrs) -> None:
+    """Write MXFP4 entries keys[i] = (layer, expert) into host memory at ptrs[i] with the GPU
+    build of this generator (the same bytes as fill_mxfp4_entry_at)."""
+    keys = list(keys)
+    if not keys:
+        return
+    streams = (ctypes.c_uint64 * len(keys))(*[stream_id(KIND_EXPERT, l, e) for l, e in keys])
+    dsts = (ctypes.c_void_p * len(keys))(*[int(p) for p in ptrs])
+    err = ctypes.create_string_buffer(256)
+    rc = gpu_lib().mi_gpu_mxfp4_entries_to_host(seed, len(keys), streams, H, I, 0.02, dsts, err, 256)
     if rc != 0:
         raise RuntimeError("GPU input generator: " + err.value.decode(errors="replace"))
 

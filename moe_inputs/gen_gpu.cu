@@ -9,6 +9,7 @@
 #include <cuda_runtime.h>
 #include <stdio.h>
 
+#include "mxfp4_core.h"
 #include "normal_core.h"
 
 __global__ void mi_normal_bf16_kernel(uint64_t seed, uint64_t stream, uint64_t n, double stddev, uint16_t* out) {
@@ -20,6 +21,35 @@ __global__ void mi_normal_bf16_kernel(uint64_t seed, uint64_t stream, uint64_t n
             const uint64_t i = q * 4 + w;
             if (i < n) out[i] = mi_bf16_rne((float)(z[w] * stddev));
         }
+    }
+}
+
+// One thread per block of 32 weights of a bf16 entry (W_gate [I x H] | W_up [I x H] |
+// W_down [H x I]): its E2M1 bytes at the block's element offset / 2, its scale in the entry's
+// [K/64][rows][2] scale layout -- the bytes mi_mxfp4_entry of gen.c writes.
+__global__ void mi_mxfp4_entry_kernel(const uint16_t* w, int H, int I, uint8_t* out) {
+    const uint64_t n = 3ull * H * I, gate = (uint64_t)I * H;
+    const uint64_t nblk = n / 32;
+    for (uint64_t blk = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; blk < nblk;
+         blk += (uint64_t)gridDim.x * blockDim.x) {
+        const uint64_t elem = blk * 32;
+        int mat, rows, row, b;
+        if (elem < 2 * gate) {
+            mat = (int)(elem / gate);
+            const uint64_t within = elem % gate;
+            rows = I;
+            row = (int)(within / H);
+            b = (int)((within % H) / 32);
+        } else {
+            mat = 2;
+            const uint64_t within = elem - 2 * gate;
+            rows = H;
+            row = (int)(within / I);
+            b = (int)((within % I) / 32);
+        }
+        uint8_t sb;
+        mi_mxfp4_block(w + elem, out + elem / 2, &sb);
+        out[n / 2 + (uint64_t)mat * (gate / 32) + ((uint64_t)(b / 2) * rows + row) * 2 + (b % 2)] = sb;
     }
 }
 
@@ -65,6 +95,42 @@ extern "C" int mi_gpu_normal_bf16_to_host(uint64_t seed, int n_streams, const ui
         if (buf[b]) cudaFree(buf[b]);
         if (done[b]) cudaEventDestroy(done[b]);
     }
+    cudaStreamDestroy(st);
+    return rc;
+}
+
+/*
+ * MXFP4 entries on the GPU: for each stream, the N(0, stddev) bf16 entry (3*H*I weights) is
+ * generated and quantized as gen.c's mi_mxfp4_entry does, and the 3*H*I*17/32 bytes are copied
+ * to host_dst[i]. Returns 0, or -1 with a message in err.
+ */
+extern "C" int mi_gpu_mxfp4_entries_to_host(uint64_t seed, int n_streams, const uint64_t* streams, int H, int I,
+                                            double stddev, void* const* host_dst, char* err, int err_len) {
+    if (n_streams <= 0) return 0;
+    const uint64_t n = 3ull * H * I, bytes = n / 2 + n / 32;
+    uint16_t* w = nullptr;
+    uint8_t* buf[2] = {nullptr, nullptr};
+    cudaStream_t st = nullptr;
+    cudaError_t e = cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking);
+    if (e != cudaSuccess) return report(e, "stream", err, err_len);
+    int rc = 0;
+    if ((e = cudaMalloc(&w, n * sizeof(uint16_t))) != cudaSuccess) rc = report(e, "cudaMalloc", err, err_len);
+    for (int b = 0; b < 2 && rc == 0; ++b)
+        if ((e = cudaMalloc(&buf[b], bytes)) != cudaSuccess) rc = report(e, "cudaMalloc", err, err_len);
+    const uint64_t nq = (n + 3) / 4;
+    const unsigned grid = (unsigned)((nq + 255) / 256 < 148 * 16 ? (nq + 255) / 256 : 148 * 16);
+    const unsigned qgrid = (unsigned)((n / 32 + 255) / 256 < 148 * 16 ? (n / 32 + 255) / 256 : 148 * 16);
+    for (int i = 0; i < n_streams && rc == 0; ++i) {
+        mi_normal_bf16_kernel<<<grid, 256, 0, st>>>(seed, streams[i], n, stddev, w);
+        mi_mxfp4_entry_kernel<<<qgrid, 256, 0, st>>>(w, H, I, buf[i & 1]);
+        if ((e = cudaGetLastError()) != cudaSuccess) rc = report(e, "generator launch", err, err_len);
+        else if ((e = cudaMemcpyAsync(host_dst[i], buf[i & 1], bytes, cudaMemcpyDeviceToHost, st)) != cudaSuccess)
+            rc = report(e, "copy to host", err, err_len);
+    }
+    if (rc == 0 && (e = cudaStreamSynchronize(st)) != cudaSuccess) rc = report(e, "synchronize", err, err_len);
+    if (w) cudaFree(w);
+    for (int b = 0; b < 2; ++b)
+        if (buf[b]) cudaFree(buf[b]);
     cudaStreamDestroy(st);
     return rc;
 }

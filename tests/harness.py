@@ -21,7 +21,7 @@ def f32_dev(a: np.ndarray):
 
 
 def make_cache(W: mi.Workload, max_tokens: int, L: int | None = None, capacity: int | None = None,
-               flags: int = moe.MOE_TRACE) -> moe.MoeCache:
+               flags: int = moe.MOE_TRACE, pool=None) -> moe.MoeCache:
     import torch
     L = W.L if L is None else L
     # one stream for torch's work (inputs, resid = x.float(), ...) and the library's compute,
@@ -31,28 +31,42 @@ def make_cache(W: mi.Workload, max_tokens: int, L: int | None = None, capacity: 
     cache = moe.MoeCache(moe.LayerShape(L, W.E, W.H, W.I, W.k, W.C if capacity is None else capacity, max_tokens),
                          flags=flags, stream_compute=stream)
     cache.torch_stream = stream
-    fill_pool(cache, W, L)
+    if pool is None:
+        fill_pool(cache, W, L)
+    else:
+        pool(cache, W, L)
     return cache
 
 
 def fill_pool(cache: moe.MoeCache, W: mi.Workload, L: int):
     """Write every seeded entry into the context's pinned pool, with the GPU build of the input
-    generator (the same bits as the CPU build, which the oracle uses for its own copy)."""
+    generator (the same bits as the CPU build, which the oracle uses for its own copy): bf16, or
+    MXFP4 for a context created with MOE_MXFP4."""
     keys = [(l, e) for l in range(L) for e in range(W.E)]
-    mi.gpu_fill_entries(W.seed, keys, W.H, W.I, [cache.host_entry(l, e) for l, e in keys])
+    ptrs = [cache.host_entry(l, e) for l, e in keys]
+    if cache.shape_flags & moe.MOE_MXFP4:
+        mi.gpu_fill_mxfp4_entries(W.seed, keys, W.H, W.I, ptrs)
+    else:
+        mi.gpu_fill_entries(W.seed, keys, W.H, W.I, ptrs)
 
 
 class OracleEntries:
-    """The oracle's own copy of the expert entries, regenerated from the seed."""
+    """The oracle's own copy of the expert entries, regenerated from the seed (bf16; or the
+    MXFP4 entries read back by the oracle as the bf16 values they encode, when fp4)."""
 
-    def __init__(self, W: mi.Workload):
+    def __init__(self, W: mi.Workload, fp4: bool = False):
         self.W = W
+        self.fp4 = fp4
         self.cache = {}
 
     def __call__(self, layer: int, expert: int) -> np.ndarray:
         key = (layer, expert)
         if key not in self.cache:
-            self.cache[key] = mi.expert_entry(self.W.seed, layer, expert, self.W.H, self.W.I)
+            W = self.W
+            if self.fp4:
+                self.cache[key] = oracle.mxfp4_entry_as_bf16(mi.mxfp4_entry(W.seed, layer, expert, W.H, W.I), W.H, W.I)
+            else:
+                self.cache[key] = mi.expert_entry(W.seed, layer, expert, W.H, W.I)
         return self.cache[key]
 
     def layer(self, layer: int):
