@@ -66,12 +66,17 @@ extern "C" {
  * back into the compute stream (no prefill overlap); moe_stats reports fill_ms = 0. Run one
  * call of each shape before capturing, and keep MOE_PROFILE timing off while capturing. */
 #define MOE_DEVICE_POLICY 8u
-/* Expert entries in MXFP4 (OCP Microscaling: E2M1 weights, one E8M0 scale per 32 along each
- * row): 3*hidden*inter/2 bytes of E2M1 pairs (W_gate, W_up, W_down row-major, the even element
- * in the low nibble) followed by 3*hidden*inter/32 scale bytes (each matrix as [K/64][rows][2]).
- * An entry is 17/64 of its bf16 size, so fills move 3.8x fewer bytes. The kernels expand the
- * weights to bf16 on chip -- every MXFP4 value is exact in bf16 -- and run the decode kernels
- * (MOE_PATH_GEMM is refused); activations stay bf16. */
+/* Expert entries in MXFP4 (OCP Microscaling: E2M1 weights, the even element in the low nibble,
+ * one E8M0 scale per 32 consecutive weights of a row), stored in the order the kernels stream
+ * them: stages of 4352 bytes, each the 4096 code bytes of a 128-row tile x 64-column slab
+ * followed by its 256 scale bytes. W_gate/W_up come first, per 64-row tile (tile-major) and
+ * slab: gate rows (64 x 32 bytes), up rows (64 x 32), gate scales (64 x 2), up scales (64 x 2);
+ * then W_down per 128-row tile and slab: rows (128 x 32), scales (128 x 2). Within a row, its
+ * two 32-blocks of the slab take bytes 0-15 and 16-31 and scale bytes 2r and 2r+1. An entry is
+ * 3*hidden*inter*17/32 bytes, 17/64 of bf16, so fills move 3.8x fewer bytes. The kernels expand
+ * the weights to bf16 on chip -- every MXFP4 value is exact in bf16 -- and run the decode
+ * kernels (MOE_PATH_GEMM is refused); activations stay bf16. Needs inter % 128 == 0 and
+ * hidden % 256 == 0 (as for every context). */
 #define MOE_MXFP4 16u
 
 /* ---- fill modes (moe_cache_fill) ---- */

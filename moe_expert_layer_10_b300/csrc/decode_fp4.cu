@@ -10,14 +10,15 @@
 // power-of-two scale, so it is exact in bf16: the kernel expands the weights to bf16 in shared
 // memory and runs the same tcgen05 kind::f16 products as the bf16 kernel (decode_mma.cu),
 // with the tokens as the N side; the epilogue is the shared one (decode_common.cuh).
-// Entry layout: E2M1 bytes of W_gate [I x H], W_up [I x H], W_down [H x I] row-major, then the
-// E8M0 scales of each matrix as [K/64][rows][2].
-// Roles (14 warps):
-//  * warp 0, one lane: producer -- per 64-column slab of a unit, the tile's E2M1 bytes (128 rows
-//    x 32 bytes, a 3-D TMA over (bytes, rows, slot)) and its 256 scale bytes (a bulk copy), into
-//    a 16-deep raw ring, so about 68 KB of weights are in flight per SM;
-//  * warps 6-13 (256 threads): converters -- thread (row, half) expands 32 codes of one row with
-//    one scale into bf16 inside the 128-byte-swizzled A tile of an MMA stage, with byte-permute
+// Entry layout: the blocks are stored in the order this kernel streams them, in stages of
+// 4352 bytes (4096 bytes of E2M1 codes of a 128-row tile x 64-column slab, then its 256 scale
+// bytes): W_gate/W_up per 64-row tile and slab (gate rows, up rows, gate scales, up scales),
+// then W_down per 128-row tile and slab. A unit's weights are one contiguous run of stages.
+// Roles (22 warps):
+//  * warp 0, one lane: producer -- one 4352-byte bulk copy per stage into an 8-deep raw ring
+//    (about 34 KB of weights in flight per SM);
+//  * warps 6-21 (512 threads): converters -- thread (row, quarter) expands 16 codes of one row
+//    into bf16 inside the 128-byte-swizzled A tile of an MMA stage, with byte-permute
 //    lookups (two 4-byte tables per scale for the high and the low byte of the bf16 pattern);
 //    converter 0 also loads the stage's token tile (TMA);
 //  * warp 1, one lane: MMA issuer, as in the bf16 kernel; warps 2-5: epilogue.
@@ -39,12 +40,12 @@ using dec::Unit;
 constexpr int kRawA = 128 * 32;                // E2M1 bytes of a 128-row tile slab
 constexpr int kRawScales = 256;                // its E8M0 scales: 128 rows x 2
 constexpr int kRawStage = kRawA + kRawScales;  // 4352 bytes (34 x 128)
-constexpr int kRawStages = 16;
+constexpr int kRawStages = 8;
 constexpr int kA16 = 128 * BK * 2;             // bf16 A tile: 16 KB
 constexpr int kB16 = kNMax * BK * 2;           // token tile: up to 8 KB
 constexpr int kMmaStage = kA16 + kB16;         // 24 KB
-constexpr int kMaxMmaStages = 6;
-constexpr int kConvWarps = 8;
+constexpr int kMaxMmaStages = 7;
+constexpr int kConvWarps = 16;
 constexpr int kConvBase = 192;                 // first converter thread
 constexpr int kThreads = kConvBase + 32 * kConvWarps;
 constexpr uint32_t kTmemCols = 128;
@@ -59,7 +60,7 @@ struct __align__(8) Shared {
 
 template <bool GATEUP>
 struct Layout {
-    static constexpr int MMA_STAGES = GATEUP ? 5 : 6;
+    static constexpr int MMA_STAGES = 7;
     static constexpr int XCHG_BYTES = GATEUP ? kXchgFloats * 4 : 0;
     static constexpr int SMEM =
         MMA_STAGES * kMmaStage + kRawStages * kRawStage + XCHG_BYTES + static_cast<int>(sizeof(Shared)) + 1024;
@@ -105,9 +106,8 @@ __device__ __forceinline__ void expand8(uint32_t v, uint32_t h_lo, uint32_t h_hi
 
 template <bool GATEUP>
 __global__ void __launch_bounds__(kThreads, 1)
-    decode_fp4_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-                      const uint8_t* __restrict__ arena, uint64_t entry_bytes, const GemvWork* __restrict__ work,
-                      int n_work, int n_units, int S, const int32_t* __restrict__ slot_row,
+    decode_fp4_kernel(const __grid_constant__ CUtensorMap tm_b, const uint8_t* __restrict__ arena,
+                      uint64_t entry_bytes, const GemvWork* __restrict__ work, int n_work, int n_units, int S, const int32_t* __restrict__ slot_row,
                       const uint32_t* __restrict__ fill_flag, int H, int I, uint16_t* __restrict__ h_out,
                       const float* __restrict__ w_perm, float* __restrict__ pair_out, float* __restrict__ ws,
                       int* __restrict__ cnt, int* status, uint64_t fill_wait_ns, const int* __restrict__ dyn) {
@@ -128,8 +128,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int K = GATEUP ? H : I;
     const int KB = K / BK;
     const int R = GATEUP ? I / 64 : H / 128;
-    const uint64_t q_bytes = 3ull * H * I / 2;        // the E2M1 part of an entry
-    const uint64_t s_mat = static_cast<uint64_t>(H) * I / 32;  // scale bytes of one matrix
+    // stages of the gate/up part of an entry (the down part follows)
+    const uint64_t gu_bytes = static_cast<uint64_t>(I / 64) * (H / 64) * kRawStage;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kRawStages; ++s) {
@@ -158,8 +158,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ producer (weights)
         if (lane == 0) {
-            prefetch_tmap(&tm_a);
-            const uint64_t pol = policy_evict_first();
             int stage = 0;
             uint32_t phase = 0, used = 0, last_phase = 0;
             bool ok = true;
@@ -179,7 +177,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     raise_status(status, kDevBadSlot);
                     slot = 0;
                 }
-                const uint8_t* sc = arena + static_cast<uint64_t>(slot) * entry_bytes + q_bytes;
+                // the unit's stages: one contiguous run in the slot's entry
+                const uint8_t* src = arena + static_cast<uint64_t>(slot) * entry_bytes +
+                                     (GATEUP ? static_cast<uint64_t>(un.tile) * (H / 64) * kRawStage
+                                             : gu_bytes + static_cast<uint64_t>(un.tile) * (I / 64) * kRawStage);
                 const int kb0 = un.split * KB / S, kb1 = (un.split + 1) * KB / S;
                 for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(&sh.raw_empty[stage], phase ^ 1u, consumer_wait_ns)) {
@@ -189,20 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     uint8_t* dst = raw_tiles + stage * kRawStage;
                     mbar_arrive_expect_tx(&sh.raw_full[stage], kRawStage);
-                    if (GATEUP) {
-                        const int r0 = un.tile * 64;
-                        tma_load_3d_hint(dst, &tm_a, &sh.raw_full[stage], kb * 32, r0, slot, pol);
-                        tma_load_3d_hint(dst + kRawA / 2, &tm_a, &sh.raw_full[stage], kb * 32, I + r0, slot, pol);
-                        // scales [K/64][rows][2]: this slab's pairs for rows r0.. of gate, then of up
-                        bulk_load(dst + kRawA, sc + (static_cast<uint64_t>(kb) * I + r0) * 2, 128, &sh.raw_full[stage]);
-                        bulk_load(dst + kRawA + 128, sc + s_mat + (static_cast<uint64_t>(kb) * I + r0) * 2, 128,
-                                  &sh.raw_full[stage]);
-                    } else {
-                        const int r0 = un.tile * 128;
-                        tma_load_3d_hint(dst, &tm_a, &sh.raw_full[stage], kb * 32, 2 * H + r0, slot, pol);
-                        bulk_load(dst + kRawA, sc + 2 * s_mat + (static_cast<uint64_t>(kb) * H + r0) * 2, 256,
-                                  &sh.raw_full[stage]);
-                    }
+                    bulk_load(dst, src + static_cast<uint64_t>(kb) * kRawStage, kRawStage, &sh.raw_full[stage]);
                     used |= 1u << stage;
                     last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
                     if (++stage == kRawStages) {
@@ -269,9 +257,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         decode_epilogue<GATEUP>(sh.acc_full, sh.acc_empty, sh.ok, sh.last, tmem, xchg, work, n_work, n_units, S, R, H,
                                 I, h_out, w_perm, pair_out, ws, cnt, status, consumer_wait_ns, 64);
     } else {
-        // ------------------------------------------------------------ converters (warps 6-13)
+        // ------------------------------------------------------------ converters (warps 6-21)
         const int c = threadIdx.x - kConvBase;
-        const int row = c >> 1, half = c & 1;
+        const int row = c >> 2, quarter = c & 3;  // 16 codes of one row: bytes 8*quarter .. +7
         const bool token_loader = c == 0;
         if (token_loader) prefetch_tmap(&tm_b);
         int rs = 0, ms = 0;
@@ -300,16 +288,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     last_phase = (last_phase & ~(1u << ms)) | (mphase << ms);
                 }
                 const uint8_t* raw = raw_tiles + rs * kRawStage;
-                const uint4 codes = *reinterpret_cast<const uint4*>(raw + row * 32 + half * 16);
-                const uint32_t sc = raw[kRawA + row * 2 + half];
+                const uint2 codes = *reinterpret_cast<const uint2*>(raw + row * 32 + quarter * 8);
+                const uint32_t sc = raw[kRawA + row * 2 + (quarter >> 1)];  // the 32-block's scale
                 uint32_t h_lo, h_hi, l_lo, l_hi;
                 scale_tables(sc, h_lo, h_hi, l_lo, l_hi);
-                const uint32_t words[4] = {codes.x, codes.y, codes.z, codes.w};
+                const uint32_t words[2] = {codes.x, codes.y};
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
+                for (int q = 0; q < 2; ++q) {
                     uint32_t w[4];
                     expand8(words[q], h_lo, h_hi, l_lo, l_hi, w);
-                    const int chunk = half * 4 + q;  // 16-byte chunk of the 128-byte row
+                    const int chunk = quarter * 2 + q;  // 16-byte chunk of the 128-byte row
                     *reinterpret_cast<uint4*>(sm + row * 128 + ((chunk ^ (row & 7)) << 4)) =
                         make_uint4(w[0], w[1], w[2], w[3]);
                 }
@@ -344,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <bool GATEUP>
-cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const uint8_t* arena, uint64_t entry_bytes,
+cudaError_t launch(const CUtensorMap& tb, const uint8_t* arena, uint64_t entry_bytes,
                    const GemvWork* work, int n_work, int n_units, int S, const int32_t* slot_row,
                    const uint32_t* fill_flag, int H, int I, uint16_t* h_out, const float* w_perm, float* pair_out,
                    float* ws, int* cnt, int* status, uint64_t fill_wait_ns, int num_sms, cudaStream_t st,
@@ -363,7 +351,7 @@ cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const uint8_t* 
         attr = true;
     }
     const int grid = dyn ? num_sms : std::min(n_units, num_sms);
-    kern<<<grid, kThreads, smem, st>>>(ta, tb, arena, entry_bytes, work, n_work, n_units, S, slot_row, fill_flag, H, I,
+    kern<<<grid, kThreads, smem, st>>>(tb, arena, entry_bytes, work, n_work, n_units, S, slot_row, fill_flag, H, I,
                                        h_out, w_perm, pair_out, ws, cnt, status, fill_wait_ns, dyn);
     return cudaGetLastError();
 }
@@ -376,9 +364,9 @@ cudaError_t launch_decode_fp4(bool gateup, const DecodeMaps& m, const uint8_t* a
                               const float* w_perm, float* pair_out, float* ws, int* cnt, int* status,
                               uint64_t fill_wait_ns, int num_sms, cudaStream_t st) {
     if (gateup)
-        return launch<true>(m.a_gu4, m.b_x, arena, entry_bytes, work, n_work, n_units, S, slot_row, fill_flag, H, I,
+        return launch<true>(m.b_x, arena, entry_bytes, work, n_work, n_units, S, slot_row, fill_flag, H, I,
                             h_perm, nullptr, nullptr, ws, cnt, status, fill_wait_ns, num_sms, st, dyn);
-    return launch<false>(m.a_d4, m.b_h, arena, entry_bytes, work, n_work, n_units, S, slot_row, fill_flag, H, I,
+    return launch<false>(m.b_h, arena, entry_bytes, work, n_work, n_units, S, slot_row, fill_flag, H, I,
                          nullptr, w_perm, pair_out, ws, cnt, status, fill_wait_ns, num_sms, st, dyn);
 }
 

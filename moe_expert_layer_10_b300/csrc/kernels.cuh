@@ -44,10 +44,6 @@ struct DecodeMaps {
     CUtensorMap a_d;   // arena [C*3H rows x I], box 64 x 128 rows
     CUtensorMap b_x;   // x_perm [P_max x H], box 64 x 16 rows
     CUtensorMap b_h;   // h_perm [P_max x I], box 64 x 16 rows
-    // MXFP4 entries: bytes [H/2 x 3I rows x C slots] (box 32 x 64 x 1) and [I/2 x 3H x C]
-    // (box 32 x 128 x 1) over the E2M1 part of each slot
-    CUtensorMap a_gu4;
-    CUtensorMap a_d4;
 };
 
 int decode_row_tiles(bool gateup, int H, int I);   // row tiles per token chunk

@@ -438,27 +438,10 @@ int access_keys(moe_ctx* c, const std::vector<int>& keys, bool prefetch) {
     return rc;
 }
 
-// 3-D byte view [d0 x d1 x d2] with strides (bytes) s1 between d1 rows and s2 between d2
-// planes, box [b0 x b1 x 1], no swizzle.
-bool make_map3_u8(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1, uint64_t s2,
-                  uint32_t b0, uint32_t b1) {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[3] = {d0, d1, d2};
-    cuuint64_t strides[2] = {s1, s2};
-    cuuint32_t box[3] = {b0, b1, 1};
-    cuuint32_t es[3] = {1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // TMA views of the slot arena (they change when the arena is reallocated).
 bool make_arena_maps(moe_ctx* c) {
     const uint64_t H = c->H, I = c->I, C = c->C;
-    if (c->fp4)  // the E2M1 part of each slot, viewed as rows of H/2 (gate/up) or I/2 (down) bytes
-        return make_map3_u8(&c->dec_maps.a_gu4, c->arena, H / 2, 3 * I, C, H / 2, c->entry_bytes, 32, 64) &&
-               make_map3_u8(&c->dec_maps.a_d4, c->arena, I / 2, 3 * H, C, I / 2, c->entry_bytes, 32, 128);
+    if (c->fp4) return true;  // MXFP4 stages are fetched with plain bulk copies
     return make_map(&c->dec_maps.a_gu, c->arena, H, C * 3 * I, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
            make_map(&c->dec_maps.a_d, c->arena, I, C * 3 * H, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) &&
            make_map(&c->gemm_maps.b_gu, c->arena, H, C * 3 * I, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) &&

@@ -191,32 +191,24 @@ int mi_trace_reuse(uint64_t seed, uint64_t stream, int L, int steps, int B, int 
 /*
  * Expert entry (layer, expert) in MXFP4: the seeded bf16 entry of stream `stream`
  * (W_gate [I x H] | W_up [I x H] | W_down [H x I]) quantized in blocks of 32 along each row
- * (mxfp4_core.h). Layout:
- *  - the E2M1 bytes of gate, up, down, row-major (3*H*I/2 bytes);
- *  - then the E8M0 scales of gate, up, down (3*H*I/32 bytes), each matrix stored as
- *    [K/64][rows][2]: for every 64 columns, each row's two block scales -- so the scales of a
- *    run of rows for one 64-column slab are contiguous.
+ * (mxfp4_core.h), the blocks placed in the streaming order of mi_mxfp4_place.
  */
 void mi_mxfp4_entry(uint64_t seed, uint64_t stream, int H, int I, uint8_t* out) {
     const uint64_t n = 3ull * H * I;
     uint16_t* w = (uint16_t*)malloc(n * sizeof(uint16_t));
     if (!w) return;
     mi_normal_bf16(seed, stream, 0, n, 0.02, w);
-    uint8_t* q = out;
-    uint8_t* s = out + n / 2;
     const uint64_t gate = (uint64_t)I * H;
 #pragma omp parallel for schedule(static)
     for (int r = 0; r < 2 * I + H; ++r) {
         const int K = r < 2 * I ? H : I;
-        const int rows = r < 2 * I ? I : H;
         const int mat = r < I ? 0 : (r < 2 * I ? 1 : 2);
         const int row = r < I ? r : (r < 2 * I ? r - I : r - 2 * I);
         const uint64_t elem0 = r < 2 * I ? (uint64_t)r * H : 2 * gate + (uint64_t)(r - 2 * I) * I;
-        uint8_t* s_mat = s + (uint64_t)mat * (gate / 32);
         for (int b = 0; b < K / 32; ++b) {
-            uint8_t sb;
-            mi_mxfp4_block(w + elem0 + 32 * b, q + (elem0 + 32 * b) / 2, &sb);
-            s_mat[((uint64_t)(b / 2) * rows + row) * 2 + (b % 2)] = sb;
+            uint64_t co, so;
+            mi_mxfp4_place(H, I, mat, row, b, &co, &so);
+            mi_mxfp4_block(w + elem0 + 32 * b, out + co, out + so);
         }
     }
     free(w);

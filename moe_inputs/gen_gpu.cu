@@ -25,31 +25,29 @@ __global__ void mi_normal_bf16_kernel(uint64_t seed, uint64_t stream, uint64_t n
 }
 
 // One thread per block of 32 weights of a bf16 entry (W_gate [I x H] | W_up [I x H] |
-// W_down [H x I]): its E2M1 bytes at the block's element offset / 2, its scale in the entry's
-// [K/64][rows][2] scale layout -- the bytes mi_mxfp4_entry of gen.c writes.
+// W_down [H x I]): its E2M1 bytes and scale placed as mi_mxfp4_place says -- the bytes
+// mi_mxfp4_entry of gen.c writes.
 __global__ void mi_mxfp4_entry_kernel(const uint16_t* w, int H, int I, uint8_t* out) {
     const uint64_t n = 3ull * H * I, gate = (uint64_t)I * H;
     const uint64_t nblk = n / 32;
     for (uint64_t blk = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; blk < nblk;
          blk += (uint64_t)gridDim.x * blockDim.x) {
         const uint64_t elem = blk * 32;
-        int mat, rows, row, b;
+        int mat, row, b;
         if (elem < 2 * gate) {
             mat = (int)(elem / gate);
             const uint64_t within = elem % gate;
-            rows = I;
             row = (int)(within / H);
             b = (int)((within % H) / 32);
         } else {
             mat = 2;
             const uint64_t within = elem - 2 * gate;
-            rows = H;
             row = (int)(within / I);
             b = (int)((within % I) / 32);
         }
-        uint8_t sb;
-        mi_mxfp4_block(w + elem, out + elem / 2, &sb);
-        out[n / 2 + (uint64_t)mat * (gate / 32) + ((uint64_t)(b / 2) * rows + row) * 2 + (b % 2)] = sb;
+        uint64_t co, so;
+        mi_mxfp4_place(H, I, mat, row, b, &co, &so);
+        mi_mxfp4_block(w + elem, out + co, out + so);
     }
 }
 

@@ -106,4 +106,31 @@ MI_HD void mi_mxfp4_rows(const uint16_t* x, int rows, int K, uint8_t* q, uint8_t
             mi_mxfp4_block(x + (size_t)r * K + 32 * b, q + (size_t)r * (K / 2) + 16 * b, s + (size_t)r * (K / 32) + b);
 }
 
+/*
+ * Place of a block in an MXFP4 expert entry. The entry is stored in the order the decode
+ * kernels stream it, in stages of 4352 bytes = 4096 bytes of E2M1 codes + 256 scale bytes:
+ *  - W_gate and W_up [I x H]: for each 64-row tile t and 64-column slab k (t-major), one stage
+ *    = gate rows (64 x 32 bytes), up rows (64 x 32 bytes), gate scales (64 x 2), up scales (64 x 2);
+ *  - then W_down [H x I]: for each 128-row tile t and 64-column slab k, one stage = the rows
+ *    (128 x 32 bytes), then their scales (128 x 2).
+ * Within a row of a stage, block `half` (0 or 1) of the slab takes bytes 16*half .. +15 and
+ * scale byte 2*row + half. mat: 0 gate, 1 up, 2 down; b: the 32-block index along the row.
+ */
+MI_HD void mi_mxfp4_place(int H, int I, int mat, int row, int b, uint64_t* code_off, uint64_t* scale_off) {
+    const uint64_t stage_bytes = 4352;
+    const int k = b / 2, half = b % 2;
+    if (mat < 2) {
+        const uint64_t stage = ((uint64_t)(row / 64) * (H / 64) + k) * stage_bytes;
+        const int rr = row % 64;
+        *code_off = stage + (uint64_t)mat * 2048 + rr * 32 + half * 16;
+        *scale_off = stage + 4096 + (uint64_t)mat * 128 + rr * 2 + half;
+    } else {
+        const uint64_t gu = (uint64_t)(I / 64) * (H / 64) * stage_bytes;
+        const uint64_t stage = gu + ((uint64_t)(row / 128) * (I / 64) + k) * stage_bytes;
+        const int rr = row % 128;
+        *code_off = stage + rr * 32 + half * 16;
+        *scale_off = stage + 4096 + rr * 2 + half;
+    }
+}
+
 #endif /* MOE_INPUTS_MXFP4_CORE_H */

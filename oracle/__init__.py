@@ -201,22 +201,25 @@ def mxfp4_dequant(q: np.ndarray, s: np.ndarray, n: int) -> np.ndarray:
 
 
 def mxfp4_entry_as_bf16(entry: np.ndarray, H: int, I: int) -> np.ndarray:
-    """An MXFP4 expert entry as the bf16 entry of the same values, for the bf16 expert FFN.
-    Entry layout: E2M1 bytes of W_gate [I x H], W_up [I x H], W_down [H x I] (row-major), then
-    their E8M0 scales, each matrix as [K/64][rows][2] (every 64 columns, each row's two block
-    scales)."""
-    n = 3 * H * I
-    q = entry[: n // 2]
-    s_all = entry[n // 2:]
-    mats = [(I, H), (I, H), (H, I)]
-    s_rows = []
-    off = 0
-    for rows, K in mats:
-        blk = s_all[off: off + rows * K // 32].reshape(K // 64, rows, 2)
-        s_rows.append(blk.transpose(1, 0, 2).reshape(rows, K // 32))  # back to [rows][K/32]
-        off += rows * K // 32
-    s = np.concatenate([a.ravel() for a in s_rows])
-    return mxfp4_dequant(q, s, n)
+    """An MXFP4 expert entry as the bf16 entry (W_gate | W_up | W_down, row-major) of the same
+    values, for the bf16 expert FFN. Entry layout, in stages of 4096 code bytes + 256 scale
+    bytes: for W_gate/W_up, per 64-row tile and 64-column slab: gate rows (64 x 32 bytes), up
+    rows (64 x 32), gate scales (64 x 2), up scales (64 x 2); then for W_down, per 128-row tile
+    and slab: rows (128 x 32), scales (128 x 2). A row's 32 bytes hold its two 32-blocks of the
+    slab, with the scale bytes in the same order."""
+    st = 4352
+    gu = (I // 64) * (H // 64) * st
+    a = entry[:gu].reshape(I // 64, H // 64, st)
+    gate_q = a[:, :, :2048].reshape(I // 64, H // 64, 64, 32).transpose(0, 2, 1, 3).reshape(I, H // 2)
+    up_q = a[:, :, 2048:4096].reshape(I // 64, H // 64, 64, 32).transpose(0, 2, 1, 3).reshape(I, H // 2)
+    gate_s = a[:, :, 4096:4224].reshape(I // 64, H // 64, 64, 2).transpose(0, 2, 1, 3).reshape(I, H // 32)
+    up_s = a[:, :, 4224:4352].reshape(I // 64, H // 64, 64, 2).transpose(0, 2, 1, 3).reshape(I, H // 32)
+    d = entry[gu:].reshape(H // 128, I // 64, st)
+    down_q = d[:, :, :4096].reshape(H // 128, I // 64, 128, 32).transpose(0, 2, 1, 3).reshape(H, I // 2)
+    down_s = d[:, :, 4096:].reshape(H // 128, I // 64, 128, 2).transpose(0, 2, 1, 3).reshape(H, I // 32)
+    q = np.concatenate([gate_q.ravel(), up_q.ravel(), down_q.ravel()])
+    s = np.concatenate([gate_s.ravel(), up_s.ravel(), down_s.ravel()])
+    return mxfp4_dequant(q, s, 3 * H * I)
 
 
 def layer_accesses(idx: np.ndarray, E: int) -> np.ndarray:

@@ -126,18 +126,27 @@ def test_mxfp4_quantizer_hand_worked_blocks():
 
 
 def test_mxfp4_entry_is_the_blocks_of_the_bf16_entry():
-    """An MXFP4 entry is the seeded bf16 entry quantized block by block: the E2M1 bytes of
-    gate, up, down row-major, then each matrix's scales as [K/64][rows][2]."""
+    """An MXFP4 entry is the seeded bf16 entry quantized block by block, each block at the place
+    the streaming layout gives it: stages of 4096 code bytes + 256 scale bytes, per 64-row tile
+    and 64-column slab for gate/up (gate rows, up rows, gate scales, up scales), then per 128-row
+    tile and slab for down (rows, scales)."""
     H, I = 256, 128
     w = mi.expert_entry(0, 2, 5, H, I)
     e = mi.mxfp4_entry(0, 2, 5, H, I)
     n = 3 * H * I
     assert e.size == mi.mxfp4_entry_bytes(H, I) == n // 2 + n // 32
-    # (matrix, row, 32-block) -> element offset, and the scale's place in the layout
-    for mat, row, b in [(0, 0, 0), (0, 3, 5), (1, 127, 7), (2, 0, 0), (2, 255, 3), (1, 64, 6)]:
-        rows, K = ((I, H), (I, H), (H, I))[mat]
-        elem0 = mat * I * H + row * K + 32 * b
+    gu = (I // 64) * (H // 64) * 4352
+    for mat, row, b in [(0, 0, 0), (0, 3, 5), (1, 127, 7), (1, 64, 6), (2, 0, 0), (2, 255, 3), (2, 130, 1)]:
+        K = H if mat < 2 else I
+        elem0 = (mat * I * H + row * K if mat < 2 else 2 * I * H + row * K) + 32 * b
         q, s = mi.mxfp4_block(w[elem0: elem0 + 32])
-        assert e[elem0 // 2: elem0 // 2 + 16].tolist() == q.tolist()
-        s_off = n // 2 + mat * (I * H // 32) + ((b // 2) * rows + row) * 2 + b % 2
-        assert e[s_off] == s, (mat, row, b)
+        k, half = b // 2, b % 2
+        if mat < 2:
+            stage = ((row // 64) * (H // 64) + k) * 4352
+            co = stage + mat * 2048 + (row % 64) * 32 + half * 16
+            so = stage + 4096 + mat * 128 + (row % 64) * 2 + half
+        else:
+            stage = gu + ((row // 128) * (I // 64) + k) * 4352
+            co = stage + (row % 128) * 32 + half * 16
+            so = stage + 4096 + (row % 128) * 2 + half
+        assert e[co: co + 16].tolist() == q.tolist() and e[so] == s, (mat, row, b)
