@@ -117,7 +117,8 @@ typedef struct {
     uint64_t prefetch_hits;  /* whole-layer prefetches that found the entry resident */
     uint64_t evictions;      /* fills that replaced a resident entry */
     uint64_t fill_bytes;     /* bytes copied host -> device by fills */
-    double fill_ms;          /* copy-stream time of completed fill batches (CUDA events) */
+    double fill_ms;          /* copy-stream time of completed fills, per call that filled (CUDA events;
+                                0 under MOE_DEVICE_POLICY) */
     uint64_t trace_len;      /* events recorded since the last reset (the ring keeps the newest) */
     uint64_t forwards;       /* moe_layer_forward calls */
     uint64_t waves;          /* expert waves run (a layer routing to more than C experts runs several) */

@@ -11,10 +11,17 @@
 //    GPU cache; the runtime console reports cache activity (moe_stats).
 //
 // B300 design: one context owns a pinned pool (cudaHostAlloc), a device arena of C whole
-// entries, a device slot table slot_of[L][E], a compute stream and a copy stream. Fills are
-// single cudaMemcpyAsync copies of a contiguous entry on the copy stream. Ordering is by
-// events: a fill into a slot waits for the last compute wave that read the slot; a wave
-// waits for the last fill batch of its slots. Every host wait polls with a deadline.
+// entries, a device slot table slot_of[L][E], a compute stream and a copy stream.
+//  * Host policy (default): the LRU runs here. A fill is one cudaMemcpyAsync of a contiguous
+//    entry on the copy stream, followed by a write of the slot's fill generation to a device
+//    flag. A fill into a slot waits (event) for the last compute wave that read the slot. The
+//    decode kernels of a wave wait on the device for the flags of the entries the wave filled,
+//    so resident experts compute while the copies cross the link; the prefill GEMM waits
+//    (event) for its wave's fills.
+//  * Device policy (MOE_DEVICE_POLICY): the LRU, the trace and the fills run in kernels
+//    (device_policy.cu); a forward enqueues work only, so a decode step can be graph-captured.
+//  * Elastic capacity (moe_cache_resize) and MXFP4 entries (MOE_MXFP4) apply to both.
+// Every host wait polls with a deadline.
 #include <algorithm>
 #include <chrono>
 #include <cstdarg>
@@ -53,7 +60,7 @@ int fail(int code, const char* fmt, ...) {
                                            __FILE__, __LINE__);                                        \
     } while (0)
 
-constexpr int kEvRing = 256;     // compute-wave and fill-batch events
+constexpr int kEvRing = 256;     // compute-wave and per-fill completion events
 constexpr int kStageRing = 16;   // pinned staging buffers for small H2D copies
 constexpr uint64_t kFillWaitNs = 20000000000ull;  // 20 s: a wave's own fills must land by then
 constexpr uint64_t kInjectedFillWaitNs = 200000000ull;  // 0.2 s under injection kind 3
@@ -1244,7 +1251,8 @@ int moe_layer_forward(moe_ctx* c, int layer, const void* x, const float* resid, 
         wk[nw] = GemvWork{-1, 0, 0, units_gu, -1, 0, 0, 0};
         wk2[nw] = GemvWork{-1, 0, 0, units_d, -1, 0, 0, 0};
         // both lists in one copy: gate/up at work_dev, down at work_dev + E + 1
-        CUDA_TRY(cudaMemcpyAsync(c->work_dev, wk, 2 * (E + 1) * sizeof(GemvWork), cudaMemcpyHostToDevice, c->s_comp));
+        CUDA_TRY(cudaMemcpyAsync(c->work_dev, wk, kWorkEntries(E) * sizeof(GemvWork), cudaMemcpyHostToDevice,
+                                 c->s_comp));
         CUDA_TRY(cudaEventRecord(c->stage_ev[s], c->s_comp));
         {
             ProfScope ps(c, kDecodeGateUp, 2.0 * nw * I * H * weight_bytes(c) + 2.0 * pw * H + 2.0 * pw * I,
