@@ -37,7 +37,8 @@ UNIT = "tok/s"
 BATCHES = (1, 4, 16)  # replaced by --batches
 FALLBACK_HBM_GBS = 6400.0
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_gateup.md")
-DECODE_SOURCE = os.path.join(ROOT, "moe_expert_layer_10_b300", "csrc", "decode_mma.cu")
+DECODE_SOURCES = [os.path.join(ROOT, "moe_expert_layer_10_b300", "csrc", f)
+                  for f in ("decode_mma.cu", "decode_common.cuh", "ptx.cuh", "umma.cuh")]
 
 
 def parse_args():
@@ -85,6 +86,14 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def decode_source_sha256():
+    """sha256 over the decode kernel's source files, in a fixed order."""
+    h = hashlib.sha256()
+    for f in DECODE_SOURCES:
+        h.update(open(f, "rb").read())
+    return h.hexdigest()
+
+
 def traffic_ratio_from_profile():
     """DRAM bytes / algorithmic bytes of the decode gate/up launch captured in the committed ncu
     summary, or None if the summary is missing or was taken on a different kernel source."""
@@ -95,7 +104,7 @@ def traffic_ratio_from_profile():
     h = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
     if not m or not h:
         return None
-    cur = hashlib.sha256(open(DECODE_SOURCE, "rb").read()).hexdigest()
+    cur = decode_source_sha256()
     return float(m.group(1)) if h.group(1) == cur else None
 
 
