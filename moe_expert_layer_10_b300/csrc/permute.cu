@@ -43,6 +43,37 @@ __device__ int block_exclusive_scan(int v, int* scratch /* >= 33 ints */, int* t
     return res;
 }
 
+// The routed expert of pair p, checked (an id outside [0, E) raises the status and counts as 0).
+__device__ __forceinline__ int checked_expert(const int32_t* idx, int p, int E, int* status) {
+    int e = idx[p];
+    if (e < 0 || e >= E) {
+        raise_status(status, kDevBadIndex);
+        e = 0;
+    }
+    return e;
+}
+
+// The lanes of the warp holding the same expert id as this lane (e >= 0), from one ballot
+// per bit of the id: a lane is a peer when it agrees on every bit. Lanes with e < 0 hold no
+// pair and are never peers.
+__device__ __forceinline__ uint32_t warp_peers(int e, int nbits) {
+    uint32_t peers = __ballot_sync(0xffffffffu, e >= 0);
+    for (int b = 0; b < nbits; ++b) {
+        const bool bit = (e >> b) & 1;
+        const uint32_t m = __ballot_sync(0xffffffffu, bit);
+        peers &= bit ? m : ~m;
+    }
+    return peers;
+}
+
+// A counting sort in one CTA. Warp w owns the contiguous pair range [32*r0, 32*r1) (rounds of
+// 32 pairs), so the pairs of an expert come out ordered by (warp, round, lane) = pair id.
+//  1. each warp counts its pairs per expert into its own column cnt[w][e] (shared-memory
+//     atomic increments: a count does not depend on their order);
+//  2. one exclusive scan over the counts in (expert, warp) order turns each cell into the first
+//     position of that warp's pairs of that expert;
+//  3. each warp walks its pairs again and places pair p at its cell's position plus its rank
+//     among the equal lanes of the round, advancing the cell after each round.
 __global__ void __launch_bounds__(kPermThreads) permute_kernel(const int32_t* __restrict__ idx,
                                                                const float* __restrict__ w, int P, int E,
                                                                int32_t* __restrict__ offsets,
@@ -52,73 +83,82 @@ __global__ void __launch_bounds__(kPermThreads) permute_kernel(const int32_t* __
                                                                int32_t* __restrict__ active,
                                                                int32_t* __restrict__ n_active, int* status) {
     extern __shared__ int smem[];
-    int* base = smem;             // [E] first position of each expert, advanced per chunk
-    int* ctot = base + E;         // [E] pairs of each expert in the current chunk
-    int* scan = ctot + E;         // [33]
-    uint16_t* wc = reinterpret_cast<uint16_t*>(scan + 36);  // [kPermWarps][E]
+    const int Es = E + 1;                     // column stride (odd: the scan's reads spread over banks)
+    int* cnt = smem;                          // [kPermWarps][Es]
+    int* scan = cnt + kPermWarps * Es;        // [33]
+    int* first = scan + 36;                   // [E + 1] first position of each expert
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-
-    for (int e = tid; e < E; e += kPermThreads) ctot[e] = 0;
-    for (int i = tid; i < kPermWarps * E; i += kPermThreads) wc[i] = 0;
+    for (int i = tid; i < kPermWarps * Es; i += kPermThreads) cnt[i] = 0;
     __syncthreads();
-    for (int p = tid; p < P; p += kPermThreads) {
-        int e = idx[p];
-        if (e < 0 || e >= E) {
-            raise_status(status, kDevBadIndex);
-            e = 0;
+    const int rounds = (P + 31) / 32;
+    const int per_warp = (rounds + kPermWarps - 1) / kPermWarps;
+    const int r0 = min(rounds, warp * per_warp), r1 = min(rounds, r0 + per_warp);
+    int* col = cnt + warp * Es;
+    constexpr int kBatch = 8;  // rounds whose expert ids are loaded before any is used
+    for (int r = r0; r < r1; ++r) {
+        const int p = 32 * r + lane;
+        if (p < P) atomicAdd(&col[checked_expert(idx, p, E, status)], 1);  // counts: order-free
+    }
+    __syncthreads();
+    // exclusive scan of the cells in (expert, warp) order: cell (e, w) is element e*32 + w
+    {
+        const int n_cells = kPermWarps * E;
+        const int per_thread = (n_cells + kPermThreads - 1) / kPermThreads;
+        const int i0 = min(n_cells, tid * per_thread), i1 = min(n_cells, i0 + per_thread);
+        int run = 0;
+        for (int i = i0; i < i1; ++i) run += cnt[(i % kPermWarps) * Es + i / kPermWarps];
+        int total;
+        int pos = block_exclusive_scan(run, scan, &total);
+        for (int i = i0; i < i1; ++i) {
+            int& c = cnt[(i % kPermWarps) * Es + i / kPermWarps];
+            const int v = c;
+            c = pos;
+            if (i % kPermWarps == 0) first[i / kPermWarps] = pos;
+            pos += v;
         }
-        atomicAdd(&ctot[e], 1);  // counts only: order-independent
+        if (tid == 0) first[E] = total;
     }
     __syncthreads();
     // offsets and the active list (E <= 1024 -> one expert per thread)
     {
-        const int c = tid < E ? ctot[tid] : 0;
-        int tot;
-        const int ex = block_exclusive_scan(c, scan, &tot);
-        if (tid < E) {
-            base[tid] = ex;
-            offsets[tid] = ex;
-        }
-        if (tid == 0) offsets[E] = tot;
+        const int c = tid < E ? first[tid + 1] - first[tid] : 0;
+        if (tid < E) offsets[tid] = first[tid];
+        if (tid == 0) offsets[E] = first[E];
         int nact;
         const int apos = block_exclusive_scan(c > 0 ? 1 : 0, scan, &nact);
         if (tid < E && c > 0) active[apos] = tid;
         if (tid == 0) *n_active = nact;
     }
-    __syncthreads();
-    // stable ranks, 1024 pairs per chunk: rank = earlier warps of the chunk + earlier lanes
-    for (int c0 = 0; c0 < P; c0 += kPermThreads) {
-        const int p = c0 + tid;
-        const bool valid = p < P;
-        int e = valid ? idx[p] : -1;
-        if (valid && (e < 0 || e >= E)) e = 0;
-        const uint32_t peers = __match_any_sync(0xffffffffu, e);
-        const int lane_rank = __popc(peers & ((1u << lane) - 1u));
-        const bool leader = lane == (__ffs(peers) - 1);
-        if (valid && leader) wc[warp * E + e] = static_cast<uint16_t>(__popc(peers));
-        __syncthreads();
-        for (int x = tid; x < E; x += kPermThreads) {
-            int run = 0;
-            for (int q = 0; q < kPermWarps; ++q) {
-                const int cnt = wc[q * E + x];
-                wc[q * E + x] = static_cast<uint16_t>(run);
-                run += cnt;
+    // placement: each warp only touches its own cells, so no CTA barrier is needed
+    const int nbits = E > 1 ? 32 - __clz(E - 1) : 0;
+    for (int rb = r0; rb < r1; rb += kBatch) {
+        int eb[kBatch];
+        float wb[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int p = 32 * (rb + u) + lane;
+            const bool valid = rb + u < r1 && p < P;
+            int e = valid ? idx[p] : -1;
+            if (valid && (e < 0 || e >= E)) e = 0;  // already raised in the counting pass
+            eb[u] = e;
+            wb[u] = valid ? w[p] : 0.0f;
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            if (rb + u >= r1) break;
+            const int p = 32 * (rb + u) + lane;
+            const int e = eb[u];
+            const uint32_t peers = warp_peers(e, nbits);
+            if (e >= 0) {
+                const int pos = col[e] + __popc(peers & ((1u << lane) - 1u));
+                perm[pos] = p;
+                inv_perm[p] = pos;
+                w_perm[pos] = wb[u];
             }
-            ctot[x] = run;
+            __syncwarp();
+            if (e >= 0 && lane == __ffs(peers) - 1) col[e] += __popc(peers);
+            __syncwarp();
         }
-        __syncthreads();
-        if (valid) {
-            const int pos = base[e] + wc[warp * E + e] + lane_rank;
-            perm[pos] = p;
-            inv_perm[p] = pos;
-            w_perm[pos] = w[p];
-        }
-        __syncthreads();
-        for (int x = tid; x < E; x += kPermThreads) {
-            base[x] += ctot[x];
-            for (int q = 0; q < kPermWarps; ++q) wc[q * E + x] = 0;
-        }
-        __syncthreads();
     }
 }
 
@@ -140,11 +180,11 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __rest
 cudaError_t launch_permute(const int32_t* idx, const float* w, int P, int E, int32_t* offsets, int32_t* perm,
                            int32_t* inv_perm, float* w_perm, int32_t* active, int32_t* n_active, int* status,
                            cudaStream_t st) {
-    const size_t smem = sizeof(int) * (2 * E + 36) + sizeof(uint16_t) * kPermWarps * E;
+    const size_t smem = sizeof(int) * (kPermWarps * (E + 1) + 36 + E + 1);
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t err = cudaFuncSetAttribute(permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               sizeof(int) * (2 * 1024 + 36) + sizeof(uint16_t) * kPermWarps * 1024);
+                                               sizeof(int) * (kPermWarps * 1025 + 36 + 1024 + 1));
         if (err != cudaSuccess) return err;
         attr_set = true;
     }

@@ -20,19 +20,31 @@ namespace moe {
 namespace {
 
 // Large batches (prefill): a register-tiled evaluation of the same order. A CTA of 16 warps
-// owns a tile of 32 tokens x 16 experts and walks H in chunks of 256 columns, staged in
-// shared memory with cp.async (a ring of 4 chunks). Warp w owns the 8 x 4 sub-tile of tokens
-// 8*(w/4).. and experts 4*(w%4)..; its lane l keeps the 32 partials s_l(t, e), each
-// accumulated with fused multiply-adds over exactly the columns 256m + 8l + r (m, then
-// r = 0..7) that the one-warp-per-dot-product kernels give lane l, so the fold yields the
-// same bits. Partials of two tokens share one packed f32x2 instruction (two independent
-// round-to-nearest fused multiply-adds).
-constexpr int kTT = 32, kTE = 16;
-constexpr int kXBytes = kTT * 512;   // 32 rows x 256 bf16
-constexpr int kWBytes = kTE * 1024;  // 16 rows x 256 fp32
+// owns a tile of 32 tokens x 32 experts and walks H in chunks of 256 columns (a ring of 3
+// chunks in shared memory). The 32 lanes of the order are split over warps, not over the lanes
+// of a warp: warp w evaluates the partials s_w and s_{w+16} of every (token, expert) of the
+// tile, each accumulated with fused multiply-adds over exactly the columns 256m + 8l + r
+// (m, then r = 0..7) that define s_l. Within the warp, lane (g, f) = (lane / 8, lane % 8) owns
+// tokens g + 4i (i < 8) and experts f + 8j (j < 4), so the lanes of a warp read the same
+// columns and shared memory serves them by broadcast. The 16 sums s_w + s_{w+16} -- the first
+// xor-fold step -- go through shared memory and the remaining steps (distances 8, 4, 2, 1) are
+// taken in the same pairing, then the bias.
+//
+// x is staged as fp32 pairs: token pair P = (P % 4 + 8 (P / 4), that token + 4) keeps, per
+// column, the two tokens' values side by side, so one 16-byte read gives the f32x2 operands
+// of two columns and two fused multiply-adds share one instruction (fma.rn.f32x2, two
+// independent round-to-nearest results). W_r is copied as is with cp.async.
+constexpr int kTT = 32, kTE = 32;
+constexpr int kTiledThreads = 512;
+constexpr int kXRow = 256 * 8 + 16;                 // bytes per token pair row (+16: bank spread)
+constexpr int kWRow = 256 * 4 + 16;                 // bytes per expert row
+constexpr int kXBytes = 16 * kXRow;
+constexpr int kWBytes = kTE * kWRow;
 constexpr int kTiledStage = kXBytes + kWBytes;
-constexpr int kTiledStages = 4;  // chunks in flight: the next three load while one is used
+constexpr int kTiledStages = 3;
 constexpr int kTiledSmem = kTiledStages * kTiledStage;
+constexpr int kFoldRow = 40;                        // floats per token row of the fold buffer
+static_assert(16 * kTT * kFoldRow * 4 <= kTiledSmem, "fold buffer must fit in the stage ring");
 
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
@@ -40,28 +52,6 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-
-// Stage columns [256m, 256m+256) of the tile. x rows keep their order (lane l reads the 16
-// bytes at 16l). A W_r row's 8-float run of lane l is split into its halves, stored at
-// 16l and 512 + 16l, so the lanes' 16-byte reads of one half are contiguous.
-constexpr int kTiledThreads = 512;
-
-__device__ __forceinline__ void router_stage(uint8_t* buf, const uint16_t* x, const float* Wr, int t0, int e0, int T,
-                                             int E, int H, int m) {
-    for (int i = threadIdx.x; i < 2048; i += kTiledThreads) {
-        if (i < 1024) {
-            const int row = i >> 5, c = i & 31;
-            const int t = min(t0 + row, T - 1);
-            cp_async16(buf + row * 512 + c * 16, x + static_cast<size_t>(t) * H + 256 * m + 8 * c);
-        } else {
-            const int j = i - 1024;
-            const int row = j >> 6, c = j & 63;
-            const int e = min(e0 + row, E - 1);
-            const int l = c >> 1, h = c & 1;
-            cp_async16(buf + kXBytes + row * 1024 + h * 512 + l * 16, Wr + static_cast<size_t>(e) * H + 256 * m + 4 * c);
-        }
-    }
-}
 
 // Two independent fp32 fused multiply-adds in one instruction (round to nearest each), on
 // register pairs: d = (a.lo * b.lo + c.lo, a.hi * b.hi + c.hi) -- the same two fmaf results.
@@ -78,6 +68,37 @@ __device__ __forceinline__ uint64_t pack2(float lo, float hi) {
 __device__ __forceinline__ float lo_of(uint64_t v) { return __uint_as_float(static_cast<uint32_t>(v)); }
 __device__ __forceinline__ float hi_of(uint64_t v) { return __uint_as_float(static_cast<uint32_t>(v >> 32)); }
 
+// The x granule (8 columns) of the two tokens of pair row P that thread tid stages.
+struct XGranule {
+    uint4 a, b;
+};
+__device__ __forceinline__ XGranule load_x_granule(const uint16_t* x, int t0, int T, int H, int m) {
+    const int P = threadIdx.x & 15, g = threadIdx.x >> 4;
+    const int ta = (P & 3) + 8 * (P >> 2);
+    const size_t col = static_cast<size_t>(256) * m + 8 * g;
+    XGranule r;
+    r.a = __ldg(reinterpret_cast<const uint4*>(x + static_cast<size_t>(min(t0 + ta, T - 1)) * H + col));
+    r.b = __ldg(reinterpret_cast<const uint4*>(x + static_cast<size_t>(min(t0 + ta + 4, T - 1)) * H + col));
+    return r;
+}
+__device__ __forceinline__ void store_x_granule(uint8_t* xs, const XGranule& r) {
+    const int P = threadIdx.x & 15, g = threadIdx.x >> 4;
+    float4* dst = reinterpret_cast<float4*>(xs + P * kXRow + g * 64);
+    const uint32_t a[4] = {r.a.x, r.a.y, r.a.z, r.a.w}, b[4] = {r.b.x, r.b.y, r.b.z, r.b.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q)  // columns 2q, 2q+1: (a, b) of each, column-major
+        dst[q] = make_float4(bf16lo(a[q]), bf16lo(b[q]), bf16hi(a[q]), bf16hi(b[q]));
+}
+__device__ __forceinline__ void stage_w(uint8_t* ws, const float* Wr, int e0, int E, int H, int m) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int i = threadIdx.x + kTiledThreads * k;
+        const int row = i >> 6, c = i & 63;
+        const int e = min(e0 + row, E - 1);
+        cp_async16(ws + row * kWRow + c * 16, Wr + static_cast<size_t>(e) * H + 256 * m + 4 * c);
+    }
+}
+
 __global__ void __launch_bounds__(kTiledThreads, 1) router_logits_tiled_kernel(const uint16_t* __restrict__ x,
                                                                      const float* __restrict__ Wr,
                                                                      const float* __restrict__ bias, int T, int H,
@@ -85,72 +106,93 @@ __global__ void __launch_bounds__(kTiledThreads, 1) router_logits_tiled_kernel(c
     extern __shared__ __align__(16) uint8_t rsm[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t0 = blockIdx.y * kTT, e0 = blockIdx.x * kTE;
-    const int tw = (warp >> 2) * 8, ew = (warp & 3) * 4;
-    // acc[e][p] holds the partials of tokens 2p and 2p+1 for expert e (one f32x2 pair)
-    uint64_t acc[4][4];
+    const int g = lane >> 3, f = lane & 7;
+    // acc[c][j][p]: partial s_{warp + 16c} of expert f + 8j for the token pair (g + 8p, g + 8p + 4)
+    uint64_t acc[2][4][4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e)
+    for (int c = 0; c < 2; ++c)
 #pragma unroll
-        for (int p = 0; p < 4; ++p) acc[e][p] = 0ull;
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int p = 0; p < 4; ++p) acc[c][j][p] = 0ull;
     const int M = H / 256;
-    // ring of kTiledStages chunks; one commit group per chunk (empty groups past the end keep
-    // the count uniform)
 #pragma unroll
     for (int m = 0; m < kTiledStages - 1; ++m) {
-        if (m < M) router_stage(rsm + m * kTiledStage, x, Wr, t0, e0, T, E, H, m);
+        if (m < M) {
+            uint8_t* st = rsm + m * kTiledStage;
+            store_x_granule(st, load_x_granule(x, t0, T, H, m));
+            stage_w(st + kXBytes, Wr, e0, E, H, m);
+        }
         cp_async_commit();
     }
     for (int m = 0; m < M; ++m) {
-        cp_async_wait<kTiledStages - 2>();  // chunk m has landed (this thread's copies)
-        __syncthreads();                    // ... everyone's; and chunk m-1's buffer is free
-        if (m + kTiledStages - 1 < M)
-            router_stage(rsm + ((m + kTiledStages - 1) % kTiledStages) * kTiledStage, x, Wr, t0, e0, T, E, H,
-                         m + kTiledStages - 1);
+        cp_async_wait<kTiledStages - 2>();  // chunk m's W_r rows have landed (this thread's copies)
+        __syncthreads();                    // ... everyone's, and chunk m-1's buffer is free
+        const int mn = m + kTiledStages - 1;
+        uint8_t* nst = rsm + (mn % kTiledStages) * kTiledStage;
+        XGranule nx;
+        if (mn < M) {
+            nx = load_x_granule(x, t0, T, H, mn);  // in flight while chunk m is evaluated
+            stage_w(nst + kXBytes, Wr, e0, E, H, mn);
+        }
         cp_async_commit();
         const uint8_t* xs = rsm + (m % kTiledStages) * kTiledStage;
         const uint8_t* ws = xs + kXBytes;
-        // x: the lane's 8 columns of each of 8 tokens (16 bytes each)
-        uint4 xv[8];
 #pragma unroll
-        for (int t = 0; t < 8; ++t) xv[t] = *reinterpret_cast<const uint4*>(xs + (tw + t) * 512 + lane * 16);
+        for (int c = 0; c < 2; ++c) {
+            const int l = warp + 16 * c;  // the lane of the order evaluated: columns 8l .. 8l+7
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            float4 wv[4];
+            for (int cp = 0; cp < 4; ++cp) {  // columns 8l + 2cp, 8l + 2cp + 1
+                uint4 xq[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-                wv[e] = *reinterpret_cast<const float4*>(ws + (ew + e) * 1024 + h * 512 + lane * 16);
+                for (int p = 0; p < 4; ++p)
+                    xq[p] = *reinterpret_cast<const uint4*>(xs + (g + 4 * p) * kXRow + (8 * l + 2 * cp) * 8);
+                float2 wq[4];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {  // column r = 4h + q, in order
-                uint64_t xp[4];
+                for (int j = 0; j < 4; ++j)
+                    wq[j] = *reinterpret_cast<const float2*>(ws + (f + 8 * j) * kWRow + (8 * l + 2 * cp) * 4);
 #pragma unroll
-                for (int p = 0; p < 4; ++p) {
-                    const uint32_t w0 = (h == 0) ? ((q < 2) ? xv[2 * p].x : xv[2 * p].y)
-                                                 : ((q < 2) ? xv[2 * p].z : xv[2 * p].w);
-                    const uint32_t w1 = (h == 0) ? ((q < 2) ? xv[2 * p + 1].x : xv[2 * p + 1].y)
-                                                 : ((q < 2) ? xv[2 * p + 1].z : xv[2 * p + 1].w);
-                    xp[p] = pack2((q & 1) ? bf16hi(w0) : bf16lo(w0), (q & 1) ? bf16hi(w1) : bf16lo(w1));
-                }
+                for (int q = 0; q < 2; ++q) {
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float wf = q == 0 ? wv[e].x : q == 1 ? wv[e].y : q == 2 ? wv[e].z : wv[e].w;
-                    const uint64_t wd = pack2(wf, wf);
+                    for (int j = 0; j < 4; ++j) {
+                        const float wf = q == 0 ? wq[j].x : wq[j].y;
+                        const uint64_t wd = pack2(wf, wf);
 #pragma unroll
-                    for (int p = 0; p < 4; ++p) acc[e][p] = fma2(wd, xp[p], acc[e][p]);
+                        for (int p = 0; p < 4; ++p) {
+                            const uint64_t xp = q == 0 ? (static_cast<uint64_t>(xq[p].y) << 32 | xq[p].x)
+                                                       : (static_cast<uint64_t>(xq[p].w) << 32 | xq[p].z);
+                            acc[c][j][p] = fma2(wd, xp, acc[c][j][p]);
+                        }
+                    }
                 }
             }
         }
+        if (mn < M) store_x_granule(nst, nx);  // chunk m-1's buffer: free since the barrier above
     }
+    cp_async_wait<0>();
+    __syncthreads();  // every thread is done with the ring: reuse it for the fold
+    float* fold = reinterpret_cast<float*>(rsm);  // [16][kTT][kFoldRow]
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
+    for (int j = 0; j < 4; ++j)
 #pragma unroll
-        for (int t = 0; t < 8; ++t) {
-            float v = (t & 1) ? hi_of(acc[e][t >> 1]) : lo_of(acc[e][t >> 1]);
-#pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
-            const int tt = t0 + tw + t, ee = e0 + ew + e;
-            if (lane == t * 4 + e && tt < T && ee < E)
-                z[static_cast<size_t>(tt) * E + ee] = __fadd_rn(v, bias ? __ldg(bias + ee) : 0.0f);
+        for (int p = 0; p < 4; ++p) {
+            const int e = f + 8 * j, ta = g + 8 * p;
+            fold[(warp * kTT + ta) * kFoldRow + e] = __fadd_rn(lo_of(acc[0][j][p]), lo_of(acc[1][j][p]));
+            fold[(warp * kTT + ta + 4) * kFoldRow + e] = __fadd_rn(hi_of(acc[0][j][p]), hi_of(acc[1][j][p]));
         }
+    __syncthreads();
+#pragma unroll
+    for (int o = threadIdx.x; o < kTT * kTE; o += kTiledThreads) {
+        const int t = o / kTE, e = o % kTE;
+        float v[16];
+#pragma unroll
+        for (int l = 0; l < 16; ++l) v[l] = fold[(l * kTT + t) * kFoldRow + e];
+#pragma unroll
+        for (int d = 8; d >= 1; d >>= 1)
+#pragma unroll
+            for (int l = 0; l < d; ++l) v[l] = __fadd_rn(v[l], v[l + d]);
+        const int tt = t0 + t, ee = e0 + e;
+        if (tt < T && ee < E) z[static_cast<size_t>(tt) * E + ee] = __fadd_rn(v[0], bias ? __ldg(bias + ee) : 0.0f);
     }
 }
 
