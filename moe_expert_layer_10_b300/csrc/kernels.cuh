@@ -15,10 +15,14 @@ cudaError_t launch_router_logits(const uint16_t* x, const float* Wr, const float
 cudaError_t launch_router_topk(const float* z, int T, int E, int k, const int32_t* forced, int32_t* idx, float* w,
                                int* status, cudaStream_t st);
 
-// --- permutation: stable grouping of the T*k pairs by expert (one CTA) ---
+// --- permutation: stable grouping of the T*k pairs by expert ---
+// Up to 1024 pairs: one CTA. More: permute_grid(P) CTAs of 1024 pairs, with `cells` holding
+// 2 * permute_grid(P) * E ints of scratch and `done` an arrival counter that is 0 before the
+// first launch (the kernels leave it 0).
+int permute_grid(int P);
 cudaError_t launch_permute(const int32_t* idx, const float* w, int P, int E, int32_t* offsets, int32_t* perm,
                            int32_t* inv_perm, float* w_perm, int32_t* active, int32_t* n_active, int* status,
-                           cudaStream_t st);
+                           int32_t* cells, unsigned* done, cudaStream_t st);
 // x_perm[pos] = x[perm[pos] / k]  (bf16 rows of H)
 cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* perm, int P, int k, int H, uint16_t* x_perm,
                                cudaStream_t st);

@@ -94,7 +94,6 @@ __global__ void __launch_bounds__(kPermThreads) permute_kernel(const int32_t* __
     const int per_warp = (rounds + kPermWarps - 1) / kPermWarps;
     const int r0 = min(rounds, warp * per_warp), r1 = min(rounds, r0 + per_warp);
     int* col = cnt + warp * Es;
-    constexpr int kBatch = 8;  // rounds whose expert ids are loaded before any is used
     for (int r = r0; r < r1; ++r) {
         const int p = 32 * r + lane;
         if (p < P) atomicAdd(&col[checked_expert(idx, p, E, status)], 1);  // counts: order-free
@@ -131,6 +130,7 @@ __global__ void __launch_bounds__(kPermThreads) permute_kernel(const int32_t* __
     }
     // placement: each warp only touches its own cells, so no CTA barrier is needed
     const int nbits = E > 1 ? 32 - __clz(E - 1) : 0;
+    constexpr int kBatch = 8;  // rounds whose expert ids are loaded before any is used
     for (int rb = r0; rb < r1; rb += kBatch) {
         int eb[kBatch];
         float wb[kBatch];
@@ -175,21 +175,139 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __rest
     for (int c = lane; c < H / 8; c += 32) dst[c] = __ldg(src + c);
 }
 
+// Larger batches (more than 1024 pairs): the same counting sort over many CTAs, so that the
+// scattered writes of perm and w_perm leave from many SMs. CTA g owns the pairs
+// [1024 g, 1024 g + 1024), one per thread; warp w of it the 32 pairs 1024 g + 32 w + lane.
+// The global order (expert, g, w, lane) is the order (expert, pair id).
+//  permute_count_kernel: CTA g counts its pairs per expert into cells[g][e]; the last CTA to
+//    finish (arrival counter) scans the cells in (expert, g) order into starts[g][e] and writes
+//    offsets, the active list and n_active, then resets the counter for the next launch.
+//  permute_place_kernel: CTA g turns starts[g][e] into per-warp starts (exclusive prefix over
+//    its warps' counts) and places each pair at its warp's start plus its rank among the equal
+//    lanes.
+constexpr int kChunkPairs = kPermThreads;
+
+__global__ void __launch_bounds__(kPermThreads) permute_count_kernel(const int32_t* __restrict__ idx, int P, int E,
+                                                                     int32_t* __restrict__ cells,
+                                                                     int32_t* __restrict__ starts,
+                                                                     int32_t* __restrict__ offsets,
+                                                                     int32_t* __restrict__ active,
+                                                                     int32_t* __restrict__ n_active,
+                                                                     unsigned* done, int* status) {
+    extern __shared__ int smem[];
+    int* cnt = smem;             // [E] this CTA's pairs per expert, later first position per expert
+    int* scan = cnt + E + 1;     // [33]
+    __shared__ bool s_last;
+    const int tid = threadIdx.x, G = gridDim.x, g = blockIdx.x;
+    for (int e = tid; e < E; e += kPermThreads) cnt[e] = 0;
+    __syncthreads();
+    const int p = g * kChunkPairs + tid;
+    if (p < P) atomicAdd(&cnt[checked_expert(idx, p, E, status)], 1);
+    __syncthreads();
+    for (int e = tid; e < E; e += kPermThreads) cells[static_cast<size_t>(g) * E + e] = cnt[e];
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_last = atomicAdd(done, 1u) == static_cast<unsigned>(G - 1);
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    // the last CTA: exclusive scan of the cells in (expert, CTA) order
+    const int n_cells = E * G;
+    const int per_thread = (n_cells + kPermThreads - 1) / kPermThreads;
+    const int i0 = min(n_cells, tid * per_thread), i1 = min(n_cells, i0 + per_thread);
+    int run = 0;
+    for (int i = i0; i < i1; ++i) run += __ldcg(cells + static_cast<size_t>(i % G) * E + i / G);
+    int total;
+    int pos = block_exclusive_scan(run, scan, &total);
+    for (int i = i0; i < i1; ++i) {
+        const size_t cell = static_cast<size_t>(i % G) * E + i / G;
+        const int v = __ldcg(cells + cell);
+        starts[cell] = pos;
+        if (i % G == 0) cnt[i / G] = pos;
+        pos += v;
+    }
+    if (tid == 0) cnt[E] = total;
+    __syncthreads();
+    const int c = tid < E ? cnt[tid + 1] - cnt[tid] : 0;
+    if (tid < E) offsets[tid] = cnt[tid];
+    if (tid == 0) offsets[E] = cnt[E];
+    int nact;
+    const int apos = block_exclusive_scan(c > 0 ? 1 : 0, scan, &nact);
+    if (tid < E && c > 0) active[apos] = tid;
+    if (tid == 0) {
+        *n_active = nact;
+        *done = 0u;  // ready for the next launch (kernels on the stream run one after the other)
+    }
+}
+
+__global__ void __launch_bounds__(kPermThreads) permute_place_kernel(const int32_t* __restrict__ idx,
+                                                                     const float* __restrict__ w, int P, int E,
+                                                                     const int32_t* __restrict__ starts,
+                                                                     int32_t* __restrict__ perm,
+                                                                     int32_t* __restrict__ inv_perm,
+                                                                     float* __restrict__ w_perm) {
+    extern __shared__ int smem[];
+    const int Es = E + 1;
+    int* cnt = smem;  // [kPermWarps][Es]: the warp's pairs per expert, then the warp's first position
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g = blockIdx.x;
+    for (int i = tid; i < kPermWarps * Es; i += kPermThreads) cnt[i] = 0;
+    __syncthreads();
+    const int p = g * kChunkPairs + tid;
+    const bool valid = p < P;
+    int e = valid ? idx[p] : -1;
+    if (valid && (e < 0 || e >= E)) e = 0;  // raised by the counting kernel
+    const float wv = valid ? w[p] : 0.0f;
+    const int nbits = E > 1 ? 32 - __clz(E - 1) : 0;
+    const uint32_t peers = warp_peers(e, nbits);
+    if (e >= 0 && lane == __ffs(peers) - 1) cnt[warp * Es + e] = __popc(peers);
+    __syncthreads();
+    for (int x = tid; x < E; x += kPermThreads) {
+        int run = starts[static_cast<size_t>(g) * E + x];
+        for (int q = 0; q < kPermWarps; ++q) {
+            const int v = cnt[q * Es + x];
+            cnt[q * Es + x] = run;
+            run += v;
+        }
+    }
+    __syncthreads();
+    if (e >= 0) {
+        const int pos = cnt[warp * Es + e] + __popc(peers & ((1u << lane) - 1u));
+        perm[pos] = p;
+        inv_perm[p] = pos;
+        w_perm[pos] = wv;
+    }
+}
+
 }  // namespace
+
+int permute_grid(int P) { return P > kPermThreads ? (P + kChunkPairs - 1) / kChunkPairs : 1; }
 
 cudaError_t launch_permute(const int32_t* idx, const float* w, int P, int E, int32_t* offsets, int32_t* perm,
                            int32_t* inv_perm, float* w_perm, int32_t* active, int32_t* n_active, int* status,
-                           cudaStream_t st) {
-    const size_t smem = sizeof(int) * (kPermWarps * (E + 1) + 36 + E + 1);
+                           int32_t* cells, unsigned* done, cudaStream_t st) {
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t err = cudaFuncSetAttribute(permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                sizeof(int) * (kPermWarps * 1025 + 36 + 1024 + 1));
         if (err != cudaSuccess) return err;
+        err = cudaFuncSetAttribute(permute_place_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   sizeof(int) * kPermWarps * 1025);
+        if (err != cudaSuccess) return err;
         attr_set = true;
     }
-    permute_kernel<<<1, kPermThreads, smem, st>>>(idx, w, P, E, offsets, perm, inv_perm, w_perm, active, n_active,
-                                                  status);
+    const int G = permute_grid(P);
+    if (G == 1) {
+        const size_t smem = sizeof(int) * (kPermWarps * (E + 1) + 36 + E + 1);
+        permute_kernel<<<1, kPermThreads, smem, st>>>(idx, w, P, E, offsets, perm, inv_perm, w_perm, active,
+                                                      n_active, status);
+        return cudaGetLastError();
+    }
+    if (!cells || !done) return cudaErrorInvalidValue;
+    int32_t* starts = cells + static_cast<size_t>(G) * E;
+    permute_count_kernel<<<G, kPermThreads, sizeof(int) * (E + 1 + 36), st>>>(idx, P, E, cells, starts, offsets,
+                                                                             active, n_active, done, status);
+    permute_place_kernel<<<G, kPermThreads, sizeof(int) * kPermWarps * (E + 1), st>>>(idx, w, P, E, starts, perm,
+                                                                                      inv_perm, w_perm);
     return cudaGetLastError();
 }
 

@@ -164,6 +164,8 @@ struct moe_ctx {
     // scratch (device)
     float* logits = nullptr;
     int32_t *offsets = nullptr, *perm = nullptr, *inv_perm = nullptr, *active = nullptr, *n_active = nullptr;
+    int32_t* perm_cells = nullptr;         // multi-CTA permutation: per-CTA counts and starts
+    unsigned* perm_done = nullptr;         // its arrival counter (0 between launches)
     float *w_perm = nullptr, *pair_out = nullptr;
     uint16_t *x_perm = nullptr, *h_perm = nullptr;
     int* status = nullptr;
@@ -484,7 +486,7 @@ void free_all(moe_ctx* c) {
     if (c->ev_fork) cudaEventDestroy(c->ev_fork);
     if (c->ev_join) cudaEventDestroy(c->ev_join);
     void* dev_ptrs[] = {c->arena, c->slot_dev, c->logits, c->offsets, c->perm, c->inv_perm, c->active,
-                        c->n_active, c->w_perm, c->pair_out, c->x_perm, c->h_perm, c->status, c->work_dev,
+                        c->perm_cells, c->perm_done, c->n_active, c->w_perm, c->pair_out, c->x_perm, c->h_perm, c->status, c->work_dev,
                         c->dec_ws,   c->dec_cnt, c->fill_flag, c->d_lru,   c->d_prev, c->d_next,  c->d_key,
                         c->d_stats,  c->d_trace, c->d_fill_list, c->d_work, c->d_order, c->d_hdr, c->d_keys,
                         c->d_iota};
@@ -580,7 +582,7 @@ int forward_device(moe_ctx* c, int layer, const void* x, const float* resid, flo
     {
         ProfScope ps(c, kPermute, 8.0 * P + 12.0 * P + 8.0 * E, 0.0);
         CUDA_TRY(moe::launch_permute(idx, w, P, E, c->offsets, c->perm, c->inv_perm, c->w_perm, c->active,
-                                     c->n_active, c->status, c->s_comp));
+                                     c->n_active, c->status, c->perm_cells, c->perm_done, c->s_comp));
     }
     {
         ProfScope ps(c, kGather, 4.0 * P * H, 0.0);
@@ -759,6 +761,9 @@ int moe_cache_init(const moe_config_t* cfg, void* stream_compute, void* stream_c
     INIT_TRY(cudaMalloc(&c->n_active, sizeof(int32_t)));
     INIT_TRY(cudaMalloc(&c->perm, c->Pmax * sizeof(int32_t)));
     INIT_TRY(cudaMalloc(&c->inv_perm, c->Pmax * sizeof(int32_t)));
+    INIT_TRY(cudaMalloc(&c->perm_cells, 2ull * moe::permute_grid(c->Pmax) * c->E * sizeof(int32_t)));
+    INIT_TRY(cudaMalloc(&c->perm_done, sizeof(unsigned)));
+    INIT_TRY(cudaMemset(c->perm_done, 0, sizeof(unsigned)));
     INIT_TRY(cudaMalloc(&c->w_perm, c->Pmax * sizeof(float)));
     INIT_TRY(cudaMalloc(&c->x_perm, static_cast<size_t>(c->Pmax) * c->H * 2));
     INIT_TRY(cudaMalloc(&c->h_perm, static_cast<size_t>(c->Pmax) * c->I * 2));
@@ -1112,7 +1117,7 @@ int moe_layer_forward(moe_ctx* c, int layer, const void* x, const float* resid, 
     {
         ProfScope ps(c, kPermute, 8.0 * P + 12.0 * P + 8.0 * E, 0.0);
         CUDA_TRY(moe::launch_permute(idx, w, P, E, c->offsets, c->perm, c->inv_perm, c->w_perm, c->active,
-                                     c->n_active, c->status, c->s_comp));
+                                     c->n_active, c->status, c->perm_cells, c->perm_done, c->s_comp));
     }
     {
         ProfScope ps(c, kGather, 4.0 * P * H, 0.0);

@@ -1,8 +1,8 @@
 """GPU parity of the router on its own: fp32 logits bitwise equal to the oracle's fixed
 evaluation order, and top-k indices bit-exact, for every router kernel variant -- the
 shared-memory kernels of small batches (T <= 32) and the register-tiled kernel of large
-batches (32-token x 16-expert tiles) -- including ragged tiles (T and E not multiples of the
-tile) and several chunks of 256 hidden columns."""
+batches (32-token x 32-expert tiles, the lanes of the order split over warps) -- including
+ragged tiles (T and E not multiples of the tile) and several chunks of 256 hidden columns."""
 import numpy as np
 import pytest
 
@@ -16,7 +16,7 @@ CASES = [
     # (T, E, H, k)
     (1, 256, 4096, 6), (2, 256, 4096, 6), (3, 16, 256, 2), (8, 256, 4096, 6), (13, 100, 512, 4),
     (16, 256, 4096, 6), (32, 128, 2048, 8), (33, 256, 4096, 6), (77, 100, 768, 5), (300, 16, 256, 2),
-    (1000, 256, 4096, 6), (4096, 256, 4096, 6),
+    (1000, 256, 4096, 6), (4096, 256, 4096, 6), (65, 70, 256, 3), (130, 200, 1024, 8),
 ]
 
 
