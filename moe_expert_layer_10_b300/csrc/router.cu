@@ -142,26 +142,29 @@ __global__ void __launch_bounds__(kTiledThreads, 1) router_logits_tiled_kernel(c
         for (int c = 0; c < 2; ++c) {
             const int l = warp + 16 * c;  // the lane of the order evaluated: columns 8l .. 8l+7
 #pragma unroll
-            for (int cp = 0; cp < 4; ++cp) {  // columns 8l + 2cp, 8l + 2cp + 1
-                uint4 xq[4];
-#pragma unroll
-                for (int p = 0; p < 4; ++p)
-                    xq[p] = *reinterpret_cast<const uint4*>(xs + (g + 4 * p) * kXRow + (8 * l + 2 * cp) * 8);
-                float2 wq[4];
+            for (int hq = 0; hq < 2; ++hq) {  // columns 8l + 4hq .. 8l + 4hq + 3
+                float4 wq[4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
-                    wq[j] = *reinterpret_cast<const float2*>(ws + (f + 8 * j) * kWRow + (8 * l + 2 * cp) * 4);
+                    wq[j] = *reinterpret_cast<const float4*>(ws + (f + 8 * j) * kWRow + (8 * l + 4 * hq) * 4);
 #pragma unroll
-                for (int q = 0; q < 2; ++q) {
+                for (int cp = 0; cp < 2; ++cp) {  // columns 8l + 4hq + 2cp, + 1
+                    uint4 xq[4];
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const float wf = q == 0 ? wq[j].x : wq[j].y;
-                        const uint64_t wd = pack2(wf, wf);
+                    for (int p = 0; p < 4; ++p)
+                        xq[p] = *reinterpret_cast<const uint4*>(xs + (g + 4 * p) * kXRow + (8 * l + 4 * hq + 2 * cp) * 8);
 #pragma unroll
-                        for (int p = 0; p < 4; ++p) {
-                            const uint64_t xp = q == 0 ? (static_cast<uint64_t>(xq[p].y) << 32 | xq[p].x)
-                                                       : (static_cast<uint64_t>(xq[p].w) << 32 | xq[p].z);
-                            acc[c][j][p] = fma2(wd, xp, acc[c][j][p]);
+                    for (int q = 0; q < 2; ++q) {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const float wf = cp == 0 ? (q == 0 ? wq[j].x : wq[j].y) : (q == 0 ? wq[j].z : wq[j].w);
+                            const uint64_t wd = pack2(wf, wf);
+#pragma unroll
+                            for (int p = 0; p < 4; ++p) {
+                                const uint64_t xp = q == 0 ? (static_cast<uint64_t>(xq[p].y) << 32 | xq[p].x)
+                                                           : (static_cast<uint64_t>(xq[p].w) << 32 | xq[p].z);
+                                acc[c][j][p] = fma2(wd, xp, acc[c][j][p]);
+                            }
                         }
                     }
                 }
@@ -283,7 +286,9 @@ __device__ __forceinline__ bool ranks_before(float za, int ea, float zb, int eb)
     return za > zb || (za == zb && ea < eb);
 }
 
-// One warp per token. Lane l holds the logits of experts l, l+32, ... (E <= 1024).
+// One warp per token. Lane l holds the logits of experts l, l+32, ..., l + 32(NS-1)
+// (NS >= ceil(E / 32), E <= 1024).
+template <int NS>
 __global__ void __launch_bounds__(256) router_topk_kernel(const float* __restrict__ z, int T, int E, int k,
                                                           const int32_t* __restrict__ forced,
                                                           int32_t* __restrict__ idx, float* __restrict__ w,
@@ -295,15 +300,15 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float* __restric
     int my_e = -1;       // lane j < k: the expert it outputs at position j
     float my_z = 0.0f;   // and its logit
     if (forced == nullptr) {
-        float v[32];
+        float v[NS];
         uint32_t taken = 0;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = (lane + 32 * i < E) ? zt[lane + 32 * i] : -FLT_MAX;
+        for (int i = 0; i < NS; ++i) v[i] = (lane + 32 * i < E) ? zt[lane + 32 * i] : -FLT_MAX;
         for (int j = 0; j < k; ++j) {
             float bv = -INFINITY;
             int be = INT_MAX;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
+            for (int i = 0; i < NS; ++i) {
                 const int e = lane + 32 * i;
                 if (e < E && !((taken >> i) & 1u) && ranks_before(v[i], e, bv, be)) {
                     bv = v[i];
@@ -396,7 +401,14 @@ cudaError_t launch_router_logits(const uint16_t* x, const float* Wr, const float
 cudaError_t launch_router_topk(const float* z, int T, int E, int k, const int32_t* forced, int32_t* idx, float* w,
                                int* status, cudaStream_t st) {
     if (T <= 0) return cudaSuccess;
-    router_topk_kernel<<<(T + 7) / 8, 256, 0, st>>>(z, T, E, k, forced, idx, w, status);
+    const int blocks = (T + 7) / 8;
+    const int ns = (E + 31) / 32;
+    if (ns <= 1) router_topk_kernel<1><<<blocks, 256, 0, st>>>(z, T, E, k, forced, idx, w, status);
+    else if (ns <= 2) router_topk_kernel<2><<<blocks, 256, 0, st>>>(z, T, E, k, forced, idx, w, status);
+    else if (ns <= 4) router_topk_kernel<4><<<blocks, 256, 0, st>>>(z, T, E, k, forced, idx, w, status);
+    else if (ns <= 8) router_topk_kernel<8><<<blocks, 256, 0, st>>>(z, T, E, k, forced, idx, w, status);
+    else if (ns <= 16) router_topk_kernel<16><<<blocks, 256, 0, st>>>(z, T, E, k, forced, idx, w, status);
+    else router_topk_kernel<32><<<blocks, 256, 0, st>>>(z, T, E, k, forced, idx, w, status);
     return cudaGetLastError();
 }
 
