@@ -3,6 +3,7 @@
 // in j order by one thread per (token, 4 columns): no atomics, so the result is
 // deterministic. resid may alias out (each element is read before it is written).
 #include "kernels.cuh"
+#include "ptx.cuh"
 
 namespace moe {
 namespace {
@@ -10,6 +11,7 @@ namespace {
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ pair_out,
                                                       const int32_t* __restrict__ inv_perm, const float* resid,
                                                       float* out, int T, int k, int H) {
+    pdl_gate();  // may start while the previous kernel of the stream finishes
     const int H4 = H / 4;
     const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (i >= static_cast<long long>(T) * H4) return;
@@ -32,8 +34,8 @@ cudaError_t launch_combine(const float* pair_out, const int32_t* inv_perm, const
                            int k, int H, cudaStream_t st) {
     if (T <= 0) return cudaSuccess;
     const long long n = static_cast<long long>(T) * (H / 4);
-    combine_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(pair_out, inv_perm, resid, out, T, k, H);
-    return cudaGetLastError();
+    return launch_pdl(combine_kernel, dim3(static_cast<unsigned>((n + 255) / 256)), dim3(256), 0, st, pair_out, inv_perm,
+                      resid, out, T, k, H);
 }
 
 }  // namespace moe

@@ -111,6 +111,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const uint32_t* __restrict__ fill_flag, int H, int I, uint16_t* __restrict__ h_out,
                       const float* __restrict__ w_perm, float* __restrict__ pair_out, float* __restrict__ ws,
                       int* __restrict__ cnt, int* status, uint64_t fill_wait_ns, const int* __restrict__ dyn) {
+    pdl_gate();  // may start while the previous kernel of the stream finishes
     using Lay = Layout<GATEUP>;
     constexpr int kMma = Lay::MMA_STAGES;
     if (dyn) {
@@ -351,9 +352,8 @@ cudaError_t launch(const CUtensorMap& tb, const uint8_t* arena, uint64_t entry_b
         attr = true;
     }
     const int grid = dyn ? num_sms : std::min(n_units, num_sms);
-    kern<<<grid, kThreads, smem, st>>>(tb, arena, entry_bytes, work, n_work, n_units, S, slot_row, fill_flag, H, I,
-                                       h_out, w_perm, pair_out, ws, cnt, status, fill_wait_ns, dyn);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, st, tb, arena, entry_bytes, work, n_work, n_units, S,
+                      slot_row, fill_flag, H, I, h_out, w_perm, pair_out, ws, cnt, status, fill_wait_ns, dyn);
 }
 
 }  // namespace

@@ -81,6 +81,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                       uint16_t* __restrict__ h_out,
                       const float* __restrict__ w_perm, float* __restrict__ pair_out, float* __restrict__ ws,
                       int* __restrict__ cnt, int* status, uint64_t fill_wait_ns, const int* __restrict__ dyn) {
+    pdl_gate();  // may start while the previous kernel of the stream finishes
     using Lay = Layout<GATEUP>;
     if (dyn) {  // work size written on the device (device-resident policy)
         n_work = dyn[0];
@@ -262,9 +263,8 @@ cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const GemvWork*
         attr = true;
     }
     const int grid = dyn ? num_sms : std::min(n_units, num_sms);
-    kern<<<grid, kThreads, smem, st>>>(ta, tb, work, n_work, n_units, S, slot_row, fill_flag, H, I, h_out, w_perm,
-                                       pair_out, ws, cnt, status, fill_wait_ns, dyn);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, st, ta, tb, work, n_work, n_units, S, slot_row, fill_flag,
+                      H, I, h_out, w_perm, pair_out, ws, cnt, status, fill_wait_ns, dyn);
 }
 
 }  // namespace

@@ -67,6 +67,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int32_t* __restrict__ offsets, const int32_t* __restrict__ active, int a_begin, int a_end,
                 const int32_t* __restrict__ slot_row, int H, int I, uint16_t* __restrict__ h_out,
                 const float* __restrict__ w_perm, float* __restrict__ pair_out, int* status) {
+    pdl_wait();  // may start while the previous kernel of the stream finishes
     extern __shared__ uint8_t smem_raw[];
     uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Shared& sh = *reinterpret_cast<Shared*>(tiles + kStages * STAGE_BYTES);
@@ -290,9 +291,8 @@ cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const int32_t* 
         attr = true;
     }
     const int grid = std::min(total_tiles, num_sms);
-    kern<<<grid, kThreads, SMEM_BYTES, st>>>(ta, tb, offsets, active, a_begin, a_end, slot_row, H, I, h_out, w_perm,
-                                             pair_out, status);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(kThreads), SMEM_BYTES, st, ta, tb, offsets, active, a_begin, a_end,
+                      slot_row, H, I, h_out, w_perm, pair_out, status);
 }
 
 }  // namespace

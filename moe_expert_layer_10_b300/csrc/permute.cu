@@ -82,6 +82,7 @@ __global__ void __launch_bounds__(kPermThreads) permute_kernel(const int32_t* __
                                                                float* __restrict__ w_perm,
                                                                int32_t* __restrict__ active,
                                                                int32_t* __restrict__ n_active, int* status) {
+    pdl_gate();  // may start while the previous kernel of the stream finishes
     extern __shared__ int smem[];
     const int Es = E + 1;                     // column stride (odd: the scan's reads spread over banks)
     int* cnt = smem;                          // [kPermWarps][Es]
@@ -166,6 +167,7 @@ __global__ void __launch_bounds__(kPermThreads) permute_kernel(const int32_t* __
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __restrict__ x,
                                                           const int32_t* __restrict__ perm, int P, int k, int H,
                                                           uint16_t* __restrict__ x_perm) {
+    pdl_gate();  // may start while the previous kernel of the stream finishes
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int pos = blockIdx.x * 8 + warp;
     if (pos >= P) return;
@@ -194,6 +196,7 @@ __global__ void __launch_bounds__(kPermThreads) permute_count_kernel(const int32
                                                                      int32_t* __restrict__ active,
                                                                      int32_t* __restrict__ n_active,
                                                                      unsigned* done, int* status) {
+    pdl_gate();  // may start while the previous kernel of the stream finishes
     extern __shared__ int smem[];
     int* cnt = smem;             // [E] this CTA's pairs per expert, later first position per expert
     int* scan = cnt + E + 1;     // [33]
@@ -246,6 +249,7 @@ __global__ void __launch_bounds__(kPermThreads) permute_place_kernel(const int32
                                                                      int32_t* __restrict__ perm,
                                                                      int32_t* __restrict__ inv_perm,
                                                                      float* __restrict__ w_perm) {
+    pdl_gate();  // may start while the previous kernel of the stream finishes
     extern __shared__ int smem[];
     const int Es = E + 1;
     int* cnt = smem;  // [kPermWarps][Es]: the warp's pairs per expert, then the warp's first position
@@ -298,24 +302,22 @@ cudaError_t launch_permute(const int32_t* idx, const float* w, int P, int E, int
     const int G = permute_grid(P);
     if (G == 1) {
         const size_t smem = sizeof(int) * (kPermWarps * (E + 1) + 36 + E + 1);
-        permute_kernel<<<1, kPermThreads, smem, st>>>(idx, w, P, E, offsets, perm, inv_perm, w_perm, active,
-                                                      n_active, status);
-        return cudaGetLastError();
+        return launch_pdl(permute_kernel, dim3(1), dim3(kPermThreads), smem, st, idx, w, P, E, offsets, perm,
+                          inv_perm, w_perm, active, n_active, status);
     }
     if (!cells || !done) return cudaErrorInvalidValue;
     int32_t* starts = cells + static_cast<size_t>(G) * E;
-    permute_count_kernel<<<G, kPermThreads, sizeof(int) * (E + 1 + 36), st>>>(idx, P, E, cells, starts, offsets,
-                                                                             active, n_active, done, status);
-    permute_place_kernel<<<G, kPermThreads, sizeof(int) * kPermWarps * (E + 1), st>>>(idx, w, P, E, starts, perm,
-                                                                                      inv_perm, w_perm);
-    return cudaGetLastError();
+    cudaError_t err = launch_pdl(permute_count_kernel, dim3(G), dim3(kPermThreads), sizeof(int) * (E + 1 + 36), st, idx,
+                                 P, E, cells, starts, offsets, active, n_active, done, status);
+    if (err != cudaSuccess) return err;
+    return launch_pdl(permute_place_kernel, dim3(G), dim3(kPermThreads), sizeof(int) * kPermWarps * (E + 1), st, idx,
+                      w, P, E, static_cast<const int32_t*>(starts), perm, inv_perm, w_perm);
 }
 
 cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* perm, int P, int k, int H, uint16_t* x_perm,
                                cudaStream_t st) {
     if (P <= 0) return cudaSuccess;
-    gather_rows_kernel<<<(P + 7) / 8, 256, 0, st>>>(x, perm, P, k, H, x_perm);
-    return cudaGetLastError();
+    return launch_pdl(gather_rows_kernel, dim3((P + 7) / 8), dim3(256), 0, st, x, perm, P, k, H, x_perm);
 }
 
 }  // namespace moe

@@ -27,6 +27,20 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     return t;
 }
 
+// Programmatic dependent launch. The kernels of the layer's chain are launched with
+// launch_pdl (kernels.cuh), so the next kernel of the stream may be scheduled before this one
+// ends. pdl_gate comes first in each of them: it lets the next kernel be scheduled, then waits
+// until the previous kernel of the stream has completed and its writes are visible. A kernel
+// thus overlaps its predecessor only with its launch and scheduling, never with memory traffic.
+// Without a programmatic predecessor both instructions return at once.
+__device__ __forceinline__ void pdl_gate() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// The wait alone: the next kernel is scheduled only when this one ends (for long kernels, whose
+// SMs waiting successors would otherwise share).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void raise_status(int* status, int code) {
     if (status) atomicCAS(status, kDevOk, code);
 }

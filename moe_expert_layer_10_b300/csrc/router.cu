@@ -103,6 +103,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1) router_logits_tiled_kernel(c
                                                                      const float* __restrict__ Wr,
                                                                      const float* __restrict__ bias, int T, int H,
                                                                      int E, float* __restrict__ z) {
+    pdl_gate();  // may start while the previous kernel of the stream finishes
     extern __shared__ __align__(16) uint8_t rsm[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t0 = blockIdx.y * kTT, e0 = blockIdx.x * kTE;
@@ -208,6 +209,7 @@ __global__ void __launch_bounds__(256) router_logits_staged_kernel(const uint16_
                                                                    const float* __restrict__ Wr,
                                                                    const float* __restrict__ bias, int T, int H,
                                                                    int E, float* __restrict__ z) {
+    pdl_gate();  // may start while the previous kernel of the stream finishes
     extern __shared__ __align__(16) uint8_t smem[];
     float* wr = reinterpret_cast<float*>(smem);                   // [EPB][H]
     uint16_t* xs = reinterpret_cast<uint16_t*>(wr + EPB * H);     // [T][H]
@@ -278,8 +280,7 @@ cudaError_t launch_staged(const uint16_t* x, const float* Wr, const float* b, in
         attr = true;
     }
     const size_t smem = static_cast<size_t>(EPB) * H * 4 + static_cast<size_t>(T) * H * 2;
-    kern<<<(E + EPB - 1) / EPB, 256, smem, st>>>(x, Wr, b, T, H, E, z);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3((E + EPB - 1) / EPB), dim3(256), smem, st, x, Wr, b, T, H, E, z);
 }
 
 __device__ __forceinline__ bool ranks_before(float za, int ea, float zb, int eb) {
@@ -293,6 +294,7 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float* __restric
                                                           const int32_t* __restrict__ forced,
                                                           int32_t* __restrict__ idx, float* __restrict__ w,
                                                           int* status) {
+    pdl_gate();  // may start while the previous kernel of the stream finishes
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = blockIdx.x * (blockDim.x >> 5) + warp;
     if (t >= T) return;
@@ -393,9 +395,8 @@ cudaError_t launch_router_logits(const uint16_t* x, const float* Wr, const float
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    router_logits_tiled_kernel<<<dim3((E + kTE - 1) / kTE, (T + kTT - 1) / kTT), kTiledThreads, kTiledSmem, st>>>(
-        x, Wr, b, T, H, E, z);
-    return cudaGetLastError();
+    return launch_pdl(router_logits_tiled_kernel, dim3((E + kTE - 1) / kTE, (T + kTT - 1) / kTT), dim3(kTiledThreads),
+                      kTiledSmem, st, x, Wr, b, T, H, E, z);
 }
 
 cudaError_t launch_router_topk(const float* z, int T, int E, int k, const int32_t* forced, int32_t* idx, float* w,
@@ -403,13 +404,15 @@ cudaError_t launch_router_topk(const float* z, int T, int E, int k, const int32_
     if (T <= 0) return cudaSuccess;
     const int blocks = (T + 7) / 8;
     const int ns = (E + 31) / 32;
-    if (ns <= 1) router_topk_kernel<1><<<blocks, 256, 0, st>>>(z, T, E, k, forced, idx, w, status);
-    else if (ns <= 2) router_topk_kernel<2><<<blocks, 256, 0, st>>>(z, T, E, k, forced, idx, w, status);
-    else if (ns <= 4) router_topk_kernel<4><<<blocks, 256, 0, st>>>(z, T, E, k, forced, idx, w, status);
-    else if (ns <= 8) router_topk_kernel<8><<<blocks, 256, 0, st>>>(z, T, E, k, forced, idx, w, status);
-    else if (ns <= 16) router_topk_kernel<16><<<blocks, 256, 0, st>>>(z, T, E, k, forced, idx, w, status);
-    else router_topk_kernel<32><<<blocks, 256, 0, st>>>(z, T, E, k, forced, idx, w, status);
-    return cudaGetLastError();
+    auto go = [&](auto kern) {
+        return launch_pdl(kern, dim3(blocks), dim3(256), 0, st, z, T, E, k, forced, idx, w, status);
+    };
+    if (ns <= 1) return go(router_topk_kernel<1>);
+    if (ns <= 2) return go(router_topk_kernel<2>);
+    if (ns <= 4) return go(router_topk_kernel<4>);
+    if (ns <= 8) return go(router_topk_kernel<8>);
+    if (ns <= 16) return go(router_topk_kernel<16>);
+    return go(router_topk_kernel<32>);
 }
 
 }  // namespace moe
