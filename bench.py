@@ -208,23 +208,36 @@ def cpu_baseline(W, Wr, b, target_s: float = 15.0):
     entries = make_entries(W)
     xs0 = step_inputs(W, 0)
     cpu_oracle_step(W, Wr, b, xs0, entries)  # warm: builds the oracle, fetches hot entries
-    steps, t_tot = 0, 0.0
-    while t_tot < target_s and steps < 64:
-        xs = step_inputs(W, steps + 1)
-        # fetch this step's entries untimed
-        import numpy as np
-        for B in BATCHES:
-            idx, _, _, _ = oracle.route(xs[B], Wr, b, W.k)
-            for e in np.unique(idx):
-                entries(int(e))
-        t0 = time.perf_counter()
-        cpu_oracle_step(W, Wr, b, xs, entries)
-        t_tot += time.perf_counter() - t0
-        steps += 1
+    import numpy as np
+
+    def timed(first_step, budget_s, max_steps):
+        steps, t_tot = 0, 0.0
+        while t_tot < budget_s and steps < max_steps:
+            xs = step_inputs(W, first_step + steps)
+            for B in BATCHES:  # fetch this step's entries untimed
+                idx, _, _, _ = oracle.route(xs[B], Wr, b, W.k)
+                for e in np.unique(idx):
+                    entries(int(e))
+            t0 = time.perf_counter()
+            cpu_oracle_step(W, Wr, b, xs, entries)
+            t_tot += time.perf_counter() - t0
+            steps += 1
+        return steps, t_tot
+
+    cores = oracle.num_threads()
+    steps, t_tot = timed(1, target_s, 64)
     tokens = steps * sum(BATCHES)
-    return {"value": tokens / t_tot, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+    prev = oracle.set_num_threads(1)
+    try:
+        steps1, t1 = timed(1000, target_s / 3, 4)
+    finally:
+        oracle.set_num_threads(prev)
+    tokens1 = steps1 * sum(BATCHES)
+    return {"value": tokens / t_tot, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"{steps} whole benchmark steps ({tokens} tokens: batches {list(BATCHES)}), "
-                      f"{t_tot:.1f} s of oracle time"}
+                      f"{t_tot:.1f} s of oracle time",
+            "single_thread": {"value": tokens1 / t1, "unit": UNIT, "cores": 1,
+                              "sample": f"{steps1} other whole steps ({tokens1} tokens), {t1:.1f} s"}}
 
 
 # ----------------------------------------------------------------------------- b300 arm

@@ -42,6 +42,8 @@ def lib():
         L = ctypes.CDLL(_SO)
         i32, dbl, vp = ctypes.c_int, ctypes.c_double, ctypes.c_void_p
         L.orc_num_threads.restype = i32
+        L.orc_set_num_threads.restype = i32
+        L.orc_set_num_threads.argtypes = [i32]
         L.orc_router_logits.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp]
         L.orc_topk.argtypes = [vp, i32, i32, i32, vp, vp]
         L.orc_forced_gates.argtypes = [vp, vp, i32, i32, i32, vp, vp]
@@ -73,6 +75,11 @@ def _p(a) -> int:
 
 def num_threads() -> int:
     return int(lib().orc_num_threads())
+
+
+def set_num_threads(n: int) -> int:
+    """Threads of the oracle's later parallel regions; returns the previous count."""
+    return int(lib().orc_set_num_threads(int(n)))
 
 
 def router_logits(x_bf16: np.ndarray, Wr: np.ndarray, b: np.ndarray, want_double: bool = True):

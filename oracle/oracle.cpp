@@ -74,6 +74,19 @@ int orc_num_threads(void) {
 #endif
 }
 
+/* Threads of later parallel regions (the host's cores by default); returns the previous count.
+   Used to time the oracle single-threaded beside the all-cores figure. */
+int orc_set_num_threads(int n) {
+#ifdef _OPENMP
+    const int prev = omp_get_max_threads();
+    if (n >= 1) omp_set_num_threads(n);
+    return prev;
+#else
+    (void)n;
+    return 1;
+#endif
+}
+
 // Router logits z[t,e] = sum_h W_r[e,h] x[t,h] + b[e].
 // R1: z32 is evaluated in fp32 in this order. 32 partial sums s_l (l = 0..31); s_l
 // accumulates fmaf(W_r[e,h], x[t,h], s_l) over h = 256*m + 8*l + r, m ascending, then
