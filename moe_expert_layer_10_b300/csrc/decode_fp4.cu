@@ -19,8 +19,9 @@
 //    (about 34 KB of weights in flight per SM);
 //  * warps 6-21 (512 threads): converters -- thread (row, quarter) expands 16 codes of one row
 //    into bf16 inside the 128-byte-swizzled A tile of an MMA stage, with byte-permute
-//    lookups (two 4-byte tables per scale for the high and the low byte of the bf16 pattern);
-//    converter 0 also loads the stage's token tile (TMA);
+//    lookups (two 4-byte tables per scale for the high and the low byte of the bf16 pattern,
+//    read from a 4 KB table of all 256 scales that the CTA builds once), 15 integer operations
+//    per 8 weights; converter 0 also loads the stage's token tile (TMA);
 //  * warp 1, one lane: MMA issuer, as in the bf16 kernel; warps 2-5: epilogue.
 // Waits are bounded; the fill-flag wait and the split-K scheme are those of the bf16 kernel.
 #include <algorithm>
@@ -49,6 +50,7 @@ constexpr int kConvWarps = 16;
 constexpr int kConvBase = 192;                 // first converter thread
 constexpr int kThreads = kConvBase + 32 * kConvWarps;
 constexpr uint32_t kTmemCols = 128;
+constexpr int kScaleLutBytes = 256 * 16;      // scale_tables of every E8M0 scale, built once per CTA
 
 struct __align__(8) Shared {
     uint64_t raw_full[kRawStages], raw_empty[kRawStages];
@@ -62,8 +64,8 @@ template <bool GATEUP>
 struct Layout {
     static constexpr int MMA_STAGES = 7;
     static constexpr int XCHG_BYTES = GATEUP ? kXchgFloats * 4 : 0;
-    static constexpr int SMEM =
-        MMA_STAGES * kMmaStage + kRawStages * kRawStage + XCHG_BYTES + static_cast<int>(sizeof(Shared)) + 1024;
+    static constexpr int SMEM = MMA_STAGES * kMmaStage + kRawStages * kRawStage + XCHG_BYTES + kScaleLutBytes +
+                                static_cast<int>(sizeof(Shared)) + 1024;
     static_assert(MMA_STAGES <= kMaxMmaStages, "stages");
     static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
 };
@@ -86,22 +88,20 @@ __device__ __forceinline__ void scale_tables(uint32_t s, uint32_t& h_lo, uint32_
 }
 
 // 8 E2M1 codes (one word, element k in nibble k) -> 4 words of bf16 pairs (element 2j low).
+// The magnitude (low 3 bits of a nibble) selects the pattern's high and low byte from the
+// scale's tables; the sign (bit 3 of nibble k, bit 4k+3 of v) goes to bit 7 of the high byte
+// before the bytes are interleaved: byte k of prmt(v << 4, v, 0x5140) holds bit 4k+3 of v in
+// its bit 7 for k = 0..3, and prmt(v << 4, v, 0x7362) does the same for k = 4..7.
 __device__ __forceinline__ void expand8(uint32_t v, uint32_t h_lo, uint32_t h_hi, uint32_t l_lo, uint32_t l_hi,
                                         uint32_t (&w)[4]) {
-    const uint32_t mags = v & 0x77777777u;
-    const uint32_t ha = prmt(h_lo, h_hi, mags), la = prmt(l_lo, l_hi, mags);
-    const uint32_t mh = mags >> 16;
-    const uint32_t hb = prmt(h_lo, h_hi, mh), lb = prmt(l_lo, l_hi, mh);
+    const uint32_t mags = v & 0x77777777u, mh = mags >> 16, v4 = v << 4;
+    const uint32_t ha = or_and(prmt(h_lo, h_hi, mags), prmt(v4, v, 0x5140), 0x80808080u);
+    const uint32_t hb = or_and(prmt(h_lo, h_hi, mh), prmt(v4, v, 0x7362), 0x80808080u);
+    const uint32_t la = prmt(l_lo, l_hi, mags), lb = prmt(l_lo, l_hi, mh);
     w[0] = prmt(la, ha, 0x5140);
     w[1] = prmt(la, ha, 0x7362);
     w[2] = prmt(lb, hb, 0x5140);
     w[3] = prmt(lb, hb, 0x7362);
-    // signs: bit 3 of nibble 2j -> bit 15 of word j, bit 3 of nibble 2j+1 -> bit 31
-    const uint32_t t = v & 0x88888888u, t4 = t << 4;
-    w[0] = or_and(w[0], prmt(t4, t, 0x4000), 0x80008000u);
-    w[1] = or_and(w[1], prmt(t4, t, 0x5010), 0x80008000u);
-    w[2] = or_and(w[2], prmt(t4, t, 0x6020), 0x80008000u);
-    w[3] = or_and(w[3], prmt(t4, t, 0x7030), 0x80008000u);
 }
 
 template <bool GATEUP>
@@ -124,7 +124,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* mma_tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* raw_tiles = mma_tiles + kMma * kMmaStage;
     float* xchg = reinterpret_cast<float*>(raw_tiles + kRawStages * kRawStage);
-    Shared& sh = *reinterpret_cast<Shared*>(raw_tiles + kRawStages * kRawStage + Lay::XCHG_BYTES);
+    uint4* scale_lut = reinterpret_cast<uint4*>(raw_tiles + kRawStages * kRawStage + Lay::XCHG_BYTES);
+    Shared& sh = *reinterpret_cast<Shared*>(raw_tiles + kRawStages * kRawStage + Lay::XCHG_BYTES + kScaleLutBytes);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int K = GATEUP ? H : I;
     const int KB = K / BK;
@@ -150,6 +151,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) {
         tmem_alloc(&sh.tmem_base, kTmemCols);
         tmem_relinquish();
+    }
+    for (int sc = threadIdx.x; sc < 256; sc += kThreads) {
+        uint4 t;
+        scale_tables(static_cast<uint32_t>(sc), t.x, t.y, t.z, t.w);
+        scale_lut[sc] = t;
     }
     tc_fence_before();
     __syncthreads();
@@ -291,13 +297,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint8_t* raw = raw_tiles + rs * kRawStage;
                 const uint2 codes = *reinterpret_cast<const uint2*>(raw + row * 32 + quarter * 8);
                 const uint32_t sc = raw[kRawA + row * 2 + (quarter >> 1)];  // the 32-block's scale
-                uint32_t h_lo, h_hi, l_lo, l_hi;
-                scale_tables(sc, h_lo, h_hi, l_lo, l_hi);
+                const uint4 tab = scale_lut[sc];
                 const uint32_t words[2] = {codes.x, codes.y};
 #pragma unroll
                 for (int q = 0; q < 2; ++q) {
                     uint32_t w[4];
-                    expand8(words[q], h_lo, h_hi, l_lo, l_hi, w);
+                    expand8(words[q], tab.x, tab.y, tab.z, tab.w, w);
                     const int chunk = quarter * 2 + q;  // 16-byte chunk of the 128-byte row
                     *reinterpret_cast<uint4*>(sm + row * 128 + ((chunk ^ (row & 7)) << 4)) =
                         make_uint4(w[0], w[1], w[2], w[3]);
