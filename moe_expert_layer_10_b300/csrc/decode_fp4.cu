@@ -17,7 +17,8 @@
 // Roles (22 warps):
 //  * warp 0, one lane: producer -- one 4352-byte bulk copy per stage into an 8-deep raw ring
 //    (about 34 KB of weights in flight per SM);
-//  * warps 6-21 (512 threads): converters -- thread (row, quarter) expands 16 codes of one row
+//  * warps 6-21 (512 threads): converters, in groups that take successive MMA stages side by
+//    side -- a thread expands 16 codes per group of one row
 //    into bf16 inside the 128-byte-swizzled A tile of an MMA stage, with byte-permute
 //    lookups (two 4-byte tables per scale for the high and the low byte of the bf16 pattern,
 //    read from a 4 KB table of all 256 scales that the CTA builds once), 15 integer operations
@@ -47,6 +48,12 @@ constexpr int kB16 = kNMax * BK * 2;           // token tile: up to 8 KB
 constexpr int kMmaStage = kA16 + kB16;         // 24 KB
 constexpr int kMaxMmaStages = 7;
 constexpr int kConvWarps = 16;
+// The converter warps form kConvGroups groups that expand successive MMA stages side by side
+// (group g takes the stages n with n % kConvGroups == g), so several stages are in conversion at
+// once; a thread of a group expands 16 * kConvGroups codes of one row.
+constexpr int kConvGroups = 4;
+constexpr int kGroupWarps = kConvWarps / kConvGroups;
+constexpr int kThreadsPerRow = 4 / kConvGroups;
 constexpr int kConvBase = 192;                 // first converter thread
 constexpr int kThreads = kConvBase + 32 * kConvWarps;
 constexpr uint32_t kTmemCols = 128;
@@ -62,11 +69,14 @@ struct __align__(8) Shared {
 
 template <bool GATEUP>
 struct Layout {
-    static constexpr int MMA_STAGES = 7;
+    static constexpr int MMA_STAGES = kConvGroups == 4 ? 4 : 6;  // a multiple of kConvGroups
     static constexpr int XCHG_BYTES = GATEUP ? kXchgFloats * 4 : 0;
     static constexpr int SMEM = MMA_STAGES * kMmaStage + kRawStages * kRawStage + XCHG_BYTES + kScaleLutBytes +
                                 static_cast<int>(sizeof(Shared)) + 1024;
     static_assert(MMA_STAGES <= kMaxMmaStages, "stages");
+    // every raw and MMA slot then belongs to one converter group, so a group's waits and its
+    // final drain only ever see its own phases
+    static_assert(MMA_STAGES % kConvGroups == 0 && kRawStages % kConvGroups == 0, "slots per group");
     static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
 };
 
@@ -136,10 +146,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < kRawStages; ++s) {
             mbar_init(&sh.raw_full[s], 1);
-            mbar_init(&sh.raw_empty[s], kConvWarps);
+            mbar_init(&sh.raw_empty[s], kGroupWarps);
         }
         for (int s = 0; s < kMma; ++s) {
-            mbar_init(&sh.mma_full[s], kConvWarps + 1);  // the converter warps + the token-tile arrival
+            mbar_init(&sh.mma_full[s], kGroupWarps + 1);  // a group's warps + the token-tile arrival
             mbar_init(&sh.mma_empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -266,12 +276,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ------------------------------------------------------------ converters (warps 6-21)
         const int c = threadIdx.x - kConvBase;
-        const int row = c >> 2, quarter = c & 3;  // 16 codes of one row: bytes 8*quarter .. +7
-        const bool token_loader = c == 0;
+        const int grp = c / (32 * kGroupWarps), cl = c % (32 * kGroupWarps);
+        const int row = cl / kThreadsPerRow, part = cl % kThreadsPerRow;  // codes 16G*part .. +16G-1
+        const bool token_loader = cl == 0;
         if (token_loader) prefetch_tmap(&tm_b);
-        int rs = 0, ms = 0;
-        uint32_t rphase = 0, mphase = 0, used = 0, last_phase = 0;
+        uint32_t used = 0, last_phase = 0;
         bool ok = true;
+        int n = 0;  // stage index over the whole run, as the producer and the MMA issuer count it
         for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
             const Unit un = locate_unit(work, n_work, u, R, S);
             const GemvWork wk = work[un.a];
@@ -279,7 +290,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int nt = min(kNMax, wk.n_tok - un.chunk * kNMax);
             const int nb = (nt + 15) >> 4;
             const int kb0 = un.split * KB / S, kb1 = (un.split + 1) * KB / S;
-            for (int kb = kb0; kb < kb1; ++kb) {
+            for (int kb = kb0; kb < kb1; ++kb, ++n) {
+                if (n % kConvGroups != grp) continue;
+                const int rs = n % kRawStages, ms = n % kMma;
+                const uint32_t rphase = (n / kRawStages) & 1, mphase = (n / kMma) & 1;
                 if (!mbar_wait(&sh.raw_full[rs], rphase, consumer_wait_ns) ||
                     !mbar_wait(&sh.mma_empty[ms], mphase ^ 1u, consumer_wait_ns)) {
                     raise_status(status, kDevWaitTimeout);
@@ -295,15 +309,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     last_phase = (last_phase & ~(1u << ms)) | (mphase << ms);
                 }
                 const uint8_t* raw = raw_tiles + rs * kRawStage;
-                const uint2 codes = *reinterpret_cast<const uint2*>(raw + row * 32 + quarter * 8);
-                const uint32_t sc = raw[kRawA + row * 2 + (quarter >> 1)];  // the 32-block's scale
-                const uint4 tab = scale_lut[sc];
-                const uint32_t words[2] = {codes.x, codes.y};
+                uint32_t words[2 * kConvGroups];
 #pragma unroll
-                for (int q = 0; q < 2; ++q) {
+                for (int h = 0; h < kConvGroups; ++h) {
+                    const uint2 cw = *reinterpret_cast<const uint2*>(raw + row * 32 + part * 8 * kConvGroups + 8 * h);
+                    words[2 * h] = cw.x;
+                    words[2 * h + 1] = cw.y;
+                }
+#pragma unroll
+                for (int q = 0; q < 2 * kConvGroups; ++q) {
+                    const int chunk = part * 2 * kConvGroups + q;  // 16-byte chunk of the 128-byte row = 8 codes
+                    const uint4 tab = scale_lut[raw[kRawA + row * 2 + (chunk >> 2)]];  // its 32-block's scale
                     uint32_t w[4];
                     expand8(words[q], tab.x, tab.y, tab.z, tab.w, w);
-                    const int chunk = quarter * 2 + q;  // 16-byte chunk of the 128-byte row
                     *reinterpret_cast<uint4*>(sm + row * 128 + ((chunk ^ (row & 7)) << 4)) =
                         make_uint4(w[0], w[1], w[2], w[3]);
                 }
@@ -312,14 +330,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) {
                     mbar_arrive(&sh.mma_full[ms]);
                     mbar_arrive(&sh.raw_empty[rs]);
-                }
-                if (++rs == kRawStages) {
-                    rs = 0;
-                    rphase ^= 1u;
-                }
-                if (++ms == kMma) {
-                    ms = 0;
-                    mphase ^= 1u;
                 }
             }
         }
