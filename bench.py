@@ -44,7 +44,9 @@ DECODE_SOURCES = [os.path.join(ROOT, "moe_expert_layer_10_b300", "csrc", f)
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=64)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: 256 for the decode layer, 512 for stream8, 32 for stack48, "
+                         "64 for --impl reference)")
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["b300", "reference"], default="b300")
     ap.add_argument("--no-e2e", action="store_true")
@@ -637,7 +639,7 @@ def run_stream8(args):
     import moe_inputs as mi
     W = mi.WORKLOADS["stream8"]
     B = 8
-    steps = args.steps if args.steps != 64 else 512
+    steps = args.steps
     total = args.warmup + steps
     t0 = time.time()
     stream = torch.cuda.Stream()
@@ -738,7 +740,7 @@ def run_stack48(args):
     import moe_inputs as mi
     W = mi.WORKLOADS["stack48"]
     T, B = 2048, 32
-    steps = args.steps if args.steps != 64 else 32
+    steps = args.steps
     t0 = time.time()
     stream = torch.cuda.Stream()
     cache = moe.MoeCache(moe.LayerShape(W.L, W.E, W.H, W.I, W.k, W.C, T), flags=moe.MOE_PREFILL_DB,
@@ -903,6 +905,8 @@ def main():
     rank, world, local = dist_env()
     if args.warmup < 3:
         args.warmup = 3
+    if args.steps is None:
+        args.steps = 64 if args.impl == "reference" else {"decode": 256, "stream8": 512, "stack48": 32}[args.workload]
     if args.impl == "reference":
         if rank == 0:
             print(json.dumps(run_reference(args)), flush=True)
