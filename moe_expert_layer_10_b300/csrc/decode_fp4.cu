@@ -360,12 +360,9 @@ cudaError_t launch(const CUtensorMap& tb, const uint8_t* arena, uint64_t entry_b
     }
     auto kern = decode_fp4_kernel<GATEUP>;
     constexpr int smem = Layout<GATEUP>::SMEM;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+    static std::atomic<uint64_t> attr{0};
+    const cudaError_t e = ensure_smem_limit(kern, smem, attr);
+    if (e != cudaSuccess) return e;
     const int grid = dyn ? num_sms : std::min(n_units, num_sms);
     return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, st, tb, arena, entry_bytes, work, n_work, n_units, S,
                       slot_row, fill_flag, H, I, h_out, w_perm, pair_out, ws, cnt, status, fill_wait_ns, dyn);

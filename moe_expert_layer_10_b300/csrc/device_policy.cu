@@ -246,11 +246,10 @@ __global__ void __launch_bounds__(512) fill_kernel(const uint4* __restrict__ poo
 cudaError_t launch_policy(const DevPolicyArgs& a, cudaStream_t st) {
     const size_t smem = 3ull * a.C * sizeof(int);
     if (smem > 200 * 1024) return cudaErrorInvalidValue;
-    static size_t attr = 48 * 1024;  // dynamic shared memory the kernel is allowed so far
-    if (smem > attr) {
-        cudaError_t e = cudaFuncSetAttribute(policy_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    if (smem > 48 * 1024) {  // above the default limit: raise it to 200 KB once per device
+        static std::atomic<uint64_t> attr{0};
+        const cudaError_t e = ensure_smem_limit(policy_kernel, 200 * 1024, attr);
         if (e != cudaSuccess) return e;
-        attr = 200 * 1024;
     }
     policy_kernel<<<1, kPolicyThreads, smem, st>>>(a);
     return cudaGetLastError();

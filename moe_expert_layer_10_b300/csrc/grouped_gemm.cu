@@ -284,12 +284,9 @@ cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const int32_t* 
     if (a_end <= a_begin || total_tiles <= 0) return cudaSuccess;
     if (a_end - a_begin > kMaxActive) return cudaErrorInvalidValue;
     auto kern = gemm_kernel<GATEUP>;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+    static std::atomic<uint64_t> attr{0};
+    const cudaError_t e = ensure_smem_limit(kern, SMEM_BYTES, attr);
+    if (e != cudaSuccess) return e;
     const int grid = std::min(total_tiles, num_sms);
     return launch_pdl(kern, dim3(grid), dim3(kThreads), SMEM_BYTES, st, ta, tb, offsets, active, a_begin, a_end,
                       slot_row, H, I, h_out, w_perm, pair_out, status);

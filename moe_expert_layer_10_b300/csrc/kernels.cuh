@@ -6,9 +6,24 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <utility>
 
 namespace moe {
+
+// Raise a kernel's dynamic shared-memory limit to `bytes` once per device: `done` keeps one bit
+// per device id (ids >= 64 share bit 63 and simply set the attribute again).
+template <typename... KArgs>
+inline cudaError_t ensure_smem_limit(void (*kern)(KArgs...), size_t bytes, std::atomic<uint64_t>& done) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = dev < 63 ? (1ull << dev) : 0ull;
+    if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+    if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
+}
 
 // Launch a kernel of the layer's chain with programmatic stream serialization: it may be
 // scheduled while the previous kernel of the stream is still running, and waits for it in

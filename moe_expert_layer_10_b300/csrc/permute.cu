@@ -289,15 +289,13 @@ int permute_grid(int P) { return P > kPermThreads ? (P + kChunkPairs - 1) / kChu
 cudaError_t launch_permute(const int32_t* idx, const float* w, int P, int E, int32_t* offsets, int32_t* perm,
                            int32_t* inv_perm, float* w_perm, int32_t* active, int32_t* n_active, int* status,
                            int32_t* cells, unsigned* done, cudaStream_t st) {
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t err = cudaFuncSetAttribute(permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               sizeof(int) * (kPermWarps * 1025 + 36 + 1024 + 1));
+    static std::atomic<uint64_t> attr_one{0}, attr_place{0};
+    {
+        cudaError_t err =
+            ensure_smem_limit(permute_kernel, sizeof(int) * (kPermWarps * 1025 + 36 + 1024 + 1), attr_one);
         if (err != cudaSuccess) return err;
-        err = cudaFuncSetAttribute(permute_place_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   sizeof(int) * kPermWarps * 1025);
+        err = ensure_smem_limit(permute_place_kernel, sizeof(int) * kPermWarps * 1025, attr_place);
         if (err != cudaSuccess) return err;
-        attr_set = true;
     }
     const int G = permute_grid(P);
     if (G == 1) {

@@ -273,12 +273,9 @@ template <int EPB, int TPW>
 cudaError_t launch_staged(const uint16_t* x, const float* Wr, const float* b, int T, int H, int E, float* z,
                           cudaStream_t st) {
     auto kern = router_logits_staged_kernel<EPB, TPW>;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+    static std::atomic<uint64_t> attr{0};
+    const cudaError_t e = ensure_smem_limit(kern, 227 * 1024, attr);
+    if (e != cudaSuccess) return e;
     const size_t smem = static_cast<size_t>(EPB) * H * 4 + static_cast<size_t>(T) * H * 2;
     return launch_pdl(kern, dim3((E + EPB - 1) / EPB), dim3(256), smem, st, x, Wr, b, T, H, E, z);
 }
@@ -388,13 +385,9 @@ cudaError_t launch_router_logits(const uint16_t* x, const float* Wr, const float
     if (T <= 8 && smem4 <= 200 * 1024) return launch_staged<4, 4>(x, Wr, b, T, H, E, z, st);
     if (T <= 16 && smem4 <= 200 * 1024) return launch_staged<4, 8>(x, Wr, b, T, H, E, z, st);
     if (T <= 32 && smem4 <= 200 * 1024) return launch_staged<4, 16>(x, Wr, b, T, H, E, z, st);
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(router_logits_tiled_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kTiledSmem);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+    static std::atomic<uint64_t> attr{0};
+    const cudaError_t e = ensure_smem_limit(router_logits_tiled_kernel, kTiledSmem, attr);
+    if (e != cudaSuccess) return e;
     return launch_pdl(router_logits_tiled_kernel, dim3((E + kTE - 1) / kTE, (T + kTT - 1) / kTT), dim3(kTiledThreads),
                       kTiledSmem, st, x, Wr, b, T, H, E, z);
 }
