@@ -30,6 +30,7 @@ KIND_EXPERT, KIND_ROUTER, KIND_X, KIND_PERM, KIND_TRACE = 1, 2, 3, 4, 5
 
 _CORE = os.path.join(_HERE, "normal_core.h")
 _CORE_FP4 = os.path.join(_HERE, "mxfp4_core.h")
+_CORE_NVFP4 = os.path.join(_HERE, "nvfp4_core.h")
 _SO_FMA = os.path.join(_HERE, "libmoe_inputs_fma.so")
 
 
@@ -58,7 +59,7 @@ def build(force: bool = False) -> str:
     # (loaded only on CPUs that have it); fused multiply-add rounds once either way, so the
     # bits are the same
     for so, extra in ((_SO, []), (_SO_FMA, ["-mfma"])):
-        if force or _stale(so, _SRC, _CORE, _CORE_FP4):
+        if force or _stale(so, _SRC, _CORE, _CORE_FP4, _CORE_NVFP4):
             tmp = so + f".tmp{os.getpid()}"
             subprocess.check_call(["gcc", "-O2", "-ffp-contract=off", "-fopenmp", "-shared", "-fPIC", "-std=c11"] +
                                   extra + [_SRC, "-o", tmp, "-lm"])
@@ -92,6 +93,16 @@ def lib():
         L.mi_f32_to_bf16.restype = ctypes.c_uint16
         L.mi_mxfp4_entry.argtypes = [u64, u64, i32, i32, vp]
         L.mi_mxfp4_block32.argtypes = [vp, vp, vp]
+        L.mi_nvfp4_entry.argtypes = [u64, u64, i32, i32, vp]
+        L.mi_nvfp4_block16.argtypes = [vp, ctypes.c_float, vp, vp]
+        L.mi_e4m3_encode.argtypes = [ctypes.c_float]
+        L.mi_e4m3_encode.restype = ctypes.c_uint8
+        L.mi_e4m3_decode.argtypes = [ctypes.c_uint8]
+        L.mi_e4m3_decode.restype = ctypes.c_float
+        L.mi_nvfp4_tscale.argtypes = [ctypes.c_float]
+        L.mi_nvfp4_tscale.restype = ctypes.c_float
+        L.mi_nvfp4_bytes.argtypes = [i32, i32]
+        L.mi_nvfp4_bytes.restype = u64
         L.mi_log_unit.argtypes = [dbl]
         L.mi_log_unit.restype = dbl
         L.mi_sincos_2pi.argtypes = [dbl, vp, vp]
@@ -201,6 +212,43 @@ def mxfp4_block(x_bf16_bits: np.ndarray):
     s = np.empty(1, np.uint8)
     lib().mi_mxfp4_block32(_ptr(x), _ptr(q), _ptr(s))
     return q, int(s[0])
+
+
+def nvfp4_entry_bytes(H: int, I: int) -> int:
+    """Bytes of one NVFP4 entry: E2M1 pairs (3*H*I/2), E4M3 scales (3*H*I/16), 16-byte trailer."""
+    return int(lib().mi_nvfp4_bytes(H, I))
+
+
+def nvfp4_entry(seed: int, layer: int, expert: int, H: int, I: int) -> np.ndarray:
+    """Entry (layer, expert) quantized to NVFP4 (uint8 bytes; layout in nvfp4_core.h)."""
+    out = np.empty(nvfp4_entry_bytes(H, I), np.uint8)
+    lib().mi_nvfp4_entry(seed, stream_id(KIND_EXPERT, layer, expert), H, I, _ptr(out))
+    return out
+
+
+def nvfp4_block(x_bf16_bits: np.ndarray, tensor_scale: float):
+    """Quantize one block of 16 bf16 values: (8 bytes of E2M1 pairs, E4M3 scale byte)."""
+    x = np.ascontiguousarray(x_bf16_bits, dtype=np.uint16)
+    assert x.size == 16
+    q = np.empty(8, np.uint8)
+    s = np.empty(1, np.uint8)
+    lib().mi_nvfp4_block16(_ptr(x), float(tensor_scale), _ptr(q), _ptr(s))
+    return q, int(s[0])
+
+
+def e4m3_encode(v: float) -> int:
+    """The quantizer's E4M3 code of v >= 0 (round to nearest even, saturating at 448)."""
+    return int(lib().mi_e4m3_encode(float(v)))
+
+
+def e4m3_decode(c: int) -> float:
+    """The quantizer's value of an E4M3 code (used when it divides by the stored scale)."""
+    return float(lib().mi_e4m3_decode(int(c)))
+
+
+def nvfp4_tensor_scale(amax: float) -> float:
+    """The quantizer's tensor scale for a matrix whose largest magnitude is amax."""
+    return float(lib().mi_nvfp4_tscale(float(amax)))
 
 
 def fill_mxfp4_entry_at(ptr: int, seed: int, layer: int, expert: int, H: int, I: int) -> None:

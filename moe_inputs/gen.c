@@ -20,6 +20,7 @@
 
 #include "mxfp4_core.h"
 #include "normal_core.h"
+#include "nvfp4_core.h"
 
 void mi_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]) { mi_philox_10(ctr, key, out); }
 
@@ -216,3 +217,49 @@ void mi_mxfp4_entry(uint64_t seed, uint64_t stream, int H, int I, uint8_t* out) 
 
 /* One block of 32 bf16 values quantized (for the pins). */
 void mi_mxfp4_block32(const uint16_t* x, uint8_t* q16, uint8_t* s1) { mi_mxfp4_block(x, q16, s1); }
+
+
+/*
+ * Expert entry (layer, expert) in NVFP4: the seeded bf16 entry of stream `stream` quantized
+ * per matrix (tensor scale) and per block of 16 along each row (nvfp4_core.h), the blocks
+ * placed by mi_nvfp4_place, then the three fp32 tensor scales and 4 zero bytes.
+ */
+void mi_nvfp4_entry(uint64_t seed, uint64_t stream, int H, int I, uint8_t* out) {
+    const uint64_t n = 3ull * H * I;
+    uint16_t* w = (uint16_t*)malloc(n * sizeof(uint16_t));
+    if (!w) return;
+    mi_normal_bf16(seed, stream, 0, n, 0.02, w);
+    const uint64_t mat_elems = (uint64_t)I * H;
+    float t[3];
+    for (int m = 0; m < 3; ++m) {
+        float amax = 0.0f;
+        for (uint64_t i = 0; i < mat_elems; ++i) {
+            const float a = mi_bf16_to_f32(w[m * mat_elems + i] & 0x7fff);
+            if (a > amax) amax = a;
+        }
+        t[m] = mi_nvfp4_tensor_scale(amax);
+    }
+#pragma omp parallel for schedule(static)
+    for (int r = 0; r < 2 * I + H; ++r) {
+        const int K = r < 2 * I ? H : I;
+        const int mat = r < I ? 0 : (r < 2 * I ? 1 : 2);
+        const int row = r < I ? r : (r < 2 * I ? r - I : r - 2 * I);
+        const uint64_t elem0 = r < 2 * I ? (uint64_t)r * H : 2 * mat_elems + (uint64_t)(r - 2 * I) * I;
+        for (int b = 0; b < K / 16; ++b) {
+            uint64_t co, so;
+            mi_nvfp4_place(H, I, mat, row, b, &co, &so);
+            mi_nvfp4_block(w + elem0 + 16 * b, t[mat], out + co, out + so);
+        }
+    }
+    uint8_t* trailer = out + mi_nvfp4_entry_bytes(H, I) - 16;
+    memcpy(trailer, t, 12);
+    memset(trailer + 12, 0, 4);
+    free(w);
+}
+
+/* Pieces of the NVFP4 quantizer, for the pins. */
+void mi_nvfp4_block16(const uint16_t* x, float t, uint8_t* q8, uint8_t* s1) { mi_nvfp4_block(x, t, q8, s1); }
+uint8_t mi_e4m3_encode(float v) { return mi_e4m3_rne(v); }
+float mi_e4m3_decode(uint8_t c) { return mi_e4m3_value(c); }
+float mi_nvfp4_tscale(float amax) { return mi_nvfp4_tensor_scale(amax); }
+uint64_t mi_nvfp4_bytes(int H, int I) { return mi_nvfp4_entry_bytes(H, I); }

@@ -57,6 +57,9 @@ def lib():
         L.orc_moe_dense.argtypes = [vp, i32, i32, i32, vp, vp, i32, i32, vp, vp, vp]
         L.orc_mxfp4_dequant.argtypes = [vp, vp, ctypes.c_int64, vp]
         L.orc_mxfp4_dequant.restype = ctypes.c_int64
+        L.orc_nvfp4_dequant.argtypes = [vp, vp, ctypes.c_int64, ctypes.c_float, vp]
+        L.orc_nvfp4_dequant.restype = ctypes.c_int64
+        L.orc_expert_ffn_f64.argtypes = [vp, i32, i32, vp, vp]
         L.orc_layer_accesses.argtypes = [vp, i32, i32, i32, vp]
         L.orc_layer_accesses.restype = i32
         L.orc_lru_run.argtypes = [i32, i32, vp, vp, vp, i32, vp, vp, vp, vp, vp, vp]
@@ -227,6 +230,48 @@ def mxfp4_entry_as_bf16(entry: np.ndarray, H: int, I: int) -> np.ndarray:
     q = np.concatenate([gate_q.ravel(), up_q.ravel(), down_q.ravel()])
     s = np.concatenate([gate_s.ravel(), up_s.ravel(), down_s.ravel()])
     return mxfp4_dequant(q, s, 3 * H * I)
+
+
+def nvfp4_dequant(q: np.ndarray, s: np.ndarray, n: int, tensor_scale: float) -> np.ndarray:
+    """NVFP4 elements of one matrix (E2M1 bytes q, E4M3 scales s per 16, fp32 tensor scale)
+    -> their exact values in float64."""
+    qq, ss = _c(q, np.uint8), _c(s, np.uint8)
+    out = np.empty(n, np.float64)
+    bad = lib().orc_nvfp4_dequant(_p(qq), _p(ss), n, float(tensor_scale), _p(out))
+    if bad:
+        raise ValueError(f"{bad} NVFP4 block scales are not valid E4M3 scales")
+    return out
+
+
+def nvfp4_entry_as_f64(entry: np.ndarray, H: int, I: int) -> np.ndarray:
+    """An NVFP4 expert entry as the float64 weights W_gate | W_up | W_down (row-major). Entry
+    layout, in stages of 4096 code bytes + 512 scale bytes: for W_gate/W_up, per 64-row tile
+    and 64-column slab: gate rows (64 x 32 bytes), up rows (64 x 32), gate scales (64 x 4), up
+    scales (64 x 4); then for W_down, per 128-row tile and slab: rows (128 x 32), scales
+    (128 x 4); then the fp32 tensor scales of W_gate, W_up, W_down and 4 zero bytes."""
+    st = 4608
+    gu = (I // 64) * (H // 64) * st
+    a = entry[:gu].reshape(I // 64, H // 64, st)
+    gate_q = a[:, :, :2048].reshape(I // 64, H // 64, 64, 32).transpose(0, 2, 1, 3).reshape(I, H // 2)
+    up_q = a[:, :, 2048:4096].reshape(I // 64, H // 64, 64, 32).transpose(0, 2, 1, 3).reshape(I, H // 2)
+    gate_s = a[:, :, 4096:4352].reshape(I // 64, H // 64, 64, 4).transpose(0, 2, 1, 3).reshape(I, H // 16)
+    up_s = a[:, :, 4352:4608].reshape(I // 64, H // 64, 64, 4).transpose(0, 2, 1, 3).reshape(I, H // 16)
+    dn = (H // 128) * (I // 64) * st
+    d = entry[gu:gu + dn].reshape(H // 128, I // 64, st)
+    down_q = d[:, :, :4096].reshape(H // 128, I // 64, 128, 32).transpose(0, 2, 1, 3).reshape(H, I // 2)
+    down_s = d[:, :, 4096:].reshape(H // 128, I // 64, 128, 4).transpose(0, 2, 1, 3).reshape(H, I // 16)
+    t = np.frombuffer(entry[gu + dn:gu + dn + 12].tobytes(), dtype=np.float32)
+    return np.concatenate([nvfp4_dequant(gate_q, gate_s, I * H, t[0]), nvfp4_dequant(up_q, up_s, I * H, t[1]),
+                           nvfp4_dequant(down_q, down_s, H * I, t[2])])
+
+
+def expert_ffn_f64(W: np.ndarray, H: int, I: int, x_row: np.ndarray) -> np.ndarray:
+    """orc_expert_ffn with float64 weights W_gate | W_up | W_down (row-major)."""
+    w = _c(W, np.float64)
+    x = _c(x_row, np.uint16)
+    y = np.empty(H, dtype=np.float64)
+    lib().orc_expert_ffn_f64(_p(w), H, I, _p(x), _p(y))
+    return y
 
 
 def layer_accesses(idx: np.ndarray, E: int) -> np.ndarray:

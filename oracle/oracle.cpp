@@ -289,6 +289,59 @@ int64_t orc_mxfp4_dequant(const uint8_t* q, const uint8_t* s, int64_t n, uint16_
     return inexact;
 }
 
+// NVFP4 weights: element i of a matrix is the E2M1 code in nibble i%2 of byte i/2 (low nibble
+// first; bit 3 the sign; bits 2-1 the exponent e with bias 1, bit 0 the mantissa m: value
+// m/2 when e = 0, else (1 + m/2) * 2^(e-1)) times the FP8 E4M3 scale of its block of 16
+// (exponent field f with bias 7, mantissa m3: m3/8 * 2^-6 when f = 0, else (1 + m3/8) *
+// 2^(f-7); sign and the all-ones NaN pattern are never valid scales) times the matrix's fp32
+// tensor scale. In double every such product is exact. Returns the number of invalid scales.
+static double orc_e2m1_value(int code) {
+    const int e = (code >> 1) & 3, m = code & 1;
+    const double mag = e == 0 ? 0.5 * m : (1.0 + 0.5 * m) * std::ldexp(1.0, e - 1);
+    return (code & 8) ? -mag : mag;
+}
+
+static double orc_e4m3_value(int c, bool* ok) {
+    const int f = (c >> 3) & 15, m3 = c & 7;
+    *ok = !(c & 0x80) && !(f == 15 && m3 == 7);
+    return f == 0 ? std::ldexp(m3 / 8.0, -6) : std::ldexp(1.0 + m3 / 8.0, f - 7);
+}
+
+int64_t orc_nvfp4_dequant(const uint8_t* q, const uint8_t* s, int64_t n, float tensor_scale, double* out) {
+    int64_t invalid = 0;
+    for (int64_t b = 0; b < n / 16; ++b) {
+        bool ok;
+        const double scale = orc_e4m3_value(s[b], &ok) * static_cast<double>(tensor_scale);
+        if (!ok) ++invalid;
+        for (int64_t i = 16 * b; i < 16 * b + 16; ++i)
+            out[i] = orc_e2m1_value((q[i / 2] >> (4 * (i % 2))) & 15) * scale;
+    }
+    return invalid;
+}
+
+// The expert FFN of orc_expert_ffn with the weights given as doubles (W_gate | W_up | W_down,
+// row-major), for entries whose values are not bf16 (NVFP4 with its tensor scales).
+void orc_expert_ffn_f64(const double* W, int H, int I, const uint16_t* x, double* y) {
+    const double* Wg = W;
+    const double* Wu = W + static_cast<size_t>(I) * H;
+    const double* Wd = W + 2 * static_cast<size_t>(I) * H;
+    std::vector<double> h(I);
+    for (int i = 0; i < I; ++i) {
+        double g = 0.0, u = 0.0;
+        for (int c = 0; c < H; ++c) {
+            const double xc = bf16_to_double(x[c]);
+            g += Wg[static_cast<size_t>(i) * H + c] * xc;
+            u += Wu[static_cast<size_t>(i) * H + c] * xc;
+        }
+        h[i] = g / (1.0 + std::exp(-g)) * u;
+    }
+    for (int n = 0; n < H; ++n) {
+        double acc = 0.0;
+        for (int i = 0; i < I; ++i) acc += Wd[static_cast<size_t>(n) * I + i] * h[i];
+        y[n] = acc;
+    }
+}
+
 // R5: the distinct experts routed in one layer invocation, in ascending id (the order in
 // which the LRU sees them). Returns their number.
 int orc_layer_accesses(const int32_t* idx, int T, int k, int E, int32_t* experts) {
