@@ -576,7 +576,7 @@ int dev_policy_run(moe_ctx* c, moe::DevPolicyArgs a, bool join) {
 // kernels after the fills, then the combine. Enqueues only; never waits on the host.
 int forward_device(moe_ctx* c, int layer, const void* x, const float* resid, float* out, int T, const int32_t* idx,
                    const float* w) {
-    const int P = T * c->k, E = c->E, H = c->H, I = c->I;
+    const int P = T * c->k, E = c->E, H = c->H;
     if (c->path == MOE_PATH_GEMM)
         return fail(MOE_E_INVAL, "the device-resident policy runs the decode kernels only (MOE_PATH_GEMM unsupported)");
     {
