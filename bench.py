@@ -35,6 +35,7 @@ sys.path.insert(0, ROOT)
 METRIC = "MoE-layer decode tok/s (batch 1/4/16, 256 experts top-6, 64-entry LRU cache)"
 UNIT = "tok/s"
 BATCHES = (1, 4, 16)  # replaced by --batches
+PER_BATCH_STEPS = 256  # steps of each per-batch run (the workload defines 256 steps per batch size)
 FALLBACK_HBM_GBS = 6400.0
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_gateup.md")
 DECODE_SOURCES = [os.path.join(ROOT, "moe_expert_layer_10_b300", "csrc", f)
@@ -54,6 +55,8 @@ def parse_args():
     ap.add_argument("--batches", default="1,4,16", help="decode batch sizes of one step (profiling cases)")
     ap.add_argument("--capacity", type=int, default=0, help="override the cache capacity (profiling cases)")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-per-batch", action="store_true",
+                    help="skip the per-batch runs (B = 1, 4, 16 each through its own 256 LRU steps)")
     ap.add_argument("--prefetch-all", action="store_true",
                     help="comparison case: prefetch every expert before timing (needs --capacity >= 256), so every "
                          "routed access hits and the step time is compute plus control")
@@ -381,6 +384,8 @@ def run_b300(args, rank, world, local):
                "h2d_bytes_per_step": sum(B * W.H * (2 + 4) for B in BATCHES),
                "d2h_bytes_per_step": sum(B * W.H * 4 for B in BATCHES)}
 
+    per_batch = None if args.no_per_batch else run_per_batch(cache, W, Wr, bias, stream)
+
     # profiled pass of the same LRU workload (untimed): per-kernel CUDA-event times. The
     # decode gate/up kernel of a wave that fills entries waits on the device for those copies,
     # so its time here includes PCIe time by design.
@@ -490,6 +495,7 @@ def run_b300(args, rank, world, local):
         "resident_pass": {"ms_per_step": round(ms_resident, 4),
                           "tok_s": round(sum(BATCHES) / (ms_resident / 1e3), 1),
                           "note": "the same steps with every expert resident (no fills), timed without events"},
+        "per_batch": per_batch,
         "kernels_resident_pass": table(kst), "kernels_by_batch_resident": by_batch,
         "kernels_lru_pass": table(kst_lru),
     }
@@ -502,6 +508,50 @@ def run_b300(args, rank, world, local):
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(W, Wr_h, b_h)
     return result
+
+
+def run_per_batch(cache, W, Wr, bias, stream, steps: int = PER_BATCH_STEPS, warmup: int = 3):
+    """The decode workload as its definition runs it: for each batch size B, its own run of
+    `steps` decode steps at batch B through the 64-entry LRU (fresh seeded activations per step),
+    timed with CUDA events on the compute stream. The cache starts from the state the previous
+    run left; the warm-up steps bring it to this batch's steady state. Reports tok/s, hit rate
+    and the share of the step spent on fills, per batch."""
+    import numpy as np
+    import torch
+
+    import moe_inputs as mi
+    res = {}
+    for B in BATCHES:
+        total = warmup + steps
+        x = torch.from_numpy(np.stack([mi.activations(W.seed, 2_000_000 + 1000 * B + s, B, W.H)
+                                       for s in range(total)]).view(np.int16)).view(torch.bfloat16).cuda()
+        r = x.float()
+        idx = torch.empty((B, W.k), dtype=torch.int32, device="cuda")
+        w = torch.empty((B, W.k), dtype=torch.float32, device="cuda")
+        out = torch.empty((B, W.H), dtype=torch.float32, device="cuda")
+        torch.cuda.synchronize()
+
+        def one(s):
+            cache.route(0, x[s], Wr, bias, idx, w)
+            cache.layer_forward(0, x[s], r[s], out, idx, w)
+
+        for s in range(warmup):
+            one(s)
+        cache.sync()
+        cache.stats(reset=True)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for s in range(warmup, total):
+            one(s)
+        e1.record(stream)
+        cache.sync()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        st = cache.stats()
+        res[f"B{B}"] = {"tok_s": round(steps * B / (ms / 1e3), 1), "ms_per_step": round(ms / steps, 4),
+                        "steps": steps, **_stats_summary(st, ms),
+                        "fills_per_step": st["misses"] / steps, "experts_per_step": st["expert_reads"] / steps}
+    return res
 
 
 def resident_context(args, W, E=None, fp4: bool = False):

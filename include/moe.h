@@ -143,6 +143,10 @@ typedef struct {
 } moe_kernel_stat_t;
 
 /*
+ * Source: "FreeToken rtx 4090", "How the MoE Memory Hierarchy Works" -- the host keeps the
+ * complete expert pool as the source of truth, the GPU keeps a cache of complete layer-expert
+ * entries; "FreeToken benchmark", "How FreeToken Serves Large MoE Models" -- remaining VRAM is
+ * an elastic expert cache. This call sets up both tiers.
  * Create a context: pinned host pool of L*E entries (zeroed), device arena of C entries,
  * slot-indirection table slot_of[L][E] (all -1), host LRU, scratch for max_tokens.
  * stream_compute / stream_copy: cudaStream_t handles to use, or NULL to create private
@@ -183,6 +187,9 @@ int moe_cache_resize(moe_ctx* ctx, int new_capacity);
 uint64_t moe_entry_bytes(const moe_ctx* ctx);
 
 /*
+ * Source: "FreeToken rtx 4090", "How the MoE Memory Hierarchy Works" -- each token activates a
+ * small subset of the routed experts per layer ("six of 256"). The gating arithmetic below is
+ * this library's specification (the pages state none).
  * Router for one layer: logits z[t,e] = fp32(sum_h W_r[e,h] x[t,h]) + b[e] in a fixed
  * order (32 lane partials over h = 256m + 8l + r, m then r ascending, fmaf; pairwise folds
  * at distances 16,8,4,2,1; bias last), top-k by (z desc, id asc), gates = softmax over the
@@ -207,6 +214,10 @@ int moe_route_forced(moe_ctx* ctx, int layer, const void* x_bf16, int T, const f
                      float* logits_or_null);
 
 /*
+ * Source: "FreeToken rtx 4090", "How the MoE Memory Hierarchy Works" -- during prefill the
+ * runtime loads the next layer's experts while the GPU computes the current layer (full-layer
+ * streaming, MOE_FILL_FULL_LAYER); "FreeToken benchmark", "How FreeToken Serves Large MoE
+ * Models" -- the PCIe link moves selected experts into the GPU cache (MOE_FILL_DEMAND).
  * Cache fill without compute.
  *  MOE_FILL_DEMAND: topk_idx_host holds n host int32 expert ids (e.g. a T*k top-k block);
  *    their distinct values are accessed in ascending id. Errors: MOE_E_CAPACITY if more than
@@ -221,6 +232,11 @@ int moe_route_forced(moe_ctx* ctx, int layer, const void* x_bf16, int T, const f
 int moe_cache_fill(moe_ctx* ctx, int layer, const int32_t* topk_idx_host, int n, int mode);
 
 /*
+ * Source: "FreeToken rtx 4090", "How the MoE Memory Hierarchy Works" -- decode keeps a shared
+ * LRU expert cache across layers and tokens, and a cached entry is executed through one logical
+ * mapping (here the slot table); "FreeToken benchmark", "How FreeToken Serves Large MoE Models"
+ * -- recently routed experts stay in VRAM and misses are filled over PCIe. The SwiGLU expert
+ * form and the weighted combine are this library's specification (the pages state neither).
  * One MoE layer on T tokens (device pointers): out = resid + sum_j w_j y_{e_j}(x).
  * x_bf16 [T x H], resid fp32 [T x H] (may equal out), out fp32 [T x H],
  * topk_idx int32 [T x k], topk_w fp32 [T x k] (as written by moe_route).
@@ -240,6 +256,9 @@ int moe_layer_forward(moe_ctx* ctx, int layer, const void* x_bf16, const float* 
                       const int32_t* topk_idx, const float* topk_w);
 
 /*
+ * Source: "FreeToken benchmark", overview -- the runtime reports token speed, processed tokens,
+ * requests and cache activity; "FreeToken rtx 4090", "Benchmarks, Comparisons, and Tradeoffs"
+ * -- the miss rate over expert reads is the measure of the cache (hits / expert_reads here).
  * Counters and trace. out may be NULL. trace_or_null receives up to trace_cap of the
  * newest events, oldest first; the return value is the number written (>= 0), or a
  * negative error. reset != 0 clears counters and trace after reading.
@@ -288,8 +307,10 @@ int moe_lru_simulate(int capacity, int n, const int32_t* layer, const int32_t* e
  * timeout (kind 2), or the next `count` decode waves that fill entries tell their kernels to
  * wait for a fill generation that the copy stream does not write, with a 0.2 s device-side
  * deadline (kind 3): the kernels give up, raise device status 5 (MOE_E_DEVICE at the next
- * synchronising call) and the context stays usable. kind 0 clears. No GPU fault is ever
- * produced.
+ * synchronising call) and the context stays usable; or the next `count` fills report a failed
+ * fill-flag write after their copy was enqueued (kind 4): the call fails with MOE_E_CUDA, the
+ * entry is not made resident, and the entry the copy overwrites is evicted. kind 0 clears. No
+ * GPU fault is ever produced.
  */
 int moe_debug_inject(moe_ctx* ctx, int kind, int count);
 
@@ -327,9 +348,12 @@ int moe_debug_read(moe_ctx* ctx, int what, void* host_dst, uint64_t bytes);
  * [1, min(num_experts, 32)], T < 0 and NULL pointers. T == 0 is a no-op.
  * The array is shared by every call and keeps the last call's logits: calls that overlap on
  * the GPU (other streams, other host threads on the same device) race on it, so issue them
- * in order on one stream. The first call on each device looks up the array's device address
- * with that device current (cudaGetSymbolAddress); make that first call before any stream
- * capture begins. Errors: MOE_E_INVAL, MOE_E_CUDA.
+ * in order on one stream. The first call in each CUDA context looks up the array's device
+ * address with that context current (cudaGetSymbolAddress) and keeps it with the context's id;
+ * a later call in another context -- a different context made current on the device, or the
+ * primary context created again after cudaDeviceReset -- looks it up again, so a stale address
+ * is never used. Make the first call in each context before any stream capture begins.
+ * Errors: MOE_E_INVAL, MOE_E_CUDA.
  */
 #define MOE_NOALLOC_MAX_LOGITS 65536
 int moe_route_noalloc(const void* x_bf16, int T, int hidden, int num_experts, int top_k, const float* router_w,

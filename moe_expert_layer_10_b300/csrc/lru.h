@@ -10,7 +10,8 @@
 // it takes the slot of the least recently used entry. A capacity change (elastic cache)
 // keeps the most recently used entries that fit, evicts the others least recent first, and
 // renumbers the survivors 0, 1, ... in the order of their old slots, so the used slots are
-// always 0 .. n_used-1. O(1) touch and evict: an intrusive
+// always 0 .. n_used-1 (release_slot, for a fill that failed after its copy was enqueued, is
+// the one operation that frees a slot in the middle). O(1) touch and evict: an intrusive
 // doubly-linked recency list over slots plus a key -> slot array. Decisions are planned
 // first and committed only after the fill copy was enqueued, so a failed fill leaves the
 // policy exactly as it was.
@@ -146,6 +147,18 @@ class ExpertLru {
         key_in_[p.slot] = p.key;
         slot_of_[p.key] = p.slot;
         push_front(p.slot);
+    }
+
+    // Forget the entry in `slot` (if any) and return the slot to the free set: used when a
+    // fill copy into the slot was enqueued but the fill could not be completed, so the slot
+    // holds neither its old entry nor a usable new one.
+    void release_slot(int slot) {
+        const int key = key_in_[slot];
+        if (key < 0) return;
+        unlink(slot);
+        slot_of_[key] = -1;
+        key_in_[slot] = -1;
+        free_.insert(slot);
     }
 
    private:

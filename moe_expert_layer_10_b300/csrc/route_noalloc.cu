@@ -22,7 +22,39 @@ static __device__ __align__(256) float g_noalloc_logits[MOE_NOALLOC_MAX_LOGITS];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
-float* g_logits_addr[kMaxDevices] = {};  // device address of the array, per device
+// Per device: the array's device address and the id of the context it was looked up in. A
+// context that is destroyed and created again (cudaDeviceReset, or another context made current
+// on the device) gets a new id, and the address is looked up again in the new context.
+struct SymbolAddr {
+    unsigned long long ctx_id = 0;
+    bool valid = false;
+    float* addr = nullptr;
+};
+SymbolAddr g_logits_addr[kMaxDevices];
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+template <typename Fn>
+Fn driver_fn(const char* name) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+        return nullptr;
+    return reinterpret_cast<Fn>(p);
+}
+
+// Id of the calling thread's current context (cuCtxGetId: unique for the life of the process).
+cudaError_t current_ctx_id(unsigned long long* id) {
+    static CtxGetCurrentFn get_cur = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+    static CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
+    if (!get_cur || !get_id) return cudaErrorNotSupported;
+    CUcontext ctx = nullptr;
+    if (get_cur(&ctx) != CUDA_SUCCESS || !ctx) return cudaErrorContextIsDestroyed;
+    if (get_id(ctx, id) != CUDA_SUCCESS) return cudaErrorContextIsDestroyed;
+    return cudaSuccess;
+}
 
 int err(int code, const char* fmt, long long a = 0, long long b = 0) {
     char buf[256];
@@ -50,14 +82,26 @@ extern "C" int moe_route_noalloc(const void* x, int T, int H, int E, int k, cons
     if (dev < 0 || dev >= kMaxDevices) return err(MOE_E_INVAL, "device %lld beyond the %lld supported", dev, kMaxDevices);
     float* z = nullptr;
     {
+        unsigned long long ctx_id = 0;
+        if (current_ctx_id(&ctx_id) != cudaSuccess) {
+            // no context is current on this thread yet: cudaSetDevice creates (or, after a
+            // cudaDeviceReset, re-creates) the device's primary context and makes it current
+            e = cudaSetDevice(dev);
+            if (e != cudaSuccess) return moe::set_error(MOE_E_CUDA, cudaGetErrorString(e));
+            if (current_ctx_id(&ctx_id) != cudaSuccess)
+                return moe::set_error(MOE_E_CUDA, "no current CUDA context to look the scratch up in");
+        }
         std::lock_guard<std::mutex> lock(g_mu);
-        if (!g_logits_addr[dev]) {
+        SymbolAddr& a = g_logits_addr[dev];
+        if (!a.valid || a.ctx_id != ctx_id) {
             void* p = nullptr;
             e = cudaGetSymbolAddress(&p, g_noalloc_logits);
             if (e != cudaSuccess) return moe::set_error(MOE_E_CUDA, cudaGetErrorString(e));
-            g_logits_addr[dev] = static_cast<float*>(p);
+            a.addr = static_cast<float*>(p);
+            a.ctx_id = ctx_id;
+            a.valid = true;
         }
-        z = g_logits_addr[dev];
+        z = a.addr;
     }
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     e = moe::launch_router_logits(static_cast<const uint16_t*>(x), Wr, b, T, H, E, z, st);

@@ -352,6 +352,17 @@ int upload_table(moe_ctx* c) {
     return MOE_OK;
 }
 
+// A fill copy into p.slot was enqueued but the fill failed before it was committed: the slot's
+// previous entry (p.victim, if any) is overwritten, so it leaves the cache and the slot returns
+// to the free set. A later copy into the slot runs after this one on the copy stream.
+void abandon_slot(moe_ctx* c, const ExpertLru::Plan& p) {
+    if (p.victim < 0) return;  // the slot was free and stays free
+    c->lru.release_slot(p.slot);
+    c->slot_host[p.victim] = -1;
+    c->stats.evictions++;
+    c->table_dirty = true;
+}
+
 void record_event(moe_ctx* c, int kind, int key, int slot, int victim) {
     c->stats.trace_len++;
     if (!(c->cfg.flags & MOE_TRACE) || c->trace.empty()) return;
@@ -368,7 +379,9 @@ void record_event(moe_ctx* c, int kind, int key, int slot, int victim) {
 // Access the given keys in order (routed or prefetch), enqueue the fills as one batch on
 // the copy stream. Each filled slot remembers the batch, whose event compute waits for.
 // On any failure the batch opened so far is still closed with its event, and the access
-// that failed is not committed, so the policy and the slot table stay consistent.
+// that failed is not committed, so the policy and the slot table stay consistent. If the
+// failure comes after the copy into the slot was enqueued, the slot's previous entry is
+// evicted as well (its bytes are being overwritten) and the slot returns to the free set.
 int access_keys(moe_ctx* c, const std::vector<int>& keys, bool prefetch) {
     bool batch_open = false;
     FillRec fr{nullptr, nullptr};
@@ -400,15 +413,23 @@ int access_keys(moe_ctx* c, const std::vector<int>& keys, bool prefetch) {
                           cudaGetErrorString(e));
                 break;
             }
+            // from here on the slot's old bytes are being overwritten
             const uint32_t gen = c->fill_gen[p.slot] + 1;
-            const CUresult r = write_value_fn()(reinterpret_cast<CUstream>(c->s_copy),
-                                                reinterpret_cast<CUdeviceptr>(c->fill_flag + p.slot), gen, 0);
+            CUresult r = write_value_fn()(reinterpret_cast<CUstream>(c->s_copy),
+                                          reinterpret_cast<CUdeviceptr>(c->fill_flag + p.slot), gen, 0);
+            if (c->inject_kind == 4 && c->inject_count > 0) {
+                c->inject_count--;
+                r = CUDA_ERROR_UNKNOWN;  // injected: report the flag write as failed
+            }
+            // the generation is used up even if the write failed (it may have landed), so the
+            // next fill of the slot waits for a strictly newer one
+            c->fill_gen[p.slot] = gen;
             if (r != CUDA_SUCCESS) {
                 rc = fail(MOE_E_CUDA, "fill flag write for layer %d expert %d: driver error %d", key / c->E,
                           key % c->E, static_cast<int>(r));
+                abandon_slot(c, p);
                 break;
             }
-            c->fill_gen[p.slot] = gen;
         }
         c->lru.commit(p);
         record_event(c, p.kind, key, p.slot, p.victim);
@@ -432,7 +453,10 @@ int access_keys(moe_ctx* c, const std::vector<int>& keys, bool prefetch) {
             c->table_dirty = true;
             cudaError_t e = cudaEventRecord(c->fill_ev[c->fill_seq % kEvRing], c->s_copy);
             if (e != cudaSuccess) {
+                // compute could not be ordered after this copy: the new entry is not usable
                 rc = fail(MOE_E_CUDA, "fill event: %s", cudaGetErrorString(e));
+                c->lru.release_slot(p.slot);
+                c->slot_host[key] = -1;
                 break;
             }
         }
@@ -585,7 +609,9 @@ int forward_device(moe_ctx* c, int layer, const void* x, const float* resid, flo
                                      c->n_active, c->status, c->perm_cells, c->perm_done, c->s_comp));
     }
     {
-        ProfScope ps(c, kGather, 4.0 * P * H, 0.0);
+        // the method's bytes: each of the T rows read once (L2 serves its k - 1 repeats),
+        // each of the P permuted rows written once
+        ProfScope ps(c, kGather, 2.0 * T * H + 2.0 * P * H, 0.0);
         CUDA_TRY(moe::launch_gather_rows(static_cast<const uint16_t*>(x), c->perm, P, c->k, H, c->x_perm, c->s_comp));
     }
     const int32_t* slot_row = c->slot_dev + static_cast<size_t>(layer) * E;
@@ -997,7 +1023,7 @@ int moe_resident_slot(moe_ctx* c, int layer, int expert) {
 
 int moe_debug_inject(moe_ctx* c, int kind, int count) {
     if (!c) return fail(MOE_E_INVAL, "null context");
-    if (kind < 0 || kind > 3 || count < 0) return fail(MOE_E_INVAL, "bad injection");
+    if (kind < 0 || kind > 4 || count < 0) return fail(MOE_E_INVAL, "bad injection");
     c->inject_kind = kind;
     c->inject_count = kind ? count : 0;
     return MOE_OK;
@@ -1120,7 +1146,9 @@ int moe_layer_forward(moe_ctx* c, int layer, const void* x, const float* resid, 
                                      c->n_active, c->status, c->perm_cells, c->perm_done, c->s_comp));
     }
     {
-        ProfScope ps(c, kGather, 4.0 * P * H, 0.0);
+        // the method's bytes: each of the T rows read once (L2 serves its k - 1 repeats),
+        // each of the P permuted rows written once
+        ProfScope ps(c, kGather, 2.0 * T * H + 2.0 * P * H, 0.0);
         CUDA_TRY(moe::launch_gather_rows(static_cast<const uint16_t*>(x), c->perm, P, c->k, H, c->x_perm, c->s_comp));
     }
     rc = wait_event(c, c->ev_d2h, "routed indices copy");

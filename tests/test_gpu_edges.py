@@ -153,3 +153,31 @@ def test_device_fill_wait_deadline_reports_and_recovers():
         assert np.array_equal(idx, idx_o)
         ref = oracle.moe_layer([ents(0, e_) for e_ in range(W.E)], W.H, W.I, x2, resid, idx_o, w_o)
         hz.assert_out_close(out, ref, resid)
+
+
+def test_fill_failing_after_its_copy_evicts_the_overwritten_entry():
+    """A fill whose copy was already enqueued when it failed (an injected fill-flag write error)
+    leaves neither the old nor the new entry resident in that slot: the old entry's bytes are
+    being overwritten, so a later hit on it must not read the slot. The next forward refills
+    what it needs and matches the oracle."""
+    ents = hz.OracleEntries(W)
+    with hz.make_cache(W, max_tokens=8, capacity=4) as c:
+        c.cache_fill(0, np.array([1, 2, 3, 4]), moe.MOE_FILL_DEMAND)
+        c.sync()
+        assert [c.resident_slot(0, e) for e in (1, 2, 3, 4)] == [0, 1, 2, 3]
+        c.debug_inject(4, 1)
+        with pytest.raises(moe.MoeError) as e:
+            c.cache_fill(0, np.array([9]), moe.MOE_FILL_DEMAND)  # evicts expert 1 from slot 0
+        assert e.value.code == moe.MOE_E_CUDA
+        c.sync()
+        assert c.resident_slot(0, 1) == -1 and c.resident_slot(0, 9) == -1
+        assert [c.resident_slot(0, e) for e in (2, 3, 4)] == [1, 2, 3]
+        c.cache_fill(0, np.array([1]), moe.MOE_FILL_DEMAND)  # the freed slot is taken first
+        c.sync()
+        assert c.resident_slot(0, 1) == 0
+        x = mi.activations(0, 7, 8, W.H)
+        idx, w, out, resid, Wr, b = _layer(c, x, 8)
+        idx_o, w_o, _, _ = oracle.route(x, Wr, b, W.k)
+        assert np.array_equal(idx, idx_o)
+        ref = oracle.moe_layer([ents(0, e_) for e_ in range(W.E)], W.H, W.I, x, resid, idx_o, w_o)
+        hz.assert_out_close(out, ref, resid)

@@ -70,6 +70,5 @@ def test_prefill_layer_full_size():
                                            rng.choice(on_big, 20, replace=False)]))
         ref = oracle.moe_layer_rows(ents.layer(0), W.H, W.I, x[sample], resid[sample], idx_o[sample], w_o[sample])
         hz.assert_out_close(out[sample], ref, resid[sample])
-        # h for one sampled pair, straight from the grouped GEMM's SwiGLU epilogue
         st = cache.stats()
         assert st["expert_reads"] == len(np.unique(idx_o))
