@@ -63,8 +63,9 @@ def parse_args():
     ap.add_argument("--only-prefill", action="store_true", help="profiling cases: run the prefill leg alone")
     ap.add_argument("--prefill-tokens", type=int, default=4096)
     ap.add_argument("--prefill-experts", type=int, default=0, help="fewer experts for profiling cases")
-    ap.add_argument("--format", choices=["bf16", "mxfp4"], default="bf16",
-                    help="expert weight format in the pool and the cache (mxfp4: 4-bit entries, 17/64 of the bytes)")
+    ap.add_argument("--format", choices=["bf16", "mxfp4", "nvfp4"], default="bf16",
+                    help="expert weight format in the pool and the cache (mxfp4: 4-bit entries with an E8M0 scale "
+                         "per 32, 17/64 of the bytes; nvfp4: an E4M3 scale per 16 and a tensor scale, 9/32)")
     ap.add_argument("--policy", choices=["host", "device"], default="host",
                     help="host: LRU on the host (one sync per forward); device: LRU and fills on the GPU, the "
                          "whole decode step captured in a CUDA graph and replayed")
@@ -161,14 +162,19 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------- workload
-def fill_pool(cache, W, L: int, E: int, fp4: bool = False):
+FORMAT_FLAGS = {"bf16": 0, "mxfp4": 16, "nvfp4": 32}  # MOE_MXFP4, MOE_NVFP4
+
+
+def fill_pool(cache, W, L: int, E: int, fmt: str = "bf16"):
     """Seeded entries into the context's pinned pool, generated on the GPU (the same bits as
-    the CPU generator that the oracle uses), bf16 or MXFP4."""
+    the CPU generator that the oracle uses): bf16, MXFP4 or NVFP4."""
     import moe_inputs as mi
     keys = [(l, e) for l in range(L) for e in range(E)]
     ptrs = [cache.host_entry(l, e) for l, e in keys]
-    if fp4:
+    if fmt == "mxfp4":
         mi.gpu_fill_mxfp4_entries(W.seed, keys, W.H, W.I, ptrs)
+    elif fmt == "nvfp4":
+        mi.gpu_fill_nvfp4_entries(W.seed, keys, W.H, W.I, ptrs)
     else:
         mi.gpu_fill_entries(W.seed, keys, W.H, W.I, ptrs)
 
@@ -259,11 +265,12 @@ def run_b300(args, rank, world, local):
     C = args.capacity or W.C
     # per-launch event timing stays off in the timed regions; a separate pass profiles
     device = args.policy == "device"
-    fp4 = args.format == "mxfp4"
-    fmt_flags = moe.MOE_MXFP4 if fp4 else 0
+    fmt = args.format
+    fp4 = fmt != "bf16"
+    fmt_flags = FORMAT_FLAGS[fmt]
     cache = moe.MoeCache(moe.LayerShape(1, W.E, W.H, W.I, W.k, C, max(BATCHES)),
                          flags=(moe.MOE_DEVICE_POLICY if device else 0) | fmt_flags, stream_compute=stream)
-    fill_pool(cache, W, 1, W.E, fp4)
+    fill_pool(cache, W, 1, W.E, fmt)
     if args.prefetch_all:
         cache.cache_fill(0, None, moe.MOE_FILL_FULL_LAYER)
         cache.sync()
@@ -409,7 +416,7 @@ def run_b300(args, rank, world, local):
             c.route(0, xs[s][B], Wr, bias, idx[B], wts[B])
             c.layer_forward(0, xs[s][B], resid[s][B], out[B], idx[B], wts[B])
 
-    res = resident_context(args, W, E=W.E, fp4=fp4)
+    res = resident_context(args, W, E=W.E, fmt=fmt)
     rc = res["cache"]
     for s in range(args.warmup):
         step(rc, s)
@@ -476,12 +483,12 @@ def run_b300(args, rank, world, local):
         "metric": METRIC, "value": round(tokens / (ms_max / 1e3), 2), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "mxfp4 weights, bf16 activations, fp32 accumulate" if fp4 else "bf16",
-        "data": "synthetic (seeded Philox: N(0,0.02) bf16 weights" + (" quantized to MXFP4" if fp4 else "") +
+        "dtype": f"{fmt} weights, bf16 activations, fp32 accumulate" if fp4 else "bf16",
+        "data": "synthetic (seeded Philox: N(0,0.02) bf16 weights" + (f" quantized to {fmt.upper()}" if fp4 else "") +
                 ", N(0,1) activations, Zipf(1.1) router bias)",
         "config": {"workload": "decode layer: hidden 4096, intermediate 1536, 256 experts top-6, "
                                "64-entry LRU cache, batches 1+4+16 per step" +
-                               (", MXFP4 expert entries" if fp4 else ""),
+                               (f", {fmt.upper()} expert entries" if fp4 else ""),
                    "policy": "device (CUDA graph per step)" if device else "host",
                    "tokens_per_step": sum(BATCHES), "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2: each step streams >= 226 MB of expert weights (L2 126 MB)",
@@ -500,7 +507,7 @@ def run_b300(args, rank, world, local):
         "kernels_lru_pass": table(kst_lru),
     }
     if fp4:
-        result["prefill"] = {"skipped": "MXFP4 entries run on the decode kernels; the prefill leg measures the "
+        result["prefill"] = {"skipped": "4-bit entries run on the decode kernels; the prefill leg measures the "
                                         "bf16 grouped GEMM"}
     elif not args.no_prefill:
         result["prefill"] = run_prefill(args, res if not args.prefill_experts else None)
@@ -554,7 +561,7 @@ def run_per_batch(cache, W, Wr, bias, stream, steps: int = PER_BATCH_STEPS, warm
     return res
 
 
-def resident_context(args, W, E=None, fp4: bool = False):
+def resident_context(args, W, E=None, fmt: str = "bf16"):
     """A context holding every expert of the layer (256 entries, 9.66 GB), sized for the prefill
     leg's tokens; shared by the decode roofline pass and the prefill leg."""
     import torch
@@ -564,9 +571,9 @@ def resident_context(args, W, E=None, fp4: bool = False):
     T = max(args.prefill_tokens, max(BATCHES))
     E = E or args.prefill_experts or W.E
     stream = torch.cuda.Stream()
-    cache = moe.MoeCache(moe.LayerShape(1, E, W.H, W.I, W.k, E, T), flags=moe.MOE_MXFP4 if fp4 else 0,
+    cache = moe.MoeCache(moe.LayerShape(1, E, W.H, W.I, W.k, E, T), flags=FORMAT_FLAGS[fmt],
                          stream_compute=stream)
-    fill_pool(cache, W, 1, E, fp4)
+    fill_pool(cache, W, 1, E, fmt)
     cache.cache_fill(0, None, moe.MOE_FILL_FULL_LAYER)
     cache.sync()
     return {"cache": cache, "stream": stream, "E": E, "T": T}

@@ -78,6 +78,16 @@ extern "C" {
  * kernels (MOE_PATH_GEMM is refused); activations stay bf16. Needs inter % 128 == 0 and
  * hidden % 256 == 0 (as for every context). */
 #define MOE_MXFP4 16u
+/* Expert entries in NVFP4: E2M1 weights as in MOE_MXFP4, one FP8 E4M3 scale per 16 consecutive
+ * weights of a row, and one fp32 tensor scale per matrix; a weight's value is
+ * e2m1 * e4m3(block scale) * tensor scale. Same streaming order as MOE_MXFP4, in stages of 4608
+ * bytes (4096 code bytes, then 4 scale bytes per row: block j of a row's 64-column slab takes
+ * code bytes 8j .. 8j+7 and scale byte 4r + j; gate/up stages hold gate scales (64 x 4) then up
+ * scales (64 x 4)), then a 16-byte trailer: the tensor scales of W_gate, W_up, W_down (fp32) and
+ * 4 zero bytes. An entry is 3*hidden*inter*9/16 + 16 bytes. The kernels expand code times block
+ * scale to bf16 on chip (exact: at most six significant bits) and multiply the fp32 accumulator
+ * by the tensor scale; decode kernels only (MOE_PATH_GEMM is refused). Exclusive with MOE_MXFP4. */
+#define MOE_NVFP4 32u
 
 /* ---- fill modes (moe_cache_fill) ---- */
 #define MOE_FILL_DEMAND 0     /* access the distinct experts of the given top-k indices */
@@ -94,6 +104,7 @@ extern "C" {
 #define MOE_EV_PREFETCH_FILL 2 /* whole-layer prefetch copied the entry in */
 #define MOE_EV_PREFETCH_HIT 3  /* whole-layer prefetch found the entry resident */
 #define MOE_EV_RESIZE_EVICT 4  /* moe_cache_resize evicted the entry (slot = the slot it held) */
+#define MOE_EV_HOST_EXEC 5     /* q-star simulation: a miss executed on the host (not filled; slot -1) */
 
 typedef struct moe_ctx moe_ctx; /* opaque: pinned pool, slot arena, LRU, streams, scratch */
 
@@ -105,7 +116,7 @@ typedef struct {
     int32_t top_k;       /* k */
     int32_t capacity;    /* C: cache slots, in whole entries */
     int32_t max_tokens;  /* largest T passed to moe_route / moe_layer_forward */
-    uint32_t flags;      /* MOE_TRACE | MOE_PROFILE | MOE_PREFILL_DB | MOE_DEVICE_POLICY | MOE_MXFP4 */
+    uint32_t flags;      /* MOE_TRACE | MOE_PROFILE | MOE_PREFILL_DB | MOE_DEVICE_POLICY | MOE_MXFP4 | MOE_NVFP4 */
     uint64_t trace_capacity; /* events kept by MOE_TRACE (0: 1<<20) */
 } moe_config_t;
 
@@ -183,7 +194,8 @@ void* moe_host_entry(moe_ctx* ctx, int layer, int expert);
  */
 int moe_cache_resize(moe_ctx* ctx, int new_capacity);
 
-/* Bytes of one entry: 3 * hidden * inter * 2 (bf16), or 3 * hidden * inter * 17/32 (MOE_MXFP4). */
+/* Bytes of one entry: 3 * hidden * inter * 2 (bf16), 3 * hidden * inter * 17/32 (MOE_MXFP4), or
+ * 3 * hidden * inter * 9/16 + 16 (MOE_NVFP4). */
 uint64_t moe_entry_bytes(const moe_ctx* ctx);
 
 /*
@@ -358,6 +370,70 @@ int moe_debug_read(moe_ctx* ctx, int what, void* host_dst, uint64_t bytes);
 #define MOE_NOALLOC_MAX_LOGITS 65536
 int moe_route_noalloc(const void* x_bf16, int T, int hidden, int num_experts, int top_k, const float* router_w,
                       const float* router_b, int32_t* topk_idx, float* topk_w, void* cuda_stream);
+
+/* ---- q-star: bandwidth-adaptive split of cache misses between fills and host execution ----
+ *
+ * Source: "FreeToken benchmark" (freetoken.wiki/performance), "How FreeToken Serves Large MoE
+ * Models" -- misses are divided between GPU cache fills and direct CPU execution by the q-star
+ * policy, which profiles host-side expert bandwidth and PCIe transfer bandwidth ("Adaptive
+ * Misses"); "FreeToken rtx 4090" (freetoken.wiki/hardware), "Measure the Machine" and its tuning
+ * table. The pages give no formula; this library's reading: a layer's miss time is
+ * max(n_fill / B_pcie, n_host / B_host) * entry bytes (the link and the host cores work side by
+ * side), smallest at the fill fraction q* = B_pcie / (B_pcie + B_host); ties go to more fills (a
+ * fill also serves later hits). The misses with the most routed tokens fill first (ties: lower
+ * expert id). These calls measure, decide and simulate; moe_layer_forward never executes an
+ * expert on the host.
+ */
+
+typedef struct {
+    double pcie_h2d_gbps;    /* pinned host -> device copies of whole entries (copy stream) */
+    double host_expert_gbps; /* entry bytes / time of moe_host_expert_ffn on one token (0: not measured,
+                                e.g. 4-bit entries) */
+    int32_t host_threads;    /* threads the host expert FFN used */
+    int32_t pad;
+    double entry_bytes;
+} moe_bandwidth_t;
+
+/* Measure both bandwidths on this context's pool and device: `reps` timed copies of entry (0, 0)
+ * into a temporary device buffer (cudaMalloc'd for the call), and `reps` host expert FFNs on it
+ * with one token and host_threads threads (bf16 contexts only). Waits for its own work.
+ * Errors: MOE_E_INVAL, MOE_E_NOMEM, MOE_E_CUDA. */
+int moe_measure_bandwidth(moe_ctx* ctx, int host_threads, int reps, moe_bandwidth_t* out);
+
+/* Expert FFN on the host cores, fp32 arithmetic: y[t] = W_down (silu(W_gate x_t) * (W_up x_t)) for
+ * n_tok tokens, weights read from a bf16 entry in host memory (the entry layout above),
+ * x_bf16 [n_tok x hidden] host bf16, y [n_tok x hidden] host fp32, `threads` worker threads.
+ * Needs hidden % 16 == 0 and inter % 16 == 0. Errors: MOE_E_INVAL. */
+int moe_host_expert_ffn(const void* entry_bf16, int hidden, int inter, const void* x_bf16, int n_tok, float* y,
+                        int threads);
+
+/* Number of a layer's n_miss misses to fill under the q-star rule for the given bandwidths
+ * (host_gbps == 0: all; pcie_gbps == 0: none). Returns the count (>= 0) or MOE_E_INVAL. */
+int moe_qstar_fills(double pcie_gbps, double host_gbps, int n_miss);
+
+typedef struct {
+    uint64_t expert_reads; /* routed accesses (distinct experts per invocation) */
+    uint64_t hits;         /* resident when accessed */
+    uint64_t fills;        /* misses filled (they enter the LRU) */
+    uint64_t host_execs;   /* misses executed on the host (the LRU does not see them) */
+    uint64_t evictions;
+    uint64_t events;       /* events written */
+    double modeled_ms;     /* sum over invocations of max(link, host) + GPU streaming time */
+    double link_ms, host_ms;
+} moe_qstar_sim_t;
+
+/* Host-only run of the LRU under the q-star split (no GPU, no context). Invocation v (one layer
+ * forward) holds accesses inv_offsets[v] .. inv_offsets[v+1]-1: (layer, expert, routed token
+ * count), the distinct experts of that forward in ascending id. Per invocation: the misses at
+ * its start are split -- q in [0, 1]: round(q * n_miss) fill; q < 0: moe_qstar_fills(pcie, host)
+ * -- the fills in the order above; then the accesses run in order through the LRU, except the
+ * host-executed ones (event MOE_EV_HOST_EXEC). Modeled time per invocation: max(n_fill * entry /
+ * B_pcie, n_host * entry / B_host) + (n_hit + n_fill) * entry / B_hbm. events may be NULL.
+ * Returns the number of events written, or MOE_E_INVAL. */
+int moe_qstar_simulate(int capacity, int n_inv, const int32_t* inv_offsets, const int32_t* layer,
+                       const int32_t* expert, const int32_t* n_tok, double q, double pcie_gbps, double host_gbps,
+                       double hbm_gbps, double entry_bytes, moe_qstar_sim_t* out, moe_event_t* events,
+                       uint64_t events_cap);
 
 #ifdef __cplusplus
 }

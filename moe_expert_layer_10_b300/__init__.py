@@ -19,16 +19,17 @@ LIB_PATH = os.path.join(PKG, "libmoe_b300.so")
 HEADER = os.path.join(os.path.dirname(PKG), "include", "moe.h")
 
 MOE_OK, MOE_E_INVAL, MOE_E_NOMEM, MOE_E_CUDA, MOE_E_TIMEOUT, MOE_E_CAPACITY, MOE_E_DEVICE = 0, -1, -2, -3, -4, -5, -6
-MOE_TRACE, MOE_PROFILE, MOE_PREFILL_DB, MOE_DEVICE_POLICY, MOE_MXFP4 = 1, 2, 4, 8, 16
+MOE_TRACE, MOE_PROFILE, MOE_PREFILL_DB, MOE_DEVICE_POLICY, MOE_MXFP4, MOE_NVFP4 = 1, 2, 4, 8, 16, 32
 MOE_FILL_DEMAND, MOE_FILL_FULL_LAYER = 0, 1
 MOE_PATH_AUTO, MOE_PATH_GEMV, MOE_PATH_GEMM = 0, 1, 2
-EV_HIT, EV_FILL, EV_PREFETCH_FILL, EV_PREFETCH_HIT, EV_RESIZE_EVICT = 0, 1, 2, 3, 4
+EV_HIT, EV_FILL, EV_PREFETCH_FILL, EV_PREFETCH_HIT, EV_RESIZE_EVICT, EV_HOST_EXEC = 0, 1, 2, 3, 4, 5
 
 # every symbol include/moe.h declares
 EXPORTS = ["moe_cache_init", "moe_cache_destroy", "moe_host_entry", "moe_entry_bytes", "moe_route",
            "moe_route_forced", "moe_cache_fill", "moe_layer_forward", "moe_stats", "moe_last_error",
            "moe_set_path", "moe_set_profile", "moe_sync", "moe_resident_slot", "moe_kernel_stats", "moe_lru_simulate",
-           "moe_debug_inject", "moe_debug_read", "moe_route_noalloc", "moe_cache_resize"]
+           "moe_debug_inject", "moe_debug_read", "moe_route_noalloc", "moe_cache_resize", "moe_measure_bandwidth",
+           "moe_host_expert_ffn", "moe_qstar_fills", "moe_qstar_simulate"]
 MOE_NOALLOC_MAX_LOGITS = 65536
 MOE_DBG_OFFSETS, MOE_DBG_PERM, MOE_DBG_INV_PERM, MOE_DBG_ACTIVE, MOE_DBG_N_ACTIVE, MOE_DBG_SLOT_TABLE, \
     MOE_DBG_H_PERM = range(7)
@@ -60,6 +61,20 @@ class Stats(ctypes.Structure):
 class Event(ctypes.Structure):
     _fields_ = [("kind", ctypes.c_int32), ("layer", ctypes.c_int32), ("expert", ctypes.c_int32),
                 ("slot", ctypes.c_int32), ("ev_layer", ctypes.c_int32), ("ev_expert", ctypes.c_int32)]
+
+
+class Bandwidth(ctypes.Structure):
+    _fields_ = [("pcie_h2d_gbps", ctypes.c_double), ("host_expert_gbps", ctypes.c_double),
+                ("host_threads", ctypes.c_int32), ("pad", ctypes.c_int32), ("entry_bytes", ctypes.c_double)]
+
+
+class QstarSim(ctypes.Structure):
+    _fields_ = [("expert_reads", ctypes.c_uint64), ("hits", ctypes.c_uint64), ("fills", ctypes.c_uint64),
+                ("host_execs", ctypes.c_uint64), ("evictions", ctypes.c_uint64), ("events", ctypes.c_uint64),
+                ("modeled_ms", ctypes.c_double), ("link_ms", ctypes.c_double), ("host_ms", ctypes.c_double)]
+
+    def as_dict(self):
+        return {f: getattr(self, f) for f, _ in self._fields_}
 
 
 class KernelStat(ctypes.Structure):
@@ -102,6 +117,12 @@ def lib():
     L.moe_debug_inject.argtypes = [vp, i32, i32]
     L.moe_debug_read.argtypes = [vp, i32, vp, u64]
     L.moe_route_noalloc.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp, vp, vp]
+    dbl = ctypes.c_double
+    L.moe_measure_bandwidth.argtypes = [vp, i32, i32, ctypes.POINTER(Bandwidth)]
+    L.moe_host_expert_ffn.argtypes = [vp, i32, i32, vp, i32, vp, i32]
+    L.moe_qstar_fills.argtypes = [dbl, dbl, i32]
+    L.moe_qstar_simulate.argtypes = [i32, i32, vp, vp, vp, vp, dbl, dbl, dbl, dbl, dbl, ctypes.POINTER(QstarSim),
+                                     vp, u64]
     _lib = L
     return L
 
@@ -157,6 +178,49 @@ def route_noalloc(x, router_w, router_b, topk_idx, topk_w, top_k: int, stream=No
     T = x.shape[0] if T is None else T
     _check(lib().moe_route_noalloc(_ptr(x), T, x.shape[1], router_w.shape[0], top_k, _ptr(router_w), _ptr(router_b),
                                    _ptr(topk_idx), _ptr(topk_w), _stream_handle(stream)), "moe_route_noalloc")
+
+
+def host_expert_ffn(entry_bf16, hidden: int, inter: int, x_bf16, threads: int = 1):
+    """moe_host_expert_ffn: the expert FFN on the host cores (numpy uint16 entry and tokens [n x hidden]);
+    returns fp32 [n x hidden]."""
+    import numpy as np
+    e = np.ascontiguousarray(entry_bf16, dtype=np.uint16)
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16).reshape(-1, hidden)
+    y = np.empty((x.shape[0], hidden), dtype=np.float32)
+    _check(lib().moe_host_expert_ffn(e.ctypes.data, hidden, inter, x.ctypes.data, x.shape[0], y.ctypes.data, threads),
+           "moe_host_expert_ffn")
+    return y
+
+
+def qstar_fills(pcie_gbps: float, host_gbps: float, n_miss: int) -> int:
+    """moe_qstar_fills: how many of n_miss misses fill under the q-star split."""
+    return _check(lib().moe_qstar_fills(float(pcie_gbps), float(host_gbps), int(n_miss)), "moe_qstar_fills")
+
+
+def qstar_simulate(capacity: int, invocations, q: float, pcie_gbps: float, host_gbps: float, hbm_gbps: float,
+                   entry_bytes: float, want_events: bool = False):
+    """moe_qstar_simulate on a list of invocations, each a list of (layer, expert, n_tok) in
+    ascending expert id. q < 0 uses the bandwidth rule. Returns (summary dict, events or None)."""
+    import numpy as np
+    offs = np.zeros(len(invocations) + 1, np.int32)
+    rows = []
+    for v, inv in enumerate(invocations):
+        rows += list(inv)
+        offs[v + 1] = len(rows)
+    a = np.array(rows, np.int32).reshape(-1, 3) if rows else np.zeros((0, 3), np.int32)
+    lay, exp_, ntk = (np.ascontiguousarray(a[:, i]) for i in range(3))
+    s = QstarSim()
+    cap = len(rows) + 1 if want_events else 0
+    ev = (Event * cap)() if want_events else None
+    got = _check(lib().moe_qstar_simulate(capacity, len(invocations), offs.ctypes.data, lay.ctypes.data,
+                                          exp_.ctypes.data, ntk.ctypes.data, float(q), float(pcie_gbps),
+                                          float(host_gbps), float(hbm_gbps), float(entry_bytes), ctypes.byref(s),
+                                          ctypes.addressof(ev) if want_events else None, cap), "moe_qstar_simulate")
+    events = None
+    if want_events:
+        events = np.array([[ev[i].kind, ev[i].layer, ev[i].expert, ev[i].slot, ev[i].ev_layer, ev[i].ev_expert]
+                           for i in range(got)], dtype=np.int32).reshape(got, 6)
+    return s.as_dict(), events
 
 
 @dataclass
@@ -285,6 +349,13 @@ class MoeCache:
             return s.as_dict(), tr
         _check(lib().moe_stats(self._h, ctypes.byref(s), None, 0, int(reset)), "moe_stats")
         return s.as_dict()
+
+    def measure_bandwidth(self, host_threads: int, reps: int = 5):
+        """moe_measure_bandwidth: pinned H2D and host expert-FFN bandwidth (GB/s) on entry (0, 0)."""
+        b = Bandwidth()
+        _check(lib().moe_measure_bandwidth(self._h, host_threads, reps, ctypes.byref(b)), "moe_measure_bandwidth")
+        return {"pcie_h2d_gbps": b.pcie_h2d_gbps, "host_expert_gbps": b.host_expert_gbps,
+                "host_threads": b.host_threads, "entry_bytes": b.entry_bytes}
 
     def kernel_stats(self, reset: bool = False):
         arr = (KernelStat * 16)()

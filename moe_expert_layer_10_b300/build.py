@@ -26,12 +26,20 @@ def _headers():
         glob.glob(os.path.join(ROOT, "include", "*.h"))
 
 
+CXX = os.environ.get("CXX", "g++")
+# host-only sources (the host expert FFN): g++, multi-versioned for the CPU's instruction set
+CXXFLAGS = ["-O3", "-std=c++17", "-fPIC", "-Wall", "-pthread", "-fno-fast-math", "-I", os.path.join(ROOT, "include")]
+
+
 def _compile(src: str, verbose: bool) -> str:
     obj = os.path.join(OBJ, os.path.basename(src) + ".o")
     newest_dep = max(os.path.getmtime(p) for p in [src] + _headers())
     if os.path.exists(obj) and os.path.getmtime(obj) >= newest_dep:
         return obj
-    cmd = [NVCC] + FLAGS + (["-Xptxas", "-v"] if verbose else []) + ["-c", src, "-o", obj + ".tmp"]
+    if src.endswith(".cpp"):
+        cmd = [CXX] + CXXFLAGS + ["-c", src, "-o", obj + ".tmp"]
+    else:
+        cmd = [NVCC] + FLAGS + (["-Xptxas", "-v"] if verbose else []) + ["-c", src, "-o", obj + ".tmp"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
@@ -43,7 +51,7 @@ def _compile(src: str, verbose: bool) -> str:
 
 def build(force: bool = False, verbose: bool = False) -> str:
     os.makedirs(OBJ, exist_ok=True)
-    srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
     if force:
         for o in glob.glob(os.path.join(OBJ, "*.o")):
             os.remove(o)
@@ -53,7 +61,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
         return LIB
     tmp = LIB + f".tmp{os.getpid()}"
     cmd = [NVCC] + ARCH + ["-shared", "-cudart", "shared", "-o", tmp] + objs + \
-        ["-Xlinker", "-rpath,/usr/local/cuda/lib64"]
+        ["-Xlinker", "-rpath,/usr/local/cuda/lib64", "-lpthread"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

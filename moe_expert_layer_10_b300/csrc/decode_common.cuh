@@ -43,19 +43,29 @@ __device__ __forceinline__ int atomic_add_acq_rel_gpu(int* p, int v) {
     return old;
 }
 
+// Per-matrix fp32 scales that multiply the accumulator before the epilogue's arithmetic (the
+// tensor scales of NVFP4 entries): the last 16 bytes of each entry hold the scales of W_gate,
+// W_up and W_down. None for bf16 and MXFP4 entries.
+struct TensorScales {
+    const uint8_t* arena = nullptr;  // slot s's entry starts at arena + s * entry_bytes
+    uint64_t entry_bytes = 0;
+    const int32_t* slot_row = nullptr;
+};
+
 // The epilogue role: four consecutive warps (TMEM lane quadrant = warp % 4), named barrier 1
 // over their 128 threads, leader_tid = the first of them. Per unit: wait for the accumulator
 // (one thread waits, the outcome is shared), then either write the split's partial and arrive
 // on the tile counter, or (single split / last split) produce h = silu(g)*u (gate/up) or
-// pair_out = w_p * y (down) for the chunk's tokens.
-template <bool GATEUP>
+// pair_out = w_p * y (down) for the chunk's tokens. With TSCALE the (summed) accumulator of a
+// row is first multiplied by its matrix's tensor scale.
+template <bool GATEUP, bool TSCALE = false>
 __device__ __forceinline__ void decode_epilogue(uint64_t* acc_full, uint64_t* acc_empty, int* sh_ok, int* sh_last,
                                                 uint32_t tmem, float* xchg, const GemvWork* __restrict__ work,
                                                 int n_work, int n_units, int S, int R, int H, int I,
                                                 uint16_t* __restrict__ h_out, const float* __restrict__ w_perm,
                                                 float* __restrict__ pair_out, float* __restrict__ ws,
                                                 int* __restrict__ cnt, int* status, uint64_t consumer_wait_ns,
-                                                int leader_tid) {
+                                                int leader_tid, TensorScales tsc = TensorScales{}) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     struct {
         uint64_t *acc_full, *acc_empty;
@@ -112,6 +122,14 @@ __device__ __forceinline__ void decode_epilogue(uint64_t* acc_full, uint64_t* ac
             }
             from_ws = true;
         }
+        float tscale = 1.0f;  // this row's tensor scale (gate rows, up rows, or W_down rows)
+        if (TSCALE) {
+            int slot = tsc.slot_row[wk.expert];
+            if (slot < 0) slot = 0;  // the producer raised the status; results are discarded
+            const float* ts = reinterpret_cast<const float*>(tsc.arena + static_cast<uint64_t>(slot) * tsc.entry_bytes +
+                                                             tsc.entry_bytes - 16);
+            tscale = __ldg(ts + (GATEUP ? (q >= 2 ? 1 : 0) : 2));
+        }
         const float* ws0 = ws + static_cast<size_t>(u - un.split) * tile_floats;
         // 16 accumulator columns of this thread's row: TMEM, or the sum of the S partials
         auto fetch = [&](int c, float (&v)[16]) {
@@ -129,6 +147,10 @@ __device__ __forceinline__ void decode_epilogue(uint64_t* acc_full, uint64_t* ac
                 tmem_ld_wait();
 #pragma unroll
                 for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+            }
+            if (TSCALE) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) v[j] *= tscale;
             }
         };
         auto release = [&]() {

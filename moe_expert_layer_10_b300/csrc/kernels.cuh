@@ -110,9 +110,12 @@ cudaError_t launch_decode_down(const DecodeMaps& maps, const GemvWork* work, int
                                float* pair_out, float* ws, int* cnt, int* status, uint64_t fill_wait_ns, int num_sms,
                                cudaStream_t st);
 
-// --- decode expert FFN with MXFP4 entries (expanded to bf16 on chip; decode_fp4.cu) ---
-// Same work lists, splits and epilogues as the bf16 kernels; dyn as for the _dyn launchers.
-cudaError_t launch_decode_fp4(bool gateup, const DecodeMaps& maps, const uint8_t* arena, uint64_t entry_bytes,
+// --- decode expert FFN with 4-bit entries (expanded to bf16 on chip; decode_fp4.cu) ---
+// fmt: kFp4Mx (MXFP4: E8M0 scale per 32 weights) or kFp4Nv (NVFP4: E4M3 scale per 16 weights
+// and an fp32 tensor scale per matrix, in the entry's last 16 bytes). Same work lists, splits
+// and epilogues as the bf16 kernels; dyn as for the _dyn launchers.
+enum : int { kFp4Mx = 1, kFp4Nv = 2 };
+cudaError_t launch_decode_fp4(int fmt, bool gateup, const DecodeMaps& maps, const uint8_t* arena, uint64_t entry_bytes,
                               const GemvWork* work, int n_work, int n_units, int S, const int* dyn,
                               const int32_t* slot_row, const uint32_t* fill_flag, int H, int I, uint16_t* h_perm,
                               const float* w_perm, float* pair_out, float* ws, int* cnt, int* status,

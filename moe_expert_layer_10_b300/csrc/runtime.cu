@@ -149,7 +149,8 @@ struct moe_ctx {
     int L = 0, E = 0, H = 0, I = 0, k = 0, C = 0, Tmax = 0, Pmax = 0;
     size_t entry_elems = 0, entry_bytes = 0;
     int path = MOE_PATH_AUTO;
-    bool fp4 = false;  // MXFP4 entries (MOE_MXFP4)
+    bool fp4 = false;  // 4-bit entries (MOE_MXFP4 or MOE_NVFP4)
+    int fp4_fmt = 0;   // moe::kFp4Mx or moe::kFp4Nv when fp4
 
     uint16_t* pool = nullptr;   // pinned host, L*E entries
     uint16_t* arena = nullptr;  // device, C entries
@@ -474,7 +475,7 @@ int access_keys(moe_ctx* c, const std::vector<int>& keys, bool prefetch) {
 // TMA views of the slot arena (they change when the arena is reallocated).
 bool make_arena_maps(moe_ctx* c) {
     const uint64_t H = c->H, I = c->I, C = c->C;
-    if (c->fp4) return true;  // MXFP4 stages are fetched with plain bulk copies
+    if (c->fp4) return true;  // 4-bit stages are fetched with plain bulk copies
     return make_map(&c->dec_maps.a_gu, c->arena, H, C * 3 * I, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
            make_map(&c->dec_maps.a_d, c->arena, I, C * 3 * H, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) &&
            make_map(&c->gemm_maps.b_gu, c->arena, H, C * 3 * I, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) &&
@@ -533,7 +534,7 @@ namespace {
 cudaError_t run_gateup(moe_ctx* c, const GemvWork* work, int n_work, int n_units, int S, const int* dyn,
                        const int32_t* slot_row, uint64_t fill_wait_ns) {
     if (c->fp4)
-        return moe::launch_decode_fp4(true, c->dec_maps, reinterpret_cast<const uint8_t*>(c->arena), c->entry_bytes,
+        return moe::launch_decode_fp4(c->fp4_fmt, true, c->dec_maps, reinterpret_cast<const uint8_t*>(c->arena), c->entry_bytes,
                                       work, n_work, n_units, S, dyn, slot_row, c->fill_flag, c->H, c->I, c->h_perm,
                                       nullptr, nullptr, c->dec_ws, c->dec_cnt, c->status, fill_wait_ns, c->num_sms,
                                       c->s_comp);
@@ -547,7 +548,7 @@ cudaError_t run_gateup(moe_ctx* c, const GemvWork* work, int n_work, int n_units
 cudaError_t run_down(moe_ctx* c, const GemvWork* work, int n_work, int n_units, int S, const int* dyn,
                      const int32_t* slot_row, uint64_t fill_wait_ns) {
     if (c->fp4)
-        return moe::launch_decode_fp4(false, c->dec_maps, reinterpret_cast<const uint8_t*>(c->arena), c->entry_bytes,
+        return moe::launch_decode_fp4(c->fp4_fmt, false, c->dec_maps, reinterpret_cast<const uint8_t*>(c->arena), c->entry_bytes,
                                       work, n_work, n_units, S, dyn, slot_row, c->fill_flag, c->H, c->I, nullptr,
                                       c->w_perm, c->pair_out, c->dec_ws, c->dec_cnt, c->status, fill_wait_ns,
                                       c->num_sms, c->s_comp);
@@ -559,8 +560,12 @@ cudaError_t run_down(moe_ctx* c, const GemvWork* work, int n_work, int n_units, 
                                    c->s_comp);
 }
 
-// Bytes of one weight as stored: 2 (bf16) or 17/32 (E2M1 half byte plus a scale per 32).
-double weight_bytes(const moe_ctx* c) { return c->fp4 ? 17.0 / 32.0 : 2.0; }
+// Bytes of one weight as stored: 2 (bf16), 17/32 (MXFP4: E2M1 half byte plus a scale per 32) or
+// 9/16 (NVFP4: a scale per 16; the 16-byte tensor-scale trailer is not counted).
+double weight_bytes(const moe_ctx* c) {
+    if (!c->fp4) return 2.0;
+    return c->fp4_fmt == moe::kFp4Nv ? 9.0 / 16.0 : 17.0 / 32.0;
+}
 
 // The device policy on one key set, then the fills it chose on the copy stream (forked from
 // and, when `join`, joined back into the compute stream). No host wait: capturable.
@@ -713,6 +718,8 @@ int moe_cache_init(const moe_config_t* cfg, void* stream_compute, void* stream_c
         f.max_tokens < 1)
         return fail(MOE_E_INVAL, "shape outside the limits (hidden %% 256, inter %% 128, 1 <= k <= min(E, 32), "
                                  "E <= 1024, max_tokens >= 1)");
+    if ((f.flags & MOE_MXFP4) && (f.flags & MOE_NVFP4))
+        return fail(MOE_E_INVAL, "MOE_MXFP4 and MOE_NVFP4 are exclusive");
     if (f.capacity < 1) return fail(MOE_E_CAPACITY, "capacity must be >= 1");
     if ((f.flags & MOE_PREFILL_DB) && f.capacity < 2 * f.num_experts)
         return fail(MOE_E_CAPACITY, "double buffering needs capacity >= 2 * num_experts (%d < %d)", f.capacity,
@@ -735,9 +742,13 @@ int moe_cache_init(const moe_config_t* cfg, void* stream_compute, void* stream_c
     c->C = f.capacity;
     c->Tmax = f.max_tokens;
     c->Pmax = f.max_tokens * f.top_k;
-    c->fp4 = (f.flags & MOE_MXFP4) != 0;
-    // bf16: 2 bytes per weight; MXFP4: E2M1 halves plus one scale byte per 32 weights
-    c->entry_bytes = c->fp4 ? entry_elems / 2 + entry_elems / 32 : entry_elems * 2;
+    c->fp4 = (f.flags & (MOE_MXFP4 | MOE_NVFP4)) != 0;
+    c->fp4_fmt = (f.flags & MOE_NVFP4) ? moe::kFp4Nv : ((f.flags & MOE_MXFP4) ? moe::kFp4Mx : 0);
+    // bf16: 2 bytes per weight; MXFP4: E2M1 halves plus one scale byte per 32 weights; NVFP4:
+    // E2M1 halves, one scale byte per 16 weights and a 16-byte trailer of tensor scales
+    if (!c->fp4) c->entry_bytes = entry_elems * 2;
+    else if (c->fp4_fmt == moe::kFp4Mx) c->entry_bytes = entry_elems / 2 + entry_elems / 32;
+    else c->entry_bytes = entry_elems / 2 + entry_elems / 16 + 16;
     c->entry_elems = c->entry_bytes / 2;  // 16-bit units (pool and arena pointers are uint16_t)
     c->lru.reset(c->C, static_cast<int>(keys));
     c->slot_host.assign(keys, -1);
@@ -1176,7 +1187,7 @@ int moe_layer_forward(moe_ctx* c, int layer, const void* x, const float* resid, 
     const int U = static_cast<int>(distinct.size());
     int path = c->path;
     if (c->fp4 && path == MOE_PATH_GEMM)
-        return fail(MOE_E_INVAL, "MXFP4 entries run on the decode kernels only (MOE_PATH_GEMM unsupported)");
+        return fail(MOE_E_INVAL, "4-bit entries run on the decode kernels only (MOE_PATH_GEMM unsupported)");
     if (path == MOE_PATH_AUTO) path = (c->fp4 || max_n <= kDecodeMaxTokens) ? MOE_PATH_GEMV : MOE_PATH_GEMM;
 
     // 4. waves of at most C experts
@@ -1419,6 +1430,58 @@ int moe_debug_read(moe_ctx* c, int what, void* dst, uint64_t bytes) {
     int rc = moe_sync(c);
     if (rc) return rc;
     CUDA_TRY(cudaMemcpy(dst, src, bytes, cudaMemcpyDeviceToHost));
+    return MOE_OK;
+}
+
+int moe_measure_bandwidth(moe_ctx* c, int host_threads, int reps, moe_bandwidth_t* out) {
+    g_last_error.clear();
+    if (!c || !out || host_threads < 1 || reps < 1) return fail(MOE_E_INVAL, "bad arguments");
+    CUDA_TRY(cudaSetDevice(c->dev));
+    *out = moe_bandwidth_t{};
+    out->entry_bytes = static_cast<double>(c->entry_bytes);
+    out->host_threads = host_threads;
+    // pinned host -> device: whole-entry copies on the copy stream, into a scratch buffer
+    void* scratch = nullptr;
+    cudaError_t e = cudaMalloc(&scratch, c->entry_bytes);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(MOE_E_NOMEM, "bandwidth probe buffer: %s", cudaGetErrorString(e));
+    }
+    cudaEvent_t e0 = pool_event(c), e1 = pool_event(c);
+    int rc = MOE_OK;
+    if (!e0 || !e1) rc = fail(MOE_E_CUDA, "event creation failed");
+    for (int i = 0; i <= reps && rc == MOE_OK; ++i) {  // copy 0 warms up, the next reps are timed
+        if (i == 1 && cudaEventRecord(e0, c->s_copy) != cudaSuccess) rc = fail(MOE_E_CUDA, "event record");
+        if (rc == MOE_OK && cudaMemcpyAsync(scratch, c->pool, c->entry_bytes, cudaMemcpyHostToDevice, c->s_copy) !=
+                                cudaSuccess)
+            rc = fail(MOE_E_CUDA, "probe copy failed");
+    }
+    if (rc == MOE_OK && cudaEventRecord(e1, c->s_copy) != cudaSuccess) rc = fail(MOE_E_CUDA, "event record");
+    if (rc == MOE_OK) rc = wait_event(c, e1, "bandwidth probe");
+    if (rc == MOE_OK) {
+        float ms = 0.f;
+        cudaEventElapsedTime(&ms, e0, e1);
+        out->pcie_h2d_gbps = ms > 0.f ? reps * static_cast<double>(c->entry_bytes) / (ms * 1e-3) / 1e9 : 0.0;
+    }
+    if (e0) c->ev_pool.push_back(e0);
+    if (e1) c->ev_pool.push_back(e1);
+    cudaFree(scratch);
+    if (rc) return rc;
+    // host expert FFN on entry (0, 0) with one token (bf16 entries only)
+    if (!c->fp4) {
+        std::vector<uint16_t> x(c->H, 0x3f80);  // 1.0
+        std::vector<float> y(c->H);
+        std::vector<double> t;
+        for (int i = 0; i <= reps; ++i) {
+            const auto t0 = std::chrono::steady_clock::now();
+            rc = moe_host_expert_ffn(c->pool, c->H, c->I, x.data(), 1, y.data(), host_threads);
+            if (rc) return rc;
+            if (i > 0) t.push_back(std::chrono::duration<double>(std::chrono::steady_clock::now() - t0).count());
+        }
+        std::sort(t.begin(), t.end());
+        const double med = t[t.size() / 2];
+        out->host_expert_gbps = med > 0 ? static_cast<double>(c->entry_bytes) / med / 1e9 : 0.0;
+    }
     return MOE_OK;
 }
 

@@ -64,7 +64,7 @@ def build(force: bool = False) -> str:
             subprocess.check_call(["gcc", "-O2", "-ffp-contract=off", "-fopenmp", "-shared", "-fPIC", "-std=c11"] +
                                   extra + [_SRC, "-o", tmp, "-lm"])
             os.replace(tmp, so)
-    if os.path.exists(_NVCC) and (force or _stale(_GPU_SO, _GPU_SRC, _CORE, _CORE_FP4)):
+    if os.path.exists(_NVCC) and (force or _stale(_GPU_SO, _GPU_SRC, _CORE, _CORE_FP4, _CORE_NVFP4)):
         tmp = _GPU_SO + f".tmp{os.getpid()}"
         subprocess.check_call([_NVCC, "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-fmad=false",
                                "-std=c++17", "-shared", "-Xcompiler", "-fPIC", "-Xcompiler", "-ffp-contract=off",
@@ -122,6 +122,9 @@ def gpu_lib():
         L.mi_gpu_normal_bf16_to_host.argtypes = [ctypes.c_uint64, ctypes.c_int, ctypes.c_void_p, ctypes.c_uint64,
                                                  ctypes.c_double, ctypes.c_void_p, ctypes.c_char_p, ctypes.c_int]
         L.mi_gpu_mxfp4_entries_to_host.argtypes = [ctypes.c_uint64, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
+                                                   ctypes.c_int, ctypes.c_double, ctypes.c_void_p, ctypes.c_char_p,
+                                                   ctypes.c_int]
+        L.mi_gpu_nvfp4_entries_to_host.argtypes = [ctypes.c_uint64, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
                                                    ctypes.c_int, ctypes.c_double, ctypes.c_void_p, ctypes.c_char_p,
                                                    ctypes.c_int]
         _gpu_lib = L
@@ -285,6 +288,20 @@ def gpu_fill_mxfp4_entries(seed: int, keys, H: int, I: int, ptrs) -> None:
     dsts = (ctypes.c_void_p * len(keys))(*[int(p) for p in ptrs])
     err = ctypes.create_string_buffer(256)
     rc = gpu_lib().mi_gpu_mxfp4_entries_to_host(seed, len(keys), streams, H, I, 0.02, dsts, err, 256)
+    if rc != 0:
+        raise RuntimeError("GPU input generator: " + err.value.decode(errors="replace"))
+
+
+def gpu_fill_nvfp4_entries(seed: int, keys, H: int, I: int, ptrs) -> None:
+    """Write NVFP4 entries keys[i] = (layer, expert) into host memory at ptrs[i] with the GPU
+    build of this generator (the same bytes as nvfp4_entry)."""
+    keys = list(keys)
+    if not keys:
+        return
+    streams = (ctypes.c_uint64 * len(keys))(*[stream_id(KIND_EXPERT, l, e) for l, e in keys])
+    dsts = (ctypes.c_void_p * len(keys))(*[int(p) for p in ptrs])
+    err = ctypes.create_string_buffer(256)
+    rc = gpu_lib().mi_gpu_nvfp4_entries_to_host(seed, len(keys), streams, H, I, 0.02, dsts, err, 256)
     if rc != 0:
         raise RuntimeError("GPU input generator: " + err.value.decode(errors="replace"))
 

@@ -60,6 +60,7 @@ def lib():
         L.orc_nvfp4_dequant.argtypes = [vp, vp, ctypes.c_int64, ctypes.c_float, vp]
         L.orc_nvfp4_dequant.restype = ctypes.c_int64
         L.orc_expert_ffn_f64.argtypes = [vp, i32, i32, vp, vp]
+        L.orc_moe_layer_f64.argtypes = [vp, i32, i32, vp, vp, i32, i32, vp, vp, vp]
         L.orc_layer_accesses.argtypes = [vp, i32, i32, i32, vp]
         L.orc_layer_accesses.restype = i32
         L.orc_lru_run.argtypes = [i32, i32, vp, vp, vp, i32, vp, vp, vp, vp, vp, vp]
@@ -272,6 +273,25 @@ def expert_ffn_f64(W: np.ndarray, H: int, I: int, x_row: np.ndarray) -> np.ndarr
     y = np.empty(H, dtype=np.float64)
     lib().orc_expert_ffn_f64(_p(w), H, I, _p(x), _p(y))
     return y
+
+
+def moe_layer_rows_f64(entry_of, H: int, I: int, x_bf16, resid, idx, w) -> np.ndarray:
+    """moe_layer_rows for experts given as float64 weights: entry_of(e) returns expert e's
+    W_gate | W_up | W_down as float64 (e.g. nvfp4_entry_as_f64); only routed experts are fetched."""
+    x = _c(x_bf16, np.uint16)
+    T = x.shape[0]
+    idx = _c(idx, np.int32)
+    k = idx.shape[1]
+    used = sorted(set(int(e) for e in idx.ravel()))
+    E = max(used) + 1
+    cache = {e: _c(entry_of(e), np.float64) for e in used}
+    dummy = np.zeros(1, dtype=np.float64)
+    table = (ctypes.c_void_p * E)(*[(cache[e].ctypes.data if e in cache else dummy.ctypes.data) for e in range(E)])
+    out = np.empty((T, H), dtype=np.float64)
+    lib().orc_moe_layer_f64(ctypes.addressof(table), H, I, _p(x), _p(_c(resid, np.float32)), T, k, _p(idx),
+                            _p(_c(w, np.float64)), _p(out))
+    del cache
+    return out
 
 
 def layer_accesses(idx: np.ndarray, E: int) -> np.ndarray:

@@ -342,6 +342,26 @@ void orc_expert_ffn_f64(const double* W, int H, int I, const uint16_t* x, double
     }
 }
 
+// orc_moe_layer for entries given as float64 weights (orc_expert_ffn_f64): out[t] = resid[t] +
+// sum_{j<k} w[t,j] * y_{idx[t,j]}(x[t]), summed in j order. entries[e] points at expert e's
+// weights W_gate | W_up | W_down.
+void orc_moe_layer_f64(const double* const* entries, int H, int I, const uint16_t* x, const float* resid, int T,
+                       int k, const int32_t* idx, const double* w, double* out) {
+    const int P = T * k;
+    std::vector<double> y(static_cast<size_t>(P) * H);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int p = 0; p < P; ++p) {
+        int t = p / k;
+        orc_expert_ffn_f64(entries[idx[p]], H, I, x + static_cast<size_t>(t) * H, &y[static_cast<size_t>(p) * H]);
+    }
+    for (int t = 0; t < T; ++t)
+        for (int n = 0; n < H; ++n) {
+            double acc = static_cast<double>(resid[static_cast<size_t>(t) * H + n]);
+            for (int j = 0; j < k; ++j) acc += w[static_cast<size_t>(t) * k + j] * y[(static_cast<size_t>(t) * k + j) * H + n];
+            out[static_cast<size_t>(t) * H + n] = acc;
+        }
+}
+
 // R5: the distinct experts routed in one layer invocation, in ascending id (the order in
 // which the LRU sees them). Returns their number.
 int orc_layer_accesses(const int32_t* idx, int T, int k, int E, int32_t* experts) {

@@ -46,17 +46,21 @@ def fill_pool(cache: moe.MoeCache, W: mi.Workload, L: int):
     ptrs = [cache.host_entry(l, e) for l, e in keys]
     if cache.shape_flags & moe.MOE_MXFP4:
         mi.gpu_fill_mxfp4_entries(W.seed, keys, W.H, W.I, ptrs)
+    elif cache.shape_flags & moe.MOE_NVFP4:
+        mi.gpu_fill_nvfp4_entries(W.seed, keys, W.H, W.I, ptrs)
     else:
         mi.gpu_fill_entries(W.seed, keys, W.H, W.I, ptrs)
 
 
 class OracleEntries:
     """The oracle's own copy of the expert entries, regenerated from the seed (bf16; or the
-    MXFP4 entries read back by the oracle as the bf16 values they encode, when fp4)."""
+    MXFP4 entries read back by the oracle as the bf16 values they encode, when fp4; or the
+    NVFP4 entries read back as float64 weights, when nvfp4 -- use oracle.moe_layer_rows_f64)."""
 
-    def __init__(self, W: mi.Workload, fp4: bool = False):
+    def __init__(self, W: mi.Workload, fp4: bool = False, nvfp4: bool = False):
         self.W = W
         self.fp4 = fp4
+        self.nvfp4 = nvfp4
         self.cache = {}
 
     def __call__(self, layer: int, expert: int) -> np.ndarray:
@@ -65,6 +69,8 @@ class OracleEntries:
             W = self.W
             if self.fp4:
                 self.cache[key] = oracle.mxfp4_entry_as_bf16(mi.mxfp4_entry(W.seed, layer, expert, W.H, W.I), W.H, W.I)
+            elif self.nvfp4:
+                self.cache[key] = oracle.nvfp4_entry_as_f64(mi.nvfp4_entry(W.seed, layer, expert, W.H, W.I), W.H, W.I)
             else:
                 self.cache[key] = mi.expert_entry(W.seed, layer, expert, W.H, W.I)
         return self.cache[key]

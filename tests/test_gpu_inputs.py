@@ -28,3 +28,14 @@ def test_gpu_mxfp4_entries_are_bitwise_the_cpu_ones(H, I):
         ref = mi.mxfp4_entry(0, l, e, H, I)
         diff = np.nonzero(b != ref)[0]
         assert diff.size == 0, f"entry {(l, e)}: {diff.size} bytes differ, first at {diff[0]}"
+
+
+@pytest.mark.parametrize("H,I", [(256, 128), (4096, 1536)])
+def test_gpu_nvfp4_entries_are_bitwise_the_cpu_ones(H, I):
+    keys = [(0, 3), (1, 77)]
+    bufs = [np.empty(mi.nvfp4_entry_bytes(H, I), np.uint8) for _ in keys]
+    mi.gpu_fill_nvfp4_entries(0, keys, H, I, [b.ctypes.data for b in bufs])
+    for (l, e), b in zip(keys, bufs):
+        ref = mi.nvfp4_entry(0, l, e, H, I)
+        diff = np.nonzero(b != ref)[0]
+        assert diff.size == 0, f"entry {(l, e)}: {diff.size} bytes differ, first at {diff[0]}"

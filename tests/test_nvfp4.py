@@ -152,3 +152,26 @@ def test_ffn_on_float64_weights_is_the_bf16_ffn():
     y16 = oracle.expert_ffn(ent, H, I, x)
     y64 = oracle.expert_ffn_f64(mi.bf16_bits_to_f32(ent).astype(np.float64), H, I, x)
     assert np.array_equal(y16, y64)
+
+
+def test_layer_on_float64_weights_is_the_bf16_layer():
+    """The float64-weight layer restates the bf16 layer (which the dense zero-masked reference
+    pins): on weights that are bf16 values, with routing from the oracle's router, it gives the
+    same bits -- so a dropped term, a wrong gate or a wrong index in its combine would show."""
+    H, I, E, k, T = 256, 128, 16, 2, 6
+    ents = [mi.expert_entry(0, 0, e, H, I) for e in range(E)]
+    x = mi.activations(0, 11, T, H)
+    Wr = mi.router_weights(0, 0, E, H)
+    b = np.zeros(E, np.float32)
+    idx, w, _, _ = oracle.route(x, Wr, b, k)
+    resid = mi.bf16_bits_to_f32(x)
+    ref = oracle.moe_layer(ents, H, I, x, resid, idx, w)
+    got = oracle.moe_layer_rows_f64(lambda e: mi.bf16_bits_to_f32(ents[e]).astype(np.float64), H, I, x, resid, idx, w)
+    assert np.array_equal(ref, got)
+    # and it is linear in a power-of-two scaling of W_down (a tensor scale on the down matrix)
+    scaled = lambda e: np.concatenate([mi.bf16_bits_to_f32(ents[e][:2 * I * H]).astype(np.float64),
+                                       0.25 * mi.bf16_bits_to_f32(ents[e][2 * I * H:]).astype(np.float64)])
+    got4 = oracle.moe_layer_rows_f64(scaled, H, I, x, resid, idx, w)
+    d = (got4 - resid) - 0.25 * (ref - resid)  # equal up to the rounding of the residual add
+    assert np.abs(d).max() <= 1e-12 * np.abs(ref).max()
+    assert np.abs(ref - resid).max() > 1e-3  # the experts contribute
