@@ -37,9 +37,12 @@ UNIT = "tok/s"
 BATCHES = (1, 4, 16)  # replaced by --batches
 PER_BATCH_STEPS = 256  # steps of each per-batch run (the workload defines 256 steps per batch size)
 FALLBACK_HBM_GBS = 6400.0
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_gateup.md")
-DECODE_SOURCES = [os.path.join(ROOT, "moe_expert_layer_10_b300", "csrc", f)
-                  for f in ("decode_mma.cu", "decode_common.cuh", "ptx.cuh", "umma.cuh")]
+# the committed ncu summary of each roofline kernel and the sources its counters were taken on
+PROFILE_SUMMARY = {"decode_gateup": os.path.join(ROOT, "profiles", "decode_gateup.md"),
+                   "decode_fused": os.path.join(ROOT, "profiles", "decode_fused.md")}
+DECODE_SOURCES = {k: [os.path.join(ROOT, "moe_expert_layer_10_b300", "csrc", f)
+                      for f in (main, "decode_common.cuh", "ptx.cuh", "umma.cuh")]
+                  for k, main in (("decode_gateup", "decode_mma.cu"), ("decode_fused", "decode_fused.cu"))}
 
 
 def parse_args():
@@ -69,9 +72,10 @@ def parse_args():
     ap.add_argument("--policy", choices=["host", "device"], default="host",
                     help="host: LRU on the host (one sync per forward); device: LRU and fills on the GPU, the "
                          "whole decode step captured in a CUDA graph and replayed")
-    ap.add_argument("--workload", choices=["decode", "stream8", "stack48"], default="decode",
+    ap.add_argument("--workload", choices=["decode", "stream8", "stack48", "qstar"], default="decode",
                     help="decode: the default decode layer; stream8: the 8-layer decode stream with a shared "
-                         "30%% cache; stack48: the 48-layer stack (double-buffered prefill, then decode)")
+                         "30%% cache; stack48: the 48-layer stack (double-buffered prefill, then decode); qstar: "
+                         "the q-star miss split simulated on the stream's reuse trace with measured bandwidths")
     return ap.parse_args()
 
 
@@ -92,26 +96,26 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def decode_source_sha256():
-    """sha256 over the decode kernel's source files, in a fixed order."""
+def decode_source_sha256(kernel: str = "decode_fused"):
+    """sha256 over a decode kernel's source files, in a fixed order."""
     h = hashlib.sha256()
-    for f in DECODE_SOURCES:
+    for f in DECODE_SOURCES[kernel]:
         h.update(open(f, "rb").read())
     return h.hexdigest()
 
 
-def traffic_ratio_from_profile():
-    """DRAM bytes / algorithmic bytes of the decode gate/up launch captured in the committed ncu
+def traffic_ratio_from_profile(kernel: str):
+    """DRAM bytes / algorithmic bytes of the kernel's launch captured in its committed ncu
     summary, or None if the summary is missing or was taken on a different kernel source."""
-    if not os.path.exists(PROFILE_SUMMARY):
+    path = PROFILE_SUMMARY.get(kernel)
+    if not path or not os.path.exists(path):
         return None
-    text = open(PROFILE_SUMMARY).read()
+    text = open(path).read()
     m = re.search(r"traffic_ratio:\s*([0-9.eE+]+)", text)
     h = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
     if not m or not h:
         return None
-    cur = decode_source_sha256()
-    return float(m.group(1)) if h.group(1) == cur else None
+    return float(m.group(1)) if h.group(1) == decode_source_sha256(kernel) else None
 
 
 class ClockSampler:
@@ -450,19 +454,21 @@ def run_b300(args, rank, world, local):
 
     tokens = args.steps * sum(BATCHES) * world
     peak, peak_kind = measured_peaks()
-    g = kst["decode_gateup"]
+    # the dominant decode kernel: the fused gate/up + down launch (bf16), else the gate/up launch
+    kname = "decode_fused" if kst.get("decode_fused", {}).get("launches") else "decode_gateup"
+    g = kst[kname]
     roof = None
     if g["launches"]:
         avg_ms = g["total_ms"] / g["launches"]
         bytes_per_launch = g["bytes"] / g["launches"]
         achieved = bytes_per_launch / (avg_ms / 1e3) / 1e9
-        roof = {"kernel": "decode_gateup", "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+        roof = {"kernel": kname, "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                 "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
                 "traffic": None, "bytes_per_launch": bytes_per_launch, "avg_launch_ms": avg_ms,
                 "launches": g["launches"],
                 "pass": "the timed steps' batches replayed with every routed expert resident (256-entry cache), "
                         "CUDA events on the compute stream"}
-        ratio = None if fp4 else traffic_ratio_from_profile()
+        ratio = None if fp4 else traffic_ratio_from_profile(kname)
         if ratio is not None:
             # the captured launch's DRAM bytes per algorithmic byte, applied to this pass's
             # average launch (the capture is one batch-16 launch, not this pass's mix)
@@ -474,8 +480,8 @@ def run_b300(args, rank, world, local):
                     "GB/s": round(v["bytes"] / (v["total_ms"] / 1e3) / 1e9, 1)}
                 for n, v in ks.items() if v["launches"]}
     # launches of this library's kernels in the timed region: route (2) + permute, gather,
-    # combine (3) per forward, and two expert kernels per wave
-    launches = args.steps * (5 * len(BATCHES)) + 2 * st["waves"]
+    # combine (3) per forward, and per wave one fused expert launch (bf16) or two (4-bit)
+    launches = args.steps * (5 * len(BATCHES)) + (2 if fp4 else 1) * st["waves"]
     if device:  # per forward: policy, fill and 4 decode launches for each possible wave
         launches = args.steps * sum(5 + 6 * ((min(B * W.k, W.E) + C - 1) // C) for B in BATCHES)
 
@@ -781,7 +787,7 @@ def run_stream8(args):
                        "policy": "device (CUDA graph per step)" if device else "host",
                        "pool_GB": W.L * W.E * 3 * W.H * W.I * 2 / 1e9, "setup_s": round(setup_s, 1),
                        **_stats_summary(st, ms)},
-            "clocks": clk, "gpu_launches": int(steps * W.L * 5 + 2 * st["waves"])}
+            "clocks": clk, "gpu_launches": int(steps * W.L * 5 + (6 if device else 1) * st["waves"])}
 
 
 def run_stack48(args):
@@ -872,7 +878,52 @@ def run_stack48(args):
                        **_stats_summary(st, ms)},
             "prefill": {"tokens": T, "ms": round(ms_pre, 2), "tok_s": round(T / (ms_pre / 1e3), 1),
                         **_stats_summary(st_pre, ms_pre)},
-            "clocks": clk, "gpu_launches": int(steps * W.L * 5 + 2 * st["waves"])}
+            "clocks": clk, "gpu_launches": int(steps * W.L * 5 + st["waves"])}
+
+
+def run_qstar(args):
+    """The q-star miss split on the 8-layer decode stream's reuse trace (hidden 4096, intermediate
+    1536, 256 experts top-6 per layer, batch 8, 614-entry LRU): measure pinned PCIe H2D and the
+    host expert FFN's bandwidth on this machine, then run the host-only split simulation for fill
+    fractions q = 0, 0.1, .., 1 and for the bandwidth rule q*, and report the modeled step time.
+    Nothing here executes experts inside moe_layer_forward; the simulation models the two paths."""
+    import numpy as np
+
+    import moe_expert_layer_10_b300 as moe
+    import moe_inputs as mi
+    W = mi.WORKLOADS["stream8"]
+    steps, B = args.steps, 8
+    threads = len(os.sched_getaffinity(0))
+    probe = moe.MoeCache(moe.LayerShape(1, 1, W.H, W.I, W.k, 1, 1))
+    fill_pool(probe, W, 1, 1)
+    bw = probe.measure_bandwidth(threads, reps=8)
+    probe.close()
+    bp = [mi.router_bias(W.seed, l, W.E, W.zipf_s) for l in range(W.L)]
+    trace = mi.trace_reuse(W.seed, W.L, steps, B, W.E, W.k, W.zipf_s, 0.7, np.stack([p for _, p in bp]))
+    invs = []
+    for st in range(steps):
+        for l in range(W.L):
+            ex, cnt = np.unique(trace[st, l].ravel(), return_counts=True)
+            invs.append([(l, int(e), int(c)) for e, c in zip(ex, cnt)])
+    hbm, _ = measured_peaks()
+    entry = 3 * W.H * W.I * 2
+    rows = {}
+    for q in [round(0.1 * i, 1) for i in range(11)] + [-1.0]:
+        r, _ = moe.qstar_simulate(W.C, invs, q, bw["pcie_h2d_gbps"], bw["host_expert_gbps"], hbm, entry)
+        rows["q*" if q < 0 else f"{q:.1f}"] = {
+            "ms_per_step": round(r["modeled_ms"] / steps, 3), "tok_s": round(steps * B / (r["modeled_ms"] / 1e3), 1),
+            "hit_rate": round(r["hits"] / r["expert_reads"], 4), "fills_per_step": round(r["fills"] / steps, 2),
+            "host_execs_per_step": round(r["host_execs"] / steps, 2)}
+    qstar = bw["pcie_h2d_gbps"] / (bw["pcie_h2d_gbps"] + bw["host_expert_gbps"]) if bw["host_expert_gbps"] else 1.0
+    best = min(rows, key=lambda k: rows[k]["ms_per_step"])
+    return {"metric": "q-star split, modeled 8-layer decode step time (host-only simulation on measured bandwidths)",
+            "value": rows["q*"]["tok_s"], "unit": "tok/s (modeled)", "n_gpus": 1, "steps": steps,
+            "higher_is_better": True, "dtype": "bf16", "data": "synthetic reuse trace (seeded Philox)",
+            "config": {"workload": "8-layer decode stream: 256 experts top-6, batch 8, reuse p=0.7, 614-entry LRU",
+                       "host_threads": threads, "hbm_gbps": hbm, "entry_bytes": entry},
+            "bandwidth": bw, "q_star": round(qstar, 4), "best_q": best, "by_q": rows,
+            "note": "modeled time per layer = max(fills * entry / B_pcie, host execs * entry / B_host) + "
+                    "(hits + fills) * entry / B_hbm; the library's forward never runs experts on the host"}
 
 
 # ----------------------------------------------------------------------------- reference arm
@@ -963,7 +1014,8 @@ def main():
     if args.warmup < 3:
         args.warmup = 3
     if args.steps is None:
-        args.steps = 64 if args.impl == "reference" else {"decode": 256, "stream8": 512, "stack48": 32}[args.workload]
+        args.steps = 64 if args.impl == "reference" else {"decode": 256, "stream8": 512, "stack48": 32,
+                                                          "qstar": 512}[args.workload]
     if args.impl == "reference":
         if rank == 0:
             print(json.dumps(run_reference(args)), flush=True)
@@ -972,7 +1024,7 @@ def main():
     if args.workload != "decode":
         import torch
         torch.cuda.set_device(local)
-        res = run_stream8(args) if args.workload == "stream8" else run_stack48(args)
+        res = {"stream8": run_stream8, "stack48": run_stack48, "qstar": run_qstar}[args.workload](args)
         if rank == 0:
             print(json.dumps(res), flush=True)
         return

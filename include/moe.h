@@ -97,6 +97,9 @@ extern "C" {
 #define MOE_PATH_AUTO 0 /* decode kernels when every routed expert has <= 64 tokens, else grouped GEMM */
 #define MOE_PATH_GEMV 1 /* decode kernels: weight-streaming tcgen05 products, tokens as the narrow side */
 #define MOE_PATH_GEMM 2 /* tcgen05 grouped GEMM kernels (prefill) */
+/* decode kernels as two launches per wave (gate/up, then down); MOE_PATH_AUTO and MOE_PATH_GEMV
+ * run bf16 entries' gate/up and down units in one persistent launch per wave */
+#define MOE_PATH_GEMV_UNFUSED 3
 
 /* ---- LRU event kinds ---- */
 #define MOE_EV_HIT 0           /* routed access, entry resident */

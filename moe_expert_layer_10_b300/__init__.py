@@ -21,7 +21,7 @@ HEADER = os.path.join(os.path.dirname(PKG), "include", "moe.h")
 MOE_OK, MOE_E_INVAL, MOE_E_NOMEM, MOE_E_CUDA, MOE_E_TIMEOUT, MOE_E_CAPACITY, MOE_E_DEVICE = 0, -1, -2, -3, -4, -5, -6
 MOE_TRACE, MOE_PROFILE, MOE_PREFILL_DB, MOE_DEVICE_POLICY, MOE_MXFP4, MOE_NVFP4 = 1, 2, 4, 8, 16, 32
 MOE_FILL_DEMAND, MOE_FILL_FULL_LAYER = 0, 1
-MOE_PATH_AUTO, MOE_PATH_GEMV, MOE_PATH_GEMM = 0, 1, 2
+MOE_PATH_AUTO, MOE_PATH_GEMV, MOE_PATH_GEMM, MOE_PATH_GEMV_UNFUSED = 0, 1, 2, 3
 EV_HIT, EV_FILL, EV_PREFETCH_FILL, EV_PREFETCH_HIT, EV_RESIZE_EVICT, EV_HOST_EXEC = 0, 1, 2, 3, 4, 5
 
 # every symbol include/moe.h declares

@@ -110,6 +110,23 @@ cudaError_t launch_decode_down(const DecodeMaps& maps, const GemvWork* work, int
                                float* pair_out, float* ws, int* cnt, int* status, uint64_t fill_wait_ns, int num_sms,
                                cudaStream_t st);
 
+// --- decode expert FFN, gate/up and down in one persistent launch (bf16; decode_fused.cu) ---
+// work_gu / work_d: the wave's two work lists in the same entry order, each closed by its unit
+// total, with GemvWork::pad0 = the entry's first token-chunk index (chunks of all entries
+// numbered consecutively). h_ready / h_done: decode_fused_chunk_slots(E, P) ints each, zero
+// before the first launch (every launch leaves them zero). The down phase's split-K tiles follow
+// the gate/up phase's in ws and cnt.
+int decode_fused_chunk_slots(int E, int P);
+cudaError_t launch_decode_fused(const DecodeMaps& maps, const GemvWork* work_gu, int n_work, int units_gu, int S_gu,
+                                const GemvWork* work_d, int units_d, int S_d, const int32_t* slot_row,
+                                const uint32_t* fill_flag, int H, int I, uint16_t* h_perm, const float* w_perm,
+                                float* pair_out, float* ws, int* cnt, int* h_ready, int* h_done, int* status,
+                                uint64_t fill_wait_ns, int num_sms, cudaStream_t st);
+// K splits (S_gu, S_d) of a fused launch: the pair that minimises the largest per-CTA load
+// under the round-robin assignment of the concatenated unit list. chunk_tok: token count of each
+// chunk of the wave's entries, in work-list order.
+void decode_fused_choose_split(const int* chunk_tok, int n_chunks, int H, int I, int num_sms, int* S_gu, int* S_d);
+
 // --- decode expert FFN with 4-bit entries (expanded to bf16 on chip; decode_fp4.cu) ---
 // fmt: kFp4Mx (MXFP4: E8M0 scale per 32 weights) or kFp4Nv (NVFP4: E4M3 scale per 16 weights
 // and an fp32 tensor scale per matrix, in the entry's last 16 bytes). Same work lists, splits

@@ -69,10 +69,10 @@ constexpr int kDecodeMaxTokens = 64;  // AUTO path: tensor-core decode kernels u
 constexpr size_t kWorkEntries(int E) { return 2 * (static_cast<size_t>(E) + 1); }
 
 enum KernelId { kRouterLogits, kRouterTopk, kPermute, kGather, kDecodeGateUp, kDecodeDown, kGemmGateUp, kGemmDown,
-                kCombine, kPolicy, kFill, kNumKernels };
+                kCombine, kPolicy, kFill, kDecodeFused, kNumKernels };
 const char* kKernelNames[kNumKernels] = {"router_logits", "router_topk",  "permute",     "gather_rows",
                                          "decode_gateup", "decode_down",  "gemm_gateup", "gemm_down",
-                                         "combine",       "device_policy", "device_fill"};
+                                         "combine",       "device_policy", "device_fill", "decode_fused"};
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -193,6 +193,8 @@ struct moe_ctx {
     moe::DecodeMaps dec_maps{};
     float* dec_ws = nullptr;  // split-K partial tiles of the decode kernels
     int* dec_cnt = nullptr;   // per-tile arrival counters (zero between launches)
+    int *dec_ready = nullptr, *dec_done = nullptr;  // fused decode: per-chunk h counters (zero between launches)
+    int dec_chunk_slots = 0;
     moe::GemmMaps gemm_maps{};
 
     // stats and trace
@@ -321,8 +323,10 @@ int check_status(moe_ctx* c) {
         *c->status_host = 0;
         // clear the device word too, in stream order, so the context stays usable
         cudaMemsetAsync(c->status, 0, sizeof(int), c->s_comp);
-        // a kernel that stopped early may have left split-K arrival counters behind
+        // a kernel that stopped early may have left split-K arrival or h counters behind
         cudaMemsetAsync(c->dec_cnt, 0, moe::kDecodeSplitUnits * sizeof(int), c->s_comp);
+        cudaMemsetAsync(c->dec_ready, 0, c->dec_chunk_slots * sizeof(int), c->s_comp);
+        cudaMemsetAsync(c->dec_done, 0, c->dec_chunk_slots * sizeof(int), c->s_comp);
         return fail(MOE_E_DEVICE, "a kernel raised device status %d (1 wait timeout, 2 bad forced set, 3 bad slot, "
                                   "4 bad expert index, 5 fill wait timeout)", code);
     }
@@ -512,7 +516,7 @@ void free_all(moe_ctx* c) {
     if (c->ev_join) cudaEventDestroy(c->ev_join);
     void* dev_ptrs[] = {c->arena, c->slot_dev, c->logits, c->offsets, c->perm, c->inv_perm, c->active,
                         c->perm_cells, c->perm_done, c->n_active, c->w_perm, c->pair_out, c->x_perm, c->h_perm, c->status, c->work_dev,
-                        c->dec_ws,   c->dec_cnt, c->fill_flag, c->d_lru,   c->d_prev, c->d_next,  c->d_key,
+                        c->dec_ws,   c->dec_cnt, c->dec_ready, c->dec_done, c->fill_flag, c->d_lru,   c->d_prev, c->d_next,  c->d_key,
                         c->d_stats,  c->d_trace, c->d_fill_list, c->d_work, c->d_order, c->d_hdr, c->d_keys,
                         c->d_iota};
     for (void* p : dev_ptrs)
@@ -809,6 +813,11 @@ int moe_cache_init(const moe_config_t* cfg, void* stream_compute, void* stream_c
     INIT_TRY(cudaMalloc(&c->work_dev, kWorkEntries(c->E) * sizeof(GemvWork)));
     INIT_TRY(cudaMalloc(&c->dec_ws, static_cast<size_t>(moe::kDecodeSplitUnits) * moe::kDecodeTileFloats * sizeof(float)));
     INIT_TRY(cudaMalloc(&c->dec_cnt, moe::kDecodeSplitUnits * sizeof(int)));
+    c->dec_chunk_slots = moe::decode_fused_chunk_slots(c->E, c->Pmax);
+    INIT_TRY(cudaMalloc(&c->dec_ready, c->dec_chunk_slots * sizeof(int)));
+    INIT_TRY(cudaMalloc(&c->dec_done, c->dec_chunk_slots * sizeof(int)));
+    INIT_TRY(cudaMemset(c->dec_ready, 0, c->dec_chunk_slots * sizeof(int)));
+    INIT_TRY(cudaMemset(c->dec_done, 0, c->dec_chunk_slots * sizeof(int)));
     INIT_TRY(cudaMalloc(&c->fill_flag, static_cast<size_t>(c->C) * sizeof(uint32_t)));
     INIT_TRY(cudaMemset(c->fill_flag, 0, static_cast<size_t>(c->C) * sizeof(uint32_t)));
     INIT_TRY(cudaMemset(c->dec_cnt, 0, moe::kDecodeSplitUnits * sizeof(int)));
@@ -895,7 +904,7 @@ void* moe_host_entry(moe_ctx* c, int layer, int expert) {
 
 int moe_set_path(moe_ctx* c, int path) {
     if (!c) return fail(MOE_E_INVAL, "null context");
-    if (path != MOE_PATH_AUTO && path != MOE_PATH_GEMV && path != MOE_PATH_GEMM)
+    if (path != MOE_PATH_AUTO && path != MOE_PATH_GEMV && path != MOE_PATH_GEMM && path != MOE_PATH_GEMV_UNFUSED)
         return fail(MOE_E_INVAL, "unknown path %d", path);
     c->path = path;
     return MOE_OK;
@@ -1258,22 +1267,36 @@ int moe_layer_forward(moe_ctx* c, int layer, const void* x, const float* resid, 
 
         // Work lists (gate/up, then down), each closed by an entry holding the unit total.
         // Units are token chunks x row tiles x K splits; the split of each kernel fills the SMs
-        // evenly and depends only on the wave's routed set.
+        // evenly and depends only on the wave's routed set. bf16 entries run both phases in one
+        // fused launch (unless MOE_PATH_GEMV_UNFUSED), whose splits balance the joint unit list.
         int pw = 0, chunks = 0;
         for (int a = a0; a < a1; ++a) {
             pw += count[distinct[a]];
             chunks += moe::decode_token_chunks(count[distinct[a]]);
         }
         const int nw = a1 - a0;
+        const bool fused = !c->fp4 && path != MOE_PATH_GEMV_UNFUSED;
         const int Rg = moe::decode_row_tiles(true, H, I), Rd = moe::decode_row_tiles(false, H, I);
-        const int Sg = moe::decode_choose_split(chunks * Rg, true, H, I, c->num_sms);
-        const int Sd = moe::decode_choose_split(chunks * Rd, false, H, I, c->num_sms);
+        int Sg = 1, Sd = 1;
+        if (fused) {
+            std::vector<int> chunk_tok;
+            for (int i = 0; i < nw; ++i) {
+                const int e = distinct[order[i]];
+                for (int ch = 0; ch < moe::decode_token_chunks(count[e]); ++ch)
+                    chunk_tok.push_back(std::min(64, count[e] - 64 * ch));
+            }
+            moe::decode_fused_choose_split(chunk_tok.data(), static_cast<int>(chunk_tok.size()), H, I, c->num_sms,
+                                           &Sg, &Sd);
+        } else {
+            Sg = moe::decode_choose_split(chunks * Rg, true, H, I, c->num_sms);
+            Sd = moe::decode_choose_split(chunks * Rd, false, H, I, c->num_sms);
+        }
         int s;
         rc = next_stage(c, &s);
         if (rc) return rc;
         GemvWork* wk = c->work_stage + static_cast<size_t>(s) * kWorkEntries(E);
         GemvWork* wk2 = wk + (E + 1);
-        int units_gu = 0, units_d = 0;
+        int units_gu = 0, units_d = 0, chunk_base = 0;
         for (int i = 0; i < nw; ++i) {
             const int a = order[i];
             const int e = distinct[a];
@@ -1285,10 +1308,11 @@ int moe_layer_forward(moe_ctx* c, int layer, const void* x, const float* resid, 
                 gen += 1000;  // injected: a generation the copy stream will not write for a long time
                 inject_wave = true;
             }
-            wk[i] = GemvWork{e, offs[e], count[e], units_gu, wait_slot, gen, 0, 0};
-            wk2[i] = GemvWork{e, offs[e], count[e], units_d, wait_slot, gen, 0, 0};
+            wk[i] = GemvWork{e, offs[e], count[e], units_gu, wait_slot, gen, chunk_base, 0};
+            wk2[i] = GemvWork{e, offs[e], count[e], units_d, wait_slot, gen, chunk_base, 0};
             units_gu += ch * Rg * Sg;
             units_d += ch * Rd * Sd;
+            chunk_base += ch;
         }
         const uint64_t fill_wait_ns = inject_wave ? kInjectedFillWaitNs : c->fill_wait_ns;
         if (inject_wave) c->inject_count--;
@@ -1298,15 +1322,23 @@ int moe_layer_forward(moe_ctx* c, int layer, const void* x, const float* resid, 
         CUDA_TRY(cudaMemcpyAsync(c->work_dev, wk, kWorkEntries(E) * sizeof(GemvWork), cudaMemcpyHostToDevice,
                                  c->s_comp));
         CUDA_TRY(cudaEventRecord(c->stage_ev[s], c->s_comp));
-        {
-            ProfScope ps(c, kDecodeGateUp, 2.0 * nw * I * H * weight_bytes(c) + 2.0 * pw * H + 2.0 * pw * I,
-                         4.0 * pw * I * H);
-            CUDA_TRY(run_gateup(c, c->work_dev, nw, units_gu, Sg, nullptr, slot_row, fill_wait_ns));
-        }
-        {
-            ProfScope ps(c, kDecodeDown, 1.0 * nw * H * I * weight_bytes(c) + 2.0 * pw * I + 4.0 * pw * H + 4.0 * pw,
-                         2.0 * pw * I * H);
-            CUDA_TRY(run_down(c, c->work_dev + (E + 1), nw, units_d, Sd, nullptr, slot_row, fill_wait_ns));
+        const double gu_bytes = 2.0 * nw * I * H * weight_bytes(c) + 2.0 * pw * H + 2.0 * pw * I;
+        const double d_bytes = 1.0 * nw * H * I * weight_bytes(c) + 2.0 * pw * I + 4.0 * pw * H + 4.0 * pw;
+        if (fused) {
+            ProfScope ps(c, kDecodeFused, gu_bytes + d_bytes, 6.0 * pw * I * H);
+            CUDA_TRY(moe::launch_decode_fused(c->dec_maps, c->work_dev, nw, units_gu, Sg, c->work_dev + (E + 1),
+                                              units_d, Sd, slot_row, c->fill_flag, H, I, c->h_perm, c->w_perm,
+                                              c->pair_out, c->dec_ws, c->dec_cnt, c->dec_ready, c->dec_done,
+                                              c->status, fill_wait_ns, c->num_sms, c->s_comp));
+        } else {
+            {
+                ProfScope ps(c, kDecodeGateUp, gu_bytes, 4.0 * pw * I * H);
+                CUDA_TRY(run_gateup(c, c->work_dev, nw, units_gu, Sg, nullptr, slot_row, fill_wait_ns));
+            }
+            {
+                ProfScope ps(c, kDecodeDown, d_bytes, 2.0 * pw * I * H);
+                CUDA_TRY(run_down(c, c->work_dev + (E + 1), nw, units_d, Sd, nullptr, slot_row, fill_wait_ns));
+            }
         }
         c->comp_seq++;
         CUDA_TRY(cudaEventRecord(c->comp_ev[c->comp_seq % kEvRing], c->s_comp));

@@ -1,5 +1,6 @@
 """GPU parity of the tensor-core decode expert kernels (weights as the M = 128 side of
-tcgen05.mma, tokens as N = 16..64), forced onto the decode path:
+tcgen05.mma, tokens as N = 16..64), forced onto the decode path, both as one fused launch per
+wave (gate/up units, then down units that wait for their h rows) and as two launches:
 
 * the tiny layer at batch sizes that give experts of 1 to more than 64 tokens, so token
   chunks of every width (16, 32, 48, 64) and experts split over several chunks are covered;
@@ -32,14 +33,15 @@ def _forward(cache, W, x, Wr, b, T):
     return idx.cpu().numpy(), out.cpu().numpy(), resid.cpu().numpy()
 
 
+@pytest.mark.parametrize("path", [moe.MOE_PATH_GEMV, moe.MOE_PATH_GEMV_UNFUSED], ids=["fused", "two-launch"])
 @pytest.mark.parametrize("T", [1, 5, 17, 40, 100, 700])
-def test_tiny_layer_decode_path_all_chunk_widths(T):
+def test_tiny_layer_decode_path_all_chunk_widths(T, path):
     W = mi.WORKLOADS["tiny"]
     ents = hz.OracleEntries(W)
     Wr = mi.router_weights(W.seed, 0, W.E, W.H)
     b, _ = mi.router_bias(W.seed, 0, W.E, W.zipf_s)
     with hz.make_cache(W, max_tokens=T, capacity=16) as cache:
-        cache.set_path(moe.MOE_PATH_GEMV)
+        cache.set_path(path)
         x = mi.activations(W.seed, 800 + T, T, W.H)
         idx, out, resid = _forward(cache, W, x, Wr, b, T)
         idx_o, w_o, _, _ = oracle.route(x, Wr, b, W.k)
@@ -69,6 +71,33 @@ def test_decode_layer_batch1_split_k_repeatable():
                 outs.append(out)
         for s in range(3):
             assert np.array_equal(outs[s].view(np.uint32), outs[3 + s].view(np.uint32))
+
+
+@pytest.mark.parametrize("B", [1, 4, 16])
+def test_decode_layer_fused_and_two_launch_agree(B):
+    """The fused launch and the two-launch path on the same decode batches (every expert resident,
+    then with fills in the wave): both within the oracle's tolerance and close to each other."""
+    W = mi.WORKLOADS["decode"]
+    ents = hz.OracleEntries(W)
+    Wr = mi.router_weights(W.seed, 0, W.E, W.H)
+    b, _ = mi.router_bias(W.seed, 0, W.E, W.zipf_s)
+    outs = {}
+    for path in (moe.MOE_PATH_GEMV, moe.MOE_PATH_GEMV_UNFUSED):
+        with hz.make_cache(W, max_tokens=16, capacity=64) as cache:
+            cache.set_path(path)
+            res = []
+            for s in range(3):  # step 0 fills every routed expert; later steps mix hits and fills
+                x = mi.activations(W.seed, 5150 + 10 * B + s, B, W.H)
+                idx, out, resid = _forward(cache, W, x, Wr, b, B)
+                idx_o, w_o, _, _ = oracle.route(x, Wr, b, W.k)
+                assert np.array_equal(idx, idx_o)
+                ref = oracle.moe_layer_rows(ents.layer(0), W.H, W.I, x, resid, idx_o, w_o)
+                hz.assert_out_close(out, ref, resid)
+                res.append(out)
+            outs[path] = res
+    for s in range(3):
+        d = np.abs(outs[moe.MOE_PATH_GEMV][s] - outs[moe.MOE_PATH_GEMV_UNFUSED][s]).max()
+        assert d <= 1e-3 * np.abs(outs[moe.MOE_PATH_GEMV_UNFUSED][s]).max()
 
 
 def test_smaller_decode_shape_batch32():
