@@ -61,6 +61,9 @@ def test_device_policy_decode_layer_matches_oracle_and_host_policy():
     assert st["misses"] > 0 and st["hits"] > 0
     assert st["fill_bytes"] == st["misses"] * 3 * W.H * W.I * 2
     with hz.make_cache(W, max_tokens=16, flags=moe.MOE_TRACE) as cache:
+        # the device policy runs gate/up and down as two launches with the host's two-launch
+        # split rule, so its outputs equal the host policy's two-launch path bit for bit
+        cache.set_path(moe.MOE_PATH_GEMV_UNFUSED)
         outs_h, _ = _decode_batches(cache, W, check=False)
         _, tr_h = cache.stats(trace_cap=1 << 16)
     assert np.array_equal(tr_h, tr)
