@@ -169,6 +169,10 @@ class ClockSampler:
 FORMAT_FLAGS = {"bf16": 0, "mxfp4": 16, "nvfp4": 32}  # MOE_MXFP4, MOE_NVFP4
 
 
+def fmt_dtype(fmt: str) -> str:
+    return "bf16" if fmt == "bf16" else f"{fmt} weights, bf16 activations, fp32 accumulate"
+
+
 def fill_pool(cache, W, L: int, E: int, fmt: str = "bf16"):
     """Seeded entries into the context's pinned pool, generated on the GPU (the same bits as
     the CPU generator that the oracle uses): bf16, MXFP4 or NVFP4."""
@@ -708,8 +712,10 @@ def run_stream8(args):
     stream = torch.cuda.Stream()
     device = args.policy == "device"
     cache = moe.MoeCache(moe.LayerShape(W.L, W.E, W.H, W.I, W.k, W.C, B),
-                         flags=moe.MOE_DEVICE_POLICY if device else 0, stream_compute=stream)
-    fill_pool(cache, W, W.L, W.E)
+                         flags=(moe.MOE_DEVICE_POLICY if device else 0) | FORMAT_FLAGS[args.format],
+                         stream_compute=stream)
+    cache_entry_bytes = cache.entry_bytes
+    fill_pool(cache, W, W.L, W.E, args.format)
     setup_s = time.time() - t0
     Wr = [torch.from_numpy(mi.router_weights(W.seed, l, W.E, W.H)).cuda() for l in range(W.L)]
     bp = [mi.router_bias(W.seed, l, W.E, W.zipf_s) for l in range(W.L)]
@@ -781,11 +787,12 @@ def run_stream8(args):
     return {"metric": "8-layer MoE decode stream tok/s (256 experts top-6 per layer, batch 8, shared LRU of 30%)",
             "value": round(tokens / (ms / 1e3), 2), "unit": "tok/s", "n_gpus": 1, "steps": steps,
             "warmup": args.warmup, "ms_per_step": round(ms / steps, 4), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded Philox)",
+            "scaling": "weak", "vs_baseline": None, "dtype": fmt_dtype(args.format), "data": "synthetic (seeded Philox)",
             "config": {"workload": "8-layer decode stream: hidden 4096, intermediate 1536, 256 experts top-6, "
-                                   "batch 8, reuse trace p=0.7, 614-entry LRU over 2048 (layer, expert) entries",
+                                   "batch 8, reuse trace p=0.7, 614-entry LRU over 2048 (layer, expert) entries" +
+                                   ("" if args.format == "bf16" else f", {args.format.upper()} entries"),
                        "policy": "device (CUDA graph per step)" if device else "host",
-                       "pool_GB": W.L * W.E * 3 * W.H * W.I * 2 / 1e9, "setup_s": round(setup_s, 1),
+                       "pool_GB": W.L * W.E * cache_entry_bytes / 1e9, "setup_s": round(setup_s, 1),
                        **_stats_summary(st, ms)},
             "clocks": clk, "gpu_launches": int(steps * W.L * 5 + (6 if device else 1) * st["waves"])}
 
@@ -806,9 +813,10 @@ def run_stack48(args):
     steps = args.steps
     t0 = time.time()
     stream = torch.cuda.Stream()
-    cache = moe.MoeCache(moe.LayerShape(W.L, W.E, W.H, W.I, W.k, W.C, T), flags=moe.MOE_PREFILL_DB,
-                         stream_compute=stream)
-    fill_pool(cache, W, W.L, W.E)
+    cache = moe.MoeCache(moe.LayerShape(W.L, W.E, W.H, W.I, W.k, W.C, T),
+                         flags=moe.MOE_PREFILL_DB | FORMAT_FLAGS[args.format], stream_compute=stream)
+    cache_entry_bytes = cache.entry_bytes
+    fill_pool(cache, W, W.L, W.E, args.format)
     setup_s = time.time() - t0
     Wr = [torch.from_numpy(mi.router_weights(W.seed, l, W.E, W.H)).cuda() for l in range(W.L)]
     bias = [torch.from_numpy(mi.router_bias(W.seed, l, W.E, W.zipf_s)[0]).cuda() for l in range(W.L)]
@@ -870,11 +878,12 @@ def run_stack48(args):
     return {"metric": "48-layer MoE stack decode tok/s (128 experts top-8 per layer, batch 32, LRU of 25%)",
             "value": round(steps * B / (ms / 1e3), 2), "unit": "tok/s", "n_gpus": 1, "steps": steps,
             "warmup": args.warmup, "ms_per_step": round(ms / steps, 4), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded Philox)",
+            "scaling": "weak", "vs_baseline": None, "dtype": fmt_dtype(args.format), "data": "synthetic (seeded Philox)",
             "config": {"workload": "48-layer stack: hidden 2048, intermediate 768, 128 experts top-8, 1536-entry "
                                    "LRU over 6144 (layer, expert) entries; 2048-token double-buffered prefill, "
-                                   "then decode at batch 32",
-                       "pool_GB": W.L * W.E * 3 * W.H * W.I * 2 / 1e9, "setup_s": round(setup_s, 1),
+                                   "then decode at batch 32" +
+                                   ("" if args.format == "bf16" else f", {args.format.upper()} entries"),
+                       "pool_GB": W.L * W.E * cache_entry_bytes / 1e9, "setup_s": round(setup_s, 1),
                        **_stats_summary(st, ms)},
             "prefill": {"tokens": T, "ms": round(ms_pre, 2), "tok_s": round(T / (ms_pre / 1e3), 1),
                         **_stats_summary(st_pre, ms_pre)},

@@ -63,17 +63,19 @@ def test_stream8_full_size():
     assert st["evictions"] > 0  # the 614-entry cache filled up and the LRU chose victims
 
 
-def test_stack48_full_size_prefill_then_decode():
+@pytest.mark.parametrize("fmt", ["bf16", "mxfp4"])
+def test_stack48_full_size_prefill_then_decode(fmt):
     import torch
     W = mi.WORKLOADS["stack48"]
     T, B, steps = 2048, 32, 2
-    ents = hz.OracleEntries(W)
+    ents = hz.OracleEntries(W, fp4=fmt == "mxfp4")
+    fmt_flag = moe.MOE_MXFP4 if fmt == "mxfp4" else 0
     routers = [mi.router_weights(W.seed, l, W.E, W.H) for l in range(W.L)]
     biases = [mi.router_bias(W.seed, l, W.E, W.zipf_s)[0] for l in range(W.L)]
     check_layers = {0, 1, 24, W.L - 1}
     rows = np.arange(0, T, 97)  # sampled prefill tokens
     accesses = [(1, 0, e) for e in range(W.E)]
-    with hz.make_cache(W, max_tokens=T, flags=moe.MOE_TRACE | moe.MOE_PREFILL_DB) as cache:
+    with hz.make_cache(W, max_tokens=T, flags=moe.MOE_TRACE | moe.MOE_PREFILL_DB | fmt_flag) as cache:
         Wr_d = [hz.f32_dev(r) for r in routers]
         b_d = [hz.f32_dev(b) for b in biases]
         cache.cache_fill(0, None, moe.MOE_FILL_FULL_LAYER)

@@ -6,7 +6,8 @@
   every step: routing, outputs and the whole LRU trace.
 * A 6-layer stack (128 experts top-8): a prefill with full-layer double buffering -- layer
   l+1's whole expert set is prefetched on the copy stream right after layer l's compute is
-  enqueued -- then decode steps at batch 32. The trace includes the prefetch events.
+  enqueued -- then decode steps at batch 32. The trace includes the prefetch events. With bf16,
+  MXFP4 and NVFP4 entries (the 4-bit prefill runs on the decode kernels, in token chunks).
 
 Layer inputs are fresh seeded activations per (step, layer): the oracle never takes an
 input from the GPU path.
@@ -68,17 +69,28 @@ def test_decode_stream_8_layers():
     assert 0 < st["hits"] < st["expert_reads"]
 
 
-def test_stack_prefill_double_buffered_then_decode():
+FORMATS = {"bf16": 0, "mxfp4": moe.MOE_MXFP4, "nvfp4": moe.MOE_NVFP4}
+
+
+def _layer_ref(fmt, ents, l, W, x, r, idx_o, w_o):
+    """The oracle's layer on the format's own reading of the entries."""
+    if fmt == "nvfp4":
+        return oracle.moe_layer_rows_f64(ents.layer(l), W.H, W.I, x, r, idx_o, w_o)
+    return oracle.moe_layer_rows(ents.layer(l), W.H, W.I, x, r, idx_o, w_o)
+
+
+@pytest.mark.parametrize("fmt", list(FORMATS))
+def test_stack_prefill_double_buffered_then_decode(fmt):
     import torch
     base = mi.WORKLOADS["stack48"]
     L = 6
     W = mi.Workload("stack-small", 256, 128, base.E, base.k, L, 2 * base.E, base.zipf_s)
     T_pre, B, steps = 256, 32, 3
-    ents = hz.OracleEntries(W)
+    ents = hz.OracleEntries(W, fp4=fmt == "mxfp4", nvfp4=fmt == "nvfp4")
     routers = [mi.router_weights(W.seed, l, W.E, W.H) for l in range(L)]
     biases = [mi.router_bias(W.seed, l, W.E, W.zipf_s)[0] for l in range(L)]
     accesses = []
-    with hz.make_cache(W, max_tokens=T_pre, flags=moe.MOE_TRACE | moe.MOE_PREFILL_DB) as cache:
+    with hz.make_cache(W, max_tokens=T_pre, flags=moe.MOE_TRACE | moe.MOE_PREFILL_DB | FORMATS[fmt]) as cache:
         Wr_d = [hz.f32_dev(r) for r in routers]
         b_d = [hz.f32_dev(b) for b in biases]
         # prefill: prefetch layer 0, then per layer: route, forward, prefetch the next layer
@@ -109,7 +121,7 @@ def test_stack_prefill_double_buffered_then_decode():
                 accesses += [(1, l + 1, e) for e in range(W.E)]
             rows = np.arange(0, T_pre, 17)  # sampled tokens
             r = outs[l][1].cpu().numpy()
-            ref = oracle.moe_layer_rows(ents.layer(l), W.H, W.I, xs[l][rows], r[rows], idx_o[rows], w_o[rows])
+            ref = _layer_ref(fmt, ents, l, W, xs[l][rows], r[rows], idx_o[rows], w_o[rows])
             hz.assert_out_close(outs[l][0].cpu().numpy()[rows], ref, r[rows])
         # decode steps at batch 32 through every layer
         idx, w, out = _bufs(B, W)
@@ -124,7 +136,7 @@ def test_stack_prefill_double_buffered_then_decode():
                 idx_o, w_o, _, _ = oracle.route(x, routers[l], biases[l], W.k)
                 assert np.array_equal(idx.cpu().numpy(), idx_o), (s, l)
                 r = resid.cpu().numpy()
-                ref = oracle.moe_layer_rows(ents.layer(l), W.H, W.I, x, r, idx_o, w_o)
+                ref = _layer_ref(fmt, ents, l, W, x, r, idx_o, w_o)
                 hz.assert_out_close(out.cpu().numpy(), ref, r)
                 accesses += hz.routed_accesses(l, idx_o, W.E)
         st, tr = cache.stats(trace_cap=1 << 20)
