@@ -903,7 +903,7 @@ def run_qstar(args):
     W = mi.WORKLOADS["stream8"]
     steps, B = args.steps, 8
     threads = len(os.sched_getaffinity(0))
-    probe = moe.MoeCache(moe.LayerShape(1, 1, W.H, W.I, W.k, 1, 1))
+    probe = moe.MoeCache(moe.LayerShape(1, 1, W.H, W.I, 1, 1, 1))  # one expert entry, top-1
     fill_pool(probe, W, 1, 1)
     bw = probe.measure_bandwidth(threads, reps=8)
     probe.close()

@@ -24,8 +24,8 @@
 // weights are one contiguous run of stages.
 //
 // Where the bytes go, per stage and SM: the raw stage lands in shared memory by one bulk copy;
-// each converter thread reads its row's 32 code bytes (two 16-byte reads, in a lane-rotated
-// order so that every quarter-warp read is bank-conflict free) and its scale bytes, looks up
+// each converter thread reads its row's 32 code bytes (two 16-byte reads) and its scale bytes,
+// looks up
 // one 16-byte table per block scale, expands 64 codes with byte permutes (15 integer
 // operations per 8 codes) and writes the 64 bf16 values into its row's TMEM lane with one
 // tcgen05.st; the MMA then takes A from tensor memory (tcgen05.mma with an A address in TMEM)
@@ -76,6 +76,8 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemA = 2 * kNMax;         // first A column: the accumulators take 0 .. 127
 constexpr uint32_t kACols = BK / 2;            // 64 bf16 of K per row = 32 columns
 constexpr int kLutBytes = 256 * 16;            // byte tables of every scale byte, built once per CTA
+constexpr int kWorkSmem = 256;                 // work entries kept in shared memory (a wave of <= 255 experts)
+constexpr int kWorkBytes = kWorkSmem * static_cast<int>(sizeof(GemvWork));
 
 static_assert(kGroupWarps == 4, "a converter group covers the four TMEM lane quadrants");
 static_assert(kTmemA + kMma * kACols <= kTmemCols, "TMEM columns");
@@ -95,8 +97,8 @@ template <int FMT, bool GATEUP>
 struct Layout {
     static constexpr int RAW = Fp4Fmt<FMT>::kRawStage;
     static constexpr int XCHG_BYTES = GATEUP ? kXchgFloats * 4 : 0;
-    static constexpr int SMEM =
-        kMma * kB16 + kRawStages * RAW + XCHG_BYTES + kLutBytes + static_cast<int>(sizeof(Shared)) + 1024;
+    static constexpr int SMEM = kMma * kB16 + kRawStages * RAW + XCHG_BYTES + kLutBytes + kWorkBytes +
+                                static_cast<int>(sizeof(Shared)) + 1024;
     static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
 };
 
@@ -143,6 +145,19 @@ __device__ __forceinline__ void expand8(uint32_t v, const uint4& t, uint32_t* w)
     w[3] = prmt(lb, hb, 0x7362);
 }
 
+// locate_unit over a work list in shared or global memory (generic loads).
+__device__ __forceinline__ Unit locate_unit_any(const GemvWork* work, int n_work, int u, int R, int S) {
+    int lo = 0, hi = n_work - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (work[mid].unit_begin <= u) lo = mid;
+        else hi = mid - 1;
+    }
+    const int local = u - work[lo].unit_begin;
+    const int rest = local / S;
+    return Unit{lo, rest / R, rest % R, local % S};
+}
+
 // Every lane waits; the warp goes on only if all lanes saw the phase complete (a warp-uniform
 // outcome, so the warp-collective tcgen05 operations that follow stay convergent).
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint64_t deadline_ns) {
@@ -171,7 +186,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* raw_tiles = b_tiles + kMma * kB16;
     float* xchg = reinterpret_cast<float*>(raw_tiles + kRawStages * RAW);
     uint4* scale_lut = reinterpret_cast<uint4*>(raw_tiles + kRawStages * RAW + Lay::XCHG_BYTES);
-    Shared& sh = *reinterpret_cast<Shared*>(raw_tiles + kRawStages * RAW + Lay::XCHG_BYTES + kLutBytes);
+    GemvWork* work_sm = reinterpret_cast<GemvWork*>(raw_tiles + kRawStages * RAW + Lay::XCHG_BYTES + kLutBytes);
+    Shared& sh =
+        *reinterpret_cast<Shared*>(raw_tiles + kRawStages * RAW + Lay::XCHG_BYTES + kLutBytes + kWorkBytes);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int K = GATEUP ? H : I;
     const int KB = K / BK;
@@ -199,6 +216,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_relinquish();
     }
     for (int sc = threadIdx.x; sc < 256; sc += kThreads) scale_lut[sc] = scale_tables<FMT>(static_cast<uint32_t>(sc));
+    // the wave's work list (with its closing total entry) in shared memory, when it fits: the
+    // producer, MMA and converter roles look their units up there
+    const bool work_in_smem = n_work + 1 <= kWorkSmem;
+    if (work_in_smem)
+        for (int i = threadIdx.x; i <= n_work; i += kThreads) work_sm[i] = work[i];
+    const GemvWork* wl = work_in_smem ? work_sm : work;
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -212,8 +235,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             int ready_a = -1;
             for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-                const Unit un = locate_unit(work, n_work, u, R, S);
-                const GemvWork wk = work[un.a];
+                const Unit un = locate_unit_any(wl, n_work, u, R, S);
+                const GemvWork wk = wl[un.a];
                 if (wk.wait_slot >= 0 && un.a != ready_a) {
                     if (!wait_fill_flag(fill_flag + wk.wait_slot, wk.gen, fill_wait_ns)) {
                         raise_status(status, kDevFillTimeout);
@@ -261,8 +284,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t last_acc_phase = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-                const Unit un = locate_unit(work, n_work, u, R, S);
-                const GemvWork wk = work[un.a];
+                const Unit un = locate_unit_any(wl, n_work, u, R, S);
+                const GemvWork wk = wl[un.a];
                 const int nt = min(kNMax, wk.n_tok - un.chunk * kNMax);
                 const uint32_t idesc = idesc_bf16_f32(128, ((nt + 15) >> 4) * 16);
                 const int kb0 = un.split * KB / S, kb1 = (un.split + 1) * KB / S;
@@ -314,21 +337,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q = warp & 3;                 // TMEM lane quadrant of this warp
         const int row = q * 32 + lane;          // the A row (= TMEM lane) this thread expands
         const bool token_loader = (c % (32 * kGroupWarps)) == 0;
-        const uint32_t rot = (lane >> 2) & 1u;  // read order of the row's two 16-byte halves
         const uint32_t t_row = tmem + (static_cast<uint32_t>(q * 32) << 16) + kTmemA;
         if (token_loader) prefetch_tmap(&tm_b);
         uint32_t used = 0, last_phase = 0;
         bool ok = true;
-        int n = 0;  // stage index over the whole run, as the producer and the MMA issuer count it
+        int n0 = 0;  // stage index of the unit's first stage over the whole run (as the producer
+                     // and the MMA issuer count stages)
         for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-            const Unit un = locate_unit(work, n_work, u, R, S);
-            const GemvWork wk = work[un.a];
+            const Unit un = locate_unit_any(wl, n_work, u, R, S);
+            const GemvWork wk = wl[un.a];
             const int tok0 = wk.tok_off + un.chunk * kNMax;
             const int nt = min(kNMax, wk.n_tok - un.chunk * kNMax);
             const int nb = (nt + 15) >> 4;
             const int kb0 = un.split * KB / S, kb1 = (un.split + 1) * KB / S;
-            for (int kb = kb0; kb < kb1; ++kb, ++n) {
-                if (n % kConvGroups != grp) continue;
+            // this group's stages of the unit: n = n0 + (kb - kb0) with n % kConvGroups == grp
+            const int first = kb0 + ((grp - n0 % kConvGroups) + kConvGroups) % kConvGroups;
+            for (int kb = first; kb < kb1; kb += kConvGroups) {
+                const int n = n0 + (kb - kb0);
                 const int rs = n % kRawStages, ms = n % kMma;
                 const uint32_t rphase = (n / kRawStages) & 1, mphase = (n / kMma) & 1;
                 if (!warp_wait(&sh.raw_full[rs], rphase, consumer_wait_ns)) {
@@ -337,17 +362,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 const uint8_t* raw = raw_tiles + rs * RAW;
-                // this row's 32 code bytes, the halves in lane-rotated order (lanes 4-7 of each
-                // quarter-warp start with the other half: no bank conflict), and its scale bytes
-                const uint4 h0 = *reinterpret_cast<const uint4*>(raw + row * 32 + 16 * rot);
-                const uint4 h1 = *reinterpret_cast<const uint4*>(raw + row * 32 + 16 * (rot ^ 1u));
+                // this row's 32 code bytes (codes 0 .. 31 and 32 .. 63 of its slab) and its
+                // scale bytes
+                const uint4 a = *reinterpret_cast<const uint4*>(raw + row * 32);
+                const uint4 b = *reinterpret_cast<const uint4*>(raw + row * 32 + 16);
                 uint32_t sb;
                 if (FMT == kFp4Mx) sb = *reinterpret_cast<const uint16_t*>(raw + 4096 + row * 2);
                 else sb = *reinterpret_cast<const uint32_t*>(raw + 4096 + row * 4);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sh.raw_empty[rs]);  // the raw slot may be refilled
-                const uint4 a = rot ? h1 : h0;  // codes 0 .. 31 of the row's slab
-                const uint4 b = rot ? h0 : h1;  // codes 32 .. 63
                 uint32_t w[32];
                 if (FMT == kFp4Mx) {  // one E8M0 scale per 32 codes
                     const uint4 ta = scale_lut[sb & 0xffu], tb = scale_lut[(sb >> 8) & 0xffu];
@@ -394,6 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sh.mma_full[ms]);
             }
+            n0 += kb1 - kb0;
         }
         // the token tiles this thread issued must land before the CTA exits
         if (token_loader)

@@ -41,23 +41,33 @@ using dec::locate_unit;
 using dec::TensorScales;
 using dec::Unit;
 
-constexpr int A_BYTES = 128 * BK * 2;    // 16 KB of weights per stage
-constexpr int B_BYTES = kNMax * BK * 2;  // up to 8 KB of tokens per stage
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int kStages = 8;
+constexpr int A_BYTES = 128 * BK * 2;  // 16 KB of weights per stage
 constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 128;
-constexpr int XCHG_BYTES = kXchgFloats * 4;
+constexpr int kMaxStages = 12;
+
+// NB: the most 16-token boxes of a unit (1: every chunk of the wave has at most 16 tokens, as in
+// almost every decode wave; 4: up to 64). The token tile and the up-value exchange buffer are
+// sized for it, and the stages it leaves room for keep more weight bytes in flight.
+template <int NB>
+struct Cfg {
+    static constexpr int B_BYTES = NB * 16 * BK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int XCHG_BYTES = NB * 16 * 64 * 4;
+    static constexpr int STAGES = NB == 1 ? 12 : 8;
+    static constexpr int SMEM = STAGES * STAGE_BYTES + XCHG_BYTES + 1024 + 1024;  // + barriers, alignment
+    static_assert(STAGES <= kMaxStages, "stage count");
+    static_assert(STAGE_BYTES % 1024 == 0, "stages keep the 1024-byte alignment of the swizzled tiles");
+    static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
+};
 
 struct __align__(8) Shared {
-    uint64_t full[kStages], empty[kStages], acc_full[2], acc_empty[2];
+    uint64_t full[kMaxStages], empty[kMaxStages], acc_full[2], acc_empty[2];
     uint32_t tmem_base;
     int ok[2];
     int last[2];
 };
-
-constexpr int SMEM = kStages * STAGE_BYTES + XCHG_BYTES + static_cast<int>(sizeof(Shared)) + 1024;
-static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
+static_assert(sizeof(Shared) <= 1024, "barrier block");
 
 // One phase of the launch: its work list (closed by the unit total) and K split.
 struct Phase {
@@ -86,19 +96,26 @@ __device__ __forceinline__ bool wait_counter(const int* p, int target, uint64_t 
     return true;
 }
 
+// dn_prefetch: how many W_down stages (16 KB boxes) of its own down units each CTA prefetches into
+// L2 while it streams its gate/up units (one per gate/up stage), so that a small wave's down
+// phase -- which can only start once the h rows exist -- reads its weights from L2.
+template <int NB>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_fused_kernel(const __grid_constant__ CUtensorMap tm_wgu, const __grid_constant__ CUtensorMap tm_wd,
                         const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_h, Phase gu,
                         Phase dn, const int32_t* __restrict__ slot_row, const uint32_t* __restrict__ fill_flag, int H,
                         int I, uint16_t* __restrict__ h_perm, const float* __restrict__ w_perm,
                         float* __restrict__ pair_out, float* __restrict__ ws, int* __restrict__ cnt,
-                        int* __restrict__ h_ready, int* __restrict__ h_done, int* status, uint64_t fill_wait_ns) {
+                        int* __restrict__ h_ready, int* __restrict__ h_done, int* status, uint64_t fill_wait_ns,
+                        int dn_prefetch) {
     pdl_gate();
+    using C = Cfg<NB>;
+    constexpr int kStages = C::STAGES, STAGE_BYTES = C::STAGE_BYTES;
     const uint64_t consumer_wait_ns = fill_wait_ns + kWaitDeadlineNs;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float* xchg = reinterpret_cast<float*>(tiles + kStages * STAGE_BYTES);
-    Shared& sh = *reinterpret_cast<Shared*>(tiles + kStages * STAGE_BYTES + XCHG_BYTES);
+    Shared& sh = *reinterpret_cast<Shared*>(tiles + kStages * STAGE_BYTES + C::XCHG_BYTES);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int R_gu = I / 64, R_d = H / 128;
     const int n_total = gu.n_units + dn.n_units;
@@ -138,6 +155,36 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0, used = 0, last_phase = 0;
             bool ok = true;
             int ready_key = -1;  // (phase, entry) whose fill this CTA last saw land
+            // L2 prefetch cursor over this CTA's down units: unit index pf_g, stage pf_kb
+            int pf_left = dn_prefetch, pf_g = -1, pf_kb = 0, pf_kb1 = 0, pf_row = 0;
+            auto prefetch_next = [&]() {
+                while (pf_left > 0) {
+                    if (pf_g >= 0 && pf_kb < pf_kb1) {
+                        tma_prefetch_l2_2d(&tm_wd, pf_kb * BK, pf_row);
+                        ++pf_kb;
+                        --pf_left;
+                        return;
+                    }
+                    // the next down unit of this CTA
+                    pf_g = pf_g < 0 ? blockIdx.x : pf_g + static_cast<int>(gridDim.x);
+                    while (pf_g < gu.n_units) pf_g += gridDim.x;
+                    if (pf_g >= n_total) {
+                        pf_left = 0;
+                        return;
+                    }
+                    const Unit pu = locate_unit(dn.work, dn.n_work, pf_g - gu.n_units, R_d, dn.S);
+                    const GemvWork pw = dn.work[pu.a];
+                    const int ps = slot_row[pw.expert];
+                    if (ps < 0 || pw.wait_slot >= 0) {  // not resident yet: nothing to prefetch
+                        pf_kb = pf_kb1 = 0;
+                        continue;
+                    }
+                    const int KBd = I / BK;
+                    pf_kb = pu.split * KBd / dn.S;
+                    pf_kb1 = (pu.split + 1) * KBd / dn.S;
+                    pf_row = ps * 3 * H + 2 * H + pu.tile * 128;
+                }
+            };
             for (int g = blockIdx.x; g < n_total && ok; g += gridDim.x) {
                 const bool is_gu = g < gu.n_units;
                 const Phase ph = is_gu ? gu : dn;
@@ -165,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int nb = (nt + 15) >> 4;  // 16-row token boxes
                 const int KB = (is_gu ? H : I) / BK;
                 const int kb0 = un.split * KB / ph.S, kb1 = (un.split + 1) * KB / ph.S;
-                const uint32_t tx = A_BYTES + nb * 16 * BK * 2;
+                const uint32_t tx = A_BYTES + nb * 16 * BK * 2;  // nb <= NB (the host checked)
                 auto load_a = [&](int st, int kb) {
                     uint8_t* sa = tiles + st * STAGE_BYTES;
                     if (is_gu) {
@@ -202,21 +249,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // weights first for as many stages as the ring holds, then the h rows once
                     // every gate/up tile of this (expert, chunk) has written them
                     const int pre = min(kb1 - kb0, kStages);
-                    int sts[kStages];
+                    const int st0 = stage;  // the pre stages are consecutive in the ring
                     for (int i = 0; i < pre && ok; ++i) {
-                        ok = take_stage(sts[i]);
-                        if (ok) load_a(sts[i], kb0 + i);
+                        int st;
+                        ok = take_stage(st);
+                        if (ok) load_a(st, kb0 + i);
                     }
                     if (!ok) break;
+                    auto pre_stage = [&](int i) { return (st0 + i) % kStages; };
                     const int chunk_id = wk.pad0 + un.chunk;
                     if (!wait_counter(h_ready + chunk_id, R_gu, consumer_wait_ns)) {
                         raise_status(status, kDevWaitTimeout);
                         // the issued stages still expect their token bytes: complete them with
                         // the (unused) rows so that every transaction count is met before exit
-                        for (int i = 0; i < pre; ++i) load_b(sts[i], kb0 + i);
+                        for (int i = 0; i < pre; ++i) load_b(pre_stage(i), kb0 + i);
                         break;
                     }
-                    for (int i = 0; i < pre; ++i) load_b(sts[i], kb0 + i);
+                    for (int i = 0; i < pre; ++i) load_b(pre_stage(i), kb0 + i);
                     // this unit no longer reads the counters; the last reader of the chunk resets
                     // them for the next launch
                     const int readers = R_d * dn.S;
@@ -234,6 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     load_a(st, kb);
                     load_b(st, kb);
+                    if (is_gu) prefetch_next();  // one down stage into L2 per gate/up stage
                 }
             }
             // every issued copy must land before the CTA exits
@@ -365,21 +415,49 @@ void decode_fused_choose_split(const int* chunk_tok, int n_chunks, int H, int I,
     *S_d_out = best_d;
 }
 
+namespace {
+
+template <int NB>
+cudaError_t launch_nb(const DecodeMaps& m, Phase gu, Phase dn, const int32_t* slot_row, const uint32_t* fill_flag,
+                      int H, int I, uint16_t* h_perm, const float* w_perm, float* pair_out, float* ws, int* cnt,
+                      int* h_ready, int* h_done, int* status, uint64_t fill_wait_ns, int grid, int dn_prefetch,
+                      cudaStream_t st) {
+    auto kern = decode_fused_kernel<NB>;
+    constexpr int smem = Cfg<NB>::SMEM;
+    static std::atomic<uint64_t> attr{0};
+    const cudaError_t e = ensure_smem_limit(kern, smem, attr);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, st, m.a_gu, m.a_d, m.b_x, m.b_h, gu, dn, slot_row,
+                      fill_flag, H, I, h_perm, w_perm, pair_out, ws, cnt, h_ready, h_done, status, fill_wait_ns,
+                      dn_prefetch);
+}
+
+}  // namespace
+
 cudaError_t launch_decode_fused(const DecodeMaps& m, const GemvWork* work_gu, int n_work, int units_gu, int S_gu,
-                                const GemvWork* work_d, int units_d, int S_d, const int32_t* slot_row,
-                                const uint32_t* fill_flag, int H, int I, uint16_t* h_perm, const float* w_perm,
-                                float* pair_out, float* ws, int* cnt, int* h_ready, int* h_done, int* status,
-                                uint64_t fill_wait_ns, int num_sms, cudaStream_t st) {
+                                const GemvWork* work_d, int units_d, int S_d, int max_chunk_tok,
+                                const int32_t* slot_row, const uint32_t* fill_flag, int H, int I, uint16_t* h_perm,
+                                const float* w_perm, float* pair_out, float* ws, int* cnt, int* h_ready, int* h_done,
+                                int* status, uint64_t fill_wait_ns, int num_sms, cudaStream_t st) {
     if (units_gu <= 0 || units_d <= 0 || n_work <= 0) return cudaSuccess;
     if (S_gu < 1 || S_gu > kDecodeMaxSplit || S_d < 1 || S_d > kDecodeMaxSplit) return cudaErrorInvalidValue;
     if ((S_gu > 1 || S_d > 1) && units_gu + units_d > kDecodeSplitUnits) return cudaErrorInvalidValue;
-    static std::atomic<uint64_t> attr{0};
-    const cudaError_t e = ensure_smem_limit(decode_fused_kernel, SMEM, attr);
-    if (e != cudaSuccess) return e;
+    if (max_chunk_tok < 1 || max_chunk_tok > kNMax) return cudaErrorInvalidValue;
     const int grid = std::min(units_gu + units_d, num_sms);
-    return launch_pdl(decode_fused_kernel, dim3(grid), dim3(kThreads), SMEM, st, m.a_gu, m.a_d, m.b_x, m.b_h,
-                      Phase{work_gu, n_work, units_gu, S_gu}, Phase{work_d, n_work, units_d, S_d}, slot_row,
-                      fill_flag, H, I, h_perm, w_perm, pair_out, ws, cnt, h_ready, h_done, status, fill_wait_ns);
+    // a small wave's W_down (up to 80 MB: well inside L2) is prefetched into L2 during gate/up,
+    // every stage of each CTA's down units, at most 64 stages (1 MB) per CTA
+    const double down_bytes = static_cast<double>(n_work) * H * I * 2;
+    int dn_prefetch = 0;
+    if (down_bytes <= 80e6) {
+        const int per_cta = (units_d + grid - 1) / grid;
+        dn_prefetch = std::min(64, per_cta * ((I / BK + S_d - 1) / S_d));
+    }
+    const Phase gu{work_gu, n_work, units_gu, S_gu}, dn{work_d, n_work, units_d, S_d};
+    if (max_chunk_tok <= 16)
+        return launch_nb<1>(m, gu, dn, slot_row, fill_flag, H, I, h_perm, w_perm, pair_out, ws, cnt, h_ready, h_done,
+                            status, fill_wait_ns, grid, dn_prefetch, st);
+    return launch_nb<4>(m, gu, dn, slot_row, fill_flag, H, I, h_perm, w_perm, pair_out, ws, cnt, h_ready, h_done,
+                        status, fill_wait_ns, grid, dn_prefetch, st);
 }
 
 }  // namespace moe

@@ -117,8 +117,9 @@ cudaError_t launch_decode_down(const DecodeMaps& maps, const GemvWork* work, int
 // before the first launch (every launch leaves them zero). The down phase's split-K tiles follow
 // the gate/up phase's in ws and cnt.
 int decode_fused_chunk_slots(int E, int P);
+// max_chunk_tok: the most tokens of any chunk of the wave (<= 16 selects the small-token kernel).
 cudaError_t launch_decode_fused(const DecodeMaps& maps, const GemvWork* work_gu, int n_work, int units_gu, int S_gu,
-                                const GemvWork* work_d, int units_d, int S_d, const int32_t* slot_row,
+                                const GemvWork* work_d, int units_d, int S_d, int max_chunk_tok, const int32_t* slot_row,
                                 const uint32_t* fill_flag, int H, int I, uint16_t* h_perm, const float* w_perm,
                                 float* pair_out, float* ws, int* cnt, int* h_ready, int* h_done, int* status,
                                 uint64_t fill_wait_ns, int num_sms, cudaStream_t st);

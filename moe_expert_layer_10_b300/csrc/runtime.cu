@@ -1300,13 +1300,15 @@ int moe_layer_forward(moe_ctx* c, int layer, const void* x, const float* resid, 
         const int nw = a1 - a0;
         const bool fused = !c->fp4 && path != MOE_PATH_GEMV_UNFUSED;
         const int Rg = moe::decode_row_tiles(true, H, I), Rd = moe::decode_row_tiles(false, H, I);
-        int Sg = 1, Sd = 1;
+        int Sg = 1, Sd = 1, max_chunk_tok = 1;
         if (fused) {
             std::vector<int> chunk_tok;
             for (int i = 0; i < nw; ++i) {
                 const int e = distinct[order[i]];
-                for (int ch = 0; ch < moe::decode_token_chunks(count[e]); ++ch)
+                for (int ch = 0; ch < moe::decode_token_chunks(count[e]); ++ch) {
                     chunk_tok.push_back(std::min(64, count[e] - 64 * ch));
+                    max_chunk_tok = std::max(max_chunk_tok, chunk_tok.back());
+                }
             }
             moe::decode_fused_choose_split(chunk_tok.data(), static_cast<int>(chunk_tok.size()), H, I, c->num_sms,
                                            &Sg, &Sd);
@@ -1350,7 +1352,8 @@ int moe_layer_forward(moe_ctx* c, int layer, const void* x, const float* resid, 
         if (fused) {
             ProfScope ps(c, kDecodeFused, gu_bytes + d_bytes, 6.0 * pw * I * H);
             CUDA_TRY(moe::launch_decode_fused(c->dec_maps, c->work_dev, nw, units_gu, Sg, c->work_dev + (E + 1),
-                                              units_d, Sd, slot_row, c->fill_flag, H, I, c->h_perm, c->w_perm,
+                                              units_d, Sd, max_chunk_tok, slot_row, c->fill_flag, H, I, c->h_perm,
+                                              c->w_perm,
                                               c->pair_out, c->dec_ws, c->dec_cnt, c->dec_ready, c->dec_done,
                                               c->status, fill_wait_ns, c->num_sms, c->s_comp));
         } else {
