@@ -13,9 +13,7 @@
 //    at the same time read the same weight tile from L2;
 //  * warp 0 / one lane: TMA producer -- A tile [128 tokens x 64] and B tile [256 rows x 64]
 //    (GEMM1: 128 gate rows + the 128 up rows of the same columns; GEMM2: 256 W_down rows),
-//    128-byte swizzled, into a 4-stage ring (48 KB per stage). GEMM1's A rows are gathered
-//    from the layer input by token (TMA gather4, four rows per copy), so the permuted copy of
-//    x is never written or read;
+//    128-byte swizzled, into a 4-stage ring (48 KB per stage);
 //  * warp 1 / one lane: tcgen05.mma.cta_group::1.kind::f16, M=128 N=256 K=16, fp32
 //    accumulators in TMEM, two accumulator buffers of 256 columns (512 columns);
 //  * warps 2-5: epilogue -- tcgen05.ld of the thread's accumulator row (warp w reads TMEM
@@ -46,7 +44,6 @@ struct __align__(8) Shared {
     uint64_t full[kStages], empty[kStages], acc_full[2], acc_empty[2];
     uint32_t tmem_base;
     int ex[kMaxActive], off[kMaxActive], cnt[kMaxActive], mtp[kMaxActive + 1];
-    int rows[BM];  // gate/up with the row gather fused: the token row of each A row of the tile
 };
 constexpr int SMEM_BYTES = kStages * STAGE_BYTES + static_cast<int>(sizeof(Shared)) + 1024;
 
@@ -64,16 +61,12 @@ __device__ __forceinline__ void decode_tile(const Shared& sh, int na, int NT, in
     mt = local % mta;
 }
 
-// perm != nullptr (gate/up only): the A tile's rows are gathered straight from the layer input x
-// (tm_a a map over x [T x H] with a one-row box): A row r of a tile is x[perm[pos] / k] for the
-// tile's permuted position pos, four rows per TMA gather, so x_perm is never written.
 template <bool GATEUP>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                 const int32_t* __restrict__ offsets, const int32_t* __restrict__ active, int a_begin, int a_end,
                 const int32_t* __restrict__ slot_row, int H, int I, uint16_t* __restrict__ h_out,
-                const float* __restrict__ w_perm, float* __restrict__ pair_out, int* status,
-                const int32_t* __restrict__ perm, int k) {
+                const float* __restrict__ w_perm, float* __restrict__ pair_out, int* status) {
     pdl_wait();  // may start while the previous kernel of the stream finishes
     extern __shared__ uint8_t smem_raw[];
     uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -131,30 +124,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
-        // lane 0 issues the copies; with the gather fused, the whole warp first looks up the
-        // tile's 128 token rows (four per lane)
-        const bool gather = GATEUP && perm != nullptr;
         if (lane == 0) {
             prefetch_tmap(&tm_a);
             prefetch_tmap(&tm_b);
-        }
-        int stage = 0;
-        uint32_t phase = 0, used = 0, last_phase = 0;
-        bool ok = true;
-        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-            int a, nt, mt;
-            decode_tile(sh, na, NT, t, a, nt, mt);
-            if (gather) {
-                // rows past the expert's tokens read the expert's first row (their results are
-                // never stored)
-                for (int r = lane; r < BM; r += 32) {
-                    const int m = mt * BM + r;
-                    const int pos = sh.off[a] + (m < sh.cnt[a] ? m : 0);
-                    sh.rows[r] = __ldg(perm + pos) / k;
-                }
-                __syncwarp();
-            }
-            if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0, used = 0, last_phase = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+                int a, nt, mt;
+                decode_tile(sh, na, NT, t, a, nt, mt);
                 int slot = slot_row[sh.ex[a]];
                 if (slot < 0) {
                     raise_status(status, kDevBadSlot);
@@ -171,14 +149,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     uint8_t* sa = tiles + stage * STAGE_BYTES;
                     mbar_arrive_expect_tx(&sh.full[stage], STAGE_BYTES);
-                    if (gather) {
-#pragma unroll 4
-                        for (int g = 0; g < BM / 4; ++g)  // 4 rows x 128 bytes per gather, swizzled like a tile
-                            tma_gather4(sa + g * 4 * BK * 2, &tm_a, &sh.full[stage], kb * BK, sh.rows[4 * g],
-                                        sh.rows[4 * g + 1], sh.rows[4 * g + 2], sh.rows[4 * g + 3]);
-                    } else {
-                        tma_load_2d(sa, &tm_a, &sh.full[stage], kb * BK, row_a);
-                    }
+                    tma_load_2d(sa, &tm_a, &sh.full[stage], kb * BK, row_a);
                     tma_load_2d(sa + A_BYTES, &tm_b, &sh.full[stage], kb * BK, row_b);
                     tma_load_2d(sa + A_BYTES + B_BYTES / 2, &tm_b, &sh.full[stage], kb * BK, row_b2);
                     used |= 1u << stage;
@@ -189,13 +160,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-            __syncwarp();  // lane 0 has read this tile's rows before the next tile's are written
-        }
-        if (lane == 0)
             for (int s = 0; s < kStages; ++s)
                 if ((used >> s) & 1u)
                     if (!mbar_wait(&sh.full[s], (last_phase >> s) & 1u)) raise_status(status, kDevWaitTimeout);
+        }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
@@ -312,8 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <bool GATEUP>
 cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const int32_t* offsets, const int32_t* active,
                    int a_begin, int a_end, int total_tiles, const int32_t* slot_row, int H, int I, uint16_t* h_out,
-                   const float* w_perm, float* pair_out, int* status, int num_sms, cudaStream_t st,
-                   const int32_t* perm = nullptr, int k = 1) {
+                   const float* w_perm, float* pair_out, int* status, int num_sms, cudaStream_t st) {
     if (a_end <= a_begin || total_tiles <= 0) return cudaSuccess;
     if (a_end - a_begin > kMaxActive) return cudaErrorInvalidValue;
     auto kern = gemm_kernel<GATEUP>;
@@ -322,7 +289,7 @@ cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const int32_t* 
     if (e != cudaSuccess) return e;
     const int grid = std::min(total_tiles, num_sms);
     return launch_pdl(kern, dim3(grid), dim3(kThreads), SMEM_BYTES, st, ta, tb, offsets, active, a_begin, a_end,
-                      slot_row, H, I, h_out, w_perm, pair_out, status, perm, k);
+                      slot_row, H, I, h_out, w_perm, pair_out, status);
 }
 
 }  // namespace
@@ -335,11 +302,7 @@ int gemm_tiles(bool gateup, const int* counts, int n, int H, int I) {
 
 cudaError_t launch_gemm_gateup(const GemmMaps& m, const int32_t* offsets, const int32_t* active, int a_begin,
                                int a_end, int total_tiles, const int32_t* slot_row, int H, int I, uint16_t* h_perm,
-                               int* status, int num_sms, cudaStream_t st, const CUtensorMap* x_rows,
-                               const int32_t* perm, int k) {
-    if (x_rows)
-        return launch<true>(*x_rows, m.b_gu, offsets, active, a_begin, a_end, total_tiles, slot_row, H, I, h_perm,
-                            nullptr, nullptr, status, num_sms, st, perm, k);
+                               int* status, int num_sms, cudaStream_t st) {
     return launch<true>(m.a_x, m.b_gu, offsets, active, a_begin, a_end, total_tiles, slot_row, H, I, h_perm,
                         nullptr, nullptr, status, num_sms, st);
 }

@@ -196,12 +196,9 @@ struct GemmMaps {
     CUtensorMap b_d;    // arena [C*3H rows x I], box 64 x 128
 };
 int gemm_tiles(bool gateup, const int* counts, int n, int H, int I);  // grid bound for a wave
-// x_rows (or null: A from x_perm): a map over the layer input x [T x H] with a 64 x 1 box and
-// 128-byte swizzle; A row r of a tile is then x[perm[pos] / k] (TMA gather, no x_perm).
 cudaError_t launch_gemm_gateup(const GemmMaps& maps, const int32_t* offsets, const int32_t* active, int a_begin,
                                int a_end, int total_tiles, const int32_t* slot_row, int H, int I, uint16_t* h_perm,
-                               int* status, int num_sms, cudaStream_t st, const CUtensorMap* x_rows = nullptr,
-                               const int32_t* perm = nullptr, int k = 1);
+                               int* status, int num_sms, cudaStream_t st);
 cudaError_t launch_gemm_down(const GemmMaps& maps, const int32_t* offsets, const int32_t* active, int a_begin,
                              int a_end, int total_tiles, const int32_t* slot_row, int H, int I, const float* w_perm,
                              float* pair_out, int* status, int num_sms, cudaStream_t st);

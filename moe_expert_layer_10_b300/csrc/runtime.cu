@@ -1165,22 +1165,11 @@ int moe_layer_forward(moe_ctx* c, int layer, const void* x, const float* resid, 
         CUDA_TRY(moe::launch_permute(idx, w, P, E, c->offsets, c->perm, c->inv_perm, c->w_perm, c->active,
                                      c->n_active, c->status, c->perm_cells, c->perm_done, c->s_comp));
     }
-    // The row gather (x_perm for the decode kernels) runs here, hidden behind the host's wait,
-    // unless the layer will likely take the grouped GEMM, whose gate/up kernel gathers x rows
-    // itself (more than 64 pairs per expert on average).
-    auto gather_rows = [&]() -> int {
+    {
         // the method's bytes: each of the T rows read once (L2 serves its k - 1 repeats),
         // each of the P permuted rows written once
         ProfScope ps(c, kGather, 2.0 * T * H + 2.0 * P * H, 0.0);
         CUDA_TRY(moe::launch_gather_rows(static_cast<const uint16_t*>(x), c->perm, P, c->k, H, c->x_perm, c->s_comp));
-        return MOE_OK;
-    };
-    const bool gemm_likely =
-        !c->fp4 && (c->path == MOE_PATH_GEMM || (c->path == MOE_PATH_AUTO && P > kDecodeMaxTokens * E));
-    bool gathered = false;
-    if (!gemm_likely) {
-        if ((rc = gather_rows())) return rc;
-        gathered = true;
     }
     rc = wait_event(c, c->ev_d2h, "routed indices copy");
     if (rc) return rc;
@@ -1210,17 +1199,6 @@ int moe_layer_forward(moe_ctx* c, int layer, const void* x, const float* resid, 
         return fail(MOE_E_INVAL, "4-bit entries run on the decode kernels only (MOE_PATH_GEMM unsupported)");
     if (path == MOE_PATH_AUTO) path = (c->fp4 || max_n <= kDecodeMaxTokens) ? MOE_PATH_GEMV : MOE_PATH_GEMM;
 
-    // the gate/up GEMM gathers x rows itself through a one-row-box map of x (when x's address
-    // allows a tensor map); every other case needs x_perm
-    CUtensorMap x_rows{};
-    const bool fused_gather = !gathered && path == MOE_PATH_GEMM &&
-                              make_map(&x_rows, x, static_cast<uint64_t>(H), static_cast<uint64_t>(T), 64, 1,
-                                       CU_TENSOR_MAP_SWIZZLE_128B);
-    if (!gathered && !fused_gather) {
-        if ((rc = gather_rows())) return rc;
-        gathered = true;
-    }
-
     // 4. waves of at most C experts
     for (int a0 = 0; a0 < U; a0 += c->C) {
         const int a1 = std::min(U, a0 + c->C);
@@ -1249,8 +1227,7 @@ int moe_layer_forward(moe_ctx* c, int layer, const void* x, const float* resid, 
             {
                 ProfScope ps(c, kGemmGateUp, 4.0 * nw * I * H + 2.0 * pw * H + 2.0 * pw * I, 4.0 * pw * I * H);
                 CUDA_TRY(moe::launch_gemm_gateup(c->gemm_maps, c->offsets, c->active, a0, a1, tiles_gu, slot_row, H,
-                                                 I, c->h_perm, c->status, c->num_sms, c->s_comp,
-                                                 fused_gather ? &x_rows : nullptr, c->perm, c->k));
+                                                 I, c->h_perm, c->status, c->num_sms, c->s_comp));
             }
             {
                 ProfScope ps(c, kGemmDown, 2.0 * nw * H * I + 2.0 * pw * I + 4.0 * pw * H + 4.0 * pw,
