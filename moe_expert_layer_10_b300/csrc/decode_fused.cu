@@ -24,6 +24,9 @@
 // units wait on nothing but fills, and the grid is at most one CTA per SM. It is bounded all the
 // same (the fill deadline plus 2 s), like every wait here, and a timeout raises the device status.
 // Split-K partials of the two phases use disjoint parts of the workspace and counter arrays.
+// Waves whose chunks all have at most 16 tokens (nearly every decode wave) use 18 KB stages, 12
+// in flight. Tried and dropped: prefetching each CTA's down-unit weights into L2 during its
+// gate/up units (batch 1: 63.9 us against 55.2 us without).
 #include <algorithm>
 #include <vector>
 
@@ -96,9 +99,6 @@ __device__ __forceinline__ bool wait_counter(const int* p, int target, uint64_t 
     return true;
 }
 
-// dn_prefetch: how many W_down stages (16 KB boxes) of its own down units each CTA prefetches into
-// L2 while it streams its gate/up units (one per gate/up stage), so that a small wave's down
-// phase -- which can only start once the h rows exist -- reads its weights from L2.
 template <int NB>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_fused_kernel(const __grid_constant__ CUtensorMap tm_wgu, const __grid_constant__ CUtensorMap tm_wd,
@@ -106,8 +106,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         Phase dn, const int32_t* __restrict__ slot_row, const uint32_t* __restrict__ fill_flag, int H,
                         int I, uint16_t* __restrict__ h_perm, const float* __restrict__ w_perm,
                         float* __restrict__ pair_out, float* __restrict__ ws, int* __restrict__ cnt,
-                        int* __restrict__ h_ready, int* __restrict__ h_done, int* status, uint64_t fill_wait_ns,
-                        int dn_prefetch) {
+                        int* __restrict__ h_ready, int* __restrict__ h_done, int* status, uint64_t fill_wait_ns) {
     pdl_gate();
     using C = Cfg<NB>;
     constexpr int kStages = C::STAGES, STAGE_BYTES = C::STAGE_BYTES;
@@ -155,36 +154,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0, used = 0, last_phase = 0;
             bool ok = true;
             int ready_key = -1;  // (phase, entry) whose fill this CTA last saw land
-            // L2 prefetch cursor over this CTA's down units: unit index pf_g, stage pf_kb
-            int pf_left = dn_prefetch, pf_g = -1, pf_kb = 0, pf_kb1 = 0, pf_row = 0;
-            auto prefetch_next = [&]() {
-                while (pf_left > 0) {
-                    if (pf_g >= 0 && pf_kb < pf_kb1) {
-                        tma_prefetch_l2_2d(&tm_wd, pf_kb * BK, pf_row);
-                        ++pf_kb;
-                        --pf_left;
-                        return;
-                    }
-                    // the next down unit of this CTA
-                    pf_g = pf_g < 0 ? blockIdx.x : pf_g + static_cast<int>(gridDim.x);
-                    while (pf_g < gu.n_units) pf_g += gridDim.x;
-                    if (pf_g >= n_total) {
-                        pf_left = 0;
-                        return;
-                    }
-                    const Unit pu = locate_unit(dn.work, dn.n_work, pf_g - gu.n_units, R_d, dn.S);
-                    const GemvWork pw = dn.work[pu.a];
-                    const int ps = slot_row[pw.expert];
-                    if (ps < 0 || pw.wait_slot >= 0) {  // not resident yet: nothing to prefetch
-                        pf_kb = pf_kb1 = 0;
-                        continue;
-                    }
-                    const int KBd = I / BK;
-                    pf_kb = pu.split * KBd / dn.S;
-                    pf_kb1 = (pu.split + 1) * KBd / dn.S;
-                    pf_row = ps * 3 * H + 2 * H + pu.tile * 128;
-                }
-            };
             for (int g = blockIdx.x; g < n_total && ok; g += gridDim.x) {
                 const bool is_gu = g < gu.n_units;
                 const Phase ph = is_gu ? gu : dn;
@@ -283,7 +252,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     load_a(st, kb);
                     load_b(st, kb);
-                    if (is_gu) prefetch_next();  // one down stage into L2 per gate/up stage
                 }
             }
             // every issued copy must land before the CTA exits
@@ -379,7 +347,7 @@ void decode_fused_choose_split(const int* chunk_tok, int n_chunks, int H, int I,
     const int R_gu = I / 64, R_d = H / 128, KB_gu = H / BK, KB_d = I / BK;
     const double kUnitFixed = 8192.0;
     int best_gu = 1, best_d = 1;
-    double best = -1.0;
+    double best = -1.0, unsplit = 0.0;
     std::vector<double> load(num_sms);
     for (int sg = 1; sg <= kDecodeMaxSplit; ++sg) {
         if (KB_gu / sg < 4) break;
@@ -404,12 +372,21 @@ void decode_fused_choose_split(const int* chunk_tok, int n_chunks, int H, int I,
                 }
             }
             const double mx = *std::max_element(load.begin(), load.end());
+            if (sg == 1 && sd == 1) unsplit = mx;
             if (best < 0 || mx < best * (1.0 - 1e-9)) {
                 best = mx;
                 best_gu = sg;
                 best_d = sd;
             }
         }
+    }
+    // Splits cost more than this model charges (a split's units are smaller, so less of a down
+    // unit's weight stream is already in the ring when its h rows arrive, and each split adds an
+    // epilogue pass): on the decode layer at batch 1 the unsplit launch measured 52.8 us against
+    // 55.2 us for the chosen (1, 3). So a split is taken only if the model predicts 20 % or more.
+    if (best > 0.8 * unsplit) {
+        best_gu = 1;
+        best_d = 1;
     }
     *S_gu_out = best_gu;
     *S_d_out = best_d;
@@ -420,16 +397,14 @@ namespace {
 template <int NB>
 cudaError_t launch_nb(const DecodeMaps& m, Phase gu, Phase dn, const int32_t* slot_row, const uint32_t* fill_flag,
                       int H, int I, uint16_t* h_perm, const float* w_perm, float* pair_out, float* ws, int* cnt,
-                      int* h_ready, int* h_done, int* status, uint64_t fill_wait_ns, int grid, int dn_prefetch,
-                      cudaStream_t st) {
+                      int* h_ready, int* h_done, int* status, uint64_t fill_wait_ns, int grid, cudaStream_t st) {
     auto kern = decode_fused_kernel<NB>;
     constexpr int smem = Cfg<NB>::SMEM;
     static std::atomic<uint64_t> attr{0};
     const cudaError_t e = ensure_smem_limit(kern, smem, attr);
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, st, m.a_gu, m.a_d, m.b_x, m.b_h, gu, dn, slot_row,
-                      fill_flag, H, I, h_perm, w_perm, pair_out, ws, cnt, h_ready, h_done, status, fill_wait_ns,
-                      dn_prefetch);
+                      fill_flag, H, I, h_perm, w_perm, pair_out, ws, cnt, h_ready, h_done, status, fill_wait_ns);
 }
 
 }  // namespace
@@ -444,20 +419,12 @@ cudaError_t launch_decode_fused(const DecodeMaps& m, const GemvWork* work_gu, in
     if ((S_gu > 1 || S_d > 1) && units_gu + units_d > kDecodeSplitUnits) return cudaErrorInvalidValue;
     if (max_chunk_tok < 1 || max_chunk_tok > kNMax) return cudaErrorInvalidValue;
     const int grid = std::min(units_gu + units_d, num_sms);
-    // a small wave's W_down (up to 80 MB: well inside L2) is prefetched into L2 during gate/up,
-    // every stage of each CTA's down units, at most 64 stages (1 MB) per CTA
-    const double down_bytes = static_cast<double>(n_work) * H * I * 2;
-    int dn_prefetch = 0;
-    if (down_bytes <= 80e6) {
-        const int per_cta = (units_d + grid - 1) / grid;
-        dn_prefetch = std::min(64, per_cta * ((I / BK + S_d - 1) / S_d));
-    }
     const Phase gu{work_gu, n_work, units_gu, S_gu}, dn{work_d, n_work, units_d, S_d};
     if (max_chunk_tok <= 16)
         return launch_nb<1>(m, gu, dn, slot_row, fill_flag, H, I, h_perm, w_perm, pair_out, ws, cnt, h_ready, h_done,
-                            status, fill_wait_ns, grid, dn_prefetch, st);
+                            status, fill_wait_ns, grid, st);
     return launch_nb<4>(m, gu, dn, slot_row, fill_flag, H, I, h_perm, w_perm, pair_out, ws, cnt, h_ready, h_done,
-                        status, fill_wait_ns, grid, dn_prefetch, st);
+                        status, fill_wait_ns, grid, st);
 }
 
 }  // namespace moe
