@@ -27,9 +27,9 @@
 // each converter thread reads its row's 32 code bytes (two 16-byte reads) and its scale bytes,
 // looks up
 // one 16-byte table per block scale, expands 64 codes with byte permutes (15 integer
-// operations per 8 codes) and writes the 64 bf16 values into its row's TMEM lane with one
-// tcgen05.st; the MMA then takes A from tensor memory (tcgen05.mma with an A address in TMEM)
-// and only the token tile from shared memory. Keeping the expanded tile out of shared memory
+// operations per 8 codes) and writes the 64 bf16 values into its row's TMEM lane with two
+// tcgen05.st (the first overlaps the second half's expansion); the MMA then takes A from tensor
+// memory (tcgen05.mma with an A address in TMEM) and only the token tile from shared memory. Keeping the expanded tile out of shared memory
 // leaves the shared-memory pipe to the raw stages and the token tiles.
 //
 // Roles (22 warps):
@@ -371,31 +371,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 else sb = *reinterpret_cast<const uint32_t*>(raw + 4096 + row * 4);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sh.raw_empty[rs]);  // the raw slot may be refilled
-                uint32_t w[32];
-                if (FMT == kFp4Mx) {  // one E8M0 scale per 32 codes
-                    const uint4 ta = scale_lut[sb & 0xffu], tb = scale_lut[(sb >> 8) & 0xffu];
-                    expand8(a.x, ta, w + 0);
-                    expand8(a.y, ta, w + 4);
-                    expand8(a.z, ta, w + 8);
-                    expand8(a.w, ta, w + 12);
-                    expand8(b.x, tb, w + 16);
-                    expand8(b.y, tb, w + 20);
-                    expand8(b.z, tb, w + 24);
-                    expand8(b.w, tb, w + 28);
-                } else {  // one E4M3 scale per 16 codes
-                    const uint4 t0 = scale_lut[sb & 0xffu], t1 = scale_lut[(sb >> 8) & 0xffu];
-                    expand8(a.x, t0, w + 0);
-                    expand8(a.y, t0, w + 4);
-                    expand8(a.z, t1, w + 8);
-                    expand8(a.w, t1, w + 12);
-                    const uint4 t2 = scale_lut[(sb >> 16) & 0xffu], t3 = scale_lut[sb >> 24];
-                    expand8(b.x, t2, w + 16);
-                    expand8(b.y, t2, w + 20);
-                    expand8(b.z, t3, w + 24);
-                    expand8(b.w, t3, w + 28);
-                }
                 // the MMA stage is free once the products that read its A columns and token tile
-                // have completed
+                // have completed (usually long before: the converters set the pace)
                 if (!warp_wait(&sh.mma_empty[ms], mphase ^ 1u, consumer_wait_ns)) {
                     if (lane == 0) raise_status(status, kDevWaitTimeout);
                     ok = false;
@@ -410,8 +387,40 @@ __global__ void __launch_bounds__(kThreads, 1)
                     used |= 1u << ms;
                     last_phase = (last_phase & ~(1u << ms)) | (mphase << ms);
                 }
-                __syncwarp();  // converged again for the warp-collective TMEM store
-                tmem_st32(t_row + static_cast<uint32_t>(ms) * kACols, w);
+                __syncwarp();  // converged again for the warp-collective TMEM stores
+                // two halves of 32 codes: the first half's TMEM store runs while the second half
+                // is expanded
+                const uint32_t ta = t_row + static_cast<uint32_t>(ms) * kACols;
+                uint32_t w[16];
+                if (FMT == kFp4Mx) {  // one E8M0 scale per 32 codes
+                    const uint4 t0 = scale_lut[sb & 0xffu];
+                    expand8(a.x, t0, w + 0);
+                    expand8(a.y, t0, w + 4);
+                    expand8(a.z, t0, w + 8);
+                    expand8(a.w, t0, w + 12);
+                } else {  // one E4M3 scale per 16 codes
+                    const uint4 t0 = scale_lut[sb & 0xffu], t1 = scale_lut[(sb >> 8) & 0xffu];
+                    expand8(a.x, t0, w + 0);
+                    expand8(a.y, t0, w + 4);
+                    expand8(a.z, t1, w + 8);
+                    expand8(a.w, t1, w + 12);
+                }
+                tmem_st16(ta, w);
+                uint32_t w2[16];
+                if (FMT == kFp4Mx) {
+                    const uint4 t1 = scale_lut[(sb >> 8) & 0xffu];
+                    expand8(b.x, t1, w2 + 0);
+                    expand8(b.y, t1, w2 + 4);
+                    expand8(b.z, t1, w2 + 8);
+                    expand8(b.w, t1, w2 + 12);
+                } else {
+                    const uint4 t2 = scale_lut[(sb >> 16) & 0xffu], t3 = scale_lut[sb >> 24];
+                    expand8(b.x, t2, w2 + 0);
+                    expand8(b.y, t2, w2 + 4);
+                    expand8(b.z, t3, w2 + 8);
+                    expand8(b.w, t3, w2 + 12);
+                }
+                tmem_st16(ta + 16, w2);
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
