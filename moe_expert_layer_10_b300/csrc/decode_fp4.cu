@@ -64,12 +64,12 @@ struct Fp4Fmt {
     static_assert(kRawStage % 16 == 0, "bulk copies move multiples of 16 bytes");
 };
 
+constexpr int kConvGroups = 4;                 // converter groups of 4 warps (one per TMEM lane quadrant)
 constexpr int kRawStages = 12;
-constexpr int kMma = 8;                        // MMA stages: A in TMEM, token tile in smem
+constexpr int kMma = 2 * kConvGroups;          // MMA stages: A in TMEM, token tile in smem
 constexpr int kB16 = kNMax * BK * 2;           // token tile: up to 8 KB
-constexpr int kConvWarps = 16;
-constexpr int kConvGroups = 4;
-constexpr int kGroupWarps = kConvWarps / kConvGroups;
+constexpr int kGroupWarps = 4;
+constexpr int kConvWarps = kGroupWarps * kConvGroups;
 constexpr int kConvBase = 192;                 // first converter thread
 constexpr int kThreads = kConvBase + 32 * kConvWarps;
 constexpr uint32_t kTmemCols = 512;
