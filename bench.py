@@ -169,6 +169,13 @@ class ClockSampler:
 FORMAT_FLAGS = {"bf16": 0, "mxfp4": 16, "nvfp4": 32}  # MOE_MXFP4, MOE_NVFP4
 
 
+def forward_launches(P: int) -> int:
+    """This library's kernels in one layer forward besides the expert waves: the router (logits,
+    top-k), the permutation with the row gather (one launch up to 1024 pairs; else counting,
+    placement and gather) and the combine."""
+    return 2 + (1 if P <= 1024 else 3) + 1
+
+
 def fmt_dtype(fmt: str) -> str:
     return "bf16" if fmt == "bf16" else f"{fmt} weights, bf16 activations, fp32 accumulate"
 
@@ -483,11 +490,12 @@ def run_b300(args, rank, world, local):
         return {n: {"launches": v["launches"], "avg_us": round(1e3 * v["total_ms"] / v["launches"], 2),
                     "GB/s": round(v["bytes"] / (v["total_ms"] / 1e3) / 1e9, 1)}
                 for n, v in ks.items() if v["launches"]}
-    # launches of this library's kernels in the timed region: route (2) + permute, gather,
-    # combine (3) per forward, and per wave one fused expert launch (bf16) or two (4-bit)
-    launches = args.steps * (5 * len(BATCHES)) + (2 if fp4 else 1) * st["waves"]
+    # launches of this library's kernels in the timed region: the fixed ones of each forward,
+    # and per wave one fused expert launch (bf16) or two (4-bit)
+    launches = args.steps * sum(forward_launches(B * W.k) for B in BATCHES) + (2 if fp4 else 1) * st["waves"]
     if device:  # per forward: policy, fill and 4 decode launches for each possible wave
-        launches = args.steps * sum(5 + 6 * ((min(B * W.k, W.E) + C - 1) // C) for B in BATCHES)
+        launches = args.steps * sum(forward_launches(B * W.k) + 6 * ((min(B * W.k, W.E) + C - 1) // C)
+                                    for B in BATCHES)
 
     result = {
         "metric": METRIC, "value": round(tokens / (ms_max / 1e3), 2), "unit": UNIT, "n_gpus": world,
@@ -794,7 +802,7 @@ def run_stream8(args):
                        "policy": "device (CUDA graph per step)" if device else "host",
                        "pool_GB": W.L * W.E * cache_entry_bytes / 1e9, "setup_s": round(setup_s, 1),
                        **_stats_summary(st, ms)},
-            "clocks": clk, "gpu_launches": int(steps * W.L * 5 + (6 if device else 1) * st["waves"])}
+            "clocks": clk, "gpu_launches": int(steps * W.L * forward_launches(B * W.k) + (6 if device else 1) * st["waves"])}
 
 
 def run_stack48(args):
@@ -887,7 +895,7 @@ def run_stack48(args):
                        **_stats_summary(st, ms)},
             "prefill": {"tokens": T, "ms": round(ms_pre, 2), "tok_s": round(T / (ms_pre / 1e3), 1),
                         **_stats_summary(st_pre, ms_pre)},
-            "clocks": clk, "gpu_launches": int(steps * W.L * 5 + st["waves"])}
+            "clocks": clk, "gpu_launches": int(steps * W.L * forward_launches(B * W.k) + st["waves"])}
 
 
 def run_qstar(args):

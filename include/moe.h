@@ -341,6 +341,8 @@ int moe_debug_inject(moe_ctx* ctx, int kind, int count);
 #define MOE_DBG_N_ACTIVE 4   /* int32 [1] */
 #define MOE_DBG_SLOT_TABLE 5 /* int32 [L*E]: device slot table */
 #define MOE_DBG_H_PERM 6     /* bf16 [T*k x inter]: SwiGLU activations per permuted position */
+#define MOE_DBG_X_PERM 7     /* bf16 [T*k x hidden]: token row of each permuted position */
+#define MOE_DBG_W_PERM 8     /* fp32 [T*k]: gate of each permuted position */
 int moe_debug_read(moe_ctx* ctx, int what, void* host_dst, uint64_t bytes);
 
 /*

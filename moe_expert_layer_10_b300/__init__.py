@@ -32,7 +32,7 @@ EXPORTS = ["moe_cache_init", "moe_cache_destroy", "moe_host_entry", "moe_entry_b
            "moe_host_expert_ffn", "moe_qstar_fills", "moe_qstar_simulate"]
 MOE_NOALLOC_MAX_LOGITS = 65536
 MOE_DBG_OFFSETS, MOE_DBG_PERM, MOE_DBG_INV_PERM, MOE_DBG_ACTIVE, MOE_DBG_N_ACTIVE, MOE_DBG_SLOT_TABLE, \
-    MOE_DBG_H_PERM = range(7)
+    MOE_DBG_H_PERM, MOE_DBG_X_PERM, MOE_DBG_W_PERM = range(9)
 
 
 class MoeError(RuntimeError):

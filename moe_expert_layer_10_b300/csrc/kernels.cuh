@@ -59,6 +59,13 @@ int permute_grid(int P);
 cudaError_t launch_permute(const int32_t* idx, const float* w, int P, int E, int32_t* offsets, int32_t* perm,
                            int32_t* inv_perm, float* w_perm, int32_t* active, int32_t* n_active, int* status,
                            int32_t* cells, unsigned* done, cudaStream_t st);
+// Up to 1024 pairs: the permutation and x_perm[pos] = x[perm[pos] / k] in one launch, the
+// same outputs as launch_permute followed by launch_gather_rows.
+bool permute_gathers_rows(int P);
+cudaError_t launch_permute_gather(const int32_t* idx, const float* w, const uint16_t* x, int P, int k, int E, int H,
+                                  int32_t* offsets, int32_t* perm, int32_t* inv_perm, float* w_perm,
+                                  int32_t* active, int32_t* n_active, uint16_t* x_perm, int* status,
+                                  cudaStream_t st);
 // x_perm[pos] = x[perm[pos] / k]  (bf16 rows of H)
 cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* perm, int P, int k, int H, uint16_t* x_perm,
                                cudaStream_t st);

@@ -4,7 +4,9 @@
 //
 // Outputs: offsets[E+1] (first position of each expert), perm[pos] = pair id t*k+j,
 // inv_perm[pair] = pos, w_perm[pos] = gate of that pair, active[] = experts with at
-// least one pair in ascending id, n_active. x_perm rows are gathered by a second kernel.
+// least one pair in ascending id, n_active, and x_perm[pos] = the row of token perm[pos] / k.
+// Up to kSmallPairs pairs (decode batches) one launch does all of it; larger batches run the
+// counting sort, then a row-gather kernel.
 #include "kernels.cuh"
 #include "ptx.cuh"
 
@@ -14,8 +16,10 @@ namespace {
 constexpr int kPermThreads = 1024;
 constexpr int kPermWarps = kPermThreads / 32;
 
-// Exclusive prefix sum over the CTA (1024 threads, one value each); returns the total in *total.
+// Exclusive prefix sum over the CTA (NW warps, one value per thread); returns the total in *total.
+template <int NW = 32>
 __device__ int block_exclusive_scan(int v, int* scratch /* >= 33 ints */, int* total) {
+    static_assert(NW >= 1 && NW <= 32, "one warp scans the warp totals");
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int incl = v;
 #pragma unroll
@@ -26,7 +30,7 @@ __device__ int block_exclusive_scan(int v, int* scratch /* >= 33 ints */, int* t
     if (lane == 31) scratch[warp] = incl;
     __syncthreads();
     if (warp == 0) {
-        int s = scratch[lane];
+        int s = lane < NW ? scratch[lane] : 0;
         int si = s;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -282,6 +286,89 @@ __global__ void __launch_bounds__(kPermThreads) permute_place_kernel(const int32
     }
 }
 
+
+// Up to kSmallPairs pairs (decode batches): the permutation and the row gather in one launch
+// over ceil(P / 8) CTAs. Every CTA stages the P expert ids in shared memory; warp w of CTA g
+// owns pair p = 8 g + w, whose position is its rank in (expert, pair id) order,
+//   pos(p) = #{q : e_q < e_p} + #{q < p : e_q = e_p},
+// counted directly over the staged ids: the stable counting sort's result by definition. The
+// warp writes perm, inv_perm and w_perm and copies token p / k's row into x_perm[pos]. CTA 0
+// also counts the pairs per expert into offsets, the active list and n_active.
+constexpr int kSmallPairs = 1024;
+constexpr int kSmallThreads = 256;
+constexpr int kSmallWarps = kSmallThreads / 32;
+constexpr int kSmallExpertsPerThread = 1024 / kSmallThreads;  // E <= 1024
+
+__global__ void __launch_bounds__(kSmallThreads) permute_gather_small_kernel(
+    const int32_t* __restrict__ idx, const float* __restrict__ w, const uint16_t* __restrict__ x, int P, int k,
+    int E, int H, int32_t* __restrict__ offsets, int32_t* __restrict__ perm, int32_t* __restrict__ inv_perm,
+    float* __restrict__ w_perm, int32_t* __restrict__ active, int32_t* __restrict__ n_active,
+    uint16_t* __restrict__ x_perm, int* status) {
+    pdl_gate();  // may start while the previous kernel of the stream finishes
+    extern __shared__ int smem[];
+    int* es = smem;          // [P] routed expert of each pair (an id outside [0, E) counts as 0)
+    int* cnt = es + P;       // CTA 0: [E] pairs per expert
+    int* scan = cnt + E;     // CTA 0: [33]
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const bool lead = blockIdx.x == 0;
+    if (lead)
+        for (int e = tid; e < E; e += kSmallThreads) cnt[e] = 0;
+    for (int q = tid; q < P; q += kSmallThreads) {
+        int e = idx[q];
+        if (e < 0 || e >= E) {
+            if (lead) raise_status(status, kDevBadIndex);
+            e = 0;
+        }
+        es[q] = e;
+    }
+    __syncthreads();
+    const int p = blockIdx.x * kSmallWarps + warp;
+    if (p < P) {
+        const int ep = es[p];
+        int r = 0;
+        for (int q = lane; q < P; q += 32) {
+            const int eq = es[q];
+            r += (eq < ep || (eq == ep && q < p)) ? 1 : 0;
+        }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
+        if (lane == 0) {
+            perm[r] = p;
+            inv_perm[p] = r;
+            w_perm[r] = w[p];
+        }
+        const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(p / k) * H);
+        uint4* dst = reinterpret_cast<uint4*>(x_perm + static_cast<size_t>(r) * H);
+        for (int c = lane; c < H / 8; c += 32) dst[c] = __ldg(src + c);
+    }
+    if (!lead) return;
+    for (int q = tid; q < P; q += kSmallThreads) atomicAdd(&cnt[es[q]], 1);  // counts: order-free
+    __syncthreads();
+    const int e0 = tid * kSmallExpertsPerThread;
+    int c[kSmallExpertsPerThread];
+    int run = 0, nz = 0;
+#pragma unroll
+    for (int i = 0; i < kSmallExpertsPerThread; ++i) {
+        c[i] = e0 + i < E ? cnt[e0 + i] : 0;
+        run += c[i];
+        nz += c[i] > 0 ? 1 : 0;
+    }
+    int total, nact;
+    int pos = block_exclusive_scan<kSmallWarps>(run, scan, &total);
+    int apos = block_exclusive_scan<kSmallWarps>(nz, scan, &nact);
+#pragma unroll
+    for (int i = 0; i < kSmallExpertsPerThread; ++i) {
+        if (e0 + i < E) {
+            offsets[e0 + i] = pos;
+            pos += c[i];
+            if (c[i] > 0) active[apos++] = e0 + i;
+        }
+    }
+    if (tid == 0) {
+        offsets[E] = total;
+        *n_active = nact;
+    }
+}
 }  // namespace
 
 int permute_grid(int P) { return P > kPermThreads ? (P + kChunkPairs - 1) / kChunkPairs : 1; }
@@ -310,6 +397,19 @@ cudaError_t launch_permute(const int32_t* idx, const float* w, int P, int E, int
     if (err != cudaSuccess) return err;
     return launch_pdl(permute_place_kernel, dim3(G), dim3(kPermThreads), sizeof(int) * kPermWarps * (E + 1), st, idx,
                       w, P, E, static_cast<const int32_t*>(starts), perm, inv_perm, w_perm);
+}
+
+bool permute_gathers_rows(int P) { return P <= kSmallPairs; }
+
+cudaError_t launch_permute_gather(const int32_t* idx, const float* w, const uint16_t* x, int P, int k, int E, int H,
+                                  int32_t* offsets, int32_t* perm, int32_t* inv_perm, float* w_perm,
+                                  int32_t* active, int32_t* n_active, uint16_t* x_perm, int* status,
+                                  cudaStream_t st) {
+    if (P <= 0 || P > kSmallPairs || E > 1024 || H % 8) return cudaErrorInvalidValue;
+    const size_t smem = sizeof(int) * (static_cast<size_t>(P) + E + 33);
+    return launch_pdl(permute_gather_small_kernel, dim3((P + kSmallWarps - 1) / kSmallWarps), dim3(kSmallThreads),
+                      smem, st, idx, w, x, P, k, E, H, offsets, perm, inv_perm, w_perm, active, n_active, x_perm,
+                      status);
 }
 
 cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* perm, int P, int k, int H, uint16_t* x_perm,

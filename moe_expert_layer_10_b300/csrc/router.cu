@@ -201,9 +201,9 @@ __global__ void __launch_bounds__(kTiledThreads, 1) router_logits_tiled_kernel(c
 }
 
 // Small batches (decode): latency-bound, so a CTA first stages its EPB experts' router
-// rows and the whole batch of activations in shared memory, every load in flight at once,
-// then evaluates the same fixed fp32 order from shared memory. Warp w computes expert
-// e0 + w % EPB for tokens t = w / EPB + (8 / EPB) * i.
+// rows and the whole batch of activations in shared memory with asynchronous copies, every
+// one in flight at once, then evaluates the same fixed fp32 order from shared memory. Warp w
+// computes expert e0 + w % EPB for tokens t = w / EPB + (8 / EPB) * i.
 template <int EPB, int TPW>
 __global__ void __launch_bounds__(256) router_logits_staged_kernel(const uint16_t* __restrict__ x,
                                                                    const float* __restrict__ Wr,
@@ -217,14 +217,16 @@ __global__ void __launch_bounds__(256) router_logits_staged_kernel(const uint16_
     const int e0 = blockIdx.x * EPB;
     const int ne = min(EPB, E - e0);
     {
-        const float4* src = reinterpret_cast<const float4*>(Wr + static_cast<size_t>(e0) * H);
-        float4* dst = reinterpret_cast<float4*>(wr);
+        // asynchronous copies: every 16-byte piece of the CTA's share is in flight at once
+        const uint8_t* src = reinterpret_cast<const uint8_t*>(Wr + static_cast<size_t>(e0) * H);
         const int n4 = ne * H / 4;
-        for (int i = threadIdx.x; i < n4; i += 256) dst[i] = __ldg(src + i);
-        const uint4* xsrc = reinterpret_cast<const uint4*>(x);
-        uint4* xdst = reinterpret_cast<uint4*>(xs);
+        for (int i = threadIdx.x; i < n4; i += 256) cp_async16(smem + 16 * i, src + 16 * i);
+        const uint8_t* xsrc = reinterpret_cast<const uint8_t*>(x);
+        uint8_t* xdst = reinterpret_cast<uint8_t*>(xs);
         const int nx = T * H / 8;
-        for (int i = threadIdx.x; i < nx; i += 256) xdst[i] = __ldg(xsrc + i);
+        for (int i = threadIdx.x; i < nx; i += 256) cp_async16(xdst + 16 * i, xsrc + 16 * i);
+        cp_async_commit();
+        cp_async_wait<0>();
     }
     __syncthreads();
     constexpr int WPE = 8 / EPB;  // warps per expert

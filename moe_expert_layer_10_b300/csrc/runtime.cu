@@ -604,6 +604,31 @@ int dev_policy_run(moe_ctx* c, moe::DevPolicyArgs a, bool join) {
     return MOE_OK;
 }
 
+// The permutation of the T * k pairs and the gather of their token rows into x_perm: one
+// launch for decode batches, the counting sort and a row-gather kernel for larger ones.
+int permute_and_gather(moe_ctx* c, const void* x, int T, const int32_t* idx, const float* w) {
+    const int P = T * c->k, E = c->E, H = c->H;
+    const double perm_bytes = 8.0 * P + 12.0 * P + 8.0 * E;
+    // the gather's bytes: each of the T rows read once (L2 serves its k - 1 repeats), each of
+    // the P permuted rows written once
+    const double gather_bytes = 2.0 * T * H + 2.0 * P * H;
+    if (moe::permute_gathers_rows(P)) {
+        ProfScope ps(c, kPermute, perm_bytes + gather_bytes, 0.0);
+        CUDA_TRY(moe::launch_permute_gather(idx, w, static_cast<const uint16_t*>(x), P, c->k, E, H, c->offsets,
+                                            c->perm, c->inv_perm, c->w_perm, c->active, c->n_active, c->x_perm,
+                                            c->status, c->s_comp));
+        return MOE_OK;
+    }
+    {
+        ProfScope ps(c, kPermute, perm_bytes, 0.0);
+        CUDA_TRY(moe::launch_permute(idx, w, P, E, c->offsets, c->perm, c->inv_perm, c->w_perm, c->active,
+                                     c->n_active, c->status, c->perm_cells, c->perm_done, c->s_comp));
+    }
+    ProfScope ps(c, kGather, gather_bytes, 0.0);
+    CUDA_TRY(moe::launch_gather_rows(static_cast<const uint16_t*>(x), c->perm, P, c->k, H, c->x_perm, c->s_comp));
+    return MOE_OK;
+}
+
 // Decode forward with the device-resident policy: permutation, then per wave the policy,
 // the fills (copy stream) alongside the resident experts' kernels, the filled experts'
 // kernels after the fills, then the combine. Enqueues only; never waits on the host.
@@ -612,17 +637,8 @@ int forward_device(moe_ctx* c, int layer, const void* x, const float* resid, flo
     const int P = T * c->k, E = c->E, H = c->H;
     if (c->path == MOE_PATH_GEMM)
         return fail(MOE_E_INVAL, "the device-resident policy runs the decode kernels only (MOE_PATH_GEMM unsupported)");
-    {
-        ProfScope ps(c, kPermute, 8.0 * P + 12.0 * P + 8.0 * E, 0.0);
-        CUDA_TRY(moe::launch_permute(idx, w, P, E, c->offsets, c->perm, c->inv_perm, c->w_perm, c->active,
-                                     c->n_active, c->status, c->perm_cells, c->perm_done, c->s_comp));
-    }
-    {
-        // the method's bytes: each of the T rows read once (L2 serves its k - 1 repeats),
-        // each of the P permuted rows written once
-        ProfScope ps(c, kGather, 2.0 * T * H + 2.0 * P * H, 0.0);
-        CUDA_TRY(moe::launch_gather_rows(static_cast<const uint16_t*>(x), c->perm, P, c->k, H, c->x_perm, c->s_comp));
-    }
+    int rc = permute_and_gather(c, x, T, idx, w);
+    if (rc) return rc;
     const int32_t* slot_row = c->slot_dev + static_cast<size_t>(layer) * E;
     GemvWork* wh = c->d_work;
     GemvWork* wm = c->d_work + 2 * (E + 1);
@@ -1160,17 +1176,8 @@ int moe_layer_forward(moe_ctx* c, int layer, const void* x, const float* resid, 
     CUDA_TRY(cudaMemcpyAsync(c->status_host, c->status, sizeof(int), cudaMemcpyDeviceToHost, c->s_comp));
     CUDA_TRY(cudaEventRecord(c->ev_d2h, c->s_comp));
     // 2. permutation and row gather run while the host waits and plans
-    {
-        ProfScope ps(c, kPermute, 8.0 * P + 12.0 * P + 8.0 * E, 0.0);
-        CUDA_TRY(moe::launch_permute(idx, w, P, E, c->offsets, c->perm, c->inv_perm, c->w_perm, c->active,
-                                     c->n_active, c->status, c->perm_cells, c->perm_done, c->s_comp));
-    }
-    {
-        // the method's bytes: each of the T rows read once (L2 serves its k - 1 repeats),
-        // each of the P permuted rows written once
-        ProfScope ps(c, kGather, 2.0 * T * H + 2.0 * P * H, 0.0);
-        CUDA_TRY(moe::launch_gather_rows(static_cast<const uint16_t*>(x), c->perm, P, c->k, H, c->x_perm, c->s_comp));
-    }
+    rc = permute_and_gather(c, x, T, idx, w);
+    if (rc) return rc;
     rc = wait_event(c, c->ev_d2h, "routed indices copy");
     if (rc) return rc;
     harvest(c);
@@ -1458,6 +1465,8 @@ int moe_debug_read(moe_ctx* c, int what, void* dst, uint64_t bytes) {
         case MOE_DBG_N_ACTIVE: src = c->n_active; cap = 4; break;
         case MOE_DBG_SLOT_TABLE: src = c->slot_dev; cap = static_cast<uint64_t>(c->L) * c->E * 4; break;
         case MOE_DBG_H_PERM: src = c->h_perm; cap = static_cast<uint64_t>(c->Pmax) * c->I * 2; break;
+        case MOE_DBG_X_PERM: src = c->x_perm; cap = static_cast<uint64_t>(c->Pmax) * c->H * 2; break;
+        case MOE_DBG_W_PERM: src = c->w_perm; cap = c->Pmax * 4ull; break;
         default: return fail(MOE_E_INVAL, "unknown buffer %d", what);
     }
     if (bytes > cap) return fail(MOE_E_INVAL, "%llu bytes requested, buffer holds %llu",

@@ -1,8 +1,10 @@
 """GPU parity of the permutation on its own: offsets, perm, inv_perm, the active list and its
-length bit-exact with the oracle's stable counting sort, for the one-CTA kernel (up to 1024
-pairs) and the many-CTA kernels (more pairs: per-CTA counts, a scan by the last CTA to finish,
-then placement), at the boundary between them, with ragged last CTAs, a single expert, expert
-counts that are not powers of two, and heavy collisions (few experts, many pairs)."""
+length bit-exact with the oracle's stable counting sort, and the permuted gates and token rows
+bit-exact with the pairs they come from, for the one-launch kernel (up to 1024 pairs: ranks
+counted per pair, rows gathered in the same launch) and the many-CTA kernels (more pairs:
+per-CTA counts, a scan by the last CTA to finish, placement, then a row gather), at the
+boundary between them, with ragged last CTAs, a single pair, a single expert, 1024 experts,
+expert counts that are not powers of two, and heavy collisions (few experts, many pairs)."""
 import numpy as np
 import pytest
 
@@ -14,7 +16,7 @@ pytestmark = pytest.mark.gpu
 CASES = [
     # (T, E, k)
     (1, 1, 1), (170, 16, 6), (171, 16, 6), (1024, 1, 1), (1025, 1, 1), (500, 1000, 8), (3000, 7, 3),
-    (4096, 256, 6), (2731, 1024, 3),
+    (4096, 256, 6), (2731, 1024, 3), (1, 1024, 8), (16, 256, 6), (128, 64, 8), (7, 3, 2),
 ]
 
 
@@ -56,3 +58,9 @@ def test_permutation_bit_exact(T, E, k, zipf):
         n_act = int(cache.debug_read(moe.MOE_DBG_N_ACTIVE, 1)[0])
         assert n_act == active_o.size
         assert np.array_equal(cache.debug_read(moe.MOE_DBG_ACTIVE, E)[:n_act], active_o)
+        # gates and token rows follow their pairs, bit for bit
+        w_perm = cache.debug_read(moe.MOE_DBG_W_PERM, P, "float32")
+        assert np.array_equal(w_perm.view(np.uint32), w.cpu().numpy().ravel()[perm_o].view(np.uint32))
+        x_perm = cache.debug_read(moe.MOE_DBG_X_PERM, P * H, "uint16").reshape(P, H)
+        x_h = x.cpu().view(torch.int16).numpy().view(np.uint16)
+        assert np.array_equal(x_perm, x_h[perm_o // k])
