@@ -339,7 +339,17 @@ __global__ void __launch_bounds__(kSmallThreads) permute_gather_small_kernel(
         }
         const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(p / k) * H);
         uint4* dst = reinterpret_cast<uint4*>(x_perm + static_cast<size_t>(r) * H);
-        for (int c = lane; c < H / 8; c += 32) dst[c] = __ldg(src + c);
+        constexpr int kU = 8;  // 16-byte pieces per lane in flight before the first store
+        const int n = H / 8;
+        for (int c0 = lane; c0 < n; c0 += 32 * kU) {
+            uint4 v[kU];
+#pragma unroll
+            for (int u = 0; u < kU; ++u)
+                if (c0 + 32 * u < n) v[u] = __ldg(src + c0 + 32 * u);
+#pragma unroll
+            for (int u = 0; u < kU; ++u)
+                if (c0 + 32 * u < n) dst[c0 + 32 * u] = v[u];
+        }
     }
     if (!lead) return;
     for (int q = tid; q < P; q += kSmallThreads) atomicAdd(&cnt[es[q]], 1);  // counts: order-free
