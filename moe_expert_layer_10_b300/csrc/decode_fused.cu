@@ -64,18 +64,11 @@ struct Cfg {
     static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
 };
 
-// Down-unit stages issued without their h rows: ring stages st0 .. st0 + n - 1, k-blocks
-// kb0 .. kb0 + n - 1 of token chunk `chunk` (rows tok0 .., nb boxes of 16).
-struct PendSeg {
-    int chunk, tok0, nb, kb0, n, st0;
-};
-
 struct __align__(8) Shared {
     uint64_t full[kMaxStages], empty[kMaxStages], acc_full[2], acc_empty[2];
     uint32_t tmem_base;
     int ok[2];
     int last[2];
-    PendSeg pend[kMaxStages];
 };
 static_assert(sizeof(Shared) <= 1024, "barrier block");
 
@@ -102,13 +95,6 @@ __device__ __forceinline__ bool wait_counter(const int* p, int target, uint64_t 
             if (globaltimer_ns() - t0 > deadline_ns) return false;
         }
     }
-    asm volatile("fence.proxy.async.global;" ::: "memory");
-    return true;
-}
-
-// Without waiting: true once *p >= target (later TMA reads then ordered as by wait_counter).
-__device__ __forceinline__ bool counter_reached(const int* p, int target) {
-    if (ld_acquire_gpu(p) < target) return false;
     asm volatile("fence.proxy.async.global;" ::: "memory");
     return true;
 }
@@ -168,77 +154,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0, used = 0, last_phase = 0;
             bool ok = true;
             int ready_key = -1;  // (phase, entry) whose fill this CTA last saw land
-            // Down stages whose weights are issued but whose h rows still wait for the gate/up
-            // units of their chunk: segments of consecutive ring stages, one per unit, oldest first.
-            int pq_head = 0, pq_n = 0;
-            bool cur_open = false;   // the unit being issued owns the newest segment
-            bool cur_ready = false;  // the unit's chunk is ready: its stages carry their rows
-            const int readers = R_d * dn.S;
-            auto reader_done = [&](int chunk_id) {
-                // the unit no longer reads the counters; the last reader of the chunk resets them
-                // for the next launch
-                if (atomicAdd(h_done + chunk_id, 1) == readers - 1) {
-                    h_done[chunk_id] = 0;
-                    h_ready[chunk_id] = 0;
-                }
-            };
-            auto load_rows = [&](int st, int kb, const CUtensorMap* map, int tok0, int nb) {
-                uint8_t* sb = tiles + st * STAGE_BYTES + A_BYTES;
-                for (int b = 0; b < nb; ++b) tma_load_2d(sb + b * 16 * BK * 2, map, &sh.full[st], kb * BK, tok0 + 16 * b);
-            };
-            // Issue the h rows of the oldest segment. mode 0: only if its chunk is ready; 1: wait
-            // for the chunk; 2: without waiting (an error path: the stages' byte counts must
-            // complete, their results are discarded). Returns 1 when issued, 0 when not ready,
-            // -1 when the wait timed out (the rows are issued all the same).
-            auto flush_front = [&](int mode) -> int {
-                const PendSeg p = sh.pend[pq_head];
-                int r = 1;
-                if (mode == 1) {
-                    if (!wait_counter(h_ready + p.chunk, R_gu, consumer_wait_ns)) r = -1;
-                } else if (mode == 0) {
-                    if (!counter_reached(h_ready + p.chunk, R_gu)) return 0;
-                } else {
-                    r = -1;
-                }
-                for (int i = 0; i < p.n; ++i) load_rows((p.st0 + i) % kStages, p.kb0 + i, &tm_h, p.tok0, p.nb);
-                if (r > 0) reader_done(p.chunk);
-                pq_head = pq_head + 1 == kMaxStages ? 0 : pq_head + 1;
-                if (--pq_n == 0 && cur_open) {  // that was the current unit's segment
-                    cur_open = false;
-                    cur_ready = true;
-                }
-                return r;
-            };
-            // after one chunk turns ready the others often are too
-            auto flush_ready = [&]() {
-                while (pq_n > 0 && flush_front(0) > 0) {
-                }
-            };
-            // Take the next ring stage. The stage may still hold pending stages (the MMA waits for
-            // their h rows, so it would never free them): flush those first.
-            auto take_stage = [&](uint32_t tx, int& st_out) {
-                while (pq_n > 0 && sh.pend[pq_head].st0 == stage) {
-                    if (flush_front(1) < 0) {
-                        raise_status(status, kDevWaitTimeout);
-                        while (pq_n > 0) flush_front(2);
-                        return false;
-                    }
-                    flush_ready();
-                }
-                if (!mbar_wait(&sh.empty[stage], phase ^ 1u)) {
-                    raise_status(status, kDevWaitTimeout);
-                    return false;
-                }
-                mbar_arrive_expect_tx(&sh.full[stage], tx);
-                used |= 1u << stage;
-                last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
-                st_out = stage;
-                if (++stage == kStages) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
-                return true;
-            };
             for (int g = blockIdx.x; g < n_total && ok; g += gridDim.x) {
                 const bool is_gu = g < gu.n_units;
                 const Phase ph = is_gu ? gu : dn;
@@ -252,7 +167,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // (a CTA visits each phase's entries in order)
                     if (!wait_fill_flag(fill_flag + wk.wait_slot, wk.gen, fill_wait_ns)) {
                         raise_status(status, kDevFillTimeout);
-                        ok = false;
                         break;
                     }
                     ready_key = key;
@@ -268,24 +182,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int KB = (is_gu ? H : I) / BK;
                 const int kb0 = un.split * KB / ph.S, kb1 = (un.split + 1) * KB / ph.S;
                 const uint32_t tx = A_BYTES + nb * 16 * BK * 2;  // nb <= NB (the host checked)
-                // a down unit's h rows: issued with each stage once its chunk is ready, else
-                // later, by flush_front, from the unit's pending segment
-                const int chunk_id = wk.pad0 + un.chunk;
-                cur_open = false;
-                cur_ready = is_gu;
-                if (!is_gu) {
-                    flush_ready();
-                    if (counter_reached(h_ready + chunk_id, R_gu)) {
-                        cur_ready = true;
-                        reader_done(chunk_id);
-                    }
-                }
-                for (int kb = kb0; kb < kb1; ++kb) {
-                    int st;
-                    if (!take_stage(tx, st)) {
-                        ok = false;
-                        break;
-                    }
+                auto load_a = [&](int st, int kb) {
                     uint8_t* sa = tiles + st * STAGE_BYTES;
                     if (is_gu) {
                         const int row = slot * 3 * I + un.tile * 64;
@@ -295,28 +192,69 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tma_load_2d_hint(sa, &tm_wd, &sh.full[st], kb * BK, slot * 3 * H + 2 * H + un.tile * 128,
                                          pol_w);
                     }
-                    if (cur_ready) {
-                        load_rows(st, kb, is_gu ? &tm_x : &tm_h, tok0, nb);
-                    } else {
-                        if (!cur_open) {
-                            // open this unit's segment at the back of the queue (every segment
-                            // holds at least one stage in flight: at most kStages of them)
-                            sh.pend[(pq_head + pq_n) % kMaxStages] = PendSeg{chunk_id, tok0, nb, kb, 0, st};
-                            ++pq_n;
-                            cur_open = true;
-                        }
-                        sh.pend[(pq_head + pq_n - 1) % kMaxStages].n++;
+                };
+                auto load_b = [&](int st, int kb) {
+                    uint8_t* sb = tiles + st * STAGE_BYTES + A_BYTES;
+                    for (int b = 0; b < nb; ++b)
+                        tma_load_2d(sb + b * 16 * BK * 2, is_gu ? &tm_x : &tm_h, &sh.full[st], kb * BK, tok0 + 16 * b);
+                };
+                auto take_stage = [&](int& st_out) {
+                    if (!mbar_wait(&sh.empty[stage], phase ^ 1u)) {
+                        raise_status(status, kDevWaitTimeout);
+                        return false;
                     }
+                    mbar_arrive_expect_tx(&sh.full[stage], tx);
+                    used |= 1u << stage;
+                    last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
+                    st_out = stage;
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                    return true;
+                };
+                int kb = kb0;
+                if (!is_gu) {
+                    // weights first for as many stages as the ring holds, then the h rows once
+                    // every gate/up tile of this (expert, chunk) has written them
+                    const int pre = min(kb1 - kb0, kStages);
+                    const int st0 = stage;  // the pre stages are consecutive in the ring
+                    for (int i = 0; i < pre && ok; ++i) {
+                        int st;
+                        ok = take_stage(st);
+                        if (ok) load_a(st, kb0 + i);
+                    }
+                    if (!ok) break;
+                    auto pre_stage = [&](int i) { return (st0 + i) % kStages; };
+                    const int chunk_id = wk.pad0 + un.chunk;
+                    if (!wait_counter(h_ready + chunk_id, R_gu, consumer_wait_ns)) {
+                        raise_status(status, kDevWaitTimeout);
+                        // the issued stages still expect their token bytes: complete them with
+                        // the (unused) rows so that every transaction count is met before exit
+                        for (int i = 0; i < pre; ++i) load_b(pre_stage(i), kb0 + i);
+                        break;
+                    }
+                    for (int i = 0; i < pre; ++i) load_b(pre_stage(i), kb0 + i);
+                    // this unit no longer reads the counters; the last reader of the chunk resets
+                    // them for the next launch
+                    const int readers = R_d * dn.S;
+                    if (atomicAdd(h_done + chunk_id, 1) == readers - 1) {
+                        h_done[chunk_id] = 0;
+                        h_ready[chunk_id] = 0;
+                    }
+                    kb = kb0 + pre;
                 }
-                cur_open = false;  // the next unit opens its own segment
-            }
-            // the h rows of every pending stage, then every issued copy must land before exit
-            while (pq_n > 0) {
-                if (flush_front(ok ? 1 : 2) < 0) {
-                    raise_status(status, kDevWaitTimeout);
-                    ok = false;
+                for (; kb < kb1; ++kb) {
+                    int st;
+                    if (!take_stage(st)) {
+                        ok = false;
+                        break;
+                    }
+                    load_a(st, kb);
+                    load_b(st, kb);
                 }
             }
+            // every issued copy must land before the CTA exits
             for (int s = 0; s < kStages; ++s)
                 if ((used >> s) & 1u)
                     if (!mbar_wait(&sh.full[s], (last_phase >> s) & 1u)) raise_status(status, kDevWaitTimeout);
