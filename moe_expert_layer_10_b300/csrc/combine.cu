@@ -17,26 +17,13 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
     if (i >= static_cast<long long>(T) * H4) return;
     const int t = static_cast<int>(i / H4), c = static_cast<int>(i % H4);
     float4 acc = reinterpret_cast<const float4*>(resid + static_cast<size_t>(t) * H)[c];
-    // up to 8 contributions per round: their positions, then their rows, are all in flight
-    // before the first addition; the additions keep j order
-    constexpr int kJ = 8;
-    for (int j0 = 0; j0 < k; j0 += kJ) {
-        int pos[kJ];
-        float4 v[kJ];
-#pragma unroll
-        for (int u = 0; u < kJ; ++u) pos[u] = j0 + u < k ? inv_perm[t * k + j0 + u] : 0;
-#pragma unroll
-        for (int u = 0; u < kJ; ++u)
-            if (j0 + u < k) v[u] = __ldg(reinterpret_cast<const float4*>(pair_out + static_cast<size_t>(pos[u]) * H) + c);
-#pragma unroll
-        for (int u = 0; u < kJ; ++u) {
-            if (j0 + u < k) {
-                acc.x += v[u].x;
-                acc.y += v[u].y;
-                acc.z += v[u].z;
-                acc.w += v[u].w;
-            }
-        }
+    for (int j = 0; j < k; ++j) {
+        const int pos = inv_perm[t * k + j];
+        const float4 v = __ldg(reinterpret_cast<const float4*>(pair_out + static_cast<size_t>(pos) * H) + c);
+        acc.x += v.x;
+        acc.y += v.y;
+        acc.z += v.z;
+        acc.w += v.w;
     }
     reinterpret_cast<float4*>(out + static_cast<size_t>(t) * H)[c] = acc;
 }
