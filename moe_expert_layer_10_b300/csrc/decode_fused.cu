@@ -20,22 +20,14 @@
 //    arrived, fences the async proxy, and only then loads the h tiles;
 //  * the producer then adds 1 to the chunk's h_done counter; the last down unit of the chunk
 //    resets both counters to zero for the next launch.
-// Units are handed out at run time: the producer of each CTA takes the next unit of the
-// concatenated list (every gate/up unit, then every down unit) from a global counter, one unit
-// ahead of the one it is issuing, and passes the unit index to the MMA and epilogue warps through
-// a small shared-memory ring. SMs that stream faster, or got smaller units, simply take more, so
-// the launch ends nearly together on every SM. The wait cannot deadlock: a down unit waits only
-// for gate/up units, which come first in the list, so they were all taken earlier by running
-// CTAs, and gate/up units wait on nothing but fills. It is bounded all the same (the fill
-// deadline plus 2 s), like every wait here, and a timeout raises the device status. The last CTA
-// to exit resets the counter for the next launch.
+// The wait cannot deadlock: every CTA takes its gate/up units before its down units, gate/up
+// units wait on nothing but fills, and the grid is at most one CTA per SM. It is bounded all the
+// same (the fill deadline plus 2 s), like every wait here, and a timeout raises the device status.
 // Split-K partials of the two phases use disjoint parts of the workspace and counter arrays.
 // Waves whose chunks all have at most 16 tokens (nearly every decode wave) use 18 KB stages, 12
 // in flight. Tried and dropped: prefetching each CTA's down-unit weights into L2 during its
 // gate/up units (batch 1: 63.9 us against 55.2 us without).
 #include <algorithm>
-#include <functional>
-#include <queue>
 #include <vector>
 
 #include "decode_common.cuh"
@@ -72,16 +64,11 @@ struct Cfg {
     static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
 };
 
-constexpr int kUidRing = 8;  // unit indices in flight from the producer to the MMA and epilogue warps
-
 struct __align__(8) Shared {
     uint64_t full[kMaxStages], empty[kMaxStages], acc_full[2], acc_empty[2];
-    uint64_t uid_full[kUidRing], uid_empty[kUidRing];
     uint32_t tmem_base;
     int ok[2];
     int last[2];
-    int uid[kUidRing];
-    int epi_g;  // the epilogue leader's copy of the current unit for the other epilogue threads
 };
 static_assert(sizeof(Shared) <= 1024, "barrier block");
 
@@ -119,8 +106,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         Phase dn, const int32_t* __restrict__ slot_row, const uint32_t* __restrict__ fill_flag, int H,
                         int I, uint16_t* __restrict__ h_perm, const float* __restrict__ w_perm,
                         float* __restrict__ pair_out, float* __restrict__ ws, int* __restrict__ cnt,
-                        int* __restrict__ h_ready, int* __restrict__ h_done, int* __restrict__ sched, int* status,
-                        uint64_t fill_wait_ns) {
+                        int* __restrict__ h_ready, int* __restrict__ h_done, int* status, uint64_t fill_wait_ns) {
     pdl_gate();
     using C = Cfg<NB>;
     constexpr int kStages = C::STAGES, STAGE_BYTES = C::STAGE_BYTES;
@@ -145,10 +131,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&sh.acc_full[b], 1);
             mbar_init(&sh.acc_empty[b], 4);
         }
-        for (int i = 0; i < kUidRing; ++i) {
-            mbar_init(&sh.uid_full[i], 1);
-            mbar_init(&sh.uid_empty[i], 2);  // the MMA lane and the epilogue leader
-        }
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -172,20 +154,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0, used = 0, last_phase = 0;
             bool ok = true;
             int ready_key = -1;  // (phase, entry) whose fill this CTA last saw land
-            int g_next = atomicAdd(sched, 1);
-            for (int i = 0;; ++i) {
-                // hand the unit (or the end, -1) to the MMA and epilogue warps
-                const int g = ok && g_next < n_total ? g_next : -1;
-                const int ri = i % kUidRing;
-                const uint32_t rpar = static_cast<uint32_t>(i / kUidRing) & 1u;
-                if (!mbar_wait(&sh.uid_empty[ri], rpar ^ 1u, consumer_wait_ns)) {
-                    raise_status(status, kDevWaitTimeout);
-                    break;  // the consumers stopped: they exit on their own timeouts
-                }
-                sh.uid[ri] = g;
-                mbar_arrive(&sh.uid_full[ri]);
-                if (g < 0) break;
-                g_next = atomicAdd(sched, 1);  // the next unit, taken while this one streams
+            for (int g = blockIdx.x; g < n_total && ok; g += gridDim.x) {
                 const bool is_gu = g < gu.n_units;
                 const Phase ph = is_gu ? gu : dn;
                 const int u = is_gu ? g : g - gu.n_units;
@@ -198,8 +167,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // (a CTA visits each phase's entries in order)
                     if (!wait_fill_flag(fill_flag + wk.wait_slot, wk.gen, fill_wait_ns)) {
                         raise_status(status, kDevFillTimeout);
-                        ok = false;
-                        continue;  // hands the end to the consumers
+                        break;
                     }
                     ready_key = key;
                 }
@@ -251,23 +219,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // every gate/up tile of this (expert, chunk) has written them
                     const int pre = min(kb1 - kb0, kStages);
                     const int st0 = stage;  // the pre stages are consecutive in the ring
-                    for (int p = 0; p < pre && ok; ++p) {
+                    for (int i = 0; i < pre && ok; ++i) {
                         int st;
                         ok = take_stage(st);
-                        if (ok) load_a(st, kb0 + p);
+                        if (ok) load_a(st, kb0 + i);
                     }
-                    if (!ok) continue;
-                    auto pre_stage = [&](int p) { return (st0 + p) % kStages; };
+                    if (!ok) break;
+                    auto pre_stage = [&](int i) { return (st0 + i) % kStages; };
                     const int chunk_id = wk.pad0 + un.chunk;
                     if (!wait_counter(h_ready + chunk_id, R_gu, consumer_wait_ns)) {
                         raise_status(status, kDevWaitTimeout);
                         // the issued stages still expect their token bytes: complete them with
                         // the (unused) rows so that every transaction count is met before exit
-                        for (int p = 0; p < pre; ++p) load_b(pre_stage(p), kb0 + p);
-                        ok = false;
-                        continue;
+                        for (int i = 0; i < pre; ++i) load_b(pre_stage(i), kb0 + i);
+                        break;
                     }
-                    for (int p = 0; p < pre; ++p) load_b(pre_stage(p), kb0 + p);
+                    for (int i = 0; i < pre; ++i) load_b(pre_stage(i), kb0 + i);
                     // this unit no longer reads the counters; the last reader of the chunk resets
                     // them for the next launch
                     const int readers = R_d * dn.S;
@@ -300,15 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int last_acc = -1;
             uint32_t last_acc_phase = 0;
             bool ok = true;
-            for (int i = 0; ok; ++i) {
-                const int ri = i % kUidRing;
-                if (!mbar_wait(&sh.uid_full[ri], static_cast<uint32_t>(i / kUidRing) & 1u, consumer_wait_ns)) {
-                    raise_status(status, kDevWaitTimeout);
-                    break;
-                }
-                const int g = sh.uid[ri];
-                mbar_arrive(&sh.uid_empty[ri]);
-                if (g < 0) break;
+            for (int g = blockIdx.x; g < n_total && ok; g += gridDim.x) {
                 const bool is_gu = g < gu.n_units;
                 const Phase ph = is_gu ? gu : dn;
                 const int u = is_gu ? g : g - gu.n_units;
@@ -356,20 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ------------------------------------------------------------ epilogue (warps 2-5)
         EpiState st;
-        for (int i = 0;; ++i) {
-            if (threadIdx.x == 64) {  // the leader takes the unit from the ring for all 128 threads
-                const int ri = i % kUidRing;
-                int gl = -1;
-                if (mbar_wait(&sh.uid_full[ri], static_cast<uint32_t>(i / kUidRing) & 1u, consumer_wait_ns))
-                    gl = sh.uid[ri];
-                else
-                    raise_status(status, kDevWaitTimeout);
-                mbar_arrive(&sh.uid_empty[ri]);
-                sh.epi_g = gl;
-            }
-            named_bar(3, 128);
-            const int g = sh.epi_g;  // rewritten only after the unit's own barriers below
-            if (g < 0) break;
+        for (int g = blockIdx.x; g < n_total; g += gridDim.x) {
             const bool ok = g < gu.n_units
                                 ? epilogue_unit<true>(st, sh.acc_full, sh.acc_empty, sh.ok, sh.last, tmem, xchg,
                                                       gu.work, gu.n_work, g, gu.S, R_gu, H, I, h_perm, w_perm,
@@ -384,14 +330,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
-    if (threadIdx.x == 0) {
-        // every unit of this CTA is taken; the last CTA out resets the counter for the next launch
-        __threadfence();
-        if (atomicAdd(sched + 1, 1) == static_cast<int>(gridDim.x) - 1) {
-            sched[0] = 0;
-            sched[1] = 0;
-        }
-    }
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
@@ -410,6 +348,7 @@ void decode_fused_choose_split(const int* chunk_tok, int n_chunks, int H, int I,
     const double kUnitFixed = 8192.0;
     int best_gu = 1, best_d = 1;
     double best = -1.0, unsplit = 0.0;
+    std::vector<double> load(num_sms);
     for (int sg = 1; sg <= kDecodeMaxSplit; ++sg) {
         if (KB_gu / sg < 4) break;
         for (int sd = 1; sd <= kDecodeMaxSplit; ++sd) {
@@ -417,29 +356,22 @@ void decode_fused_choose_split(const int* chunk_tok, int n_chunks, int H, int I,
             long long units = 0;
             for (int c = 0; c < n_chunks; ++c) units += static_cast<long long>(R_gu) * sg + static_cast<long long>(R_d) * sd;
             if ((sg > 1 || sd > 1) && units > kDecodeSplitUnits) continue;
-            // units go, in list order, to the CTA that frees first (the run-time counter)
-            std::priority_queue<double, std::vector<double>, std::greater<double>> free_at;
-            for (int i = 0; i < num_sms; ++i) free_at.push(0.0);
+            std::fill(load.begin(), load.end(), 0.0);
+            long long g = 0;
             for (int phase = 0; phase < 2; ++phase) {
                 const int R = phase == 0 ? R_gu : R_d, S = phase == 0 ? sg : sd, KB = phase == 0 ? KB_gu : KB_d;
                 for (int c = 0; c < n_chunks; ++c) {
                     const int ntp = ((chunk_tok[c] + 15) / 16) * 16;
                     for (int t = 0; t < R; ++t)
-                        for (int sp = 0; sp < S; ++sp) {
+                        for (int sp = 0; sp < S; ++sp, ++g) {
                             const int kb = (sp + 1) * KB / S - sp * KB / S;
                             double b = kb * (A_BYTES + ntp * BK * 2.0) + kUnitFixed;
                             if (S > 1) b += 2.0 * ntp * 128 * 4;
-                            const double t0 = free_at.top();
-                            free_at.pop();
-                            free_at.push(t0 + b);
+                            load[g % num_sms] += b;
                         }
                 }
             }
-            double mx = 0.0;
-            while (!free_at.empty()) {
-                mx = std::max(mx, free_at.top());
-                free_at.pop();
-            }
+            const double mx = *std::max_element(load.begin(), load.end());
             if (sg == 1 && sd == 1) unsplit = mx;
             if (best < 0 || mx < best * (1.0 - 1e-9)) {
                 best = mx;
@@ -465,16 +397,14 @@ namespace {
 template <int NB>
 cudaError_t launch_nb(const DecodeMaps& m, Phase gu, Phase dn, const int32_t* slot_row, const uint32_t* fill_flag,
                       int H, int I, uint16_t* h_perm, const float* w_perm, float* pair_out, float* ws, int* cnt,
-                      int* h_ready, int* h_done, int* sched, int* status, uint64_t fill_wait_ns, int grid,
-                      cudaStream_t st) {
+                      int* h_ready, int* h_done, int* status, uint64_t fill_wait_ns, int grid, cudaStream_t st) {
     auto kern = decode_fused_kernel<NB>;
     constexpr int smem = Cfg<NB>::SMEM;
     static std::atomic<uint64_t> attr{0};
     const cudaError_t e = ensure_smem_limit(kern, smem, attr);
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, st, m.a_gu, m.a_d, m.b_x, m.b_h, gu, dn, slot_row,
-                      fill_flag, H, I, h_perm, w_perm, pair_out, ws, cnt, h_ready, h_done, sched, status,
-                      fill_wait_ns);
+                      fill_flag, H, I, h_perm, w_perm, pair_out, ws, cnt, h_ready, h_done, status, fill_wait_ns);
 }
 
 }  // namespace
@@ -483,9 +413,8 @@ cudaError_t launch_decode_fused(const DecodeMaps& m, const GemvWork* work_gu, in
                                 const GemvWork* work_d, int units_d, int S_d, int max_chunk_tok,
                                 const int32_t* slot_row, const uint32_t* fill_flag, int H, int I, uint16_t* h_perm,
                                 const float* w_perm, float* pair_out, float* ws, int* cnt, int* h_ready, int* h_done,
-                                int* sched, int* status, uint64_t fill_wait_ns, int num_sms, cudaStream_t st) {
+                                int* status, uint64_t fill_wait_ns, int num_sms, cudaStream_t st) {
     if (units_gu <= 0 || units_d <= 0 || n_work <= 0) return cudaSuccess;
-    if (!sched) return cudaErrorInvalidValue;
     if (S_gu < 1 || S_gu > kDecodeMaxSplit || S_d < 1 || S_d > kDecodeMaxSplit) return cudaErrorInvalidValue;
     if ((S_gu > 1 || S_d > 1) && units_gu + units_d > kDecodeSplitUnits) return cudaErrorInvalidValue;
     if (max_chunk_tok < 1 || max_chunk_tok > kNMax) return cudaErrorInvalidValue;
@@ -493,9 +422,9 @@ cudaError_t launch_decode_fused(const DecodeMaps& m, const GemvWork* work_gu, in
     const Phase gu{work_gu, n_work, units_gu, S_gu}, dn{work_d, n_work, units_d, S_d};
     if (max_chunk_tok <= 16)
         return launch_nb<1>(m, gu, dn, slot_row, fill_flag, H, I, h_perm, w_perm, pair_out, ws, cnt, h_ready, h_done,
-                            sched, status, fill_wait_ns, grid, st);
+                            status, fill_wait_ns, grid, st);
     return launch_nb<4>(m, gu, dn, slot_row, fill_flag, H, I, h_perm, w_perm, pair_out, ws, cnt, h_ready, h_done,
-                        sched, status, fill_wait_ns, grid, st);
+                        status, fill_wait_ns, grid, st);
 }
 
 }  // namespace moe

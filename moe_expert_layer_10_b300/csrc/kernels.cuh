@@ -120,19 +120,18 @@ cudaError_t launch_decode_down(const DecodeMaps& maps, const GemvWork* work, int
 // --- decode expert FFN, gate/up and down in one persistent launch (bf16; decode_fused.cu) ---
 // work_gu / work_d: the wave's two work lists in the same entry order, each closed by its unit
 // total, with GemvWork::pad0 = the entry's first token-chunk index (chunks of all entries
-// numbered consecutively). h_ready / h_done: decode_fused_chunk_slots(E, P) ints each; sched:
-// 2 ints (the unit counter and the count of CTAs that have exited); all zero before the first
-// launch (every launch leaves them zero). The down phase's split-K tiles follow the gate/up
-// phase's in ws and cnt.
+// numbered consecutively). h_ready / h_done: decode_fused_chunk_slots(E, P) ints each, zero
+// before the first launch (every launch leaves them zero). The down phase's split-K tiles follow
+// the gate/up phase's in ws and cnt.
 int decode_fused_chunk_slots(int E, int P);
 // max_chunk_tok: the most tokens of any chunk of the wave (<= 16 selects the small-token kernel).
 cudaError_t launch_decode_fused(const DecodeMaps& maps, const GemvWork* work_gu, int n_work, int units_gu, int S_gu,
                                 const GemvWork* work_d, int units_d, int S_d, int max_chunk_tok, const int32_t* slot_row,
                                 const uint32_t* fill_flag, int H, int I, uint16_t* h_perm, const float* w_perm,
-                                float* pair_out, float* ws, int* cnt, int* h_ready, int* h_done, int* sched,
-                                int* status, uint64_t fill_wait_ns, int num_sms, cudaStream_t st);
-// K splits (S_gu, S_d) of a fused launch: the pair that minimises the largest per-CTA load when
-// the units of the concatenated list go, in order, to the CTA that frees first. chunk_tok: token count of each
+                                float* pair_out, float* ws, int* cnt, int* h_ready, int* h_done, int* status,
+                                uint64_t fill_wait_ns, int num_sms, cudaStream_t st);
+// K splits (S_gu, S_d) of a fused launch: the pair that minimises the largest per-CTA load
+// under the round-robin assignment of the concatenated unit list. chunk_tok: token count of each
 // chunk of the wave's entries, in work-list order.
 void decode_fused_choose_split(const int* chunk_tok, int n_chunks, int H, int I, int num_sms, int* S_gu, int* S_d);
 

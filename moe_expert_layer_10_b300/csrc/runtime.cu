@@ -194,7 +194,6 @@ struct moe_ctx {
     float* dec_ws = nullptr;  // split-K partial tiles of the decode kernels
     int* dec_cnt = nullptr;   // per-tile arrival counters (zero between launches)
     int *dec_ready = nullptr, *dec_done = nullptr;  // fused decode: per-chunk h counters (zero between launches)
-    int* dec_sched = nullptr;                         // fused decode: unit counter, exited CTAs (zero between launches)
     int dec_chunk_slots = 0;
     moe::GemmMaps gemm_maps{};
 
@@ -328,7 +327,6 @@ int check_status(moe_ctx* c) {
         cudaMemsetAsync(c->dec_cnt, 0, moe::kDecodeSplitUnits * sizeof(int), c->s_comp);
         cudaMemsetAsync(c->dec_ready, 0, c->dec_chunk_slots * sizeof(int), c->s_comp);
         cudaMemsetAsync(c->dec_done, 0, c->dec_chunk_slots * sizeof(int), c->s_comp);
-        cudaMemsetAsync(c->dec_sched, 0, 2 * sizeof(int), c->s_comp);
         return fail(MOE_E_DEVICE, "a kernel raised device status %d (1 wait timeout, 2 bad forced set, 3 bad slot, "
                                   "4 bad expert index, 5 fill wait timeout)", code);
     }
@@ -518,7 +516,7 @@ void free_all(moe_ctx* c) {
     if (c->ev_join) cudaEventDestroy(c->ev_join);
     void* dev_ptrs[] = {c->arena, c->slot_dev, c->logits, c->offsets, c->perm, c->inv_perm, c->active,
                         c->perm_cells, c->perm_done, c->n_active, c->w_perm, c->pair_out, c->x_perm, c->h_perm, c->status, c->work_dev,
-                        c->dec_ws,   c->dec_cnt, c->dec_ready, c->dec_done, c->dec_sched, c->fill_flag, c->d_lru,   c->d_prev, c->d_next,  c->d_key,
+                        c->dec_ws,   c->dec_cnt, c->dec_ready, c->dec_done, c->fill_flag, c->d_lru,   c->d_prev, c->d_next,  c->d_key,
                         c->d_stats,  c->d_trace, c->d_fill_list, c->d_work, c->d_order, c->d_hdr, c->d_keys,
                         c->d_iota};
     for (void* p : dev_ptrs)
@@ -836,8 +834,6 @@ int moe_cache_init(const moe_config_t* cfg, void* stream_compute, void* stream_c
     INIT_TRY(cudaMalloc(&c->dec_done, c->dec_chunk_slots * sizeof(int)));
     INIT_TRY(cudaMemset(c->dec_ready, 0, c->dec_chunk_slots * sizeof(int)));
     INIT_TRY(cudaMemset(c->dec_done, 0, c->dec_chunk_slots * sizeof(int)));
-    INIT_TRY(cudaMalloc(&c->dec_sched, 2 * sizeof(int)));
-    INIT_TRY(cudaMemset(c->dec_sched, 0, 2 * sizeof(int)));
     INIT_TRY(cudaMalloc(&c->fill_flag, static_cast<size_t>(c->C) * sizeof(uint32_t)));
     INIT_TRY(cudaMemset(c->fill_flag, 0, static_cast<size_t>(c->C) * sizeof(uint32_t)));
     INIT_TRY(cudaMemset(c->dec_cnt, 0, moe::kDecodeSplitUnits * sizeof(int)));
@@ -1343,7 +1339,7 @@ int moe_layer_forward(moe_ctx* c, int layer, const void* x, const float* resid, 
                                               units_d, Sd, max_chunk_tok, slot_row, c->fill_flag, H, I, c->h_perm,
                                               c->w_perm,
                                               c->pair_out, c->dec_ws, c->dec_cnt, c->dec_ready, c->dec_done,
-                                              c->dec_sched, c->status, fill_wait_ns, c->num_sms, c->s_comp));
+                                              c->status, fill_wait_ns, c->num_sms, c->s_comp));
         } else {
             {
                 ProfScope ps(c, kDecodeGateUp, gu_bytes, 4.0 * pw * I * H);
