@@ -39,10 +39,12 @@ PER_BATCH_STEPS = 256  # steps of each per-batch run (the workload defines 256 s
 FALLBACK_HBM_GBS = 6400.0
 # the committed ncu summary of each roofline kernel and the sources its counters were taken on
 PROFILE_SUMMARY = {"decode_gateup": os.path.join(ROOT, "profiles", "decode_gateup.md"),
-                   "decode_fused": os.path.join(ROOT, "profiles", "decode_fused.md")}
+                   "decode_fused": os.path.join(ROOT, "profiles", "decode_fused.md"),
+                   "decode_fp4": os.path.join(ROOT, "profiles", "decode_fp4.md")}
 DECODE_SOURCES = {k: [os.path.join(ROOT, "moe_expert_layer_10_b300", "csrc", f)
                       for f in (main, "decode_common.cuh", "ptx.cuh", "umma.cuh")]
-                  for k, main in (("decode_gateup", "decode_mma.cu"), ("decode_fused", "decode_fused.cu"))}
+                  for k, main in (("decode_gateup", "decode_mma.cu"), ("decode_fused", "decode_fused.cu"),
+                                  ("decode_fp4", "decode_fp4.cu"))}
 
 
 def parse_args():
@@ -58,6 +60,8 @@ def parse_args():
     ap.add_argument("--batches", default="1,4,16", help="decode batch sizes of one step (profiling cases)")
     ap.add_argument("--capacity", type=int, default=0, help="override the cache capacity (profiling cases)")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--two-launch", action="store_true",
+                    help="profiling cases: bf16 decode waves as two launches (gate/up, then down), not fused")
     ap.add_argument("--no-per-batch", action="store_true",
                     help="skip the per-batch runs (B = 1, 4, 16 each through its own 256 LRU steps)")
     ap.add_argument("--prefetch-all", action="store_true",
@@ -286,6 +290,8 @@ def run_b300(args, rank, world, local):
     cache = moe.MoeCache(moe.LayerShape(1, W.E, W.H, W.I, W.k, C, max(BATCHES)),
                          flags=(moe.MOE_DEVICE_POLICY if device else 0) | fmt_flags, stream_compute=stream)
     fill_pool(cache, W, 1, W.E, fmt)
+    if args.two_launch:
+        cache.set_path(moe.MOE_PATH_GEMV_UNFUSED)
     if args.prefetch_all:
         cache.cache_fill(0, None, moe.MOE_FILL_FULL_LAYER)
         cache.sync()
@@ -433,6 +439,8 @@ def run_b300(args, rank, world, local):
 
     res = resident_context(args, W, E=W.E, fmt=fmt)
     rc = res["cache"]
+    if args.two_launch:
+        rc.set_path(moe.MOE_PATH_GEMV_UNFUSED)
     for s in range(args.warmup):
         step(rc, s)
     rc.sync()
@@ -479,7 +487,8 @@ def run_b300(args, rank, world, local):
                 "launches": g["launches"],
                 "pass": "the timed steps' batches replayed with every routed expert resident (256-entry cache), "
                         "CUDA events on the compute stream"}
-        ratio = None if fp4 else traffic_ratio_from_profile(kname)
+        # 4-bit entries run the 4-bit kernel under the gate/up launch's name
+        ratio = traffic_ratio_from_profile("decode_fp4" if fp4 else kname)
         if ratio is not None:
             # the captured launch's DRAM bytes per algorithmic byte, applied to this pass's
             # average launch (the capture is one batch-16 launch, not this pass's mix)
@@ -492,7 +501,8 @@ def run_b300(args, rank, world, local):
                 for n, v in ks.items() if v["launches"]}
     # launches of this library's kernels in the timed region: the fixed ones of each forward,
     # and per wave one fused expert launch (bf16) or two (4-bit)
-    launches = args.steps * sum(forward_launches(B * W.k) for B in BATCHES) + (2 if fp4 else 1) * st["waves"]
+    launches = args.steps * sum(forward_launches(B * W.k) for B in BATCHES) + \
+        (2 if fp4 or args.two_launch else 1) * st["waves"]
     if device:  # per forward: policy, fill and 4 decode launches for each possible wave
         launches = args.steps * sum(forward_launches(B * W.k) + 6 * ((min(B * W.k, W.E) + C - 1) // C)
                                     for B in BATCHES)
@@ -528,6 +538,7 @@ def run_b300(args, rank, world, local):
         result["prefill"] = {"skipped": "4-bit entries run on the decode kernels; the prefill leg measures the "
                                         "bf16 grouped GEMM"}
     elif not args.no_prefill:
+        res["cache"].set_path(moe.MOE_PATH_AUTO)  # the prefill leg takes the grouped GEMM
         result["prefill"] = run_prefill(args, res if not args.prefill_experts else None)
     res["cache"].close()
     if rank == 0 and not args.no_cpu_baseline:
