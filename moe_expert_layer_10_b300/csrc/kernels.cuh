@@ -7,8 +7,6 @@
 #include <stdint.h>
 
 #include <atomic>
-#include <mutex>
-#include <set>
 #include <utility>
 
 namespace moe {
@@ -27,30 +25,12 @@ inline cudaError_t ensure_smem_limit(void (*kern)(KArgs...), size_t bytes, std::
     return e;
 }
 
-// Every kernel of the layer's chain prefers the largest shared-memory carveout (once per kernel
-// and device), so consecutive kernels never make an SM change its L1 / shared-memory split
-// between them: the expert kernels need nearly all of it.
-inline cudaError_t ensure_max_carveout(const void* fn) {
-    static std::mutex mu;
-    static std::set<std::pair<const void*, int>> done;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    std::lock_guard<std::mutex> lock(mu);
-    if (done.count({fn, dev})) return cudaSuccess;
-    e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
-    if (e == cudaSuccess) done.insert({fn, dev});
-    return e;
-}
-
 // Launch a kernel of the layer's chain with programmatic stream serialization: it may be
 // scheduled while the previous kernel of the stream is still running, and waits for it in
 // pdl_gate (ptx.cuh) before touching memory.
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
                               Args&&... args) {
-    const cudaError_t ce = ensure_max_carveout(reinterpret_cast<const void*>(kern));
-    if (ce != cudaSuccess) return ce;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = grid;
     cfg.blockDim = block;
