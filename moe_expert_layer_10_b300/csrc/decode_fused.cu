@@ -58,9 +58,7 @@ struct Cfg {
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int XCHG_BYTES = NB * 16 * 64 * 4;
     static constexpr int STAGES = NB == 1 ? 12 : 8;
-    static constexpr int WORK = NB == 1 ? 128 : 512;  // work entries of both lists kept in shared memory
-    static constexpr int WORK_BYTES = WORK * static_cast<int>(sizeof(GemvWork));
-    static constexpr int SMEM = STAGES * STAGE_BYTES + XCHG_BYTES + WORK_BYTES + 1024 + 1024;  // + barriers, alignment
+    static constexpr int SMEM = STAGES * STAGE_BYTES + XCHG_BYTES + 1024 + 1024;  // + barriers, alignment
     static_assert(STAGES <= kMaxStages, "stage count");
     static_assert(STAGE_BYTES % 1024 == 0, "stages keep the 1024-byte alignment of the swizzled tiles");
     static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
@@ -86,19 +84,6 @@ __device__ __forceinline__ int ld_acquire_gpu(const int* p) {
     return v;
 }
 
-// locate_unit over a work list in shared or global memory (generic loads).
-__device__ __forceinline__ Unit locate_unit_any(const GemvWork* work, int n_work, int u, int R, int S) {
-    int lo = 0, hi = n_work - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (work[mid].unit_begin <= u) lo = mid;
-        else hi = mid - 1;
-    }
-    const int local = u - work[lo].unit_begin;
-    const int rest = local / S;
-    return Unit{lo, rest / R, rest % R, local % S};
-}
-
 // Wait (bounded) until *p >= target; then order later TMA reads after what the releasing
 // threads wrote.
 __device__ __forceinline__ bool wait_counter(const int* p, int target, uint64_t deadline_ns) {
@@ -118,7 +103,7 @@ template <int NB>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_fused_kernel(const __grid_constant__ CUtensorMap tm_wgu, const __grid_constant__ CUtensorMap tm_wd,
                         const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_h, Phase gu,
-                        Phase dn, const uint32_t* __restrict__ fill_flag, int H,
+                        Phase dn, const int32_t* __restrict__ slot_row, const uint32_t* __restrict__ fill_flag, int H,
                         int I, uint16_t* __restrict__ h_perm, const float* __restrict__ w_perm,
                         float* __restrict__ pair_out, float* __restrict__ ws, int* __restrict__ cnt,
                         int* __restrict__ h_ready, int* __restrict__ h_done, int* status, uint64_t fill_wait_ns) {
@@ -129,8 +114,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float* xchg = reinterpret_cast<float*>(tiles + kStages * STAGE_BYTES);
-    GemvWork* work_sm = reinterpret_cast<GemvWork*>(tiles + kStages * STAGE_BYTES + C::XCHG_BYTES);
-    Shared& sh = *reinterpret_cast<Shared*>(tiles + kStages * STAGE_BYTES + C::XCHG_BYTES + C::WORK_BYTES);
+    Shared& sh = *reinterpret_cast<Shared*>(tiles + kStages * STAGE_BYTES + C::XCHG_BYTES);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int R_gu = I / 64, R_d = H / 128;
     const int n_total = gu.n_units + dn.n_units;
@@ -153,14 +137,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_alloc(&sh.tmem_base, kTmemCols);
         tmem_relinquish();
     }
-    // the wave's two work lists (each closed by its unit total) in shared memory when they fit:
-    // the producer and the MMA issuer look their units up there
-    const int nw1 = gu.n_work + 1;
-    const bool work_in_smem = 2 * nw1 <= C::WORK;
-    if (work_in_smem)
-        for (int i = threadIdx.x; i < 2 * nw1; i += kThreads) work_sm[i] = i < nw1 ? gu.work[i] : dn.work[i - nw1];
-    const GemvWork* wl_gu = work_in_smem ? work_sm : gu.work;
-    const GemvWork* wl_dn = work_in_smem ? work_sm + nw1 : dn.work;
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -183,9 +159,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const Phase ph = is_gu ? gu : dn;
                 const int u = is_gu ? g : g - gu.n_units;
                 const int R = is_gu ? R_gu : R_d;
-                const GemvWork* wl = is_gu ? wl_gu : wl_dn;
-                const Unit un = locate_unit_any(wl, ph.n_work, u, R, ph.S);
-                const GemvWork wk = wl[un.a];
+                const Unit un = locate_unit(ph.work, ph.n_work, u, R, ph.S);
+                const GemvWork wk = ph.work[un.a];
                 const int key = is_gu ? un.a : (1 << 20) + un.a;
                 if (wk.wait_slot >= 0 && key != ready_key) {
                     // an entry filled by this wave: stream its weights once its copy has landed
@@ -196,7 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     ready_key = key;
                 }
-                int slot = wk.pad1;  // the entry's cache slot, resolved by the host
+                int slot = slot_row[wk.expert];
                 if (slot < 0) {
                     raise_status(status, kDevBadSlot);
                     slot = 0;  // keep every copy inside the arena; results are discarded
@@ -296,9 +271,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool is_gu = g < gu.n_units;
                 const Phase ph = is_gu ? gu : dn;
                 const int u = is_gu ? g : g - gu.n_units;
-                const GemvWork* wl = is_gu ? wl_gu : wl_dn;
-                const Unit un = locate_unit_any(wl, ph.n_work, u, is_gu ? R_gu : R_d, ph.S);
-                const GemvWork wk = wl[un.a];
+                const Unit un = locate_unit(ph.work, ph.n_work, u, is_gu ? R_gu : R_d, ph.S);
+                const GemvWork wk = ph.work[un.a];
                 const int nt = min(kNMax, wk.n_tok - un.chunk * kNMax);
                 const uint32_t idesc = idesc_bf16_f32(128, ((nt + 15) >> 4) * 16);
                 const int KB = (is_gu ? H : I) / BK;
@@ -421,7 +395,7 @@ void decode_fused_choose_split(const int* chunk_tok, int n_chunks, int H, int I,
 namespace {
 
 template <int NB>
-cudaError_t launch_nb(const DecodeMaps& m, Phase gu, Phase dn, const uint32_t* fill_flag,
+cudaError_t launch_nb(const DecodeMaps& m, Phase gu, Phase dn, const int32_t* slot_row, const uint32_t* fill_flag,
                       int H, int I, uint16_t* h_perm, const float* w_perm, float* pair_out, float* ws, int* cnt,
                       int* h_ready, int* h_done, int* status, uint64_t fill_wait_ns, int grid, cudaStream_t st) {
     auto kern = decode_fused_kernel<NB>;
@@ -429,7 +403,7 @@ cudaError_t launch_nb(const DecodeMaps& m, Phase gu, Phase dn, const uint32_t* f
     static std::atomic<uint64_t> attr{0};
     const cudaError_t e = ensure_smem_limit(kern, smem, attr);
     if (e != cudaSuccess) return e;
-    return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, st, m.a_gu, m.a_d, m.b_x, m.b_h, gu, dn,
+    return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, st, m.a_gu, m.a_d, m.b_x, m.b_h, gu, dn, slot_row,
                       fill_flag, H, I, h_perm, w_perm, pair_out, ws, cnt, h_ready, h_done, status, fill_wait_ns);
 }
 
@@ -437,7 +411,7 @@ cudaError_t launch_nb(const DecodeMaps& m, Phase gu, Phase dn, const uint32_t* f
 
 cudaError_t launch_decode_fused(const DecodeMaps& m, const GemvWork* work_gu, int n_work, int units_gu, int S_gu,
                                 const GemvWork* work_d, int units_d, int S_d, int max_chunk_tok,
-                                const uint32_t* fill_flag, int H, int I, uint16_t* h_perm,
+                                const int32_t* slot_row, const uint32_t* fill_flag, int H, int I, uint16_t* h_perm,
                                 const float* w_perm, float* pair_out, float* ws, int* cnt, int* h_ready, int* h_done,
                                 int* status, uint64_t fill_wait_ns, int num_sms, cudaStream_t st) {
     if (units_gu <= 0 || units_d <= 0 || n_work <= 0) return cudaSuccess;
@@ -447,9 +421,9 @@ cudaError_t launch_decode_fused(const DecodeMaps& m, const GemvWork* work_gu, in
     const int grid = std::min(units_gu + units_d, num_sms);
     const Phase gu{work_gu, n_work, units_gu, S_gu}, dn{work_d, n_work, units_d, S_d};
     if (max_chunk_tok <= 16)
-        return launch_nb<1>(m, gu, dn, fill_flag, H, I, h_perm, w_perm, pair_out, ws, cnt, h_ready, h_done,
+        return launch_nb<1>(m, gu, dn, slot_row, fill_flag, H, I, h_perm, w_perm, pair_out, ws, cnt, h_ready, h_done,
                             status, fill_wait_ns, grid, st);
-    return launch_nb<4>(m, gu, dn, fill_flag, H, I, h_perm, w_perm, pair_out, ws, cnt, h_ready, h_done,
+    return launch_nb<4>(m, gu, dn, slot_row, fill_flag, H, I, h_perm, w_perm, pair_out, ws, cnt, h_ready, h_done,
                         status, fill_wait_ns, grid, st);
 }
 

@@ -78,7 +78,7 @@ struct GemvWork {
     int unit_begin;  // first work unit of this expert (entry n_work holds the total)
     int wait_slot;   // slot whose fill flag must reach `gen` before its weights are read, or -1
     uint32_t gen;    // fill generation of that slot (written by the copy stream after the copy)
-    int pad0, pad1;  // fused launch: first token-chunk index, cache slot (else unused)
+    int pad0, pad1;
 };
 
 // --- decode expert FFN on the tensor cores (weights as M = 128, tokens as N <= 64) ---
@@ -120,14 +120,13 @@ cudaError_t launch_decode_down(const DecodeMaps& maps, const GemvWork* work, int
 // --- decode expert FFN, gate/up and down in one persistent launch (bf16; decode_fused.cu) ---
 // work_gu / work_d: the wave's two work lists in the same entry order, each closed by its unit
 // total, with GemvWork::pad0 = the entry's first token-chunk index (chunks of all entries
-// numbered consecutively) and GemvWork::pad1 = the entry's cache slot (the launch reads no slot
-// table). h_ready / h_done: decode_fused_chunk_slots(E, P) ints each, zero
+// numbered consecutively). h_ready / h_done: decode_fused_chunk_slots(E, P) ints each, zero
 // before the first launch (every launch leaves them zero). The down phase's split-K tiles follow
 // the gate/up phase's in ws and cnt.
 int decode_fused_chunk_slots(int E, int P);
 // max_chunk_tok: the most tokens of any chunk of the wave (<= 16 selects the small-token kernel).
 cudaError_t launch_decode_fused(const DecodeMaps& maps, const GemvWork* work_gu, int n_work, int units_gu, int S_gu,
-                                const GemvWork* work_d, int units_d, int S_d, int max_chunk_tok,
+                                const GemvWork* work_d, int units_d, int S_d, int max_chunk_tok, const int32_t* slot_row,
                                 const uint32_t* fill_flag, int H, int I, uint16_t* h_perm, const float* w_perm,
                                 float* pair_out, float* ws, int* cnt, int* h_ready, int* h_done, int* status,
                                 uint64_t fill_wait_ns, int num_sms, cudaStream_t st);

@@ -1317,8 +1317,8 @@ int moe_layer_forward(moe_ctx* c, int layer, const void* x, const float* resid, 
                 gen += 1000;  // injected: a generation the copy stream will not write for a long time
                 inject_wave = true;
             }
-            wk[i] = GemvWork{e, offs[e], count[e], units_gu, wait_slot, gen, chunk_base, slot};
-            wk2[i] = GemvWork{e, offs[e], count[e], units_d, wait_slot, gen, chunk_base, slot};
+            wk[i] = GemvWork{e, offs[e], count[e], units_gu, wait_slot, gen, chunk_base, 0};
+            wk2[i] = GemvWork{e, offs[e], count[e], units_d, wait_slot, gen, chunk_base, 0};
             units_gu += ch * Rg * Sg;
             units_d += ch * Rd * Sd;
             chunk_base += ch;
@@ -1336,7 +1336,7 @@ int moe_layer_forward(moe_ctx* c, int layer, const void* x, const float* resid, 
         if (fused) {
             ProfScope ps(c, kDecodeFused, gu_bytes + d_bytes, 6.0 * pw * I * H);
             CUDA_TRY(moe::launch_decode_fused(c->dec_maps, c->work_dev, nw, units_gu, Sg, c->work_dev + (E + 1),
-                                              units_d, Sd, max_chunk_tok, c->fill_flag, H, I, c->h_perm,
+                                              units_d, Sd, max_chunk_tok, slot_row, c->fill_flag, H, I, c->h_perm,
                                               c->w_perm,
                                               c->pair_out, c->dec_ws, c->dec_cnt, c->dec_ready, c->dec_done,
                                               c->status, fill_wait_ns, c->num_sms, c->s_comp));
