@@ -191,6 +191,9 @@ void* moe_host_entry(moe_ctx* ctx, int layer, int expert);
  *  - keeps the recency order, the host pool and every counter.
  * Later misses take the lowest free slot, then the least recently used entry, as before. The
  * old arena is freed after the copy, so the device holds both for the duration of the call.
+ * Kernel launches captured into a CUDA graph before the call hold the old arena's and state's
+ * addresses: a graph of this context's calls must be captured again after a resize, not
+ * replayed.
  * Errors: MOE_E_INVAL (new_capacity < 1, or arena too large), MOE_E_CAPACITY (MOE_PREFILL_DB
  * with new_capacity < 2*num_experts), MOE_E_NOMEM (the new arena could not be allocated; the
  * cache is unchanged), MOE_E_TIMEOUT, MOE_E_CUDA.

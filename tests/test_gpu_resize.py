@@ -1,6 +1,7 @@
 """GPU parity of the elastic cache (moe_cache_resize) on the decode layer at full size
 (hidden 4096, intermediate 1536, 256 experts top-6): decode steps at batches 1, 4 and 16 with
-the capacity grown and shrunk between them, for the host policy and the device-resident policy.
+the capacity grown and shrunk between them, for the host policy and the device-resident policy,
+with bf16 and with MXFP4 entries (a resize moves the surviving entries, whatever their size).
 Outputs against the oracle, and the whole LRU trace -- including the entries a shrink evicts --
 against the oracle's LRU run with the same capacity changes."""
 import numpy as np
@@ -16,11 +17,15 @@ pytestmark = pytest.mark.gpu
 PLAN = [(16, 40), (4, None), (16, 96), (16, 24), (1, 8), (4, 8), (16, 64), (4, None)]  # (batch, resize after)
 
 
+@pytest.mark.parametrize("fmt", ["bf16", "mxfp4"])
 @pytest.mark.parametrize("flags", [moe.MOE_TRACE, moe.MOE_TRACE | moe.MOE_DEVICE_POLICY], ids=["host", "device"])
-def test_resize_between_decode_steps(flags):
+def test_resize_between_decode_steps(flags, fmt):
     import torch
     W = mi.WORKLOADS["decode"]
-    ents = hz.OracleEntries(W)
+    fp4 = fmt == "mxfp4"
+    if fp4:
+        flags |= moe.MOE_MXFP4
+    ents = hz.OracleEntries(W, fp4=fp4)
     Wr = mi.router_weights(W.seed, 0, W.E, W.H)
     b, _ = mi.router_bias(W.seed, 0, W.E, W.zipf_s)
     Wrd, bd = hz.f32_dev(Wr), hz.f32_dev(b)
