@@ -52,9 +52,9 @@ cudaError_t launch_router_topk(const float* z, int T, int E, int k, const int32_
                                int* status, cudaStream_t st);
 
 // --- permutation: stable grouping of the T*k pairs by expert ---
-// Up to 1024 pairs: one CTA. More: permute_grid(P) CTAs of 1024 pairs, with `cells` holding
-// 2 * permute_grid(P) * E ints of scratch and `done` an arrival counter that is 0 before the
-// first launch (the kernels leave it 0).
+// permute_grid(P) CTAs of 1024 pairs, with `cells` holding 2 * permute_grid(P) * E ints of
+// scratch and `done` an arrival counter that is 0 before the first launch (the kernels leave it
+// 0). Decode batches (up to 1024 pairs) take launch_permute_gather below instead.
 int permute_grid(int P);
 cudaError_t launch_permute(const int32_t* idx, const float* w, int P, int E, int32_t* offsets, int32_t* perm,
                            int32_t* inv_perm, float* w_perm, int32_t* active, int32_t* n_active, int* status,

@@ -70,103 +70,6 @@ __device__ __forceinline__ uint32_t warp_peers(int e, int nbits) {
     return peers;
 }
 
-// A counting sort in one CTA. Warp w owns the contiguous pair range [32*r0, 32*r1) (rounds of
-// 32 pairs), so the pairs of an expert come out ordered by (warp, round, lane) = pair id.
-//  1. each warp counts its pairs per expert into its own column cnt[w][e] (shared-memory
-//     atomic increments: a count does not depend on their order);
-//  2. one exclusive scan over the counts in (expert, warp) order turns each cell into the first
-//     position of that warp's pairs of that expert;
-//  3. each warp walks its pairs again and places pair p at its cell's position plus its rank
-//     among the equal lanes of the round, advancing the cell after each round.
-__global__ void __launch_bounds__(kPermThreads) permute_kernel(const int32_t* __restrict__ idx,
-                                                               const float* __restrict__ w, int P, int E,
-                                                               int32_t* __restrict__ offsets,
-                                                               int32_t* __restrict__ perm,
-                                                               int32_t* __restrict__ inv_perm,
-                                                               float* __restrict__ w_perm,
-                                                               int32_t* __restrict__ active,
-                                                               int32_t* __restrict__ n_active, int* status) {
-    pdl_gate();  // may start while the previous kernel of the stream finishes
-    extern __shared__ int smem[];
-    const int Es = E + 1;                     // column stride (odd: the scan's reads spread over banks)
-    int* cnt = smem;                          // [kPermWarps][Es]
-    int* scan = cnt + kPermWarps * Es;        // [33]
-    int* first = scan + 36;                   // [E + 1] first position of each expert
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    for (int i = tid; i < kPermWarps * Es; i += kPermThreads) cnt[i] = 0;
-    __syncthreads();
-    const int rounds = (P + 31) / 32;
-    const int per_warp = (rounds + kPermWarps - 1) / kPermWarps;
-    const int r0 = min(rounds, warp * per_warp), r1 = min(rounds, r0 + per_warp);
-    int* col = cnt + warp * Es;
-    for (int r = r0; r < r1; ++r) {
-        const int p = 32 * r + lane;
-        if (p < P) atomicAdd(&col[checked_expert(idx, p, E, status)], 1);  // counts: order-free
-    }
-    __syncthreads();
-    // exclusive scan of the cells in (expert, warp) order: cell (e, w) is element e*32 + w
-    {
-        const int n_cells = kPermWarps * E;
-        const int per_thread = (n_cells + kPermThreads - 1) / kPermThreads;
-        const int i0 = min(n_cells, tid * per_thread), i1 = min(n_cells, i0 + per_thread);
-        int run = 0;
-        for (int i = i0; i < i1; ++i) run += cnt[(i % kPermWarps) * Es + i / kPermWarps];
-        int total;
-        int pos = block_exclusive_scan(run, scan, &total);
-        for (int i = i0; i < i1; ++i) {
-            int& c = cnt[(i % kPermWarps) * Es + i / kPermWarps];
-            const int v = c;
-            c = pos;
-            if (i % kPermWarps == 0) first[i / kPermWarps] = pos;
-            pos += v;
-        }
-        if (tid == 0) first[E] = total;
-    }
-    __syncthreads();
-    // offsets and the active list (E <= 1024 -> one expert per thread)
-    {
-        const int c = tid < E ? first[tid + 1] - first[tid] : 0;
-        if (tid < E) offsets[tid] = first[tid];
-        if (tid == 0) offsets[E] = first[E];
-        int nact;
-        const int apos = block_exclusive_scan(c > 0 ? 1 : 0, scan, &nact);
-        if (tid < E && c > 0) active[apos] = tid;
-        if (tid == 0) *n_active = nact;
-    }
-    // placement: each warp only touches its own cells, so no CTA barrier is needed
-    const int nbits = E > 1 ? 32 - __clz(E - 1) : 0;
-    constexpr int kBatch = 8;  // rounds whose expert ids are loaded before any is used
-    for (int rb = r0; rb < r1; rb += kBatch) {
-        int eb[kBatch];
-        float wb[kBatch];
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-            const int p = 32 * (rb + u) + lane;
-            const bool valid = rb + u < r1 && p < P;
-            int e = valid ? idx[p] : -1;
-            if (valid && (e < 0 || e >= E)) e = 0;  // already raised in the counting pass
-            eb[u] = e;
-            wb[u] = valid ? w[p] : 0.0f;
-        }
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-            if (rb + u >= r1) break;
-            const int p = 32 * (rb + u) + lane;
-            const int e = eb[u];
-            const uint32_t peers = warp_peers(e, nbits);
-            if (e >= 0) {
-                const int pos = col[e] + __popc(peers & ((1u << lane) - 1u));
-                perm[pos] = p;
-                inv_perm[p] = pos;
-                w_perm[pos] = wb[u];
-            }
-            __syncwarp();
-            if (e >= 0 && lane == __ffs(peers) - 1) col[e] += __popc(peers);
-            __syncwarp();
-        }
-    }
-}
-
 // One warp per permuted row, 16-byte copies.
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __restrict__ x,
                                                           const int32_t* __restrict__ perm, int P, int k, int H,
@@ -181,7 +84,7 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __rest
     for (int c = lane; c < H / 8; c += 32) dst[c] = __ldg(src + c);
 }
 
-// Larger batches (more than 1024 pairs): the same counting sort over many CTAs, so that the
+// Larger batches (more than 1024 pairs): a counting sort over many CTAs, so that the
 // scattered writes of perm and w_perm leave from many SMs. CTA g owns the pairs
 // [1024 g, 1024 g + 1024), one per thread; warp w of it the 32 pairs 1024 g + 32 w + lane.
 // The global order (expert, g, w, lane) is the order (expert, pair id).
@@ -381,26 +284,17 @@ __global__ void __launch_bounds__(kSmallThreads) permute_gather_small_kernel(
 }
 }  // namespace
 
-int permute_grid(int P) { return P > kPermThreads ? (P + kChunkPairs - 1) / kChunkPairs : 1; }
+int permute_grid(int P) { return P > 0 ? (P + kChunkPairs - 1) / kChunkPairs : 1; }
 
 cudaError_t launch_permute(const int32_t* idx, const float* w, int P, int E, int32_t* offsets, int32_t* perm,
                            int32_t* inv_perm, float* w_perm, int32_t* active, int32_t* n_active, int* status,
                            int32_t* cells, unsigned* done, cudaStream_t st) {
-    static std::atomic<uint64_t> attr_one{0}, attr_place{0};
-    {
-        cudaError_t err =
-            ensure_smem_limit(permute_kernel, sizeof(int) * (kPermWarps * 1025 + 36 + 1024 + 1), attr_one);
-        if (err != cudaSuccess) return err;
-        err = ensure_smem_limit(permute_place_kernel, sizeof(int) * kPermWarps * 1025, attr_place);
-        if (err != cudaSuccess) return err;
-    }
-    const int G = permute_grid(P);
-    if (G == 1) {
-        const size_t smem = sizeof(int) * (kPermWarps * (E + 1) + 36 + E + 1);
-        return launch_pdl(permute_kernel, dim3(1), dim3(kPermThreads), smem, st, idx, w, P, E, offsets, perm,
-                          inv_perm, w_perm, active, n_active, status);
-    }
+    static std::atomic<uint64_t> attr_place{0};
+    const cudaError_t err0 = ensure_smem_limit(permute_place_kernel, sizeof(int) * kPermWarps * 1025, attr_place);
+    if (err0 != cudaSuccess) return err0;
+    if (P <= 0) return cudaSuccess;
     if (!cells || !done) return cudaErrorInvalidValue;
+    const int G = permute_grid(P);
     int32_t* starts = cells + static_cast<size_t>(G) * E;
     cudaError_t err = launch_pdl(permute_count_kernel, dim3(G), dim3(kPermThreads), sizeof(int) * (E + 1 + 36), st, idx,
                                  P, E, cells, starts, offsets, active, n_active, done, status);
