@@ -160,6 +160,11 @@ struct moe_ctx {
     ExpertLru lru;
 
     cudaStream_t s_comp = nullptr, s_copy = nullptr;
+    // fills alternate between s_copy and this internal stream, so that one entry's copy crosses
+    // the link while the other stream finishes its previous copy (flag write, completion event);
+    // every fill batch ends with s_copy waiting for it
+    cudaStream_t s_copy2 = nullptr;
+    cudaEvent_t ev_copy2 = nullptr;
     bool own_comp = false, own_copy = false;
 
     // scratch (device)
@@ -381,16 +386,28 @@ void record_event(moe_ctx* c, int kind, int key, int slot, int victim) {
     c->trace[(c->stats.trace_len - 1) % c->trace.size()] = ev;
 }
 
+// Make `st` wait until every fill numbered <= seq has landed. Within a batch the fills alternate
+// between the two copy streams, and a batch starts after the previous one has ended, so the
+// fill's own completion event and the one before it (the other stream's) cover all of them.
+cudaError_t wait_fills_through(moe_ctx* c, cudaStream_t st, int64_t seq) {
+    if (seq < 0) return cudaSuccess;
+    cudaError_t e = cudaStreamWaitEvent(st, c->fill_ev[seq % kEvRing], 0);
+    if (e == cudaSuccess && seq >= 1) e = cudaStreamWaitEvent(st, c->fill_ev[(seq - 1) % kEvRing], 0);
+    return e;
+}
+
 // Access the given keys in order (routed or prefetch), enqueue the fills as one batch on
-// the copy stream. Each filled slot remembers the batch, whose event compute waits for.
+// the copy streams. Each filled slot remembers the batch, whose event compute waits for.
 // On any failure the batch opened so far is still closed with its event, and the access
 // that failed is not committed, so the policy and the slot table stay consistent. If the
 // failure comes after the copy into the slot was enqueued, the slot's previous entry is
 // evicted as well (its bytes are being overwritten) and the slot returns to the free set.
 int access_keys(moe_ctx* c, const std::vector<int>& keys, bool prefetch) {
-    bool batch_open = false;
+    bool batch_open = false, used2 = false;
     FillRec fr{nullptr, nullptr};
     int rc = MOE_OK;
+    int n_fill = 0;                          // fills of this batch: even ones on s_copy, odd ones on s_copy2
+    const uint64_t batch_seq0 = c->fill_seq;  // fills numbered above this one belong to this batch
     for (int key : keys) {
         ExpertLru::Plan p = c->lru.plan(key, prefetch);
         const bool fill = p.kind == ExpertLru::kFill || p.kind == ExpertLru::kPrefetchFill;
@@ -405,14 +422,25 @@ int access_keys(moe_ctx* c, const std::vector<int>& keys, bool prefetch) {
                 if (fr.start) cudaEventRecord(fr.start, c->s_copy);
                 batch_open = true;
             }
+            const bool second = (n_fill & 1) != 0;
+            const cudaStream_t cs = second ? c->s_copy2 : c->s_copy;
+            cudaError_t e = cudaSuccess;
+            if (second && !used2) {
+                // the second stream starts after everything enqueued on s_copy so far
+                if (fr.start) e = cudaStreamWaitEvent(cs, fr.start, 0);
+                used2 = true;
+            }
             // the slot's previous entry may still be read by an enqueued wave
             const int64_t last = c->slot_last_use[p.slot];
-            cudaError_t e = cudaSuccess;
-            if (last >= 0) e = cudaStreamWaitEvent(c->s_copy, c->comp_ev[last % kEvRing], 0);
+            if (e == cudaSuccess && last >= 0) e = cudaStreamWaitEvent(cs, c->comp_ev[last % kEvRing], 0);
+            // a slot filled earlier in this batch (the other stream): after that copy
+            const uint64_t prev_fill = static_cast<uint64_t>(c->slot_fill[p.slot]);
+            if (e == cudaSuccess && c->slot_fill[p.slot] >= 0 && prev_fill > batch_seq0)
+                e = cudaStreamWaitEvent(cs, c->fill_ev[prev_fill % kEvRing], 0);
             if (e == cudaSuccess)
                 e = cudaMemcpyAsync(c->arena + static_cast<size_t>(p.slot) * c->entry_elems,
                                     c->pool + static_cast<size_t>(key) * c->entry_elems, c->entry_bytes,
-                                    cudaMemcpyHostToDevice, c->s_copy);
+                                    cudaMemcpyHostToDevice, cs);
             if (e != cudaSuccess) {
                 rc = fail(MOE_E_CUDA, "fill of layer %d expert %d: %s", key / c->E, key % c->E,
                           cudaGetErrorString(e));
@@ -420,7 +448,7 @@ int access_keys(moe_ctx* c, const std::vector<int>& keys, bool prefetch) {
             }
             // from here on the slot's old bytes are being overwritten
             const uint32_t gen = c->fill_gen[p.slot] + 1;
-            CUresult r = write_value_fn()(reinterpret_cast<CUstream>(c->s_copy),
+            CUresult r = write_value_fn()(reinterpret_cast<CUstream>(cs),
                                           reinterpret_cast<CUdeviceptr>(c->fill_flag + p.slot), gen, 0);
             if (c->inject_kind == 4 && c->inject_count > 0) {
                 c->inject_count--;
@@ -456,7 +484,8 @@ int access_keys(moe_ctx* c, const std::vector<int>& keys, bool prefetch) {
             c->fill_seq++;
             c->slot_fill[p.slot] = c->fill_seq;
             c->table_dirty = true;
-            cudaError_t e = cudaEventRecord(c->fill_ev[c->fill_seq % kEvRing], c->s_copy);
+            cudaError_t e = cudaEventRecord(c->fill_ev[c->fill_seq % kEvRing], (n_fill & 1) ? c->s_copy2 : c->s_copy);
+            n_fill++;
             if (e != cudaSuccess) {
                 // compute could not be ordered after this copy: the new entry is not usable
                 rc = fail(MOE_E_CUDA, "fill event: %s", cudaGetErrorString(e));
@@ -467,6 +496,12 @@ int access_keys(moe_ctx* c, const std::vector<int>& keys, bool prefetch) {
         }
     }
     if (batch_open) {
+        // s_copy joins the second stream, so that waiting on s_copy waits for every fill
+        if (used2) {
+            cudaError_t e = cudaEventRecord(c->ev_copy2, c->s_copy2);
+            if (e == cudaSuccess) e = cudaStreamWaitEvent(c->s_copy, c->ev_copy2, 0);
+            if (e != cudaSuccess && rc == MOE_OK) rc = fail(MOE_E_CUDA, "joining the fill streams: %s", cudaGetErrorString(e));
+        }
         fr.stop = pool_event(c);
         if (fr.start && fr.stop) {
             cudaEventRecord(fr.stop, c->s_copy);
@@ -495,6 +530,7 @@ int validate_layer(moe_ctx* c, int layer) {
 void free_all(moe_ctx* c) {
     if (c->s_comp) cudaStreamSynchronize(c->s_comp);
     if (c->s_copy) cudaStreamSynchronize(c->s_copy);
+    if (c->s_copy2) cudaStreamSynchronize(c->s_copy2);
     harvest(c);
     for (auto& r : c->prof_pending) {
         cudaEventDestroy(r.start);
@@ -514,6 +550,7 @@ void free_all(moe_ctx* c) {
     if (c->ev_d2h) cudaEventDestroy(c->ev_d2h);
     if (c->ev_fork) cudaEventDestroy(c->ev_fork);
     if (c->ev_join) cudaEventDestroy(c->ev_join);
+    if (c->ev_copy2) cudaEventDestroy(c->ev_copy2);
     void* dev_ptrs[] = {c->arena, c->slot_dev, c->logits, c->offsets, c->perm, c->inv_perm, c->active,
                         c->perm_cells, c->perm_done, c->n_active, c->w_perm, c->pair_out, c->x_perm, c->h_perm, c->status, c->work_dev,
                         c->dec_ws,   c->dec_cnt, c->dec_ready, c->dec_done, c->fill_flag, c->d_lru,   c->d_prev, c->d_next,  c->d_key,
@@ -526,6 +563,7 @@ void free_all(moe_ctx* c) {
         if (p) cudaFreeHost(p);
     if (c->own_comp && c->s_comp) cudaStreamDestroy(c->s_comp);
     if (c->own_copy && c->s_copy) cudaStreamDestroy(c->s_copy);
+    if (c->s_copy2) cudaStreamDestroy(c->s_copy2);
     delete c;
 }
 
@@ -804,6 +842,8 @@ int moe_cache_init(const moe_config_t* cfg, void* stream_compute, void* stream_c
         INIT_TRY(cudaStreamCreateWithFlags(&c->s_copy, cudaStreamNonBlocking));
         c->own_copy = true;
     }
+    INIT_TRY(cudaStreamCreateWithFlags(&c->s_copy2, cudaStreamNonBlocking));
+    INIT_TRY(cudaEventCreateWithFlags(&c->ev_copy2, cudaEventDisableTiming));
     const size_t pool_bytes = keys * c->entry_bytes;
     c->dev_policy = (f.flags & MOE_DEVICE_POLICY) != 0;
     INIT_TRY(cudaHostAlloc(reinterpret_cast<void**>(&c->pool), pool_bytes,
@@ -1221,7 +1261,7 @@ int moe_layer_forward(moe_ctx* c, int layer, const void* x, const float* resid, 
         if (path == MOE_PATH_GEMM) {
             int64_t need_fill = -1;
             for (int key : keys) need_fill = std::max(need_fill, c->slot_fill[c->lru.slot_of(key)]);
-            if (need_fill >= 0) CUDA_TRY(cudaStreamWaitEvent(c->s_comp, c->fill_ev[need_fill % kEvRing], 0));
+            CUDA_TRY(wait_fills_through(c, c->s_comp, need_fill));
             std::vector<int> wc;
             int pw = 0;
             for (int a = a0; a < a1; ++a) {
@@ -1270,7 +1310,7 @@ int moe_layer_forward(moe_ctx* c, int layer, const void* x, const float* resid, 
             if (!filled_now[a - a0]) order.push_back(a);
         for (int a = a0; a < a1; ++a)
             if (filled_now[a - a0]) order.push_back(a);
-        if (older_fill >= 0) CUDA_TRY(cudaStreamWaitEvent(c->s_comp, c->fill_ev[older_fill % kEvRing], 0));
+        CUDA_TRY(wait_fills_through(c, c->s_comp, older_fill));
 
         // Work lists (gate/up, then down), each closed by an entry holding the unit total.
         // Units are token chunks x row tiles x K splits; the split of each kernel fills the SMs
