@@ -61,6 +61,7 @@ int fail(int code, const char* fmt, ...) {
     } while (0)
 
 constexpr int kEvRing = 256;     // compute-wave and per-fill completion events
+constexpr int kFillStreams = 2;  // copy streams the fills of a batch take in turn
 constexpr int kStageRing = 16;   // pinned staging buffers for small H2D copies
 constexpr uint64_t kFillWaitNs = 20000000000ull;  // 20 s: a wave's own fills must land by then
 constexpr uint64_t kInjectedFillWaitNs = 200000000ull;  // 0.2 s under injection kind 3
@@ -160,11 +161,11 @@ struct moe_ctx {
     ExpertLru lru;
 
     cudaStream_t s_comp = nullptr, s_copy = nullptr;
-    // fills alternate between s_copy and this internal stream, so that one entry's copy crosses
-    // the link while the other stream finishes its previous copy (flag write, completion event);
-    // every fill batch ends with s_copy waiting for it
-    cudaStream_t s_copy2 = nullptr;
-    cudaEvent_t ev_copy2 = nullptr;
+    // fills take s_copy and kFillStreams - 1 internal streams in turn, so that one entry's copy
+    // crosses the link while another stream finishes its previous copy (flag write, completion
+    // event); every fill batch ends with s_copy waiting for the others
+    cudaStream_t s_fill[kFillStreams] = {};
+    cudaEvent_t ev_fill_join[kFillStreams] = {};
     bool own_comp = false, own_copy = false;
 
     // scratch (device)
@@ -386,13 +387,14 @@ void record_event(moe_ctx* c, int kind, int key, int slot, int victim) {
     c->trace[(c->stats.trace_len - 1) % c->trace.size()] = ev;
 }
 
-// Make `st` wait until every fill numbered <= seq has landed. Within a batch the fills alternate
-// between the two copy streams, and a batch starts after the previous one has ended, so the
-// fill's own completion event and the one before it (the other stream's) cover all of them.
+// Make `st` wait until every fill numbered <= seq has landed. Within a batch the fills take the
+// kFillStreams copy streams in turn, and a batch starts after the previous one has ended, so the
+// completion events of fill seq and of the kFillStreams - 1 fills before it (one per other
+// stream) cover all of them.
 cudaError_t wait_fills_through(moe_ctx* c, cudaStream_t st, int64_t seq) {
-    if (seq < 0) return cudaSuccess;
-    cudaError_t e = cudaStreamWaitEvent(st, c->fill_ev[seq % kEvRing], 0);
-    if (e == cudaSuccess && seq >= 1) e = cudaStreamWaitEvent(st, c->fill_ev[(seq - 1) % kEvRing], 0);
+    cudaError_t e = cudaSuccess;
+    for (int64_t q = seq; e == cudaSuccess && q >= 0 && q > seq - kFillStreams; --q)
+        e = cudaStreamWaitEvent(st, c->fill_ev[q % kEvRing], 0);
     return e;
 }
 
@@ -403,10 +405,11 @@ cudaError_t wait_fills_through(moe_ctx* c, cudaStream_t st, int64_t seq) {
 // failure comes after the copy into the slot was enqueued, the slot's previous entry is
 // evicted as well (its bytes are being overwritten) and the slot returns to the free set.
 int access_keys(moe_ctx* c, const std::vector<int>& keys, bool prefetch) {
-    bool batch_open = false, used2 = false;
+    bool batch_open = false;
+    bool used[kFillStreams] = {};
     FillRec fr{nullptr, nullptr};
     int rc = MOE_OK;
-    int n_fill = 0;                          // fills of this batch: even ones on s_copy, odd ones on s_copy2
+    int n_fill = 0;                           // fills of this batch: fill i takes copy stream i % kFillStreams
     const uint64_t batch_seq0 = c->fill_seq;  // fills numbered above this one belong to this batch
     for (int key : keys) {
         ExpertLru::Plan p = c->lru.plan(key, prefetch);
@@ -422,18 +425,18 @@ int access_keys(moe_ctx* c, const std::vector<int>& keys, bool prefetch) {
                 if (fr.start) cudaEventRecord(fr.start, c->s_copy);
                 batch_open = true;
             }
-            const bool second = (n_fill & 1) != 0;
-            const cudaStream_t cs = second ? c->s_copy2 : c->s_copy;
+            const int si = n_fill % kFillStreams;
+            const cudaStream_t cs = c->s_fill[si];
             cudaError_t e = cudaSuccess;
-            if (second && !used2) {
-                // the second stream starts after everything enqueued on s_copy so far
+            if (si > 0 && !used[si]) {
+                // an internal stream starts after everything enqueued on s_copy so far
                 if (fr.start) e = cudaStreamWaitEvent(cs, fr.start, 0);
-                used2 = true;
+                used[si] = true;
             }
             // the slot's previous entry may still be read by an enqueued wave
             const int64_t last = c->slot_last_use[p.slot];
             if (e == cudaSuccess && last >= 0) e = cudaStreamWaitEvent(cs, c->comp_ev[last % kEvRing], 0);
-            // a slot filled earlier in this batch (the other stream): after that copy
+            // a slot filled earlier in this batch (maybe on another stream): after that copy
             const uint64_t prev_fill = static_cast<uint64_t>(c->slot_fill[p.slot]);
             if (e == cudaSuccess && c->slot_fill[p.slot] >= 0 && prev_fill > batch_seq0)
                 e = cudaStreamWaitEvent(cs, c->fill_ev[prev_fill % kEvRing], 0);
@@ -484,7 +487,7 @@ int access_keys(moe_ctx* c, const std::vector<int>& keys, bool prefetch) {
             c->fill_seq++;
             c->slot_fill[p.slot] = c->fill_seq;
             c->table_dirty = true;
-            cudaError_t e = cudaEventRecord(c->fill_ev[c->fill_seq % kEvRing], (n_fill & 1) ? c->s_copy2 : c->s_copy);
+            cudaError_t e = cudaEventRecord(c->fill_ev[c->fill_seq % kEvRing], c->s_fill[n_fill % kFillStreams]);
             n_fill++;
             if (e != cudaSuccess) {
                 // compute could not be ordered after this copy: the new entry is not usable
@@ -496,10 +499,11 @@ int access_keys(moe_ctx* c, const std::vector<int>& keys, bool prefetch) {
         }
     }
     if (batch_open) {
-        // s_copy joins the second stream, so that waiting on s_copy waits for every fill
-        if (used2) {
-            cudaError_t e = cudaEventRecord(c->ev_copy2, c->s_copy2);
-            if (e == cudaSuccess) e = cudaStreamWaitEvent(c->s_copy, c->ev_copy2, 0);
+        // s_copy joins the internal streams, so that waiting on s_copy waits for every fill
+        for (int si = 1; si < kFillStreams; ++si) {
+            if (!used[si]) continue;
+            cudaError_t e = cudaEventRecord(c->ev_fill_join[si], c->s_fill[si]);
+            if (e == cudaSuccess) e = cudaStreamWaitEvent(c->s_copy, c->ev_fill_join[si], 0);
             if (e != cudaSuccess && rc == MOE_OK) rc = fail(MOE_E_CUDA, "joining the fill streams: %s", cudaGetErrorString(e));
         }
         fr.stop = pool_event(c);
@@ -530,7 +534,8 @@ int validate_layer(moe_ctx* c, int layer) {
 void free_all(moe_ctx* c) {
     if (c->s_comp) cudaStreamSynchronize(c->s_comp);
     if (c->s_copy) cudaStreamSynchronize(c->s_copy);
-    if (c->s_copy2) cudaStreamSynchronize(c->s_copy2);
+    for (int si = 1; si < kFillStreams; ++si)
+        if (c->s_fill[si]) cudaStreamSynchronize(c->s_fill[si]);
     harvest(c);
     for (auto& r : c->prof_pending) {
         cudaEventDestroy(r.start);
@@ -550,7 +555,8 @@ void free_all(moe_ctx* c) {
     if (c->ev_d2h) cudaEventDestroy(c->ev_d2h);
     if (c->ev_fork) cudaEventDestroy(c->ev_fork);
     if (c->ev_join) cudaEventDestroy(c->ev_join);
-    if (c->ev_copy2) cudaEventDestroy(c->ev_copy2);
+    for (int si = 1; si < kFillStreams; ++si)
+        if (c->ev_fill_join[si]) cudaEventDestroy(c->ev_fill_join[si]);
     void* dev_ptrs[] = {c->arena, c->slot_dev, c->logits, c->offsets, c->perm, c->inv_perm, c->active,
                         c->perm_cells, c->perm_done, c->n_active, c->w_perm, c->pair_out, c->x_perm, c->h_perm, c->status, c->work_dev,
                         c->dec_ws,   c->dec_cnt, c->dec_ready, c->dec_done, c->fill_flag, c->d_lru,   c->d_prev, c->d_next,  c->d_key,
@@ -563,7 +569,8 @@ void free_all(moe_ctx* c) {
         if (p) cudaFreeHost(p);
     if (c->own_comp && c->s_comp) cudaStreamDestroy(c->s_comp);
     if (c->own_copy && c->s_copy) cudaStreamDestroy(c->s_copy);
-    if (c->s_copy2) cudaStreamDestroy(c->s_copy2);
+    for (int si = 1; si < kFillStreams; ++si)
+        if (c->s_fill[si]) cudaStreamDestroy(c->s_fill[si]);
     delete c;
 }
 
@@ -842,8 +849,11 @@ int moe_cache_init(const moe_config_t* cfg, void* stream_compute, void* stream_c
         INIT_TRY(cudaStreamCreateWithFlags(&c->s_copy, cudaStreamNonBlocking));
         c->own_copy = true;
     }
-    INIT_TRY(cudaStreamCreateWithFlags(&c->s_copy2, cudaStreamNonBlocking));
-    INIT_TRY(cudaEventCreateWithFlags(&c->ev_copy2, cudaEventDisableTiming));
+    c->s_fill[0] = c->s_copy;
+    for (int si = 1; si < kFillStreams; ++si) {
+        INIT_TRY(cudaStreamCreateWithFlags(&c->s_fill[si], cudaStreamNonBlocking));
+        INIT_TRY(cudaEventCreateWithFlags(&c->ev_fill_join[si], cudaEventDisableTiming));
+    }
     const size_t pool_bytes = keys * c->entry_bytes;
     c->dev_policy = (f.flags & MOE_DEVICE_POLICY) != 0;
     INIT_TRY(cudaHostAlloc(reinterpret_cast<void**>(&c->pool), pool_bytes,
