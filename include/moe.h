@@ -164,7 +164,9 @@ typedef struct {
  * Create a context: pinned host pool of L*E entries (zeroed), device arena of C entries,
  * slot-indirection table slot_of[L][E] (all -1), host LRU, scratch for max_tokens.
  * stream_compute / stream_copy: cudaStream_t handles to use, or NULL to create private
- * streams. The caller then writes each entry straight into moe_host_entry(). Ownership:
+ * streams. Fills also take one private copy stream in turn with stream_copy; every batch of
+ * fills ends with stream_copy waiting for it, so work ordered after stream_copy is ordered
+ * after every fill. The caller then writes each entry straight into moe_host_entry(). Ownership:
  * the context owns everything it allocates; moe_cache_destroy frees it.
  * Errors: MOE_E_INVAL (shape limits above), MOE_E_CAPACITY (MOE_PREFILL_DB with C < 2E, or
  * C < 1), MOE_E_NOMEM, MOE_E_CUDA.
@@ -260,9 +262,9 @@ int moe_cache_fill(moe_ctx* ctx, int layer, const int32_t* topk_idx_host, int n,
  * topk_idx int32 [T x k], topk_w fp32 [T x k] (as written by moe_route).
  * Steps: a D2H copy of topk_idx and a host wait (the host LRU needs the routed experts);
  * the distinct experts D (ascending) are accessed in the LRU in waves of at most C;
- * missing entries are copied in on the copy stream; per wave the expert FFN runs through
+ * missing entries are copied in on the copy streams; per wave the expert FFN runs through
  * the device slot table; a deterministic combine sums the k contributions in j order.
- * On the decode path each fill is followed, on the copy stream, by a write of the slot's
+ * On the decode path each fill is followed, on its copy stream, by a write of the slot's
  * fill generation to a device flag, and the expert kernels stream a filled entry only once
  * its flag shows the copy has landed: resident experts compute while the fills cross the
  * link. Results do not depend on which entries had to be filled.
