@@ -282,6 +282,7 @@ __global__ void __launch_bounds__(kSmallThreads) permute_gather_small_kernel(
         *n_active = nact;
     }
 }
+
 }  // namespace
 
 int permute_grid(int P) { return P > 0 ? (P + kChunkPairs - 1) / kChunkPairs : 1; }
