@@ -347,23 +347,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         // slot and then releasing it), then expands the current one, so the shared-memory round
         // trip of one stage overlaps the integer work of the other.
         int u = blockIdx.x, n0 = 0, kb0 = 0, kb1 = 0, kb = 0, tok0 = 0, nb = 0;
-        // from unit u on, the first unit with a stage of this group (a unit of fewer than
-        // kConvGroups K blocks has none for some groups): its K range, token rows and the group's
-        // first K block; false once the units run out
-        auto enter_unit = [&]() {
-            for (; u < n_units; u += gridDim.x) {
-                const Unit un = locate_unit_any(wl, n_work, u, R, S);
-                const GemvWork wk = wl[un.a];
-                tok0 = wk.tok_off + un.chunk * kNMax;
-                const int nt = min(kNMax, wk.n_tok - un.chunk * kNMax);
-                nb = (nt + 15) >> 4;
-                kb0 = un.split * KB / S;
-                kb1 = (un.split + 1) * KB / S;
-                kb = kb0 + ((grp - n0 % kConvGroups) + kConvGroups) % kConvGroups;
-                if (kb < kb1) return true;
-                n0 += kb1 - kb0;  // no stage of this group in the unit
-            }
-            return false;
+        auto enter_unit = [&]() {  // u < n_units: its K range, token rows and this group's first stage
+            const Unit un = locate_unit_any(wl, n_work, u, R, S);
+            const GemvWork wk = wl[un.a];
+            tok0 = wk.tok_off + un.chunk * kNMax;
+            const int nt = min(kNMax, wk.n_tok - un.chunk * kNMax);
+            nb = (nt + 15) >> 4;
+            kb0 = un.split * KB / S;
+            kb1 = (un.split + 1) * KB / S;
+            kb = kb0 + ((grp - n0 % kConvGroups) + kConvGroups) % kConvGroups;
         };
         uint4 a_nx = make_uint4(0, 0, 0, 0), b_nx = make_uint4(0, 0, 0, 0);
         uint32_t sb_nx = 0;
@@ -379,8 +371,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive(&sh.raw_empty[rs]);  // the raw slot may be refilled
             return true;
         };
-        bool have = enter_unit();
+        bool have = u < n_units;
         if (have) {
+            enter_unit();
             if (!fetch(n0 + (kb - kb0))) {
                 if (lane == 0) raise_status(status, kDevWaitTimeout);
                 ok = false;
@@ -391,12 +384,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int kb_c = kb, n = n0 + (kb - kb0), tok0_c = tok0, nb_c = nb;
             const uint4 a = a_nx, b = b_nx;
             const uint32_t sb = sb_nx;
-            // the group's next stage, over unit boundaries
+            // the group's next stage, over unit boundaries (a unit has at least kConvGroups
+            // K blocks, so every group has a stage in every unit)
             kb += kConvGroups;
             if (kb >= kb1) {
                 n0 += kb1 - kb0;
                 u += gridDim.x;
-                have = enter_unit();
+                have = u < n_units;
+                if (have) enter_unit();
             }
             bool next_ok = true;
             if (have) next_ok = fetch(n0 + (kb - kb0));
