@@ -341,120 +341,92 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (token_loader) prefetch_tmap(&tm_b);
         uint32_t used = 0, last_phase = 0;
         bool ok = true;
-        // The group's stages over the whole run, in order: stage n (counted over the run as the
-        // producer and the MMA issuer count them) of unit u at K block kb, n % kConvGroups == grp.
-        // Each iteration first fetches the NEXT stage's code and scale bytes (waiting for its raw
-        // slot and then releasing it), then expands the current one, so the shared-memory round
-        // trip of one stage overlaps the integer work of the other.
-        int u = blockIdx.x, n0 = 0, kb0 = 0, kb1 = 0, kb = 0, tok0 = 0, nb = 0;
-        auto enter_unit = [&]() {  // u < n_units: its K range, token rows and this group's first stage
+        int n0 = 0;  // stage index of the unit's first stage over the whole run (as the producer
+                     // and the MMA issuer count stages)
+        for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
             const Unit un = locate_unit_any(wl, n_work, u, R, S);
             const GemvWork wk = wl[un.a];
-            tok0 = wk.tok_off + un.chunk * kNMax;
+            const int tok0 = wk.tok_off + un.chunk * kNMax;
             const int nt = min(kNMax, wk.n_tok - un.chunk * kNMax);
-            nb = (nt + 15) >> 4;
-            kb0 = un.split * KB / S;
-            kb1 = (un.split + 1) * KB / S;
-            kb = kb0 + ((grp - n0 % kConvGroups) + kConvGroups) % kConvGroups;
-        };
-        uint4 a_nx = make_uint4(0, 0, 0, 0), b_nx = make_uint4(0, 0, 0, 0);
-        uint32_t sb_nx = 0;
-        auto fetch = [&](int n) {  // this row's code bytes (codes 0 .. 31, 32 .. 63) and scale bytes
-            const int rs = n % kRawStages;
-            if (!warp_wait(&sh.raw_full[rs], (n / kRawStages) & 1, consumer_wait_ns)) return false;
-            const uint8_t* raw = raw_tiles + rs * RAW;
-            a_nx = *reinterpret_cast<const uint4*>(raw + row * 32);
-            b_nx = *reinterpret_cast<const uint4*>(raw + row * 32 + 16);
-            if (FMT == kFp4Mx) sb_nx = *reinterpret_cast<const uint16_t*>(raw + 4096 + row * 2);
-            else sb_nx = *reinterpret_cast<const uint32_t*>(raw + 4096 + row * 4);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sh.raw_empty[rs]);  // the raw slot may be refilled
-            return true;
-        };
-        bool have = u < n_units;
-        if (have) {
-            enter_unit();
-            if (!fetch(n0 + (kb - kb0))) {
-                if (lane == 0) raise_status(status, kDevWaitTimeout);
-                ok = false;
+            const int nb = (nt + 15) >> 4;
+            const int kb0 = un.split * KB / S, kb1 = (un.split + 1) * KB / S;
+            // this group's stages of the unit: n = n0 + (kb - kb0) with n % kConvGroups == grp
+            const int first = kb0 + ((grp - n0 % kConvGroups) + kConvGroups) % kConvGroups;
+            for (int kb = first; kb < kb1; kb += kConvGroups) {
+                const int n = n0 + (kb - kb0);
+                const int rs = n % kRawStages, ms = n % kMma;
+                const uint32_t rphase = (n / kRawStages) & 1, mphase = (n / kMma) & 1;
+                if (!warp_wait(&sh.raw_full[rs], rphase, consumer_wait_ns)) {
+                    if (lane == 0) raise_status(status, kDevWaitTimeout);
+                    ok = false;
+                    break;
+                }
+                const uint8_t* raw = raw_tiles + rs * RAW;
+                // this row's 32 code bytes (codes 0 .. 31 and 32 .. 63 of its slab) and its
+                // scale bytes
+                const uint4 a = *reinterpret_cast<const uint4*>(raw + row * 32);
+                const uint4 b = *reinterpret_cast<const uint4*>(raw + row * 32 + 16);
+                uint32_t sb;
+                if (FMT == kFp4Mx) sb = *reinterpret_cast<const uint16_t*>(raw + 4096 + row * 2);
+                else sb = *reinterpret_cast<const uint32_t*>(raw + 4096 + row * 4);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sh.raw_empty[rs]);  // the raw slot may be refilled
+                // the MMA stage is free once the products that read its A columns and token tile
+                // have completed (usually long before: the converters set the pace)
+                if (!warp_wait(&sh.mma_empty[ms], mphase ^ 1u, consumer_wait_ns)) {
+                    if (lane == 0) raise_status(status, kDevWaitTimeout);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (token_loader) {
+                    uint8_t* sb_tile = b_tiles + ms * kB16;
+                    mbar_arrive_expect_tx(&sh.mma_full[ms], nb * 16 * BK * 2);
+                    for (int bx = 0; bx < nb; ++bx)
+                        tma_load_2d(sb_tile + bx * 16 * BK * 2, &tm_b, &sh.mma_full[ms], kb * BK, tok0 + 16 * bx);
+                    used |= 1u << ms;
+                    last_phase = (last_phase & ~(1u << ms)) | (mphase << ms);
+                }
+                __syncwarp();  // converged again for the warp-collective TMEM stores
+                // two halves of 32 codes: the first half's TMEM store runs while the second half
+                // is expanded
+                const uint32_t ta = t_row + static_cast<uint32_t>(ms) * kACols;
+                uint32_t w[16];
+                if (FMT == kFp4Mx) {  // one E8M0 scale per 32 codes
+                    const uint4 t0 = scale_lut[sb & 0xffu];
+                    expand8(a.x, t0, w + 0);
+                    expand8(a.y, t0, w + 4);
+                    expand8(a.z, t0, w + 8);
+                    expand8(a.w, t0, w + 12);
+                } else {  // one E4M3 scale per 16 codes
+                    const uint4 t0 = scale_lut[sb & 0xffu], t1 = scale_lut[(sb >> 8) & 0xffu];
+                    expand8(a.x, t0, w + 0);
+                    expand8(a.y, t0, w + 4);
+                    expand8(a.z, t1, w + 8);
+                    expand8(a.w, t1, w + 12);
+                }
+                tmem_st16(ta, w);
+                uint32_t w2[16];
+                if (FMT == kFp4Mx) {
+                    const uint4 t1 = scale_lut[(sb >> 8) & 0xffu];
+                    expand8(b.x, t1, w2 + 0);
+                    expand8(b.y, t1, w2 + 4);
+                    expand8(b.z, t1, w2 + 8);
+                    expand8(b.w, t1, w2 + 12);
+                } else {
+                    const uint4 t2 = scale_lut[(sb >> 16) & 0xffu], t3 = scale_lut[sb >> 24];
+                    expand8(b.x, t2, w2 + 0);
+                    expand8(b.y, t2, w2 + 4);
+                    expand8(b.z, t3, w2 + 8);
+                    expand8(b.w, t3, w2 + 12);
+                }
+                tmem_st16(ta + 16, w2);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sh.mma_full[ms]);
             }
-        }
-        while (have && ok) {
-            // the current stage: its bytes are in registers
-            const int kb_c = kb, n = n0 + (kb - kb0), tok0_c = tok0, nb_c = nb;
-            const uint4 a = a_nx, b = b_nx;
-            const uint32_t sb = sb_nx;
-            // the group's next stage, over unit boundaries (a unit has at least kConvGroups
-            // K blocks, so every group has a stage in every unit)
-            kb += kConvGroups;
-            if (kb >= kb1) {
-                n0 += kb1 - kb0;
-                u += gridDim.x;
-                have = u < n_units;
-                if (have) enter_unit();
-            }
-            bool next_ok = true;
-            if (have) next_ok = fetch(n0 + (kb - kb0));
-            const int ms = n % kMma;
-            const uint32_t mphase = (n / kMma) & 1;
-            // the MMA stage is free once the products that read its A columns and token tile
-            // have completed (usually long before: the converters set the pace)
-            if (!warp_wait(&sh.mma_empty[ms], mphase ^ 1u, consumer_wait_ns)) {
-                if (lane == 0) raise_status(status, kDevWaitTimeout);
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            if (token_loader) {
-                uint8_t* sb_tile = b_tiles + ms * kB16;
-                mbar_arrive_expect_tx(&sh.mma_full[ms], nb_c * 16 * BK * 2);
-                for (int bx = 0; bx < nb_c; ++bx)
-                    tma_load_2d(sb_tile + bx * 16 * BK * 2, &tm_b, &sh.mma_full[ms], kb_c * BK, tok0_c + 16 * bx);
-                used |= 1u << ms;
-                last_phase = (last_phase & ~(1u << ms)) | (mphase << ms);
-            }
-            __syncwarp();  // converged again for the warp-collective TMEM stores
-            // two halves of 32 codes: the first half's TMEM store runs while the second half
-            // is expanded
-            const uint32_t ta = t_row + static_cast<uint32_t>(ms) * kACols;
-            uint32_t w[16];
-            if (FMT == kFp4Mx) {  // one E8M0 scale per 32 codes
-                const uint4 t0 = scale_lut[sb & 0xffu];
-                expand8(a.x, t0, w + 0);
-                expand8(a.y, t0, w + 4);
-                expand8(a.z, t0, w + 8);
-                expand8(a.w, t0, w + 12);
-            } else {  // one E4M3 scale per 16 codes
-                const uint4 t0 = scale_lut[sb & 0xffu], t1 = scale_lut[(sb >> 8) & 0xffu];
-                expand8(a.x, t0, w + 0);
-                expand8(a.y, t0, w + 4);
-                expand8(a.z, t1, w + 8);
-                expand8(a.w, t1, w + 12);
-            }
-            tmem_st16(ta, w);
-            uint32_t w2[16];
-            if (FMT == kFp4Mx) {
-                const uint4 t1 = scale_lut[(sb >> 8) & 0xffu];
-                expand8(b.x, t1, w2 + 0);
-                expand8(b.y, t1, w2 + 4);
-                expand8(b.z, t1, w2 + 8);
-                expand8(b.w, t1, w2 + 12);
-            } else {
-                const uint4 t2 = scale_lut[(sb >> 16) & 0xffu], t3 = scale_lut[sb >> 24];
-                expand8(b.x, t2, w2 + 0);
-                expand8(b.y, t2, w2 + 4);
-                expand8(b.z, t3, w2 + 8);
-                expand8(b.w, t3, w2 + 12);
-            }
-            tmem_st16(ta + 16, w2);
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sh.mma_full[ms]);
-            if (!next_ok) {
-                if (lane == 0) raise_status(status, kDevWaitTimeout);
-                ok = false;
-            }
+            n0 += kb1 - kb0;
         }
         // the token tiles this thread issued must land before the CTA exits
         if (token_loader)
