@@ -99,18 +99,6 @@ __device__ __forceinline__ bool wait_counter(const int* p, int target, uint64_t 
     return true;
 }
 
-// The i-th unit of this CTA, or -1 past its last: its gate/up units b, b + grid, ... (round
-// robin), then its down units dn_off[b] .. dn_off[b + 1] - 1 (a contiguous run, sized on the host
-// so that the CTAs' weight streams come out level). Without dn_off, the joint list round robin.
-__device__ __forceinline__ int cta_unit(int i, int n_gu, int n_total, int d0, int d1, bool ranges) {
-    const int b = blockIdx.x, G = gridDim.x;
-    if (!ranges) return b + i * G < n_total ? b + i * G : -1;
-    const int n_mine = b < n_gu ? (n_gu - b + G - 1) / G : 0;
-    if (i < n_mine) return b + i * G;
-    const int j = d0 + (i - n_mine);
-    return j < d1 ? n_gu + j : -1;
-}
-
 template <int NB>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_fused_kernel(const __grid_constant__ CUtensorMap tm_wgu, const __grid_constant__ CUtensorMap tm_wd,
@@ -118,8 +106,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         Phase dn, const int32_t* __restrict__ slot_row, const uint32_t* __restrict__ fill_flag, int H,
                         int I, uint16_t* __restrict__ h_perm, const float* __restrict__ w_perm,
                         float* __restrict__ pair_out, float* __restrict__ ws, int* __restrict__ cnt,
-                        int* __restrict__ h_ready, int* __restrict__ h_done, const int* __restrict__ dn_off,
-                        int* status, uint64_t fill_wait_ns) {
+                        int* __restrict__ h_ready, int* __restrict__ h_done, int* status, uint64_t fill_wait_ns) {
     pdl_gate();
     using C = Cfg<NB>;
     constexpr int kStages = C::STAGES, STAGE_BYTES = C::STAGE_BYTES;
@@ -131,8 +118,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int R_gu = I / 64, R_d = H / 128;
     const int n_total = gu.n_units + dn.n_units;
-    const bool ranges = dn_off != nullptr;
-    const int d0 = ranges ? dn_off[blockIdx.x] : 0, d1 = ranges ? dn_off[blockIdx.x + 1] : 0;
     // the down phase's split-K tiles follow the gate/up phase's in the workspace and counters
     float* ws_d = ws + static_cast<size_t>(gu.n_units) * kNMax * 128;
     int* cnt_d = cnt + gu.n_units;
@@ -169,9 +154,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0, used = 0, last_phase = 0;
             bool ok = true;
             int ready_key = -1;  // (phase, entry) whose fill this CTA last saw land
-            for (int iu = 0; ok; ++iu) {
-                const int g = cta_unit(iu, gu.n_units, n_total, d0, d1, ranges);
-                if (g < 0) break;
+            for (int g = blockIdx.x; g < n_total && ok; g += gridDim.x) {
                 const bool is_gu = g < gu.n_units;
                 const Phase ph = is_gu ? gu : dn;
                 const int u = is_gu ? g : g - gu.n_units;
@@ -284,9 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int last_acc = -1;
             uint32_t last_acc_phase = 0;
             bool ok = true;
-            for (int iu = 0; ok; ++iu) {
-                const int g = cta_unit(iu, gu.n_units, n_total, d0, d1, ranges);
-                if (g < 0) break;
+            for (int g = blockIdx.x; g < n_total && ok; g += gridDim.x) {
                 const bool is_gu = g < gu.n_units;
                 const Phase ph = is_gu ? gu : dn;
                 const int u = is_gu ? g : g - gu.n_units;
@@ -334,9 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ------------------------------------------------------------ epilogue (warps 2-5)
         EpiState st;
-        for (int iu = 0;; ++iu) {
-            const int g = cta_unit(iu, gu.n_units, n_total, d0, d1, ranges);
-            if (g < 0) break;
+        for (int g = blockIdx.x; g < n_total; g += gridDim.x) {
             const bool ok = g < gu.n_units
                                 ? epilogue_unit<true>(st, sh.acc_full, sh.acc_empty, sh.ok, sh.last, tmem, xchg,
                                                       gu.work, gu.n_work, g, gu.S, R_gu, H, I, h_perm, w_perm,
@@ -413,64 +392,19 @@ void decode_fused_choose_split(const int* chunk_tok, int n_chunks, int H, int I,
     *S_d_out = best_d;
 }
 
-bool decode_fused_down_ranges(int units_gu, int units_d, int kb_gu, int kb_d, int grid, int* dn_off) {
-    if (grid < 1 || units_d < 0 || kb_gu < 1 || kb_d < 1) return false;
-    // gate/up K blocks of CTA b under the round robin
-    auto gu_load = [&](int b) -> long long {
-        return b < units_gu ? static_cast<long long>((units_gu - b + grid - 1) / grid) * kb_gu : 0;
-    };
-    auto fits = [&](long long T) {  // down units that fit under level T
-        long long n = 0;
-        for (int b = 0; b < grid; ++b) n += std::max(0LL, (T - gu_load(b)) / kb_d);
-        return n;
-    };
-    // the lowest level that holds every down unit
-    long long lo = 0, hi = gu_load(0) + static_cast<long long>(units_d) * kb_d;
-    while (lo < hi) {
-        const long long mid = (lo + hi) / 2;
-        if (fits(mid) >= units_d) hi = mid;
-        else lo = mid + 1;
-    }
-    std::vector<int> d(grid);
-    long long total = 0;
-    for (int b = 0; b < grid; ++b) {
-        d[b] = static_cast<int>(std::max(0LL, (lo - gu_load(b)) / kb_d));
-        total += d[b];
-    }
-    // the level holds a few units more than there are: take them back from the fullest CTAs
-    std::vector<int> order(grid);
-    for (int b = 0; b < grid; ++b) order[b] = b;
-    std::sort(order.begin(), order.end(), [&](int a, int b) {
-        const long long la = gu_load(a) + static_cast<long long>(d[a]) * kb_d;
-        const long long lb = gu_load(b) + static_cast<long long>(d[b]) * kb_d;
-        return la != lb ? la > lb : a > b;
-    });
-    for (int i = 0; total > units_d && i < grid; ++i)
-        if (d[order[i]] > 0) {
-            d[order[i]]--;
-            total--;
-        }
-    if (total != units_d) return false;
-    dn_off[0] = 0;
-    for (int b = 0; b < grid; ++b) dn_off[b + 1] = dn_off[b] + d[b];
-    return true;
-}
-
 namespace {
 
 template <int NB>
 cudaError_t launch_nb(const DecodeMaps& m, Phase gu, Phase dn, const int32_t* slot_row, const uint32_t* fill_flag,
                       int H, int I, uint16_t* h_perm, const float* w_perm, float* pair_out, float* ws, int* cnt,
-                      int* h_ready, int* h_done, const int* dn_off, int* status, uint64_t fill_wait_ns, int grid,
-                      cudaStream_t st) {
+                      int* h_ready, int* h_done, int* status, uint64_t fill_wait_ns, int grid, cudaStream_t st) {
     auto kern = decode_fused_kernel<NB>;
     constexpr int smem = Cfg<NB>::SMEM;
     static std::atomic<uint64_t> attr{0};
     const cudaError_t e = ensure_smem_limit(kern, smem, attr);
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, st, m.a_gu, m.a_d, m.b_x, m.b_h, gu, dn, slot_row,
-                      fill_flag, H, I, h_perm, w_perm, pair_out, ws, cnt, h_ready, h_done, dn_off, status,
-                      fill_wait_ns);
+                      fill_flag, H, I, h_perm, w_perm, pair_out, ws, cnt, h_ready, h_done, status, fill_wait_ns);
 }
 
 }  // namespace
@@ -479,7 +413,7 @@ cudaError_t launch_decode_fused(const DecodeMaps& m, const GemvWork* work_gu, in
                                 const GemvWork* work_d, int units_d, int S_d, int max_chunk_tok,
                                 const int32_t* slot_row, const uint32_t* fill_flag, int H, int I, uint16_t* h_perm,
                                 const float* w_perm, float* pair_out, float* ws, int* cnt, int* h_ready, int* h_done,
-                                const int* dn_off, int* status, uint64_t fill_wait_ns, int num_sms, cudaStream_t st) {
+                                int* status, uint64_t fill_wait_ns, int num_sms, cudaStream_t st) {
     if (units_gu <= 0 || units_d <= 0 || n_work <= 0) return cudaSuccess;
     if (S_gu < 1 || S_gu > kDecodeMaxSplit || S_d < 1 || S_d > kDecodeMaxSplit) return cudaErrorInvalidValue;
     if ((S_gu > 1 || S_d > 1) && units_gu + units_d > kDecodeSplitUnits) return cudaErrorInvalidValue;
@@ -488,9 +422,9 @@ cudaError_t launch_decode_fused(const DecodeMaps& m, const GemvWork* work_gu, in
     const Phase gu{work_gu, n_work, units_gu, S_gu}, dn{work_d, n_work, units_d, S_d};
     if (max_chunk_tok <= 16)
         return launch_nb<1>(m, gu, dn, slot_row, fill_flag, H, I, h_perm, w_perm, pair_out, ws, cnt, h_ready, h_done,
-                            dn_off, status, fill_wait_ns, grid, st);
+                            status, fill_wait_ns, grid, st);
     return launch_nb<4>(m, gu, dn, slot_row, fill_flag, H, I, h_perm, w_perm, pair_out, ws, cnt, h_ready, h_done,
-                        dn_off, status, fill_wait_ns, grid, st);
+                        status, fill_wait_ns, grid, st);
 }
 
 }  // namespace moe

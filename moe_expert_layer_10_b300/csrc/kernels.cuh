@@ -128,14 +128,8 @@ int decode_fused_chunk_slots(int E, int P);
 cudaError_t launch_decode_fused(const DecodeMaps& maps, const GemvWork* work_gu, int n_work, int units_gu, int S_gu,
                                 const GemvWork* work_d, int units_d, int S_d, int max_chunk_tok, const int32_t* slot_row,
                                 const uint32_t* fill_flag, int H, int I, uint16_t* h_perm, const float* w_perm,
-                                float* pair_out, float* ws, int* cnt, int* h_ready, int* h_done, const int* dn_off,
-                                int* status, uint64_t fill_wait_ns, int num_sms, cudaStream_t st);
-// The down units of a fused launch of `grid` CTAs as contiguous runs, dn_off[grid + 1] (CTA b runs
-// down units dn_off[b] .. dn_off[b + 1] - 1 after its round-robin gate/up units), sized so that
-// the CTAs' K-block totals come out as level as whole units allow. kb_gu / kb_d: K blocks of one
-// unit of each phase. False if no such ranges were found (the launch then takes dn_off = null,
-// the joint list round robin).
-bool decode_fused_down_ranges(int units_gu, int units_d, int kb_gu, int kb_d, int grid, int* dn_off);
+                                float* pair_out, float* ws, int* cnt, int* h_ready, int* h_done, int* status,
+                                uint64_t fill_wait_ns, int num_sms, cudaStream_t st);
 // K splits (S_gu, S_d) of a fused launch: the pair that minimises the largest per-CTA load
 // under the round-robin assignment of the concatenated unit list. chunk_tok: token count of each
 // chunk of the wave's entries, in work-list order.

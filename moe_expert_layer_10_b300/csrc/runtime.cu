@@ -67,13 +67,7 @@ constexpr uint64_t kFillWaitNs = 20000000000ull;  // 20 s: a wave's own fills mu
 constexpr uint64_t kInjectedFillWaitNs = 200000000ull;  // 0.2 s under injection kind 3
 constexpr int kDecodeMaxTokens = 64;  // AUTO path: tensor-core decode kernels up to this many tokens per expert
 // work-list entries of one wave: a gate/up and a down list, each closed by a total entry
-// A wave's uploaded work: the gate/up and down lists (E + 1 entries each), then the fused
-// launch's down-unit ranges (up to kDnOffInts ints: grid + 1 of them).
-constexpr int kDnOffInts = 512;
-static_assert(kDnOffInts * sizeof(int) % sizeof(GemvWork) == 0, "the ranges fill whole work entries");
-constexpr size_t kWorkEntries(int E) {
-    return 2 * (static_cast<size_t>(E) + 1) + kDnOffInts * sizeof(int) / sizeof(GemvWork);
-}
+constexpr size_t kWorkEntries(int E) { return 2 * (static_cast<size_t>(E) + 1); }
 
 enum KernelId { kRouterLogits, kRouterTopk, kPermute, kGather, kDecodeGateUp, kDecodeDown, kGemmGateUp, kGemmDown,
                 kCombine, kPolicy, kFill, kDecodeFused, kNumKernels };
@@ -1383,17 +1377,7 @@ int moe_layer_forward(moe_ctx* c, int layer, const void* x, const float* resid, 
         if (inject_wave) c->inject_count--;
         wk[nw] = GemvWork{-1, 0, 0, units_gu, -1, 0, 0, 0};
         wk2[nw] = GemvWork{-1, 0, 0, units_d, -1, 0, 0, 0};
-        // the fused launch's down units as level runs per CTA, after the two lists
-        const int* dn_off_dev = nullptr;
-        if (fused) {
-            int* dn_off = reinterpret_cast<int*>(wk + 2 * (E + 1));
-            const int grid = std::min(units_gu + units_d, c->num_sms);
-            if (grid + 1 <= kDnOffInts &&
-                moe::decode_fused_down_ranges(units_gu, units_d, std::max(1, (H / 64) / Sg), std::max(1, (I / 64) / Sd),
-                                              grid, dn_off))
-                dn_off_dev = reinterpret_cast<const int*>(c->work_dev + 2 * (E + 1));
-        }
-        // both lists (and the ranges) in one copy: gate/up at work_dev, down at work_dev + E + 1
+        // both lists in one copy: gate/up at work_dev, down at work_dev + E + 1
         CUDA_TRY(cudaMemcpyAsync(c->work_dev, wk, kWorkEntries(E) * sizeof(GemvWork), cudaMemcpyHostToDevice,
                                  c->s_comp));
         CUDA_TRY(cudaEventRecord(c->stage_ev[s], c->s_comp));
@@ -1405,7 +1389,7 @@ int moe_layer_forward(moe_ctx* c, int layer, const void* x, const float* resid, 
                                               units_d, Sd, max_chunk_tok, slot_row, c->fill_flag, H, I, c->h_perm,
                                               c->w_perm,
                                               c->pair_out, c->dec_ws, c->dec_cnt, c->dec_ready, c->dec_done,
-                                              dn_off_dev, c->status, fill_wait_ns, c->num_sms, c->s_comp));
+                                              c->status, fill_wait_ns, c->num_sms, c->s_comp));
         } else {
             {
                 ProfScope ps(c, kDecodeGateUp, gu_bytes, 4.0 * pw * I * H);
