@@ -28,6 +28,8 @@
 // in flight. Tried and dropped: prefetching each CTA's down-unit weights into L2 during its
 // gate/up units (batch 1: 63.9 us against 55.2 us without).
 #include <algorithm>
+#include <functional>
+#include <queue>
 #include <vector>
 
 #include "decode_common.cuh"
@@ -99,6 +101,17 @@ __device__ __forceinline__ bool wait_counter(const int* p, int target, uint64_t 
     return true;
 }
 
+// The i-th unit of this CTA, or -1 past its last: the joint list's round robin b, b + grid, ...
+// (every gate/up unit comes before every down unit), cut to the first `keep` of them, then the
+// down units pool[p0 .. p1) that the host moved here from the last round of more loaded CTAs.
+// Without a schedule (sched == null), the whole round robin.
+__device__ __forceinline__ int cta_unit(int i, int n_total, int keep, const int* pool, int p0, int p1) {
+    const int b = blockIdx.x, G = gridDim.x;
+    if (i < keep) return b + i * G;
+    const int p = p0 + (i - keep);
+    return p < p1 ? pool[p] : -1;
+}
+
 template <int NB>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_fused_kernel(const __grid_constant__ CUtensorMap tm_wgu, const __grid_constant__ CUtensorMap tm_wd,
@@ -106,7 +119,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         Phase dn, const int32_t* __restrict__ slot_row, const uint32_t* __restrict__ fill_flag, int H,
                         int I, uint16_t* __restrict__ h_perm, const float* __restrict__ w_perm,
                         float* __restrict__ pair_out, float* __restrict__ ws, int* __restrict__ cnt,
-                        int* __restrict__ h_ready, int* __restrict__ h_done, int* status, uint64_t fill_wait_ns) {
+                        int* __restrict__ h_ready, int* __restrict__ h_done, const int* __restrict__ sched,
+                        int* status, uint64_t fill_wait_ns) {
     pdl_gate();
     using C = Cfg<NB>;
     constexpr int kStages = C::STAGES, STAGE_BYTES = C::STAGE_BYTES;
@@ -118,6 +132,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int R_gu = I / 64, R_d = H / 128;
     const int n_total = gu.n_units + dn.n_units;
+    // the schedule: keep[G], then pool_off[G + 1], then the moved units
+    const int G = static_cast<int>(gridDim.x), b_cta = static_cast<int>(blockIdx.x);
+    const int rr_count = b_cta < n_total ? (n_total - b_cta + G - 1) / G : 0;
+    const int keep = sched ? sched[b_cta] : rr_count;
+    const int* pool = sched ? sched + 2 * G + 1 : nullptr;
+    const int p0 = sched ? sched[G + b_cta] : 0, p1 = sched ? sched[G + b_cta + 1] : 0;
     // the down phase's split-K tiles follow the gate/up phase's in the workspace and counters
     float* ws_d = ws + static_cast<size_t>(gu.n_units) * kNMax * 128;
     int* cnt_d = cnt + gu.n_units;
@@ -154,7 +174,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0, used = 0, last_phase = 0;
             bool ok = true;
             int ready_key = -1;  // (phase, entry) whose fill this CTA last saw land
-            for (int g = blockIdx.x; g < n_total && ok; g += gridDim.x) {
+            for (int iu = 0; ok; ++iu) {
+                const int g = cta_unit(iu, n_total, keep, pool, p0, p1);
+                if (g < 0) break;
                 const bool is_gu = g < gu.n_units;
                 const Phase ph = is_gu ? gu : dn;
                 const int u = is_gu ? g : g - gu.n_units;
@@ -267,7 +289,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             int last_acc = -1;
             uint32_t last_acc_phase = 0;
             bool ok = true;
-            for (int g = blockIdx.x; g < n_total && ok; g += gridDim.x) {
+            for (int iu = 0; ok; ++iu) {
+                const int g = cta_unit(iu, n_total, keep, pool, p0, p1);
+                if (g < 0) break;
                 const bool is_gu = g < gu.n_units;
                 const Phase ph = is_gu ? gu : dn;
                 const int u = is_gu ? g : g - gu.n_units;
@@ -315,7 +339,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ------------------------------------------------------------ epilogue (warps 2-5)
         EpiState st;
-        for (int g = blockIdx.x; g < n_total; g += gridDim.x) {
+        for (int iu = 0;; ++iu) {
+            const int g = cta_unit(iu, n_total, keep, pool, p0, p1);
+            if (g < 0) break;
             const bool ok = g < gu.n_units
                                 ? epilogue_unit<true>(st, sh.acc_full, sh.acc_empty, sh.ok, sh.last, tmem, xchg,
                                                       gu.work, gu.n_work, g, gu.S, R_gu, H, I, h_perm, w_perm,
@@ -392,19 +418,84 @@ void decode_fused_choose_split(const int* chunk_tok, int n_chunks, int H, int I,
     *S_d_out = best_d;
 }
 
+int decode_fused_schedule(int units_gu, int units_d, int kb_gu, int kb_d, int grid, int* sched, int cap) {
+    const int n_total = units_gu + units_d;
+    // keep, pool_off and at most one moved unit per CTA must fit
+    if (grid < 1 || n_total < grid || kb_gu < 1 || kb_d < 1 || 4 * grid + 1 > cap) return 0;
+    // the round robin: CTA b holds units b, b + grid, ...
+    std::vector<int> keep(grid), load(grid);
+    for (int b = 0; b < grid; ++b) {
+        const int n = (n_total - b + grid - 1) / grid;
+        const int n_gu = b < units_gu ? (units_gu - b + grid - 1) / grid : 0;
+        keep[b] = n;
+        load[b] = n_gu * kb_gu + (n - n_gu) * kb_d;
+    }
+    // Move the last unit of the most loaded CTA to the least loaded one while that lowers the
+    // largest load. Only down units move (a CTA's last unit, from the round robin's last round,
+    // so a moved unit still runs late, when its h rows exist); a CTA gives at most one unit and
+    // a receiver never gives.
+    std::vector<int> order(grid);
+    for (int b = 0; b < grid; ++b) order[b] = b;
+    std::sort(order.begin(), order.end(), [&](int a, int b) { return load[a] != load[b] ? load[a] > load[b] : a < b; });
+    std::vector<char> gave(grid, 0), got(grid, 0);
+    std::vector<std::vector<int>> recv(grid);
+    using Entry = std::pair<int, int>;  // (load, CTA)
+    std::priority_queue<Entry, std::vector<Entry>, std::greater<Entry>> low;
+    for (int b = 0; b < grid; ++b) low.push({load[b], b});
+    const int max0 = load[order[0]];
+    int max_recv = 0, max_given = 0;  // the largest loads of the receivers and of the givers
+    for (int k = 0; k < grid; ++k) {
+        const int hi = order[k];
+        // hi must hold the largest load and be able to give a down unit somewhere lower
+        if (got[hi] || load[hi] < std::max(max_recv, max_given)) break;
+        const int last = hi + (keep[hi] - 1) * grid;
+        if (keep[hi] == 0 || last < units_gu) break;
+        while (!low.empty() && (gave[low.top().second] || low.top().first != load[low.top().second]))
+            low.pop();  // stale entries
+        if (low.empty()) break;
+        const int lo = low.top().second;
+        if (lo == hi || load[lo] + kb_d >= load[hi]) break;
+        low.pop();
+        gave[hi] = 1;
+        keep[hi]--;
+        load[hi] -= kb_d;
+        got[lo] = 1;
+        recv[lo].push_back(last);
+        load[lo] += kb_d;
+        max_given = std::max(max_given, load[hi]);
+        max_recv = std::max(max_recv, load[lo]);
+        low.push({load[lo], lo});
+    }
+    int max1 = 0;
+    for (int b = 0; b < grid; ++b) max1 = std::max(max1, load[b]);
+    if (max1 >= max0) return 0;  // the moves would not lower the largest load: plain round robin
+    int* pool_off = sched + grid;
+    int* pool = sched + 2 * grid + 1;
+    int np = 0;
+    for (int b = 0; b < grid; ++b) {
+        sched[b] = keep[b];
+        pool_off[b] = np;
+        for (int u : recv[b]) pool[np++] = u;
+    }
+    pool_off[grid] = np;
+    return np > 0 ? 3 * grid + 1 + np : 0;  // 0: the plain round robin is as level
+}
+
 namespace {
 
 template <int NB>
 cudaError_t launch_nb(const DecodeMaps& m, Phase gu, Phase dn, const int32_t* slot_row, const uint32_t* fill_flag,
                       int H, int I, uint16_t* h_perm, const float* w_perm, float* pair_out, float* ws, int* cnt,
-                      int* h_ready, int* h_done, int* status, uint64_t fill_wait_ns, int grid, cudaStream_t st) {
+                      int* h_ready, int* h_done, const int* sched, int* status, uint64_t fill_wait_ns, int grid,
+                      cudaStream_t st) {
     auto kern = decode_fused_kernel<NB>;
     constexpr int smem = Cfg<NB>::SMEM;
     static std::atomic<uint64_t> attr{0};
     const cudaError_t e = ensure_smem_limit(kern, smem, attr);
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, st, m.a_gu, m.a_d, m.b_x, m.b_h, gu, dn, slot_row,
-                      fill_flag, H, I, h_perm, w_perm, pair_out, ws, cnt, h_ready, h_done, status, fill_wait_ns);
+                      fill_flag, H, I, h_perm, w_perm, pair_out, ws, cnt, h_ready, h_done, sched, status,
+                      fill_wait_ns);
 }
 
 }  // namespace
@@ -413,7 +504,7 @@ cudaError_t launch_decode_fused(const DecodeMaps& m, const GemvWork* work_gu, in
                                 const GemvWork* work_d, int units_d, int S_d, int max_chunk_tok,
                                 const int32_t* slot_row, const uint32_t* fill_flag, int H, int I, uint16_t* h_perm,
                                 const float* w_perm, float* pair_out, float* ws, int* cnt, int* h_ready, int* h_done,
-                                int* status, uint64_t fill_wait_ns, int num_sms, cudaStream_t st) {
+                                const int* sched, int* status, uint64_t fill_wait_ns, int num_sms, cudaStream_t st) {
     if (units_gu <= 0 || units_d <= 0 || n_work <= 0) return cudaSuccess;
     if (S_gu < 1 || S_gu > kDecodeMaxSplit || S_d < 1 || S_d > kDecodeMaxSplit) return cudaErrorInvalidValue;
     if ((S_gu > 1 || S_d > 1) && units_gu + units_d > kDecodeSplitUnits) return cudaErrorInvalidValue;
@@ -422,9 +513,9 @@ cudaError_t launch_decode_fused(const DecodeMaps& m, const GemvWork* work_gu, in
     const Phase gu{work_gu, n_work, units_gu, S_gu}, dn{work_d, n_work, units_d, S_d};
     if (max_chunk_tok <= 16)
         return launch_nb<1>(m, gu, dn, slot_row, fill_flag, H, I, h_perm, w_perm, pair_out, ws, cnt, h_ready, h_done,
-                            status, fill_wait_ns, grid, st);
+                            sched, status, fill_wait_ns, grid, st);
     return launch_nb<4>(m, gu, dn, slot_row, fill_flag, H, I, h_perm, w_perm, pair_out, ws, cnt, h_ready, h_done,
-                        status, fill_wait_ns, grid, st);
+                        sched, status, fill_wait_ns, grid, st);
 }
 
 }  // namespace moe

@@ -128,8 +128,15 @@ int decode_fused_chunk_slots(int E, int P);
 cudaError_t launch_decode_fused(const DecodeMaps& maps, const GemvWork* work_gu, int n_work, int units_gu, int S_gu,
                                 const GemvWork* work_d, int units_d, int S_d, int max_chunk_tok, const int32_t* slot_row,
                                 const uint32_t* fill_flag, int H, int I, uint16_t* h_perm, const float* w_perm,
-                                float* pair_out, float* ws, int* cnt, int* h_ready, int* h_done, int* status,
-                                uint64_t fill_wait_ns, int num_sms, cudaStream_t st);
+                                float* pair_out, float* ws, int* cnt, int* h_ready, int* h_done, const int* sched,
+                                int* status, uint64_t fill_wait_ns, int num_sms, cudaStream_t st);
+// A unit schedule for a fused launch of `grid` CTAs that keeps the joint list's round robin but
+// moves the last down unit of each most-loaded CTA to a least-loaded one, when that lowers the
+// largest per-CTA K-block total (kb_gu / kb_d: K blocks of one unit of each phase). Writes
+// keep[grid] (round-robin units a CTA runs), pool_off[grid + 1] and the moved units into sched
+// (at most cap ints) and returns the ints written, or 0 if the plain round robin is as level
+// (the launch then takes sched = null).
+int decode_fused_schedule(int units_gu, int units_d, int kb_gu, int kb_d, int grid, int* sched, int cap);
 // K splits (S_gu, S_d) of a fused launch: the pair that minimises the largest per-CTA load
 // under the round-robin assignment of the concatenated unit list. chunk_tok: token count of each
 // chunk of the wave's entries, in work-list order.

@@ -67,7 +67,13 @@ constexpr uint64_t kFillWaitNs = 20000000000ull;  // 20 s: a wave's own fills mu
 constexpr uint64_t kInjectedFillWaitNs = 200000000ull;  // 0.2 s under injection kind 3
 constexpr int kDecodeMaxTokens = 64;  // AUTO path: tensor-core decode kernels up to this many tokens per expert
 // work-list entries of one wave: a gate/up and a down list, each closed by a total entry
-constexpr size_t kWorkEntries(int E) { return 2 * (static_cast<size_t>(E) + 1); }
+// A wave's uploaded work: the gate/up and down lists (E + 1 entries each), then the fused
+// launch's unit schedule (up to kSchedInts ints).
+constexpr int kSchedInts = 1024;
+static_assert(kSchedInts * sizeof(int) % sizeof(GemvWork) == 0, "the schedule fills whole work entries");
+constexpr size_t kWorkEntries(int E) {
+    return 2 * (static_cast<size_t>(E) + 1) + kSchedInts * sizeof(int) / sizeof(GemvWork);
+}
 
 enum KernelId { kRouterLogits, kRouterTopk, kPermute, kGather, kDecodeGateUp, kDecodeDown, kGemmGateUp, kGemmDown,
                 kCombine, kPolicy, kFill, kDecodeFused, kNumKernels };
@@ -1377,7 +1383,16 @@ int moe_layer_forward(moe_ctx* c, int layer, const void* x, const float* resid, 
         if (inject_wave) c->inject_count--;
         wk[nw] = GemvWork{-1, 0, 0, units_gu, -1, 0, 0, 0};
         wk2[nw] = GemvWork{-1, 0, 0, units_d, -1, 0, 0, 0};
-        // both lists in one copy: gate/up at work_dev, down at work_dev + E + 1
+        // the fused launch's unit schedule, after the two lists (null: the plain round robin)
+        const int* sched_dev = nullptr;
+        if (fused) {
+            int* sched = reinterpret_cast<int*>(wk + 2 * (E + 1));
+            const int grid = std::min(units_gu + units_d, c->num_sms);
+            if (moe::decode_fused_schedule(units_gu, units_d, std::max(1, (H / 64) / Sg), std::max(1, (I / 64) / Sd),
+                                           grid, sched, kSchedInts) > 0)
+                sched_dev = reinterpret_cast<const int*>(c->work_dev + 2 * (E + 1));
+        }
+        // both lists (and the schedule) in one copy: gate/up at work_dev, down at work_dev + E + 1
         CUDA_TRY(cudaMemcpyAsync(c->work_dev, wk, kWorkEntries(E) * sizeof(GemvWork), cudaMemcpyHostToDevice,
                                  c->s_comp));
         CUDA_TRY(cudaEventRecord(c->stage_ev[s], c->s_comp));
@@ -1389,7 +1404,7 @@ int moe_layer_forward(moe_ctx* c, int layer, const void* x, const float* resid, 
                                               units_d, Sd, max_chunk_tok, slot_row, c->fill_flag, H, I, c->h_perm,
                                               c->w_perm,
                                               c->pair_out, c->dec_ws, c->dec_cnt, c->dec_ready, c->dec_done,
-                                              c->status, fill_wait_ns, c->num_sms, c->s_comp));
+                                              sched_dev, c->status, fill_wait_ns, c->num_sms, c->s_comp));
         } else {
             {
                 ProfScope ps(c, kDecodeGateUp, gu_bytes, 4.0 * pw * I * H);
