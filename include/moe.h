@@ -417,6 +417,16 @@ int moe_measure_bandwidth(moe_ctx* ctx, int host_threads, int reps, moe_bandwidt
 int moe_host_expert_ffn(const void* entry_bf16, int hidden, int inter, const void* x_bf16, int n_tok, float* y,
                         int threads);
 
+/* Host-only: the unit schedule of the fused decode launch (gate/up and down units of a wave in one
+ * launch of `grid` CTAs). Units are numbered gate/up first (units_gu of kb_gu K blocks each), then
+ * down (units_d of kb_d each); the launch deals them round robin (CTA b: b, b + grid, ...), and
+ * this schedule moves the last down unit of each most-loaded CTA to a less-loaded one when that
+ * lowers the largest per-CTA K-block total. Writes keep[grid] (round-robin units CTA b runs),
+ * pool_off[grid + 1] and the moved units (CTA b runs pool[pool_off[b] .. pool_off[b+1]) after its
+ * own) into sched, at most cap ints. Every CTA runs all its gate/up units before any down unit.
+ * Returns the ints written, 0 when the plain round robin is as level, or MOE_E_INVAL. */
+int moe_fused_schedule(int units_gu, int units_d, int kb_gu, int kb_d, int grid, int32_t* sched, int cap);
+
 /* Number of a layer's n_miss misses to fill under the q-star rule for the given bandwidths
  * (host_gbps == 0: all; pcie_gbps == 0: none). Returns the count (>= 0) or MOE_E_INVAL. */
 int moe_qstar_fills(double pcie_gbps, double host_gbps, int n_miss);

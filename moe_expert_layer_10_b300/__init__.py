@@ -29,7 +29,7 @@ EXPORTS = ["moe_cache_init", "moe_cache_destroy", "moe_host_entry", "moe_entry_b
            "moe_route_forced", "moe_cache_fill", "moe_layer_forward", "moe_stats", "moe_last_error",
            "moe_set_path", "moe_set_profile", "moe_sync", "moe_resident_slot", "moe_kernel_stats", "moe_lru_simulate",
            "moe_debug_inject", "moe_debug_read", "moe_route_noalloc", "moe_cache_resize", "moe_measure_bandwidth",
-           "moe_host_expert_ffn", "moe_qstar_fills", "moe_qstar_simulate"]
+           "moe_host_expert_ffn", "moe_qstar_fills", "moe_qstar_simulate", "moe_fused_schedule"]
 MOE_NOALLOC_MAX_LOGITS = 65536
 MOE_DBG_OFFSETS, MOE_DBG_PERM, MOE_DBG_INV_PERM, MOE_DBG_ACTIVE, MOE_DBG_N_ACTIVE, MOE_DBG_SLOT_TABLE, \
     MOE_DBG_H_PERM, MOE_DBG_X_PERM, MOE_DBG_W_PERM = range(9)
@@ -121,6 +121,7 @@ def lib():
     L.moe_measure_bandwidth.argtypes = [vp, i32, i32, ctypes.POINTER(Bandwidth)]
     L.moe_host_expert_ffn.argtypes = [vp, i32, i32, vp, i32, vp, i32]
     L.moe_qstar_fills.argtypes = [dbl, dbl, i32]
+    L.moe_fused_schedule.argtypes = [i32, i32, i32, i32, i32, vp, i32]
     L.moe_qstar_simulate.argtypes = [i32, i32, vp, vp, vp, vp, dbl, dbl, dbl, dbl, dbl, ctypes.POINTER(QstarSim),
                                      vp, u64]
     _lib = L
@@ -190,6 +191,19 @@ def host_expert_ffn(entry_bf16, hidden: int, inter: int, x_bf16, threads: int = 
     _check(lib().moe_host_expert_ffn(e.ctypes.data, hidden, inter, x.ctypes.data, x.shape[0], y.ctypes.data, threads),
            "moe_host_expert_ffn")
     return y
+
+
+def fused_schedule(units_gu: int, units_d: int, kb_gu: int, kb_d: int, grid: int, cap: int = 1024):
+    """moe_fused_schedule: (keep, pool_off, pool) of the fused decode launch's unit schedule, or
+    None when the plain round robin is as level."""
+    import numpy as np
+    buf = np.zeros(max(cap, 1), np.int32)
+    n = _check(lib().moe_fused_schedule(int(units_gu), int(units_d), int(kb_gu), int(kb_d), int(grid),
+                                        buf.ctypes.data, int(cap)), "moe_fused_schedule")
+    if n == 0:
+        return None
+    keep, off = buf[:grid].copy(), buf[grid:2 * grid + 1].copy()
+    return keep, off, buf[2 * grid + 1:2 * grid + 1 + off[grid]].copy()
 
 
 def qstar_fills(pcie_gbps: float, host_gbps: float, n_miss: int) -> int:

@@ -28,9 +28,6 @@
 // in flight. Tried and dropped: prefetching each CTA's down-unit weights into L2 during its
 // gate/up units (batch 1: 63.9 us against 55.2 us without).
 #include <algorithm>
-#include <functional>
-#include <queue>
-#include <vector>
 
 #include "decode_common.cuh"
 
@@ -365,121 +362,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 int decode_fused_chunk_slots(int E, int P) { return E + P / kNMax + 1; }
-
-void decode_fused_choose_split(const int* chunk_tok, int n_chunks, int H, int I, int num_sms, int* S_gu_out,
-                               int* S_d_out) {
-    // load of a unit in bytes: its weights (16 KB per 64-column stage), its token tiles, a
-    // fixed cost for the unit's hand-offs, and for a split the partial tile written and read
-    const int R_gu = I / 64, R_d = H / 128, KB_gu = H / BK, KB_d = I / BK;
-    const double kUnitFixed = 8192.0;
-    int best_gu = 1, best_d = 1;
-    double best = -1.0, unsplit = 0.0;
-    std::vector<double> load(num_sms);
-    for (int sg = 1; sg <= kDecodeMaxSplit; ++sg) {
-        if (KB_gu / sg < 4) break;
-        for (int sd = 1; sd <= kDecodeMaxSplit; ++sd) {
-            if (KB_d / sd < 4) break;
-            long long units = 0;
-            for (int c = 0; c < n_chunks; ++c) units += static_cast<long long>(R_gu) * sg + static_cast<long long>(R_d) * sd;
-            if ((sg > 1 || sd > 1) && units > kDecodeSplitUnits) continue;
-            std::fill(load.begin(), load.end(), 0.0);
-            long long g = 0;
-            for (int phase = 0; phase < 2; ++phase) {
-                const int R = phase == 0 ? R_gu : R_d, S = phase == 0 ? sg : sd, KB = phase == 0 ? KB_gu : KB_d;
-                for (int c = 0; c < n_chunks; ++c) {
-                    const int ntp = ((chunk_tok[c] + 15) / 16) * 16;
-                    for (int t = 0; t < R; ++t)
-                        for (int sp = 0; sp < S; ++sp, ++g) {
-                            const int kb = (sp + 1) * KB / S - sp * KB / S;
-                            double b = kb * (A_BYTES + ntp * BK * 2.0) + kUnitFixed;
-                            if (S > 1) b += 2.0 * ntp * 128 * 4;
-                            load[g % num_sms] += b;
-                        }
-                }
-            }
-            const double mx = *std::max_element(load.begin(), load.end());
-            if (sg == 1 && sd == 1) unsplit = mx;
-            if (best < 0 || mx < best * (1.0 - 1e-9)) {
-                best = mx;
-                best_gu = sg;
-                best_d = sd;
-            }
-        }
-    }
-    // Splits cost more than this model charges (a split's units are smaller, so less of a down
-    // unit's weight stream is already in the ring when its h rows arrive, and each split adds an
-    // epilogue pass): on the decode layer at batch 1 the unsplit launch measured 52.8 us against
-    // 55.2 us for the chosen (1, 3). So a split is taken only if the model predicts 20 % or more.
-    if (best > 0.8 * unsplit) {
-        best_gu = 1;
-        best_d = 1;
-    }
-    *S_gu_out = best_gu;
-    *S_d_out = best_d;
-}
-
-int decode_fused_schedule(int units_gu, int units_d, int kb_gu, int kb_d, int grid, int* sched, int cap) {
-    const int n_total = units_gu + units_d;
-    // keep, pool_off and at most one moved unit per CTA must fit
-    if (grid < 1 || n_total < grid || kb_gu < 1 || kb_d < 1 || 4 * grid + 1 > cap) return 0;
-    // the round robin: CTA b holds units b, b + grid, ...
-    std::vector<int> keep(grid), load(grid);
-    for (int b = 0; b < grid; ++b) {
-        const int n = (n_total - b + grid - 1) / grid;
-        const int n_gu = b < units_gu ? (units_gu - b + grid - 1) / grid : 0;
-        keep[b] = n;
-        load[b] = n_gu * kb_gu + (n - n_gu) * kb_d;
-    }
-    // Move the last unit of the most loaded CTA to the least loaded one while that lowers the
-    // largest load. Only down units move (a CTA's last unit, from the round robin's last round,
-    // so a moved unit still runs late, when its h rows exist); a CTA gives at most one unit and
-    // a receiver never gives.
-    std::vector<int> order(grid);
-    for (int b = 0; b < grid; ++b) order[b] = b;
-    std::sort(order.begin(), order.end(), [&](int a, int b) { return load[a] != load[b] ? load[a] > load[b] : a < b; });
-    std::vector<char> gave(grid, 0), got(grid, 0);
-    std::vector<std::vector<int>> recv(grid);
-    using Entry = std::pair<int, int>;  // (load, CTA)
-    std::priority_queue<Entry, std::vector<Entry>, std::greater<Entry>> low;
-    for (int b = 0; b < grid; ++b) low.push({load[b], b});
-    const int max0 = load[order[0]];
-    int max_recv = 0, max_given = 0;  // the largest loads of the receivers and of the givers
-    for (int k = 0; k < grid; ++k) {
-        const int hi = order[k];
-        // hi must hold the largest load and be able to give a down unit somewhere lower
-        if (got[hi] || load[hi] < std::max(max_recv, max_given)) break;
-        const int last = hi + (keep[hi] - 1) * grid;
-        if (keep[hi] == 0 || last < units_gu) break;
-        while (!low.empty() && (gave[low.top().second] || low.top().first != load[low.top().second]))
-            low.pop();  // stale entries
-        if (low.empty()) break;
-        const int lo = low.top().second;
-        if (lo == hi || load[lo] + kb_d >= load[hi]) break;
-        low.pop();
-        gave[hi] = 1;
-        keep[hi]--;
-        load[hi] -= kb_d;
-        got[lo] = 1;
-        recv[lo].push_back(last);
-        load[lo] += kb_d;
-        max_given = std::max(max_given, load[hi]);
-        max_recv = std::max(max_recv, load[lo]);
-        low.push({load[lo], lo});
-    }
-    int max1 = 0;
-    for (int b = 0; b < grid; ++b) max1 = std::max(max1, load[b]);
-    if (max1 >= max0) return 0;  // the moves would not lower the largest load: plain round robin
-    int* pool_off = sched + grid;
-    int* pool = sched + 2 * grid + 1;
-    int np = 0;
-    for (int b = 0; b < grid; ++b) {
-        sched[b] = keep[b];
-        pool_off[b] = np;
-        for (int u : recv[b]) pool[np++] = u;
-    }
-    pool_off[grid] = np;
-    return np > 0 ? 3 * grid + 1 + np : 0;  // 0: the plain round robin is as level
-}
 
 namespace {
 
